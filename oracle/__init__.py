@@ -1,0 +1,153 @@
+"""CPU oracle for the dense BF16 GEMM C = A·Bᵀ — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The CUDA library never imports, links or
+calls it, and the two share no code: the product path has no CPU fallback.
+
+The arithmetic lives in ``gemm_ref.c`` (plain C, binary64): the exact
+definition of the operation on the HipKittens "L2" detail page, §3 "Target
+operation" table (BF16 GEMM: bf16 in, FP32 accumulate, bf16 out) with the
+second operand used transposed as in the "ABt" GEMM of §7/§9.2:
+
+    C[i, j] = RNE_bf16( Σ_k  A[i, k] · B[j, k] )      (sum in binary64)
+
+This module only marshals numpy arrays of bf16 bit patterns (``uint16``) to
+that C code. Every function here is pinned by ``tests/test_oracle_pins.py``
+against exact rational arithmetic, closed forms and invariants.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gemm_ref.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+_lib = None
+_lock = threading.Lock()
+
+_I64 = ctypes.c_int64
+_P = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile ``gemm_ref.c`` into ``oracle/_build/liboracle.so`` with gcc."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-pthread", "-D_GNU_SOURCE", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+            lib.oracle_round_bf16.restype = ctypes.c_uint16
+            lib.oracle_dot_f64.argtypes = [_P, _P, _I64, _I64, _I64, _I64, _I64]
+            lib.oracle_dot_f64.restype = ctypes.c_double
+            lib.oracle_gemm_bf16.argtypes = [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
+                                             ctypes.c_int]
+            lib.oracle_gemm_bf16.restype = ctypes.c_int
+            lib.oracle_gemm_bf16_rows.argtypes = [_P, _P, _P, _I64, _I64, _I64, _I64, _P, _I64,
+                                                  ctypes.c_int]
+            lib.oracle_gemm_bf16_rows.restype = ctypes.c_int
+            lib.oracle_gemm_bf16_entries.argtypes = [_P, _P, _P, _I64, _I64, _I64, _P, _P, _I64,
+                                                     ctypes.c_int]
+            lib.oracle_gemm_bf16_entries.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _as_bits(x: np.ndarray, name: str) -> np.ndarray:
+    if x.dtype != np.uint16 or x.ndim != 2:
+        raise TypeError(f"{name} must be a 2-D uint16 array of bf16 bit patterns")
+    if x.shape[1] > 1 and x.strides[1] != 2 or x.strides[0] % 2:
+        raise ValueError(f"{name} must have a unit stride along K")
+    return x
+
+
+def _ptr(x: np.ndarray) -> int:
+    return x.ctypes.data
+
+
+def round_bf16(x: float) -> int:
+    """binary64 -> bf16 bit pattern, IEEE round-to-nearest-even."""
+    return int(_load().oracle_round_bf16(float(x)))
+
+
+def dot_f64(A: np.ndarray, B: np.ndarray, i: int, j: int) -> float:
+    """The unrounded binary64 sum Σ_k A[i,k]·B[j,k] (increasing k)."""
+    A = _as_bits(A, "A")
+    B = _as_bits(B, "B")
+    K = A.shape[1]
+    assert B.shape[1] == K
+    return float(_load().oracle_dot_f64(_ptr(A), _ptr(B), K, A.strides[0] // 2,
+                                        B.strides[0] // 2, int(i), int(j)))
+
+
+def gemm(A: np.ndarray, B: np.ndarray, threads: int = 0) -> np.ndarray:
+    """Full C = RNE_bf16(A·Bᵀ): A (M×K), B (N×K) bf16 bits -> C (M×N) bf16 bits."""
+    A = _as_bits(A, "A")
+    B = _as_bits(B, "B")
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("A and B disagree on K")
+    C = np.zeros((M, N), dtype=np.uint16)
+    if M and N:
+        _load().oracle_gemm_bf16(_ptr(A), _ptr(B), _ptr(C), M, N, K, max(A.strides[0] // 2, K),
+                                 max(B.strides[0] // 2, K), N, int(threads))
+    return C
+
+
+def gemm_rows(A: np.ndarray, B: np.ndarray, rows, threads: int = 0) -> tuple[np.ndarray, int]:
+    """Full rows ``rows`` of C. Returns (len(rows)×N bf16 bits, threads used)."""
+    A = _as_bits(A, "A")
+    B = _as_bits(B, "B")
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    M, K = A.shape
+    N = B.shape[0]
+    if rows.size and (rows.min() < 0 or rows.max() >= M):
+        raise IndexError("row index out of range")
+    out = np.zeros((rows.size, N), dtype=np.uint16)
+    used = 0
+    if rows.size and N:
+        used = _load().oracle_gemm_bf16_rows(_ptr(A), _ptr(B), _ptr(out), N, K,
+                                             A.strides[0] // 2, B.strides[0] // 2,
+                                             _ptr(rows), rows.size, int(threads))
+    return out, used
+
+
+def gemm_entries(A: np.ndarray, B: np.ndarray, rows, cols, threads: int = 0) -> tuple[np.ndarray, int]:
+    """Entries C[rows[t], cols[t]]. Returns (bf16 bits per entry, threads used)."""
+    A = _as_bits(A, "A")
+    B = _as_bits(B, "B")
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    if rows.shape != cols.shape:
+        raise ValueError("rows and cols differ in length")
+    M, K = A.shape
+    N = B.shape[0]
+    if rows.size and (rows.min() < 0 or rows.max() >= M or cols.min() < 0 or cols.max() >= N):
+        raise IndexError("entry index out of range")
+    out = np.zeros(rows.size, dtype=np.uint16)
+    used = 0
+    if rows.size:
+        used = _load().oracle_gemm_bf16_entries(_ptr(A), _ptr(B), _ptr(out), K,
+                                                A.strides[0] // 2, B.strides[0] // 2,
+                                                _ptr(rows), _ptr(cols), rows.size, int(threads))
+    return out, used

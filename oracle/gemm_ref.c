@@ -1,0 +1,179 @@
+/*
+ * CPU oracle for the dense BF16 GEMM  C = A * B^T  (TEST INFRASTRUCTURE ONLY).
+ *
+ * Only the tests, the smoke check and the CPU-baseline leg of the benchmark
+ * link this file; the CUDA library never does, and the two share no code.
+ *
+ * What it computes (HipKittens, "L2" detail page, §3 "Target operation" table:
+ * BF16 GEMM, bf16 inputs, FP32 accumulation, bf16 output; §7 code listing
+ * descriptions and §9.2: the GEMM hot loop is the "ABt" product, i.e. the
+ * second operand is stored N x K and used transposed):
+ *
+ *     C[i][j] = round_bf16_rne( sum_{k=0}^{K-1} double(A[i][k]) * double(B[j][k]) )
+ *
+ * A is M x K row-major with leading dimension lda (elements), B is N x K
+ * row-major with leading dimension ldb, C is M x N row-major with leading
+ * dimension ldc. All three hold IEEE binary16-brain-float (bf16) bit patterns.
+ *
+ * Precision: the pages fix only bf16 in / fp32 accumulate / bf16 out. The
+ * oracle is the exact definition instead: every bf16 x bf16 product is exact
+ * in binary64 (8 + 8 significant bits), the sum runs in binary64 in increasing
+ * k starting from +0.0, and the result is rounded ONCE, binary64 -> bf16, with
+ * round-to-nearest-even written out from the IEEE 754 definition (no detour
+ * through binary32, so there is no double rounding).
+ *
+ * Build: plain C99, no -ffast-math, -ffp-contract=off (a fused multiply-add
+ * would not change these exact products, but the flag keeps the arithmetic
+ * literally what is written here).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+/* bf16 bit pattern -> binary64 value: the bf16 bits are the upper half of a
+ * binary32; widening binary32 -> binary64 is exact. */
+static double bf16_bits_to_double(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* binary64 -> bf16 with IEEE round-to-nearest, ties-to-even.
+ * bf16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits.
+ * Normal numbers: |x| in [2^E, 2^(E+1)), E >= -126, quantum 2^(E-7).
+ * Subnormals (|x| < 2^-126): quantum 2^-133.
+ * Values that round to >= 2^128 overflow to infinity. */
+uint16_t oracle_round_bf16(double x) {
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x)) return (uint16_t)(sign | 0x7FC0u);
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint16_t)(sign | 0x7F80u);
+
+    int e2;
+    (void)frexp(a, &e2);          /* a = f * 2^e2, f in [0.5, 1) */
+    int E = e2 - 1;               /* a in [2^E, 2^(E+1)) */
+    int qexp = (E < -126 ? -126 : E) - 7;
+
+    double r = ldexp(a, -qexp);   /* exact: scaling by a power of two */
+    double fl = floor(r);
+    double frac = r - fl;         /* exact: r < 2^9 */
+    double n = fl;
+    if (frac > 0.5) {
+        n = fl + 1.0;
+    } else if (frac == 0.5) {
+        if (fmod(fl, 2.0) != 0.0) n = fl + 1.0;   /* tie: go to the even neighbour */
+    }
+    double v = ldexp(n, qexp);    /* exact */
+    if (v >= 0x1p128) return (uint16_t)(sign | 0x7F80u);
+
+    /* v is a bf16 value, hence exactly representable in binary32; its
+     * binary32 encoding has 16 zero low bits and the upper half is the bf16. */
+    float vf = (float)v;
+    uint32_t u;
+    memcpy(&u, &vf, sizeof u);
+    return (uint16_t)(sign | (uint16_t)(u >> 16));
+}
+
+/* The unrounded binary64 dot product of row i of A with row j of B. */
+double oracle_dot_f64(const uint16_t* A, const uint16_t* B, int64_t K,
+                      int64_t lda, int64_t ldb, int64_t i, int64_t j) {
+    const uint16_t* a = A + i * lda;
+    const uint16_t* b = B + j * ldb;
+    double s = 0.0;
+    for (int64_t k = 0; k < K; ++k) s += bf16_bits_to_double(a[k]) * bf16_bits_to_double(b[k]);
+    return s;
+}
+
+/* ---- threading: a plain static split of a list of work items ---------- */
+
+typedef struct {
+    const uint16_t* A;
+    const uint16_t* B;
+    uint16_t* out;
+    int64_t N, K, lda, ldb, ldo;
+    const int64_t* rows;   /* entry mode: row index per entry; row mode: row list */
+    const int64_t* cols;   /* entry mode only */
+    int64_t begin, end;    /* range of work items for this thread */
+    int mode;              /* 0: full rows, 1: single entries */
+} work_t;
+
+static void* worker(void* p) {
+    work_t* w = (work_t*)p;
+    for (int64_t t = w->begin; t < w->end; ++t) {
+        if (w->mode == 0) {
+            int64_t i = w->rows ? w->rows[t] : t;
+            uint16_t* o = w->out + t * w->ldo;
+            for (int64_t j = 0; j < w->N; ++j)
+                o[j] = oracle_round_bf16(oracle_dot_f64(w->A, w->B, w->K, w->lda, w->ldb, i, j));
+        } else {
+            w->out[t] = oracle_round_bf16(
+                oracle_dot_f64(w->A, w->B, w->K, w->lda, w->ldb, w->rows[t], w->cols[t]));
+        }
+    }
+    return NULL;
+}
+
+static int resolve_threads(int threads, int64_t items) {
+    if (threads <= 0) {
+        long n = sysconf(_SC_NPROCESSORS_ONLN);
+        threads = n > 0 ? (int)n : 1;
+    }
+    if (threads > 256) threads = 256;
+    if (items < threads) threads = items > 0 ? (int)items : 1;
+    return threads;
+}
+
+static int run_parallel(work_t base, int64_t items, int threads) {
+    threads = resolve_threads(threads, items);
+    pthread_t tid[256];
+    int joined[256];
+    work_t w[256];
+    for (int t = 0; t < threads; ++t) {
+        w[t] = base;
+        w[t].begin = items * t / threads;
+        w[t].end = items * (t + 1) / threads;
+        joined[t] = 0;
+        if (t == threads - 1) {
+            worker(&w[t]);
+        } else if (pthread_create(&tid[t], NULL, worker, &w[t]) == 0) {
+            joined[t] = 1;
+        } else {
+            worker(&w[t]);   /* could not start a thread: do the share inline */
+        }
+    }
+    for (int t = 0; t < threads - 1; ++t)
+        if (joined[t]) pthread_join(tid[t], NULL);
+    return threads;
+}
+
+/* Full GEMM: C (M x N, leading dimension ldc) = round(A * B^T).
+ * Returns the number of threads used. */
+int oracle_gemm_bf16(const uint16_t* A, const uint16_t* B, uint16_t* C,
+                     int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int64_t ldc, int threads) {
+    work_t w = {A, B, C, N, K, lda, ldb, ldc, NULL, NULL, 0, 0, 0};
+    return run_parallel(w, M, threads);
+}
+
+/* Selected full rows: out[t][j] = C[rows[t]][j] for t < nrows (out has
+ * leading dimension N). Returns the number of threads used. */
+int oracle_gemm_bf16_rows(const uint16_t* A, const uint16_t* B, uint16_t* out,
+                          int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                          const int64_t* rows, int64_t nrows, int threads) {
+    work_t w = {A, B, out, N, K, lda, ldb, N, rows, NULL, 0, 0, 0};
+    return run_parallel(w, nrows, threads);
+}
+
+/* Selected entries: out[t] = C[rows[t]][cols[t]]. Returns threads used. */
+int oracle_gemm_bf16_entries(const uint16_t* A, const uint16_t* B, uint16_t* out,
+                             int64_t K, int64_t lda, int64_t ldb,
+                             const int64_t* rows, const int64_t* cols, int64_t count,
+                             int threads) {
+    work_t w = {A, B, out, 0, K, lda, ldb, 0, rows, cols, 0, 0, 1};
+    return run_parallel(w, count, threads);
+}

@@ -1,0 +1,119 @@
+"""Seeded synthetic inputs for the BF16 GEMM, shared by the tests and the bench.
+
+This module holds none of the GEMM's arithmetic: it only draws random numbers,
+rounds them to bf16 bit patterns and lists the workload shapes. Both the CUDA
+path and the CPU oracle receive the bytes it produces.
+
+Recipe (the workloads the HipKittens pages measure are square BF16 GEMMs with
+M = N = K from 1024 to 14592, "L2" detail page §3 "Evaluated regimes", and the
+headline 8192³ of §2 Q3 / §5 Tab. 2; the other shapes are LLM-projection
+shapes of the same operation):
+
+* normal entries: ``numpy.random.Generator(PCG64(seed)).standard_normal`` in
+  float32, multiplied by the workload's scale in float32, rounded to bf16 with
+  round-to-nearest-even on the float32 bit pattern;
+* integer entries: ``integers(-4, 5)`` (uniform on {-4..4}), exact in bf16;
+* seeds: A = 1000 + workload id, B = 2000 + workload id (integer variant 1100+,
+  2100+), sample positions 3000 + workload id.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+_CHUNK = 1 << 24  # elements per generation chunk (keeps host temporaries small)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    wid: int        # workload id, fixes the seeds
+    M: int
+    N: int
+    K: int
+    scale: float    # standard deviation of the entries (nominal sigma)
+    sampled: bool   # oracle checks sampled entries + full rows rather than all of C
+
+
+WORKLOADS = {
+    "gemm_256": Workload("gemm_256", 1, 256, 256, 256, 1.0, False),
+    "gemm_4096": Workload("gemm_4096", 2, 4096, 4096, 4096, 1.0, False),
+    "gemm_8192": Workload("gemm_8192", 3, 8192, 8192, 8192, 0.5, True),
+    "gemm_16384": Workload("gemm_16384", 4, 16384, 16384, 16384, 1.0, True),
+    "proj_16384x28672x8192": Workload("proj_16384x28672x8192", 5, 16384, 28672, 8192, 0.02, True),
+    "skinny_128x28672x8192": Workload("skinny_128x28672x8192", 6, 128, 28672, 8192, 0.02, False),
+}
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns, round-to-nearest-even on the low 16 bits.
+
+    Inputs are finite (normal draws); NaN handling is not needed here.
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float32 values (exact)."""
+    return (np.asarray(h, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def normal_bf16(rows: int, cols: int, seed: int, scale: float = 1.0) -> np.ndarray:
+    """rows×cols bf16 bits of N(0,1)·scale, drawn row-major from PCG64(seed)."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    out = np.empty(rows * cols, dtype=np.uint16)
+    s = np.float32(scale)
+    for off in range(0, rows * cols, _CHUNK):
+        n = min(_CHUNK, rows * cols - off)
+        x = g.standard_normal(n, dtype=np.float32)
+        if scale != 1.0:
+            x *= s
+        out[off:off + n] = f32_to_bf16_bits(x)
+    return out.reshape(rows, cols)
+
+
+def int_bf16(rows: int, cols: int, seed: int, lo: int = -4, hi: int = 4) -> np.ndarray:
+    """rows×cols bf16 bits of integers uniform on {lo..hi}."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    x = g.integers(lo, hi + 1, size=(rows, cols)).astype(np.float32)
+    return f32_to_bf16_bits(x)
+
+
+def operands(w: Workload, integer: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """(A, B) bf16 bits for a workload: A is M×K, B is N×K."""
+    if integer:
+        return int_bf16(w.M, w.K, 1100 + w.wid), int_bf16(w.N, w.K, 2100 + w.wid)
+    return (normal_bf16(w.M, w.K, 1000 + w.wid, w.scale),
+            normal_bf16(w.N, w.K, 2000 + w.wid, w.scale))
+
+
+def sample_positions(M: int, N: int, seed: int, count: int = 4096,
+                     tile_m: int = 128, tile_n: int = 256) -> tuple[np.ndarray, np.ndarray]:
+    """Seeded output positions: uniform draws plus the corners of C and the
+    first/last row and column of every tile along the edges of the tile grid."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    r = list(g.integers(0, M, size=count))
+    c = list(g.integers(0, N, size=count))
+    edge_r = sorted({0, M - 1} | {min(M - 1, x) for t in range(0, M, tile_m) for x in (t, t + tile_m - 1)})
+    edge_c = sorted({0, N - 1} | {min(N - 1, x) for t in range(0, N, tile_n) for x in (t, t + tile_n - 1)})
+    for i in (0, M - 1):
+        for j in edge_c:
+            r.append(i)
+            c.append(j)
+    for j in (0, N - 1):
+        for i in edge_r:
+            r.append(i)
+            c.append(j)
+    return np.asarray(r, dtype=np.int64), np.asarray(c, dtype=np.int64)
+
+
+def full_rows(M: int, seed: int, count: int = 8) -> np.ndarray:
+    """``count`` distinct seeded row indices including rows 0 and M-1."""
+    g = np.random.Generator(np.random.PCG64(seed + 7))
+    rows = {0, M - 1}
+    while len(rows) < min(count, M):
+        rows.add(int(g.integers(0, M)))
+    return np.asarray(sorted(rows), dtype=np.int64)

@@ -1,0 +1,243 @@
+"""Pins for the CPU oracle, against things other than the oracle itself.
+
+The operation (HipKittens "L2" detail page, §3 "Target operation" table and
+§7/§9.2 "ABt" hot loop): C = RNE_bf16(A·Bᵀ), bf16 in, bf16 out, with A M×K
+and B N×K row-major. The pages print no element values for it, so the pins
+are exact rational arithmetic (brute force), hand-built rounding ties, closed
+forms, algebraic invariants and integer arithmetic. ``test_mutants_fail_pins``
+plants plausible mistakes into a copy of the oracle's C source and checks that
+the pins catch every one of them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import synth
+from exact_bf16 import bits_to_fraction, exact_gemm, fraction_to_bf16_exact, round_fraction
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+class _Lib:
+    """Minimal driver for a compiled copy of the oracle's C source."""
+
+    def __init__(self, path):
+        lib = ctypes.CDLL(path)
+        P, I = ctypes.c_void_p, ctypes.c_int64
+        lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_round_bf16.restype = ctypes.c_uint16
+        lib.oracle_gemm_bf16.argtypes = [P, P, P, I, I, I, I, I, I, ctypes.c_int]
+        lib.oracle_gemm_bf16.restype = ctypes.c_int
+        self.lib = lib
+
+    def round_bf16(self, x):
+        return int(self.lib.oracle_round_bf16(float(x)))
+
+    def gemm(self, A, B, threads=1):
+        A = np.ascontiguousarray(A, dtype=np.uint16)
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        M, K = A.shape
+        N = B.shape[0]
+        C = np.zeros((M, N), dtype=np.uint16)
+        if M and N:
+            self.lib.oracle_gemm_bf16(A.ctypes.data, B.ctypes.data, C.ctypes.data, M, N, K, K, K, N,
+                                      threads)
+        return C
+
+
+# ---------------------------------------------------------------- the pins --
+
+def _bf(x: float) -> int:
+    return fraction_to_bf16_exact(Fraction(x))
+
+
+def pin_bruteforce(o):
+    """Random bf16 normals on tiny shapes == exact rational GEMM, bit for bit."""
+    for seed, (M, N, K) in enumerate([(1, 1, 1), (3, 5, 7), (8, 8, 16), (16, 9, 13), (5, 16, 16)]):
+        A = synth.normal_bf16(M, K, 50 + seed)
+        B = synth.normal_bf16(N, K, 80 + seed, 0.5)
+        want = np.array(exact_gemm(A, B), dtype=np.uint16)
+        got = o.gemm(A, B)
+        if not np.array_equal(got, want):
+            return f"bruteforce mismatch at {(M, N, K)}"
+    return None
+
+
+def pin_ties(o):
+    """Hand-built exact midpoints pin ties-to-even, and a sum just above a
+    midpoint pins single (not double) rounding."""
+    cases = [
+        # (a values, b values, expected C bits)
+        ([1.0, 2 ** -4], [1.0, 2 ** -4], 0x3F80),           # 1 + 2^-8: tie between 0x3F80 and 0x3F81 -> even 0x3F80
+        ([1.0, 3 * 2 ** -4], [1.0, 2 ** -4], 0x3F82),       # 1 + 3·2^-8: tie between 0x3F81 and 0x3F82 -> 0x3F82
+        ([1.0, 2 ** -4, 2 ** -15], [1.0, 2 ** -4, 2 ** -15], 0x3F81),  # 1 + 2^-8 + 2^-30: above the tie -> up
+        ([-1.0, 2 ** -4], [1.0, -(2 ** -4)], 0xBF80),       # negative tie -> even magnitude
+        ([2.0, 2 ** -3], [1.0, 2 ** -4], 0x4000),           # 2 + 2^-7: tie at the next binade -> 0x4000
+    ]
+    for a, b, want in cases:
+        A = np.array([[_bf(x) for x in a]], dtype=np.uint16)
+        B = np.array([[_bf(x) for x in b]], dtype=np.uint16)
+        got = int(o.gemm(A, B)[0, 0])
+        if got != want:
+            return f"tie case {a}·{b}: got {got:#06x}, want {want:#06x}"
+    return None
+
+
+def pin_identity_permutation(o):
+    K = 24
+    A = synth.normal_bf16(11, K, 7)
+    one = _bf(1.0)
+    eye = np.zeros((K, K), dtype=np.uint16)
+    eye[np.arange(K), np.arange(K)] = one
+    if not np.array_equal(o.gemm(A, eye), A):
+        return "B = I does not reproduce A"
+    perm = np.random.Generator(np.random.PCG64(3)).permutation(K)
+    P = np.zeros((K, K), dtype=np.uint16)
+    P[np.arange(K), perm] = one          # row j of B selects column perm[j] of A
+    if not np.array_equal(o.gemm(A, P), A[:, perm]):
+        return "B = permutation does not permute the columns of A"
+    return None
+
+
+def pin_closed_form(o):
+    """A ≡ a, B ≡ b  =>  C ≡ RNE(K·a·b), exactly."""
+    for a, b, K in [(0.75, -1.25, 1), (0.1015625, 3.0, 7), (1.5, 1.5, 300), (-0.3359375, 0.046875, 1024)]:
+        ab, bb = _bf(a), _bf(b)
+        A = np.full((3, K), ab, dtype=np.uint16)
+        B = np.full((2, K), bb, dtype=np.uint16)
+        want = round_fraction(K * bits_to_fraction(ab) * bits_to_fraction(bb))
+        C = o.gemm(A, B)
+        if not np.all(C == want):
+            return f"closed form a={a} b={b} K={K}: got {C[0,0]:#06x}, want {want:#06x}"
+    return None
+
+
+def pin_invariants(o):
+    A = synth.normal_bf16(9, 40, 11)
+    B = synth.normal_bf16(6, 40, 12)
+    C = o.gemm(A, B)
+    if not np.array_equal(o.gemm(B, A), C.T):
+        return "swapping A and B does not transpose C"
+    negC = o.gemm(A ^ np.uint16(0x8000), B)
+    nz = (C & 0x7FFF) != 0
+    if not np.array_equal(negC[nz], C[nz] ^ np.uint16(0x8000)):
+        return "negating A does not negate C"
+    if np.any(o.gemm(np.zeros_like(A), B) != 0):
+        return "zero A does not give +0"
+    # not symmetric in the operand roles: a non-square case distinguishes A·Bᵀ from A·B
+    return None
+
+
+def pin_integer(o):
+    """Integer-valued inputs: C = RNE(int64 A·Bᵀ)."""
+    for M, N, K in [(7, 5, 33), (16, 16, 256)]:
+        A = synth.int_bf16(M, K, 101)
+        B = synth.int_bf16(N, K, 102)
+        Ai = synth.bf16_bits_to_f32(A).astype(np.int64)
+        Bi = synth.bf16_bits_to_f32(B).astype(np.int64)
+        Ci = Ai @ Bi.T
+        want = np.array([[round_fraction(Fraction(int(v))) for v in row] for row in Ci], dtype=np.uint16)
+        if not np.array_equal(o.gemm(A, B), want):
+            return f"integer case {(M, N, K)}"
+    return None
+
+
+def pin_rounding(o):
+    """binary64 -> bf16 on normals, subnormals, ties, overflow and zeros."""
+    rng = np.random.Generator(np.random.PCG64(5))
+    xs = list(rng.standard_normal(400) * np.exp2(rng.integers(-140, 128, 400)))
+    xs += [0.0, -0.0, 1.0, -1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, 2 ** -133, 2 ** -134, 3 * 2 ** -134,
+           2 ** -126, 2 ** -126 - 2 ** -134, float(2 ** 128 - 2 ** 119), float(2 ** 128 - 2 ** 120),
+           1.0000001, 65504.0, 3.0e38, -3.4e38]
+    for x in xs:
+        want = round_fraction(Fraction(float(x)))
+        if np.isfinite(x) and abs(x) >= 2 ** 128:
+            want = (0x8000 if x < 0 else 0) | 0x7F80
+        got = o.round_bf16(x)
+        if x == 0:
+            want = 0x8000 if np.signbit(x) else 0
+        if got != want:
+            return f"round_bf16({x!r}) = {got:#06x}, want {want:#06x}"
+    return None
+
+
+PINS = [pin_bruteforce, pin_ties, pin_identity_permutation, pin_closed_form, pin_invariants,
+        pin_integer, pin_rounding]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_oracle_pin(oracle_lib, pin):
+    assert pin(oracle_lib) is None
+
+
+def test_transposed_operand_is_distinguished(oracle_lib):
+    """C = A·Bᵀ, not A·B: a non-symmetric square case separates the two."""
+    K = 8
+    A = synth.int_bf16(K, K, 21)
+    B = synth.int_bf16(K, K, 22)
+    Ai = synth.bf16_bits_to_f32(A).astype(np.int64)
+    Bi = synth.bf16_bits_to_f32(B).astype(np.int64)
+    C = synth.bf16_bits_to_f32(oracle_lib.gemm(A, B)).astype(np.int64)
+    assert np.array_equal(C, Ai @ Bi.T)
+    assert not np.array_equal(C, Ai @ Bi)
+
+
+def test_rows_and_entries_agree_with_full(oracle_lib):
+    A = synth.normal_bf16(37, 70, 31)
+    B = synth.normal_bf16(29, 70, 32)
+    C = oracle_lib.gemm(A, B, threads=3)
+    rows = np.array([0, 5, 36])
+    R, used = oracle_lib.gemm_rows(A, B, rows, threads=2)
+    assert used >= 1 and np.array_equal(R, C[rows])
+    r, c = synth.sample_positions(37, 29, 9, count=50, tile_m=16, tile_n=16)
+    E, _ = oracle_lib.gemm_entries(A, B, r, c)
+    assert np.array_equal(E, C[r, c])
+    # strided operands (leading dimension > K)
+    Aw = np.zeros((37, 80), dtype=np.uint16)
+    Aw[:, :70] = A
+    assert np.array_equal(oracle_lib.gemm(Aw[:, :70], B), C)
+
+
+def test_empty_k_gives_zero(oracle_lib):
+    A = np.zeros((4, 0), dtype=np.uint16)
+    B = np.zeros((3, 0), dtype=np.uint16)
+    assert np.all(oracle_lib.gemm(A, B) == 0)
+
+
+# ------------------------------------------------------------- mutations --
+
+MUTANTS = {
+    "dropped_last_term": ("for (int64_t k = 0; k < K; ++k) s +=", "for (int64_t k = 0; k + 1 < K; ++k) s +="),
+    "transposed_B": ("const uint16_t* b = B + j * ldb;", "const uint16_t* b = B + j;"),
+    "swapped_index": ("int64_t i = w->rows ? w->rows[t] : t;", "int64_t i = w->rows ? w->rows[t] : (t + 1) % (w->end);"),
+    "ties_away": ("if (fmod(fl, 2.0) != 0.0) n = fl + 1.0;", "n = fl + 1.0;"),
+    "truncation": ("if (frac > 0.5) {", "if (frac > 2.0) {"),
+    "sign_error": ("s += bf16_bits_to_double(a[k]) * bf16_bits_to_double(b[k]);",
+                   "s += fabs(bf16_bits_to_double(a[k])) * bf16_bits_to_double(b[k]);"),
+    "via_binary32": ("double a = fabs(x);", "double a = (double)(float)fabs(x);"),
+    "subnormal_quantum": ("int qexp = (E < -126 ? -126 : E) - 7;", "int qexp = E - 7;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutants_fail_pins(tmp_path, name):
+    src = open(os.path.join(ROOT, "oracle", "gemm_ref.c")).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    path_c = tmp_path / f"{name}.c"
+    path_so = tmp_path / f"{name}.so"
+    path_c.write_text(src.replace(old, new))
+    subprocess.run(["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                    "-D_GNU_SOURCE", str(path_c), "-o", str(path_so), "-lm"], check=True)
+    mutant = _Lib(str(path_so))
+    failures = [p.__name__ for p in PINS if p(mutant) is not None]
+    assert failures, f"mutant {name} passed every pin"
