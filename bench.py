@@ -1,0 +1,389 @@
+"""Benchmark of the GB300 BF16 GEMM (C = A·Bᵀ, bf16 in, fp32 accumulate, bf16 out).
+
+One step = one GEMM of the workload (default: the 8192³ headline shape of the
+HipKittens "L2" detail page, §2 Q3 and §5 Tab. 2) through the C-ABI
+``hk_gemm_bf16``. Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hk|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+With N > 1 (launched by torchrun) every rank runs an independent replica of
+the workload on its own GPU (the GEMM has no exchange step); the reported
+value is the sum of all ranks' work over the slowest rank's time.
+
+``--impl reference`` times the CPU oracle (the only reference this method has)
+on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "BF16 GEMM TFLOPS at 1 GB300 and % of dense-BF16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+# DRAM traffic of one launch of the GEMM kernel from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
+# sources whose digest is given; see profiles/.
+MEASURED_TRAFFIC = {}
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_bf16_gemm_02_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def gemm_flops(M: int, N: int, K: int) -> float:
+    """Algorithmic flops of one GEMM: one multiply and one add per (i, j, k)."""
+    return 2.0 * M * N * K
+
+
+def gemm_bytes(M: int, N: int, K: int) -> float:
+    """Algorithmic bytes: read A and B once, write C once, bf16."""
+    return 2.0 * (M * K + N * K + M * N)
+
+
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        if "bf16_tflops" in peaks:
+            return peaks, "measured"
+    except (OSError, ValueError):
+        pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in a side process;
+    each line is stamped with the host time it arrived."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not inside:
+            # timed region shorter than the sampling interval: nearest samples
+            inside = [s for t, s in self.samples if t0 - 0.5 <= t <= t1 + 0.5]
+            window = "timed±0.5s"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(s[0]) for s in inside if num(s[0]) is not None]
+        smax = [num(s[1]) for s in inside if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in inside for n, v in zip(names, s[4:8]) if v.lower() == "active"})
+        power = [num(s[2]) for s in inside if num(s[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inside), "window": window,
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------- distributed --
+
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, x: float) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------- CPU oracle --
+
+def oracle_rows_timed(A, B, rows) -> tuple[float, int]:
+    import oracle
+    t0 = time.perf_counter()
+    _, used = oracle.gemm_rows(A, B, rows)
+    return time.perf_counter() - t0, used
+
+
+def cpu_baseline(w, A, B, budget_s: float = 12.0) -> dict:
+    """The oracle, as it stands, on full rows of this workload's C."""
+    probe = np.arange(min(4, w.M), dtype=np.int64)
+    t, _ = oracle_rows_timed(A, B, probe)
+    per_row = max(t / len(probe), 1e-6)
+    nrows = int(max(1, min(w.M, budget_s / per_row)))
+    rows = np.arange(nrows, dtype=np.int64)
+    t, used = oracle_rows_timed(A, B, rows)
+    tflops = gemm_flops(nrows, w.N, w.K) / t / 1e12
+    return {"value": tflops, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"rows 0..{nrows - 1} of C ({nrows}x{w.N}x{w.K}, fp64 C oracle, {t:.1f} s)"}
+
+
+def run_reference(args, w):
+    """Reference arm: the CPU oracle on a bounded sample per step."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    A, B = synth.operands(w)
+    probe = np.arange(min(4, w.M), dtype=np.int64)
+    t, _ = oracle_rows_timed(A, B, probe)
+    per_row = max(t / len(probe), 1e-6)
+    rows_per_step = int(max(1, min(64, 120.0 / (args.steps + args.warmup) / per_row)))
+    rows = np.arange(rows_per_step, dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle_rows_timed(A, B, rows)
+    total = 0.0
+    used = 0
+    for _ in range(args.steps):
+        dt, used = oracle_rows_timed(A, B, rows)
+        total += dt
+    value = gemm_flops(rows_per_step, w.N, w.K) * args.steps / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": f"{rows_per_step} full rows of C per step ({rows_per_step}x{w.N}x{w.K})"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w) -> dict:
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+            "layout": "A MxK row-major, B NxK row-major, C MxN row-major (C = A·Bᵀ)",
+            "values": f"N(0,1)·{w.scale} rounded to bf16, seeds {1000 + w.wid}/{2000 + w.wid}",
+            "l2": "no flush: inputs larger than L2 (A+B = %d MiB > 126 MiB)" % ((w.M + w.N) * w.K * 2 >> 20)
+            if (w.M + w.N) * w.K * 2 > 126 << 20 else "inputs smaller than L2 (warm L2)",
+            "accumulate": "fp32", "output": "bf16"}
+
+
+# ---------------------------------------------------------------- GPU arm --
+
+def run_hk(args, w):
+    import torch
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import dense_bf16_gemm_02_gb300 as hk
+
+    A_bits, B_bits = synth.operands(w)
+    A = torch.from_numpy(A_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    B = torch.from_numpy(B_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = int(stream.cuda_stream)
+    plan = hk.Plan(w.M, w.N, w.K, device=local)
+    info = plan.info()
+    flops = gemm_flops(w.M, w.N, w.K)
+
+    def step():
+        st = hk.hk_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, w.K, w.K, w.N, sh)
+        if st != hk.HK_OK:
+            raise hk.HKError(st, "hk_gemm_bf16")
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    if hk.hk_gemm_last_device_status(local) != hk.HK_OK:
+        raise RuntimeError("device status after warm-up: " + hk.hk_gemm_last_error_string())
+
+    # ---- device-resident timed region: K launches, one event between each
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    with torch.cuda.stream(stream):
+        events[0].record(stream)
+        for i in range(args.steps):
+            step()
+            events[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    barrier(world)
+    elapsed_ms = events[0].elapsed_time(events[-1])
+    per_launch = [events[i].elapsed_time(events[i + 1]) for i in range(args.steps)]
+    if hk.hk_gemm_last_device_status(local) != hk.HK_OK:
+        raise RuntimeError("device status after timing: " + hk.hk_gemm_last_error_string())
+    clocks = None
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+        clocks = sampler.summary(t_host0, t_host1)
+    elapsed_max = max_over_ranks(world, elapsed_ms)
+
+    # ---- end to end: pinned host inputs -> device -> GEMM -> host result
+    A_h = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    B_h = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    C_h = torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        A.copy_(A_h, non_blocking=True)
+        B.copy_(B_h, non_blocking=True)
+        step()
+        C_h.copy_(C, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
+    if not np.array_equal(C_h.view(torch.int16).numpy()[0, :16].view(np.uint16),
+                          C.view(torch.int16).cpu().numpy()[0, :16].view(np.uint16)):
+        raise RuntimeError("end-to-end result differs from the device result")
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peaks_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    value = flops * args.steps * world / (elapsed_max / 1e3) / 1e12
+    mean_launch_ms = statistics.mean(per_launch)
+    achieved = flops / (mean_launch_ms / 1e3) / 1e12
+    digest = kernel_source_digest()
+    traffic = None
+    tr = MEASURED_TRAFFIC.get(w.name)
+    if tr and tr.get("source_digest") == digest:
+        traffic = tr["bytes_per_launch"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_config(w), parallelism="replicas" if world > 1 else "single GPU",
+                       tile=f"{info['tile_m']}x{info['tile_n']}x{info['tile_k']} per CTA pair",
+                       stages=info["stages"], grid_ctas=info["grid_ctas"], group_m=info["group_m"]),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"bf16_tflops (burst) of {peaks_src}",
+                     "algorithmic_flops_per_launch": flops,
+                     "algorithmic_bytes_per_launch": gemm_bytes(w.M, w.N, w.K),
+                     "mean_launch_ms": mean_launch_ms, "p10_launch_ms": float(np.percentile(per_launch, 10)),
+                     "p90_launch_ms": float(np.percentile(per_launch, 90)), "kernel": "gemm_bf16_pair_kernel",
+                     "source_digest": digest},
+        "e2e": {"value": flops * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": int(A_h.numel() * 2 + B_h.numel() * 2),
+                "d2h_bytes_per_step": int(C_h.numel() * 2), "steps": e2e_steps},
+        "gpu_launches": args.steps * int(info["kernels_per_run"]),
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, A_bits, B_bits)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["hk", "reference"], default="hk")
+    ap.add_argument("--workload", default="gemm_8192", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_hk(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

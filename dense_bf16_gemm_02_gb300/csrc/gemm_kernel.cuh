@@ -1,0 +1,356 @@
+// Persistent, warp-specialised BF16 GEMM  C = A · Bᵀ  for sm_103a.
+//
+// The operation and its 256×256 output tile with a 64-wide K step follow the
+// HipKittens "L2" detail page (§3 "Target operation" and "Launch config";
+// §9.2 GEMM hot loop). Everything else is a Blackwell design rather than the
+// pages' AMD one:
+//
+//  * a cluster of two CTAs (a "pair") owns one 256×256 output tile at a
+//    time; each CTA loads 128 rows of A and 128 rows of B per K step with a
+//    TMA bulk-tensor copy (128-byte swizzle) into a STAGES-deep shared-memory
+//    ring guarded by full/empty mbarriers (the pages' 2-deep LDS double
+//    buffer, §4 "Design space": pipeline depth);
+//  * one thread of the pair's leader CTA issues tcgen05.mma.cta_group::2
+//    (M=256, N=256, K=16) that reads both CTAs' shared memory and
+//    accumulates in fp32 in Tensor Memory, two 256-column accumulators per
+//    CTA so the epilogue of tile i overlaps the main loop of tile i+1;
+//  * roles are warp-specialised (warp 0: TMA producer, warp 1: TMEM
+//    allocation and MMA issue, warps 2-5: epilogue) — on Blackwell a
+//    producer warp costs the MMA no registers, unlike the static register
+//    split that makes the pages reject producer waves (§5 Tab. 2);
+//  * the grid is persistent (one pair per two SMs) and walks output tiles in
+//    grouped order (GROUP_M tile rows at a time), the counterpart of the
+//    pages' cache-aware block remapping (§2 Q2 Pillar 3, §5 Tab. 4);
+//  * the epilogue reads TMEM with tcgen05.ld, rounds to bf16 (RNE), stages
+//    32×32 sub-tiles in shared memory and writes them with TMA stores.
+//
+// Every mbarrier wait is bounded: when one runs out the kernel records an
+// error code in a device status word, every role drains, TMEM is freed and
+// the kernel returns normally.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace hk {
+
+constexpr int kPairM = 256;          // rows of C per pair tile
+constexpr int kCtaM = 128;           // rows of C (and of A) per CTA
+constexpr int kTileN = 256;          // columns of C per pair tile (MMA N)
+constexpr int kCtaN = 128;           // rows of B loaded per CTA
+constexpr int kTileK = 64;           // K per pipeline stage (one 128-byte swizzle row)
+constexpr int kMmaK = 16;            // K per tcgen05.mma
+constexpr int kStages = 6;           // shared-memory ring depth
+constexpr int kAStageBytes = kCtaM * kTileK * 2;   // 16 KiB
+constexpr int kBStageBytes = kCtaN * kTileK * 2;   // 16 KiB
+constexpr int kEpiCols = 32;                        // columns per epilogue store
+constexpr int kEpiWarps = 4;
+constexpr int kEpiBufBytes = 32 * kEpiCols * 2;     // 32 rows × 64 B
+constexpr int kThreads = 64 + 32 * kEpiWarps;       // 192
+constexpr int kAccCols = kTileN;                    // TMEM columns per accumulator
+constexpr int kTmemCols = 2 * kAccCols;             // two accumulators = all 512 columns
+
+// shared-memory layout, offsets from a 1024-byte aligned base
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kAStageBytes;
+constexpr int kOffEpi = kOffB + kStages * kBStageBytes;
+constexpr int kOffBars = kOffEpi + kEpiWarps * 2 * kEpiBufBytes;
+constexpr int kNumBars = 2 * kStages + 4;   // full[S], empty[S], acc_full[2], acc_empty[2]
+constexpr int kOffTmemHolder = kOffBars + kNumBars * 8;
+constexpr int kSmemUsed = kOffTmemHolder + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024;   // slack for aligning the base
+
+// error bits written to the status word when a bounded wait runs out
+constexpr uint32_t kErrProducerEmpty = 1u << 0;
+constexpr uint32_t kErrMmaFull = 1u << 1;
+constexpr uint32_t kErrMmaAccEmpty = 1u << 2;
+constexpr uint32_t kErrEpiAccFull = 1u << 3;
+
+constexpr uint32_t kFlagDropArrive = 0x1u;
+
+struct GemmParams {
+    int32_t M, N, K;
+    int32_t tiles_m, tiles_n;     // pair tiles along M and N
+    int32_t k_blocks;             // ceil(K / 64)
+    int32_t num_tiles;
+    int32_t group_m;
+    int32_t n_tma;                // columns [0, n_tma) of C are written by TMA stores (n_tma = N & ~7)
+    int64_t ldc;                  // leading dimension of C (elements), for the ragged tail columns
+    uint16_t* c_ptr;              // C, for the columns [n_tma, N) a TMA store cannot bound exactly
+    uint32_t* status;             // [0]: error bits (sticky), [1]: launch id that aborted
+    uint32_t launch_id;
+    uint32_t flags;
+    uint64_t timeout_ns;
+};
+
+// Grouped rasterisation: tiles are numbered so that group_m consecutive tile
+// rows are swept column by column; the tiles that co-run on the GPU then
+// share a few rows of A and a few columns of B in L2.
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& tm, int& tn) {
+    const int per_group = p.group_m * p.tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * p.group_m;
+    const int rows = min(p.tiles_m - first_m, p.group_m);
+    const int local = t - g * per_group;
+    tm = first_m + local % rows;
+    tn = local / rows;
+}
+
+__device__ __forceinline__ bool aborted(const GemmParams& p) {
+    return *reinterpret_cast<volatile uint32_t*>(p.status + 1) == p.launch_id;
+}
+
+// Bounded wait for phase `parity` of `bar`. Returns false when the wait gave
+// up: either this launch was already aborted by another role, or the time
+// limit ran out (then this thread records `code` and aborts the launch).
+__device__ __noinline__ bool wait_bounded(const GemmParams& p, uint32_t bar, uint32_t parity,
+                                          uint32_t code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (aborted(p)) return false;
+            if (global_timer_ns() - t0 > p.timeout_ns) {
+                atomicOr(p.status, code);
+                atomicExch(p.status + 1, p.launch_id);
+                __threadfence();
+                return false;
+            }
+        }
+    }
+}
+
+// Warp-uniform variant: lane 0 waits, the verdict is broadcast, and every
+// lane then observes the completed phase itself (acquire per thread).
+__device__ __forceinline__ bool wait_bounded_warp(const GemmParams& p, uint32_t bar, uint32_t parity,
+                                                  uint32_t code) {
+    uint32_t ok = 0;
+    if (lane_id() == 0) ok = wait_bounded(p, bar, parity, code) ? 1u : 0u;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) (void)mbar_try_wait(bar, parity);
+    __syncwarp();
+    return ok != 0;
+}
+
+__device__ __forceinline__ void drain_after_abort() {
+    // let copies and MMAs that were already issued land before teardown
+    for (int i = 0; i < 200; ++i) __nanosleep(1000);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                      const __grid_constant__ CUtensorMap tmap_b,
+                      const __grid_constant__ CUtensorMap tmap_c, const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const smem = smem_raw + (base - raw);
+
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = lane_id();
+    const uint32_t rank = cluster_cta_rank();          // 0 = leader of the pair
+    const int pair = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
+
+    auto full_bar = [&](int s) { return base + kOffBars + 8u * s; };
+    auto empty_bar = [&](int s) { return base + kOffBars + 8u * (kStages + s); };
+    auto acc_full_bar = [&](int b) { return base + kOffBars + 8u * (2 * kStages + b); };
+    auto acc_empty_bar = [&](int b) { return base + kOffBars + 8u * (2 * kStages + 2 + b); };
+    const uint32_t tmem_holder = base + kOffTmemHolder;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full_bar(b), 1);
+            mbar_init(acc_empty_bar(b), 2 * kEpiWarps);
+        }
+        fence_mbar_init_cluster();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensor_map(&tmap_a);
+        prefetch_tensor_map(&tmap_b);
+        prefetch_tensor_map(&tmap_c);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_holder, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    cluster_sync();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemHolder);
+
+    bool abort_seen = false;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool dropped = false;
+            for (int t = pair; t < p.num_tiles && !abort_seen; t += num_pairs) {
+                int tm, tn;
+                tile_coords(p, t, tm, tn);
+                const int a_row = tm * kPairM + static_cast<int>(rank) * kCtaM;
+                const int b_row = tn * kTileN + static_cast<int>(rank) * kCtaN;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_bounded(p, empty_bar(stage), phase ^ 1u, kErrProducerEmpty)) {
+                        abort_seen = true;
+                        break;
+                    }
+                    const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
+                    if (rank == 0) {
+                        if ((p.flags & kFlagDropArrive) && !dropped) {
+                            dropped = true;   // test-only fault: withhold this arrival
+                        } else {
+                            mbar_arrive_expect_tx(full_bar(stage), 2u * (kAStageBytes + kBStageBytes));
+                        }
+                    }
+                    tma_load_2d_pair(base + kOffA + stage * kAStageBytes, &tmap_a, kb * kTileK, a_row,
+                                     leader_full);
+                    tma_load_2d_pair(base + kOffB + stage * kBStageBytes, &tmap_b, kb * kTileK, b_row,
+                                     leader_full);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer --
+        if (rank == 0 && lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kPairM, kTileN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            for (int t = pair; t < p.num_tiles && !abort_seen; t += num_pairs, ++local) {
+                const int buf = local & 1;
+                const uint32_t acc_phase = (local >> 1) & 1;
+                if (!wait_bounded(p, acc_empty_bar(buf), acc_phase ^ 1u, kErrMmaAccEmpty)) {
+                    abort_seen = true;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + buf * kAccCols;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!wait_bounded(p, full_bar(stage), phase, kErrMmaFull)) {
+                        abort_seen = true;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t a_desc = smem_desc_kmajor_sw128(base + kOffA + stage * kAStageBytes);
+                    const uint64_t b_desc = smem_desc_kmajor_sw128(base + kOffB + stage * kBStageBytes);
+#pragma unroll
+                    for (int k = 0; k < kTileK / kMmaK; ++k) {
+                        // advance 16 bf16 = 32 bytes along K inside the swizzle atom
+                        mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
+                                      (kb | k) != 0 ? 1u : 0u);
+                    }
+                    // free this stage in both CTAs once the MMAs above have read it
+                    mma_commit_pair(empty_bar(stage));
+                    mma_commit_pair(map_to_cta(empty_bar(stage), 1));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (abort_seen) break;
+                // accumulator complete: hand it to both CTAs' epilogues
+                mma_commit_pair(acc_full_bar(buf));
+                mma_commit_pair(map_to_cta(acc_full_bar(buf), 1));
+            }
+        }
+    } else {
+        // --------------------------------------------------- epilogue --
+        const uint32_t q = warp & 3u;                  // TMEM lane quarter this warp may read
+        const uint32_t epi = base + kOffEpi + (warp - 2) * 2 * kEpiBufBytes;
+        const uint32_t swz = (lane >> 1) & 3u;         // 64-byte swizzle of this lane's row
+        uint32_t chunk_count = 0;
+        int local = 0;
+        for (int t = pair; t < p.num_tiles; t += num_pairs, ++local) {
+            int tm, tn;
+            tile_coords(p, t, tm, tn);
+            const int buf = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            if (!wait_bounded_warp(p, acc_full_bar(buf), acc_phase, kErrEpiAccFull)) {
+                abort_seen = true;
+                break;
+            }
+            tc_fence_after_sync();
+            const int row0 = tm * kPairM + static_cast<int>(rank) * kCtaM + static_cast<int>(q) * 32;
+            const uint32_t t_row = tmem_base + ((q * 32u) << 16) + buf * kAccCols;
+#pragma unroll 1
+            for (int c = 0; c < kTileN / kEpiCols; ++c) {
+                uint32_t v[32];
+                if (p.k_blocks > 0) {
+                    tmem_load_32cols(t_row + c * kEpiCols, v);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0u;
+                }
+                if (c == kTileN / kEpiCols - 1) {
+                    // every TMEM read of this accumulator is done: release it to the MMA
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(map_to_cta(acc_empty_bar(buf), 0));
+                }
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2_rn(v[2 * i], v[2 * i + 1]);
+
+                const uint32_t sbuf = epi + (chunk_count & 1u) * kEpiBufBytes;
+                if (lane == 0) bulk_wait_group_read<1>();   // the store that last used sbuf has read it
+                __syncwarp();
+                const uint32_t row_addr = sbuf + lane * 64u;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ swz) << 4), w[4 * j], w[4 * j + 1],
+                                 w[4 * j + 2], w[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int col0 = tn * kTileN + c * kEpiCols;
+                if (lane == 0 && row0 < p.M && col0 < p.n_tma) {
+                    tma_store_2d(&tmap_c, sbuf, col0, row0);
+                }
+                if (lane == 0) bulk_commit_group();
+                // A TMA store bounds the innermost dimension only to 16-byte
+                // granules, so when N is not a multiple of 8 the last (< 8)
+                // columns are written with plain stores from the registers.
+                if (p.N > p.n_tma && col0 + kEpiCols > p.n_tma && col0 < p.N) {
+                    const int row = row0 + static_cast<int>(lane);
+                    if (row < p.M) {
+                        uint16_t* const crow = p.c_ptr + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll
+                        for (int e = 0; e < kEpiCols; ++e) {   // static indices keep w[] in registers
+                            const int j = col0 + e;
+                            if (j >= p.n_tma && j < p.N)
+                                crow[j] = static_cast<uint16_t>((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
+                        }
+                    }
+                }
+                ++chunk_count;
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    if (abort_seen || aborted(p)) drain_after_abort();
+    __syncwarp();
+    tc_fence_before_sync();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace hk

@@ -1,0 +1,428 @@
+// Host side of the C-ABI declared in include/hk_gemm.h: argument checks,
+// plans, TMA tensor-map encoding, the device status word and the cluster
+// launch of the persistent GEMM kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+
+#include "../../include/hk_gemm.h"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+hk_status fail(hk_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+hk_status fail(hk_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+hk_status cuda_fail(hk_status s, const char* what, cudaError_t e) {
+    return fail(s, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s per bounded wait
+constexpr int kDefaultGroupM = 8;
+
+// ----------------------------------------------------------- device info --
+
+struct DeviceInfo {
+    bool probed = false;
+    bool supported = false;
+    int sm_count = 0;
+    int max_pairs = 0;             // co-resident 2-CTA clusters of the GEMM kernel
+    std::string why;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+hk_status device_info(int device, const DeviceInfo** out) {
+    if (device < 0 || device >= kMaxDevices) return fail(HK_ERR_INVALID_ARG, "device %d out of range", device);
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo& d = g_dev[device];
+    if (!d.probed) {
+        int major = 0, minor = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device);
+        if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "querying the device", e);
+        d.probed = true;
+        if (major != 10 || minor != 3) {
+            d.supported = false;
+            d.why = "compute capability " + std::to_string(major) + "." + std::to_string(minor) +
+                    " (this library is built for 10.3, sm_103a)";
+        } else {
+            int prev = -1;
+            cudaGetDevice(&prev);
+            if (prev != device) cudaSetDevice(device);
+            e = cudaFuncSetAttribute(hk::gemm_bf16_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     hk::kSmemBytes);
+            int clusters = 0;
+            if (e == cudaSuccess) {
+                cudaLaunchConfig_t cfg = {};
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 2;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.gridDim = dim3(2 * d.sm_count, 1, 1);
+                cfg.blockDim = dim3(hk::kThreads, 1, 1);
+                cfg.dynamicSmemBytes = hk::kSmemBytes;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                e = cudaOccupancyMaxActiveClusters(&clusters, hk::gemm_bf16_pair_kernel, &cfg);
+            }
+            if (prev >= 0 && prev != device) cudaSetDevice(prev);
+            if (e != cudaSuccess) {
+                d.probed = false;
+                return cuda_fail(HK_ERR_CUDA, "configuring the GEMM kernel", e);
+            }
+            d.supported = clusters > 0;
+            d.max_pairs = clusters;
+            if (!d.supported) d.why = "no 2-CTA cluster of the GEMM kernel fits on the device";
+        }
+    }
+    if (!d.supported) return fail(HK_ERR_UNSUPPORTED_DEVICE, "device %d: %s", device, d.why.c_str());
+    *out = &d;
+    return HK_OK;
+}
+
+hk_status get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!g_encode) return fail(HK_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    return HK_OK;
+}
+
+// 2-D bf16 tensor map over a row-major (rows × cols, leading dimension ld)
+// matrix with box (box_cols × box_rows).
+hk_status encode_2d(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+                    uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle, const char* name) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t elem_strides[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                          elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(HK_ERR_INVALID_ARG, "encoding the tensor map of %s failed (CUresult %d)", name, (int)r);
+    return HK_OK;
+}
+
+// Per-device context of the one-shot entry point: its status word.
+struct StatusWord {
+    uint32_t* dev = nullptr;                 // [0] error bits, [1] aborted launch id
+    std::atomic<uint32_t> next_launch{1};
+};
+
+std::mutex g_ctx_mutex;
+StatusWord* g_ctx[kMaxDevices] = {};
+
+hk_status alloc_status(StatusWord* w) {
+    cudaError_t e = cudaMalloc(&w->dev, 4 * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaMemset(w->dev, 0, 4 * sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "allocating the device status word", e);
+    return HK_OK;
+}
+
+hk_status read_status(StatusWord* w, int device) {
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (prev != device) cudaSetDevice(device);
+    uint32_t h[2] = {0, 0};
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(h, w->dev, sizeof h, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && h[0] != 0) e = cudaMemset(w->dev, 0, sizeof(uint32_t));
+    if (prev >= 0 && prev != device) cudaSetDevice(prev);
+    if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "reading the device status word", e);
+    if (h[0] != 0)
+        return fail(HK_ERR_TIMEOUT, "a bounded wait in the GEMM kernel ran out (error bits 0x%x)", h[0]);
+    return HK_OK;
+}
+
+// ------------------------------------------------------------ validation --
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+hk_status check_shape(int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc) {
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (M < 0 || N < 0 || K < 0) return fail(HK_ERR_INVALID_ARG, "negative size (M=%lld N=%lld K=%lld)", (long long)M, (long long)N, (long long)K);
+    if (M > lim || N > lim || K > lim) return fail(HK_ERR_INVALID_ARG, "size above 2^31-1");
+    if (lda < (K > 0 ? K : 1) || ldb < (K > 0 ? K : 1) || ldc < (N > 0 ? N : 1))
+        return fail(HK_ERR_INVALID_ARG, "leading dimension too small (lda=%lld ldb=%lld ldc=%lld)", (long long)lda,
+                    (long long)ldb, (long long)ldc);
+    if (lda > lim || ldb > lim || ldc > lim) return fail(HK_ERR_INVALID_ARG, "leading dimension above 2^31-1");
+    if ((lda % 8) || (ldb % 8) || (ldc % 8))
+        return fail(HK_ERR_MISALIGNED, "leading dimensions must be multiples of 8 elements (lda=%lld ldb=%lld ldc=%lld)",
+                    (long long)lda, (long long)ldb, (long long)ldc);
+    return HK_OK;
+}
+
+hk_status check_pointers(const void* A, const void* B, const void* C, int64_t K) {
+    if (!C || (K > 0 && (!A || !B))) return fail(HK_ERR_INVALID_ARG, "null operand pointer");
+    if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B))))
+        return fail(HK_ERR_MISALIGNED, "operand pointers must be 16-byte aligned");
+    return HK_OK;
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int device) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != device) cudaSetDevice(device);
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+// ------------------------------------------------------------------ plans --
+
+struct hk_gemm_plan {
+    int64_t M, N, K, lda, ldb, ldc;
+    int device;
+    hk::GemmParams params;      // everything but status/launch id
+    int grid_ctas;
+    hk_gemm_config cfg;
+    StatusWord status;
+    bool owns_status;
+};
+
+namespace {
+
+hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                    int device, const hk_gemm_config* config, const DeviceInfo* di) {
+    p->M = M; p->N = N; p->K = K; p->lda = lda; p->ldb = ldb; p->ldc = ldc;
+    p->device = device;
+    std::memset(&p->cfg, 0, sizeof p->cfg);
+    if (config) p->cfg = *config;
+    if (p->cfg.split_k > 1) return fail(HK_ERR_INVALID_ARG, "split_k > 1 is not available for this shape");
+    if (p->cfg.group_m < 0 || p->cfg.max_clusters < 0) return fail(HK_ERR_INVALID_ARG, "negative config field");
+    const int group_m = p->cfg.group_m > 0 ? p->cfg.group_m : kDefaultGroupM;
+    hk::GemmParams& g = p->params;
+    std::memset(&g, 0, sizeof g);
+    g.M = static_cast<int32_t>(M);
+    g.N = static_cast<int32_t>(N);
+    g.K = static_cast<int32_t>(K);
+    g.tiles_m = static_cast<int32_t>((M + hk::kPairM - 1) / hk::kPairM);
+    g.tiles_n = static_cast<int32_t>((N + hk::kTileN - 1) / hk::kTileN);
+    g.k_blocks = static_cast<int32_t>((K + hk::kTileK - 1) / hk::kTileK);
+    const int64_t tiles = int64_t(g.tiles_m) * g.tiles_n;
+    if (tiles > (int64_t(1) << 30)) return fail(HK_ERR_INVALID_ARG, "too many output tiles");
+    g.num_tiles = static_cast<int32_t>(tiles);
+    g.group_m = group_m;
+    g.n_tma = static_cast<int32_t>(N & ~int64_t(7));
+    g.ldc = ldc;
+    g.flags = p->cfg.flags;
+    g.timeout_ns = p->cfg.timeout_ns ? p->cfg.timeout_ns : kDefaultTimeoutNs;
+    int pairs = di->max_pairs;
+    if (p->cfg.max_clusters > 0 && p->cfg.max_clusters < pairs) pairs = p->cfg.max_clusters;
+    if (pairs > g.num_tiles) pairs = g.num_tiles;
+    p->grid_ctas = 2 * pairs;
+    return HK_OK;
+}
+
+hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const void* B, void* C, cudaStream_t stream) {
+    if (p->M == 0 || p->N == 0) return HK_OK;
+    hk_status s = get_encoder();
+    if (s != HK_OK) return s;
+    CUtensorMap ta, tb, tc;
+    // A with K == 0 is never read; give the map a valid 1-column shape over C's memory
+    const void* a_ptr = p->K > 0 ? A : C;
+    const void* b_ptr = p->K > 0 ? B : C;
+    const int64_t kk = p->K > 0 ? p->K : 8;
+    const int64_t lda = p->K > 0 ? p->lda : p->ldc;
+    const int64_t ldb = p->K > 0 ? p->ldb : p->ldc;
+    if ((s = encode_2d(&ta, a_ptr, p->K > 0 ? p->M : 1, kk, lda, hk::kTileK, hk::kCtaM, CU_TENSOR_MAP_SWIZZLE_128B, "A")) != HK_OK) return s;
+    if ((s = encode_2d(&tb, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, hk::kTileK, hk::kCtaN, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != HK_OK) return s;
+    // the map covers N rounded down to a multiple of 8 (see the epilogue); at
+    // least 8 columns so that it stays valid when N < 8 (then it is unused)
+    const int64_t n_tma = p->N & ~int64_t(7);
+    if ((s = encode_2d(&tc, C, p->M, n_tma > 0 ? n_tma : 8, p->ldc, hk::kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B, "C")) != HK_OK) return s;
+
+    hk::GemmParams g = p->params;
+    g.c_ptr = static_cast<uint16_t*>(C);
+    g.status = sw->dev;
+    g.launch_id = sw->next_launch.fetch_add(1, std::memory_order_relaxed);
+    if (g.launch_id == 0) g.launch_id = sw->next_launch.fetch_add(1, std::memory_order_relaxed);
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(p->grid_ctas, 1, 1);
+    cfg.blockDim = dim3(hk::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = hk::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, hk::gemm_bf16_pair_kernel, ta, tb, tc, g);
+    if (e != cudaSuccess) return cuda_fail(HK_ERR_LAUNCH, "launching the GEMM kernel", e);
+    return HK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* hk_status_string(hk_status s) {
+    switch (s) {
+        case HK_OK: return "HK_OK";
+        case HK_ERR_INVALID_ARG: return "HK_ERR_INVALID_ARG: invalid size, leading dimension or pointer";
+        case HK_ERR_MISALIGNED: return "HK_ERR_MISALIGNED: pointer not 16-byte aligned or leading dimension not a multiple of 8";
+        case HK_ERR_UNSUPPORTED_DEVICE: return "HK_ERR_UNSUPPORTED_DEVICE: not a compute capability 10.3 GPU";
+        case HK_ERR_LAUNCH: return "HK_ERR_LAUNCH: kernel launch failed";
+        case HK_ERR_TIMEOUT: return "HK_ERR_TIMEOUT: a bounded wait in the kernel ran out";
+        case HK_ERR_WORKSPACE: return "HK_ERR_WORKSPACE: workspace missing, too small or misaligned";
+        case HK_ERR_CUDA: return "HK_ERR_CUDA: CUDA runtime error";
+    }
+    return "unknown hk_status";
+}
+
+const char* hk_gemm_last_error_string(void) { return g_last_error.c_str(); }
+
+hk_status hk_gemm_plan_create(hk_gemm_plan** out, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                              int64_t ldc, int device, const hk_gemm_config* config) {
+    if (!out) return fail(HK_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    hk_status s = check_shape(M, N, K, lda, ldb, ldc);
+    if (s != HK_OK) return s;
+    const DeviceInfo* di = nullptr;
+    if ((s = device_info(device, &di)) != HK_OK) return s;
+    hk_gemm_plan* p = new (std::nothrow) hk_gemm_plan();
+    if (!p) return fail(HK_ERR_INVALID_ARG, "out of host memory");
+    if ((s = fill_plan(p, M, N, K, lda, ldb, ldc, device, config, di)) != HK_OK) {
+        delete p;
+        return s;
+    }
+    {
+        DeviceGuard guard(device);
+        if ((s = alloc_status(&p->status)) != HK_OK) {
+            delete p;
+            return s;
+        }
+    }
+    p->owns_status = true;
+    *out = p;
+    return HK_OK;
+}
+
+size_t hk_gemm_plan_workspace_size(const hk_gemm_plan* plan) {
+    (void)plan;
+    return 0;
+}
+
+hk_status hk_gemm_plan_get_info(const hk_gemm_plan* p, hk_gemm_plan_info* info) {
+    if (!p || !info) return fail(HK_ERR_INVALID_ARG, "NULL plan or info");
+    std::memset(info, 0, sizeof *info);
+    info->M = p->M; info->N = p->N; info->K = p->K;
+    info->tile_m = hk::kPairM; info->tile_n = hk::kTileN; info->tile_k = hk::kTileK;
+    info->stages = hk::kStages;
+    info->num_tiles = p->params.num_tiles;
+    info->grid_ctas = (p->M == 0 || p->N == 0) ? 0 : p->grid_ctas;
+    info->group_m = p->params.group_m;
+    info->split_k = 1;
+    info->kernels_per_run = (p->M == 0 || p->N == 0) ? 0 : 1;
+    info->smem_bytes = hk::kSmemBytes;
+    info->workspace_bytes = 0;
+    return HK_OK;
+}
+
+hk_status hk_gemm_plan_run(const hk_gemm_plan* p, const void* A, const void* B, void* C, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    (void)workspace; (void)workspace_bytes;
+    if (!p) return fail(HK_ERR_INVALID_ARG, "NULL plan");
+    if (p->M == 0 || p->N == 0) return HK_OK;
+    hk_status s = check_pointers(A, B, C, p->K);
+    if (s != HK_OK) return s;
+    DeviceGuard guard(p->device);
+    return launch(p, const_cast<StatusWord*>(&p->status), A, B, C, static_cast<cudaStream_t>(stream));
+}
+
+hk_status hk_gemm_plan_device_status(hk_gemm_plan* p) {
+    if (!p) return fail(HK_ERR_INVALID_ARG, "NULL plan");
+    return read_status(&p->status, p->device);
+}
+
+void hk_gemm_plan_destroy(hk_gemm_plan* p) {
+    if (!p) return;
+    if (p->owns_status && p->status.dev) {
+        DeviceGuard guard(p->device);
+        cudaFree(p->status.dev);
+    }
+    delete p;
+}
+
+hk_status hk_gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                       int64_t ldb, int64_t ldc, void* stream) {
+    hk_status s = check_shape(M, N, K, lda, ldb, ldc);
+    if (s != HK_OK) return s;
+    if (M == 0 || N == 0) return HK_OK;
+    if ((s = check_pointers(A, B, C, K)) != HK_OK) return s;
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "cudaGetDevice", e);
+    const DeviceInfo* di = nullptr;
+    if ((s = device_info(device, &di)) != HK_OK) return s;
+    StatusWord* sw = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_ctx_mutex);
+        if (!g_ctx[device]) {
+            StatusWord* w = new (std::nothrow) StatusWord();
+            if (!w) return fail(HK_ERR_INVALID_ARG, "out of host memory");
+            if ((s = alloc_status(w)) != HK_OK) {
+                delete w;
+                return s;
+            }
+            g_ctx[device] = w;
+        }
+        sw = g_ctx[device];
+    }
+    hk_gemm_plan plan;
+    if ((s = fill_plan(&plan, M, N, K, lda, ldb, ldc, device, nullptr, di)) != HK_OK) return s;
+    plan.owns_status = false;
+    return launch(&plan, sw, A, B, C, static_cast<cudaStream_t>(stream));
+}
+
+hk_status hk_gemm_last_device_status(int device) {
+    if (device < 0 || device >= kMaxDevices) return fail(HK_ERR_INVALID_ARG, "device %d out of range", device);
+    StatusWord* sw = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_ctx_mutex);
+        sw = g_ctx[device];
+    }
+    if (!sw) return HK_OK;
+    return read_status(sw, device);
+}
+
+}  // extern "C"

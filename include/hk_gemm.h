@@ -1,0 +1,154 @@
+/*
+ * hk_gemm — dense BF16 GEMM  C = A · Bᵀ  for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one the HipKittens pages measure most ("L2" detail
+ * page, §3 "Target operation" table, row "BF16 GEMM": bf16 inputs, FP32
+ * accumulation, bf16 output; §7 and §9.2 describe its hot loop as the
+ * "ABt" product, so the second operand is stored N×K and used transposed;
+ * §3 "Launch config" fixes the 256×256 output tile and 64-wide K step).
+ *
+ * Semantics of every entry point that computes:
+ *
+ *     C[i*ldc + j] = bf16_rne( Σ_{k<K}  A[i*lda + k] · B[j*ldb + k] )
+ *
+ * for 0 ≤ i < M, 0 ≤ j < N, with products and sums in FP32 on the tensor
+ * cores (the order of the FP32 additions is unspecified), rounded once to
+ * bf16 with round-to-nearest-even. There is no alpha/beta and no
+ * accumulation into C; entries of C outside the M×N window (the padding
+ * between N and ldc) are never written.
+ *
+ * Layout: A is M×K row-major, B is N×K row-major ("TN"), C is M×N row-major,
+ * all bf16 (2 bytes per element, passed as raw device pointers). Leading
+ * dimensions are in ELEMENTS.
+ *
+ * Ownership: A, B, C and any workspace are caller-owned DEVICE memory on the
+ * device the call runs on. The library never frees them. C must not overlap
+ * A or B.
+ *
+ * Alignment (a requirement of the Tensor Memory Accelerator): A, B and C
+ * must be 16-byte aligned and lda, ldb, ldc multiples of 8, else
+ * HK_ERR_MISALIGNED.
+ *
+ * Edge values: M == 0 or N == 0 -> HK_OK, nothing launched (pointers may be
+ * NULL). K == 0 -> C (M×N) is filled with +0. Negative sizes, lda < K,
+ * ldb < K, ldc < N or sizes ≥ 2^31 -> HK_ERR_INVALID_ARG.
+ *
+ * Device: the library runs on compute capability 10.3 (GB300) only; any
+ * other device -> HK_ERR_UNSUPPORTED_DEVICE. There is no CPU fallback.
+ *
+ * Asynchrony: computing calls enqueue work on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream) and return without synchronising. Launch
+ * failures are returned as HK_ERR_LAUNCH. Every wait inside the kernel is
+ * bounded; a wait that runs out sets a device status word, the kernel drains
+ * and returns, and the status is read with hk_gemm_plan_device_status or
+ * hk_gemm_last_device_status after the stream has been synchronised.
+ *
+ * Thread safety: plans are immutable after creation and may be run from
+ * several host threads at once; hk_gemm_bf16 is thread safe.
+ */
+#ifndef HK_GEMM_H
+#define HK_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum hk_status {
+    HK_OK = 0,
+    HK_ERR_INVALID_ARG = 1,        /* a size, leading dimension or pointer is invalid */
+    HK_ERR_MISALIGNED = 2,         /* pointer not 16-byte aligned or ld not a multiple of 8 */
+    HK_ERR_UNSUPPORTED_DEVICE = 3, /* not a compute capability 10.3 device */
+    HK_ERR_LAUNCH = 4,             /* the CUDA launch (or a CUDA runtime call) failed */
+    HK_ERR_TIMEOUT = 5,            /* a bounded wait inside the kernel ran out */
+    HK_ERR_WORKSPACE = 6,          /* workspace missing, too small or misaligned */
+    HK_ERR_CUDA = 7                /* another CUDA runtime error (see hk_gemm_last_error_string) */
+} hk_status;
+
+/* Plan flags (hk_gemm_config.flags). */
+#define HK_FLAG_NONE 0u
+/* Test only: the producer withholds its arrival on the first shared-memory
+ * stage, so the MMA issuer's bounded wait runs out and the call reports
+ * HK_ERR_TIMEOUT through the device status word. No GPU fault is caused. */
+#define HK_FLAG_FAULT_DROP_ARRIVE 0x1u
+
+/* Tuning knobs of a plan. Zero in any field selects the default. */
+typedef struct hk_gemm_config {
+    int32_t group_m;        /* grouped rasterisation: height of a group in 256-row tiles (default 8) */
+    int32_t max_clusters;   /* cap on the persistent grid, in CTA pairs (default: all that fit) */
+    int32_t split_k;        /* K-split factor (default: chosen by the plan; 1 = none) */
+    int32_t reserved0;
+    uint64_t timeout_ns;    /* limit of each bounded wait in the kernel (default 1 s) */
+    uint32_t flags;         /* HK_FLAG_* */
+    uint32_t reserved1;
+} hk_gemm_config;
+
+/* What a plan chose (for logging and benchmarks). */
+typedef struct hk_gemm_plan_info {
+    int64_t M, N, K;
+    int32_t tile_m, tile_n, tile_k;   /* output tile of one CTA pair and K step */
+    int32_t stages;                   /* depth of the shared-memory ring */
+    int32_t num_tiles;                /* output tiles (times split_k) */
+    int32_t grid_ctas;                /* CTAs launched (2 per cluster) */
+    int32_t group_m;
+    int32_t split_k;
+    int32_t kernels_per_run;          /* kernel launches one run enqueues */
+    int32_t smem_bytes;               /* dynamic shared memory per CTA */
+    size_t workspace_bytes;
+} hk_gemm_plan_info;
+
+typedef struct hk_gemm_plan hk_gemm_plan;
+
+/* One-shot GEMM on the current device: C = bf16(A · Bᵀ).
+ * Equivalent to a plan with the default config run with no workspace (the
+ * default plan never needs one). The first call on a device creates a small
+ * per-device context (a 16-byte device status word) and is therefore not
+ * capturable in a CUDA graph; later calls allocate nothing. */
+hk_status hk_gemm_bf16(const void* A, const void* B, void* C,
+                       int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldc, void* stream);
+
+/* Create a plan for one problem shape on `device`. `config` may be NULL.
+ * Does all host-side work once: argument checks, device check, tile and
+ * schedule choice, and allocates the plan's 16-byte device status word.
+ * On success *out owns the plan; free it with hk_gemm_plan_destroy. */
+hk_status hk_gemm_plan_create(hk_gemm_plan** out, int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t ldc, int device,
+                              const hk_gemm_config* config);
+
+/* Bytes of device workspace a run needs (0 when no K split is used). */
+size_t hk_gemm_plan_workspace_size(const hk_gemm_plan* plan);
+
+/* Fill *info with what the plan chose. */
+hk_status hk_gemm_plan_get_info(const hk_gemm_plan* plan, hk_gemm_plan_info* info);
+
+/* Enqueue one GEMM with the plan's shape on `stream`. `workspace` must hold
+ * hk_gemm_plan_workspace_size(plan) bytes, 256-byte aligned (may be NULL when
+ * that size is 0); it is scratch, owned by the caller, and must not be used by
+ * another run that can overlap this one. The call allocates nothing. */
+hk_status hk_gemm_plan_run(const hk_gemm_plan* plan, const void* A, const void* B, void* C,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronise the plan's device and read-and-clear its status word:
+ * HK_OK, or HK_ERR_TIMEOUT if a bounded wait ran out in any run since the
+ * last read. */
+hk_status hk_gemm_plan_device_status(hk_gemm_plan* plan);
+
+/* The same for the calls hk_gemm_bf16 made on `device`. */
+hk_status hk_gemm_last_device_status(int device);
+
+void hk_gemm_plan_destroy(hk_gemm_plan* plan);
+
+/* Static description of a status code. */
+const char* hk_status_string(hk_status status);
+
+/* Detail of the last error on the calling host thread (never NULL). */
+const char* hk_gemm_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HK_GEMM_H */

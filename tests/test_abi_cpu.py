@@ -1,0 +1,98 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, and rejects invalid arguments on the host before any CUDA
+call is made. No computation is attempted here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "hk_gemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dense_bf16_gemm_02_gb300 import build
+    build.build()
+    from dense_bf16_gemm_02_gb300 import hk_gemm
+    return hk_gemm.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(hk_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("hk_gemm_bf16", "hk_gemm_plan_create", "hk_gemm_plan_run", "hk_gemm_plan_workspace_size",
+                 "hk_gemm_plan_destroy", "hk_status_string"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from dense_bf16_gemm_02_gb300 import hk_gemm
+    out = subprocess.run(["nm", "-D", "--defined-only", hk_gemm.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(lib, n)
+    assert set(hk_gemm.EXPORTED) <= set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = lib.hk_status_string(code).decode()
+        assert s.startswith("HK_")
+    assert b"unknown" in lib.hk_status_string(99)
+
+
+def test_host_validation_without_gpu(lib):
+    from dense_bf16_gemm_02_gb300 import hk_gemm as h
+    P = 1 << 20  # a 16-byte aligned fake address; never dereferenced on these paths
+    # empty problems return HK_OK without touching the device
+    assert lib.hk_gemm_bf16(None, None, None, 0, 5, 5, 8, 8, 8, None) == h.HK_OK
+    assert lib.hk_gemm_bf16(None, None, None, 5, 0, 5, 8, 8, 8, None) == h.HK_OK
+    # negative sizes / small leading dimensions
+    assert lib.hk_gemm_bf16(P, P, P, -1, 8, 8, 8, 8, 8, None) == h.HK_ERR_INVALID_ARG
+    assert lib.hk_gemm_bf16(P, P, P, 8, 8, 16, 8, 16, 8, None) == h.HK_ERR_INVALID_ARG
+    assert lib.hk_gemm_bf16(P, P, P, 8, 16, 8, 8, 8, 8, None) == h.HK_ERR_INVALID_ARG
+    assert lib.hk_gemm_bf16(P, P, P, 1 << 31, 8, 8, 8, 8, 8, None) == h.HK_ERR_INVALID_ARG
+    # leading dimensions not multiples of 8, unaligned pointers, null pointers
+    assert lib.hk_gemm_bf16(P, P, P, 8, 8, 12, 12, 16, 8, None) == h.HK_ERR_MISALIGNED
+    assert lib.hk_gemm_bf16(P + 2, P, P, 8, 8, 8, 8, 8, 8, None) == h.HK_ERR_MISALIGNED
+    assert lib.hk_gemm_bf16(P, P, P + 8, 8, 8, 8, 8, 8, 8, None) == h.HK_ERR_MISALIGNED
+    assert lib.hk_gemm_bf16(None, P, P, 8, 8, 8, 8, 8, 8, None) == h.HK_ERR_INVALID_ARG
+    assert lib.hk_gemm_bf16(P, P, None, 8, 8, 8, 8, 8, 8, None) == h.HK_ERR_INVALID_ARG
+    assert b"leading" in lib.hk_gemm_last_error_string() or b"null" in lib.hk_gemm_last_error_string()
+    # plan creation with invalid shapes fails on the host
+    handle = ctypes.c_void_p()
+    assert lib.hk_gemm_plan_create(ctypes.byref(handle), -5, 8, 8, 8, 8, 8, 0, None) == h.HK_ERR_INVALID_ARG
+    assert not handle.value
+    assert lib.hk_gemm_plan_create(None, 8, 8, 8, 8, 8, 8, 0, None) == h.HK_ERR_INVALID_ARG
+    assert lib.hk_gemm_plan_run(None, P, P, P, None, 0, None) == h.HK_ERR_INVALID_ARG
+    lib.hk_gemm_plan_destroy(None)
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    """The CUDA package never imports the oracle and has no CPU path."""
+    pkg = os.path.join(ROOT, "dense_bf16_gemm_02_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "torch.matmul" not in text and "cublas" not in text.lower(), f
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    from dense_bf16_gemm_02_gb300 import hk_gemm
+    monkeypatch.setattr(hk_gemm, "_lib", None)
+    monkeypatch.setattr(hk_gemm, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        hk_gemm.load()

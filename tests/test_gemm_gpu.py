@@ -1,0 +1,235 @@
+"""GPU parity: the CUDA GEMM through the C-ABI against the CPU oracle.
+
+Floating-point inputs: every checked entry within
+|C_gpu - C_ref| <= 2^-7·|C_ref| + 2^-12·sqrt(K)·σ_A·σ_B.
+Integer-valued inputs ({-4..4}): every partial sum is an integer below 2^24,
+so fp32 accumulation is exact in any order and the results are bit-exact.
+"""
+from __future__ import annotations
+
+import functools
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import SENTINEL, assert_bitexact, assert_close, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def hk():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("no CUDA device")
+    import dense_bf16_gemm_02_gb300 as pkg
+    pkg.load()
+    return pkg
+
+
+def run_gemm(hk, A_bits, B_bits, pad=(0, 0, 0, 0), stream=None):
+    """GEMM through hk_gemm_bf16 with guard bands around C; returns C bits and
+    checks the guard bands are untouched."""
+    import torch
+    M, K = A_bits.shape
+    N = B_bits.shape[0]
+    a_pad, b_pad, c_rows_pad, c_cols_pad = pad
+    A, Astore = to_device(A_bits, cols_pad=a_pad)
+    B, Bstore = to_device(B_bits, cols_pad=b_pad)
+    ldc_cols = N + ((-N) % 8) + c_cols_pad
+    C, Cstore = to_device(np.full((M, N), SENTINEL, dtype=np.uint16), rows_pad=c_rows_pad,
+                          cols_pad=ldc_cols - N, fill=SENTINEL)
+    lda, ldb = Astore.stride(0), Bstore.stride(0)
+    st = hk.hk_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, Cstore.stride(0),
+                         int(torch.cuda.current_stream().cuda_stream) if stream is None else stream)
+    assert st == hk.HK_OK, hk.hk_gemm_last_error_string()
+    torch.cuda.synchronize()
+    assert hk.hk_gemm_last_device_status(torch.cuda.current_device()) == hk.HK_OK
+    full = to_host(Cstore)
+    guard = full.copy()
+    guard[:M, :N] = SENTINEL
+    assert np.all(guard == SENTINEL), "a write landed outside C"
+    return full[:M, :N]
+
+
+def _pad_k(K):
+    return (-K) % 8
+
+
+# ---------------------------------------------------------- small / ragged --
+
+RAGGED = [(1, 1, 1), (7, 9, 5), (64, 64, 64), (128, 256, 64), (200, 136, 72), (256, 256, 256),
+          (257, 255, 65), (320, 264, 200), (513, 1000, 300), (1000, 520, 1032), (130, 2050, 40),
+          (1, 600, 129), (600, 1, 129), (300, 300, 8)]
+
+
+@pytest.mark.parametrize("M,N,K", RAGGED)
+def test_ragged_integer_bitexact(hk, M, N, K):
+    A = synth.int_bf16(M, K, 1100 + M)
+    B = synth.int_bf16(N, K, 2100 + N)
+    pad = _pad_k(K)
+    got = run_gemm(hk, A, B, pad=(pad, pad + 8, 3, 8))
+    assert_bitexact(got, oracle.gemm(A, B), f"int {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", RAGGED)
+def test_ragged_normal(hk, M, N, K):
+    A = synth.normal_bf16(M, K, 1000 + M)
+    B = synth.normal_bf16(N, K, 2000 + N)
+    pad = _pad_k(K)
+    got = run_gemm(hk, A, B, pad=(pad, pad, 1, 0))
+    assert_close(got, oracle.gemm(A, B), K, 1.0, 1.0, f"normal {M}x{N}x{K}")
+
+
+def test_gemm_256_workload(hk):
+    w = synth.WORKLOADS["gemm_256"]
+    A, B = synth.operands(w)
+    assert_close(run_gemm(hk, A, B), oracle.gemm(A, B), w.K, w.scale, w.scale, "256^3")
+    Ai, Bi = synth.operands(w, integer=True)
+    assert_bitexact(run_gemm(hk, Ai, Bi), oracle.gemm(Ai, Bi), "256^3 int")
+
+
+def test_k_zero_gives_zeros(hk):
+    import torch
+    M, N = 300, 200
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    A = torch.empty((M, 8), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((N, 8), dtype=torch.bfloat16, device="cuda")
+    st = hk.hk_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, 0, 8, 8, N, 0)
+    assert st == hk.HK_OK
+    torch.cuda.synchronize()
+    assert torch.all(C == 0)
+
+
+def test_empty_outputs_launch_nothing(hk):
+    assert hk.hk_gemm_bf16(0, 0, 0, 0, 64, 64, 64, 64, 64, 0) == hk.HK_OK
+    assert hk.hk_gemm_bf16(0, 0, 0, 64, 0, 64, 64, 64, 64, 0) == hk.HK_OK
+
+
+def test_misaligned_arguments_rejected(hk):
+    import torch
+    A = torch.zeros((64, 72), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    assert hk.hk_gemm_bf16(A.data_ptr() + 2, A.data_ptr(), C.data_ptr(), 64, 64, 64, 72, 72, 64, 0) == \
+        hk.HK_ERR_MISALIGNED
+    assert hk.hk_gemm_bf16(A.data_ptr(), A.data_ptr(), C.data_ptr(), 64, 64, 64, 68, 72, 64, 0) == \
+        hk.HK_ERR_MISALIGNED
+
+
+def test_deterministic(hk):
+    A = synth.normal_bf16(1024, 2048, 5)
+    B = synth.normal_bf16(768, 2048, 6)
+    a = run_gemm(hk, A, B)
+    b = run_gemm(hk, A, B)
+    assert np.array_equal(a, b)
+
+
+def test_torch_binding_and_plan(hk):
+    import torch
+    A = synth.normal_bf16(700, 520, 15)
+    B = synth.normal_bf16(900, 520, 16)
+    ref = oracle.gemm(A, B)
+    At, _ = to_device(A)
+    Bt, _ = to_device(B)
+    assert_close(to_host(hk.gemm(At, Bt)), ref, 520, 1, 1, "gemm()")
+    for group_m, max_clusters in [(1, 1), (3, 2), (8, 0), (100, 5)]:
+        plan = hk.Plan(700, 900, 520, ldc=904, group_m=group_m, max_clusters=max_clusters)
+        info = plan.info()
+        assert info["kernels_per_run"] == 1 and plan.workspace_size == 0
+        C = torch.empty((700, 904), dtype=torch.bfloat16, device="cuda")[:, :900]
+        plan.run(At, Bt, C)
+        torch.cuda.synchronize()
+        assert plan.device_status() == hk.HK_OK
+        assert_close(to_host(C), ref, 520, 1, 1, f"plan group_m={group_m} clusters={max_clusters}")
+        plan.close()
+
+
+def test_stream_argument(hk):
+    import torch
+    A = synth.int_bf16(384, 256, 1)
+    B = synth.int_bf16(512, 256, 2)
+    s = torch.cuda.Stream()
+    At, _ = to_device(A)
+    Bt, _ = to_device(B)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        C = hk.gemm(At, Bt)
+    s.synchronize()
+    assert_bitexact(to_host(C), oracle.gemm(A, B), "side stream")
+
+
+def test_bounded_wait_reports_timeout_and_recovers(hk):
+    """Fault injected on the host side of the protocol: the producer withholds
+    one arrival, the MMA issuer's bounded wait runs out, the kernel drains and
+    returns, the status word reports HK_ERR_TIMEOUT, and the context stays
+    usable."""
+    import torch
+    A = synth.int_bf16(512, 512, 3)
+    B = synth.int_bf16(512, 512, 4)
+    At, _ = to_device(A)
+    Bt, _ = to_device(B)
+    C = torch.empty((512, 512), dtype=torch.bfloat16, device="cuda")
+    plan = hk.Plan(512, 512, 512, timeout_ns=20_000_000, flags=hk.HK_FLAG_FAULT_DROP_ARRIVE)
+    plan.run(At, Bt, C)
+    torch.cuda.synchronize()
+    assert plan.device_status() == hk.HK_ERR_TIMEOUT
+    assert plan.device_status() == hk.HK_OK       # read-and-clear
+    plan.close()
+    assert_bitexact(to_host(hk.gemm(At, Bt)), oracle.gemm(A, B), "after timeout")
+
+
+# ------------------------------------------------------- full workloads --
+
+@functools.lru_cache(maxsize=1)
+def _operands(name, integer=False):
+    return synth.operands(synth.WORKLOADS[name], integer=integer)
+
+
+def _check_workload(hk, name, integer=False):
+    import torch
+    w = synth.WORKLOADS[name]
+    A, B = _operands(name, integer)
+    At, _ = to_device(A)
+    Bt, _ = to_device(B)
+    C = hk.gemm(At, Bt)
+    torch.cuda.synchronize()
+    assert hk.hk_gemm_last_device_status(torch.cuda.current_device()) == hk.HK_OK
+    got = to_host(C)
+    del At, Bt, C
+    check = assert_bitexact if integer else (
+        lambda g, r, what: assert_close(g, r, w.K, w.scale, w.scale, what))
+    if not w.sampled:
+        check(got, oracle.gemm(A, B), name)
+        return
+    r, c = synth.sample_positions(w.M, w.N, 3000 + w.wid)
+    ref, _ = oracle.gemm_entries(A, B, r, c)
+    check(got[r, c], ref, name + " samples")
+    rows = synth.full_rows(w.M, 3000 + w.wid)
+    ref_rows, _ = oracle.gemm_rows(A, B, rows)
+    check(got[rows], ref_rows, name + " rows")
+
+
+def test_workload_4096(hk):
+    _check_workload(hk, "gemm_4096")
+
+
+def test_workload_8192(hk):
+    _check_workload(hk, "gemm_8192")
+
+
+def test_workload_8192_integer(hk):
+    _check_workload(hk, "gemm_8192", integer=True)
+
+
+def test_workload_16384(hk):
+    _check_workload(hk, "gemm_16384")
+
+
+def test_workload_projection(hk):
+    _check_workload(hk, "proj_16384x28672x8192")
+
+
+def test_workload_skinny(hk):
+    _check_workload(hk, "skinny_128x28672x8192")
