@@ -84,7 +84,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
-    def __init__(self, gpu_index: int, interval_ms: int = 50):
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
         self.samples = []
         self.proc = None
         try:
@@ -178,9 +178,9 @@ def oracle_rows_timed(A, B, rows) -> tuple[float, int]:
     return time.perf_counter() - t0, used
 
 
-def cpu_baseline(w, A, B, budget_s: float = 12.0) -> dict:
+def cpu_baseline(w, A, B, budget_s: float = 15.0) -> dict:
     """The oracle, as it stands, on full rows of this workload's C."""
-    probe = np.arange(min(4, w.M), dtype=np.int64)
+    probe = np.arange(min(64, w.M), dtype=np.int64)   # enough rows to occupy every host core
     t, _ = oracle_rows_timed(A, B, probe)
     per_row = max(t / len(probe), 1e-6)
     nrows = int(max(1, min(w.M, budget_s / per_row)))
@@ -198,7 +198,7 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     A, B = synth.operands(w)
-    probe = np.arange(min(4, w.M), dtype=np.int64)
+    probe = np.arange(min(64, w.M), dtype=np.int64)
     t, _ = oracle_rows_timed(A, B, probe)
     per_row = max(t / len(probe), 1e-6)
     rows_per_step = int(max(1, min(64, 120.0 / (args.steps + args.warmup) / per_row)))
@@ -372,7 +372,7 @@ def run_hk(args, w):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["hk", "reference"], default="hk")
     ap.add_argument("--workload", default="gemm_8192", choices=sorted(synth.WORKLOADS))

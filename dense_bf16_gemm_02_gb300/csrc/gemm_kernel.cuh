@@ -102,15 +102,16 @@ __device__ __forceinline__ bool aborted(const GemmParams& p) {
     return *reinterpret_cast<volatile uint32_t*>(p.status + 1) == p.launch_id;
 }
 
-// Bounded wait for phase `parity` of `bar`. Returns false when the wait gave
-// up: either this launch was already aborted by another role, or the time
-// limit ran out (then this thread records `code` and aborts the launch).
-__device__ __noinline__ bool wait_bounded(const GemmParams& p, uint32_t bar, uint32_t parity,
-                                          uint32_t code) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Slow path of a bounded wait for phase `parity` of `bar` (kept out of line
+// so that the hot loops only carry the first probe). Returns false when the
+// wait gave up: either this launch was already aborted by another role, or
+// the time limit ran out (then this thread records `code` and aborts the
+// launch).
+__device__ __noinline__ bool wait_bounded_slow(const GemmParams& p, uint32_t bar, uint32_t parity,
+                                               uint32_t code, bool cluster_scope) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (aborted(p)) return false;
             if (global_timer_ns() - t0 > p.timeout_ns) {
@@ -121,6 +122,19 @@ __device__ __noinline__ bool wait_bounded(const GemmParams& p, uint32_t bar, uin
             }
         }
     }
+}
+
+__device__ __forceinline__ bool wait_bounded(const GemmParams& p, uint32_t bar, uint32_t parity,
+                                             uint32_t code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_bounded_slow(p, bar, parity, code, false);
+}
+
+// For barriers that the peer CTA's threads arrive on (cluster-scope acquire).
+__device__ __forceinline__ bool wait_bounded_cluster(const GemmParams& p, uint32_t bar, uint32_t parity,
+                                                     uint32_t code) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    return wait_bounded_slow(p, bar, parity, code, true);
 }
 
 // Warp-uniform variant: lane 0 waits, the verdict is broadcast, and every
@@ -233,7 +247,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             for (int t = pair; t < p.num_tiles && !abort_seen; t += num_pairs, ++local) {
                 const int buf = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
-                if (!wait_bounded(p, acc_empty_bar(buf), acc_phase ^ 1u, kErrMmaAccEmpty)) {
+                if (!wait_bounded_cluster(p, acc_empty_bar(buf), acc_phase ^ 1u, kErrMmaAccEmpty)) {
                     abort_seen = true;
                     break;
                 }
@@ -254,8 +268,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                       (kb | k) != 0 ? 1u : 0u);
                     }
                     // free this stage in both CTAs once the MMAs above have read it
-                    mma_commit_pair(empty_bar(stage));
-                    mma_commit_pair(map_to_cta(empty_bar(stage), 1));
+                    mma_commit_pair_mask(empty_bar(stage), 0x3);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -263,8 +276,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 }
                 if (abort_seen) break;
                 // accumulator complete: hand it to both CTAs' epilogues
-                mma_commit_pair(acc_full_bar(buf));
-                mma_commit_pair(map_to_cta(acc_full_bar(buf), 1));
+                mma_commit_pair_mask(acc_full_bar(buf), 0x3);
             }
         }
     } else {

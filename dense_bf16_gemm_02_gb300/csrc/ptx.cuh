@@ -64,7 +64,23 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
 }
 
 // One probe of phase `parity`; true once that phase has completed.
+// Acquire at CTA scope: enough for barriers completed by this CTA's threads,
+// by TMA transaction counts or by tcgen05.commit.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// The same with acquire at cluster scope, for barriers that threads of the
+// peer CTA arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -168,6 +184,17 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t cluster_bar) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      cluster_bar)
                  : "memory");
+}
+
+// The same, arriving once on the barrier at offset `bar` in every CTA of the
+// cluster named by the bit mask `cta_mask` (one instruction for both CTAs of
+// the pair).
+__device__ __forceinline__ void mma_commit_pair_mask(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // Warp-collective TMEM -> registers: lane l of the warp reads TMEM lane
