@@ -40,7 +40,10 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # DRAM traffic of one launch of the GEMM kernel from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources whose digest is given; see profiles/.
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {
+    "gemm_8192": {"source_digest": "61beb5cc9d56c9de", "bytes_per_launch": 1064003000 + 126472448,
+                  "profile": "profiles/gemm_bf16_pair_kernel_gemm_8192.md"},
+}
 
 
 def kernel_source_digest() -> str:
