@@ -335,7 +335,16 @@ def run_hk(args, w):
     peak = float(peaks["bf16_tflops"])
     value = flops * args.steps * world / (elapsed_max / 1e3) / 1e12
     mean_launch_ms = statistics.mean(per_launch)
-    achieved = flops / (mean_launch_ms / 1e3) / 1e12
+    nbytes = gemm_bytes(w.M, w.N, w.K)
+    hbm_bound = flops / nbytes < peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)   # below the roofline knee
+    if hbm_bound:
+        bound, rf_unit, rf_peak = "hbm", "GB/s", float(peaks["hbm_gbs"])
+        achieved = nbytes / (mean_launch_ms / 1e3) / 1e9
+        peak_source = f"hbm_gbs of {peaks_src}"
+    else:
+        bound, rf_unit, rf_peak = "tensor", UNIT, peak
+        achieved = flops / (mean_launch_ms / 1e3) / 1e12
+        peak_source = f"bf16_tflops (burst) of {peaks_src}"
     digest = kernel_source_digest()
     traffic = None
     tr = MEASURED_TRAFFIC.get(w.name)
@@ -346,16 +355,19 @@ def run_hk(args, w):
         "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(workload_config(w), parallelism="replicas" if world > 1 else "single GPU",
-                       tile=f"{info['tile_m']}x{info['tile_n']}x{info['tile_k']} per CTA pair",
+                       tile=f"{info['tile_m']}x{info['tile_n']}x{info['tile_k']} per "
+                            f"{'CTA pair' if info['ctas_per_unit'] == 2 else 'CTA'}",
                        stages=info["stages"], grid_ctas=info["grid_ctas"], group_m=info["group_m"]),
         "pct_of_peak": 100.0 * value / world / peak,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"bf16_tflops (burst) of {peaks_src}",
+        "roofline": {"bound": bound, "achieved": achieved, "peak": rf_peak, "unit": rf_unit,
+                     "frac": achieved / rf_peak, "traffic": traffic,
+                     "peak_source": peak_source,
                      "algorithmic_flops_per_launch": flops,
                      "algorithmic_bytes_per_launch": gemm_bytes(w.M, w.N, w.K),
                      "mean_launch_ms": mean_launch_ms, "p10_launch_ms": float(np.percentile(per_launch, 10)),
-                     "p90_launch_ms": float(np.percentile(per_launch, 90)), "kernel": "gemm_bf16_pair_kernel",
+                     "p90_launch_ms": float(np.percentile(per_launch, 90)),
+                     "kernel": f"gemm_bf16_kernel ({info['tile_m']}x{info['tile_n']}, "
+                               f"{info['ctas_per_unit']} CTA(s) per tile)",
                      "source_digest": digest},
         "e2e": {"value": flops * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(A_h.numel() * 2 + B_h.numel() * 2),

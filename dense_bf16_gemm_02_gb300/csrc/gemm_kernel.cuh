@@ -1,5 +1,10 @@
 // Persistent, warp-specialised BF16 GEMM  C = A · Bᵀ  for sm_103a.
 //
+// One template, two shapes of work unit: a CTA pair (cta_group::2, output
+// tile 256 × kTileN) for general shapes, and a single CTA (cta_group::1,
+// output tile 128 × kTileN) for problems with at most 128 rows, where a pair
+// would leave half of its tensor cores and half of its SMs idle.
+//
 // The operation and its 256×256 output tile with a 64-wide K step follow the
 // HipKittens "L2" detail page (§3 "Target operation" and "Launch config";
 // §9.2 GEMM hot loop). Everything else is a Blackwell design rather than the
@@ -36,31 +41,51 @@
 
 namespace hk {
 
-constexpr int kPairM = 256;          // rows of C per pair tile
 constexpr int kCtaM = 128;           // rows of C (and of A) per CTA
-constexpr int kTileN = 256;          // columns of C per pair tile (MMA N)
-constexpr int kCtaN = 128;           // rows of B loaded per CTA
 constexpr int kTileK = 64;           // K per pipeline stage (one 128-byte swizzle row)
 constexpr int kMmaK = 16;            // K per tcgen05.mma
-constexpr int kStages = 6;           // shared-memory ring depth
-constexpr int kAStageBytes = kCtaM * kTileK * 2;   // 16 KiB
-constexpr int kBStageBytes = kCtaN * kTileK * 2;   // 16 KiB
+constexpr int kABytes = kCtaM * kTileK * 2;        // 16 KiB of A per stage per CTA
 constexpr int kEpiCols = 32;                        // columns per epilogue store
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBufBytes = 32 * kEpiCols * 2;     // 32 rows × 64 B
 constexpr int kThreads = 64 + 32 * kEpiWarps;       // 192
-constexpr int kAccCols = kTileN;                    // TMEM columns per accumulator
-constexpr int kTmemCols = 2 * kAccCols;             // two accumulators = all 512 columns
+constexpr int kSmemLimit = 232448;                  // dynamic shared memory per CTA on sm_103
 
-// shared-memory layout, offsets from a 1024-byte aligned base
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kAStageBytes;
-constexpr int kOffEpi = kOffB + kStages * kBStageBytes;
-constexpr int kOffBars = kOffEpi + kEpiWarps * 2 * kEpiBufBytes;
-constexpr int kNumBars = 2 * kStages + 4;   // full[S], empty[S], acc_full[2], acc_empty[2]
-constexpr int kOffTmemHolder = kOffBars + kNumBars * 8;
-constexpr int kSmemUsed = kOffTmemHolder + 16;
-constexpr int kSmemBytes = kSmemUsed + 1024;   // slack for aligning the base
+constexpr int pow2_at_least(int x) {
+    int r = 32;
+    while (r < x) r <<= 1;
+    return r;
+}
+
+// Compile-time geometry of one kernel instance.
+template <int kCG, int kTileN_>
+struct Geometry {
+    static_assert(kCG == 1 || kCG == 2, "one CTA or a CTA pair");
+    static_assert(kTileN_ % (16 * kCG) == 0 && kTileN_ >= 32 && kTileN_ <= 256, "MMA N");
+    static constexpr int kTileM = kCtaM * kCG;              // rows of C per tile
+    static constexpr int kTileN = kTileN_;                  // columns of C per tile (MMA N)
+    static constexpr int kBRows = kTileN / kCG;             // rows of B each CTA loads per stage
+    static_assert(kBRows % 8 == 0, "B rows fill whole 8-row swizzle atoms");
+    static constexpr int kBBytes = kBRows * kTileK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kFixed = kEpiWarps * 2 * kEpiBufBytes + 256 + 1024;   // epilogue, barriers, alignment
+    static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
+    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+    static_assert(kStages >= 3, "pipeline too shallow");
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kStages * kABytes;
+    static constexpr int kOffEpi = kOffB + kStages * kBBytes;
+    static constexpr int kOffBars = kOffEpi + kEpiWarps * 2 * kEpiBufBytes;
+    static constexpr int kNumBars = 2 * kStages + 4;        // full[S], empty[S], acc_full[2], acc_empty[2]
+    static constexpr int kOffTmemHolder = kOffBars + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffTmemHolder + 16 + 1024;   // + slack for aligning the base
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory");
+    static constexpr int kAccCols = kTileN;                 // TMEM columns per accumulator
+    static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);
+    static_assert(kTmemCols <= 512, "TMEM");
+    static constexpr uint32_t kExpectBytes = kCG * kStageBytes;   // bytes landing per stage in the cluster
+    static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, kTileN);
+};
 
 // error bits written to the status word when a bounded wait runs out
 constexpr uint32_t kErrProducerEmpty = 1u << 0;
@@ -72,7 +97,7 @@ constexpr uint32_t kFlagDropArrive = 0x1u;
 
 struct GemmParams {
     int32_t M, N, K;
-    int32_t tiles_m, tiles_n;     // pair tiles along M and N
+    int32_t tiles_m, tiles_n;     // output tiles along M and N
     int32_t k_blocks;             // ceil(K / 64)
     int32_t num_tiles;
     int32_t group_m;
@@ -154,10 +179,11 @@ __device__ __forceinline__ void drain_after_abort() {
     for (int i = 0; i < 200; ++i) __nanosleep(1000);
 }
 
+template <int kCG, int kTileN>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                      const __grid_constant__ CUtensorMap tmap_b,
-                      const __grid_constant__ CUtensorMap tmap_c, const GemmParams p) {
+gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                 const __grid_constant__ CUtensorMap tmap_c, const GemmParams p) {
+    using G = Geometry<kCG, kTileN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -165,24 +191,24 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = lane_id();
-    const uint32_t rank = cluster_cta_rank();          // 0 = leader of the pair
-    const int pair = blockIdx.x >> 1;
-    const int num_pairs = gridDim.x >> 1;
+    const uint32_t rank = kCG == 2 ? cluster_cta_rank() : 0u;   // 0 = leader of the pair
+    const int unit = blockIdx.x / kCG;                          // this CTA's pair (or CTA)
+    const int num_units = gridDim.x / kCG;
 
-    auto full_bar = [&](int s) { return base + kOffBars + 8u * s; };
-    auto empty_bar = [&](int s) { return base + kOffBars + 8u * (kStages + s); };
-    auto acc_full_bar = [&](int b) { return base + kOffBars + 8u * (2 * kStages + b); };
-    auto acc_empty_bar = [&](int b) { return base + kOffBars + 8u * (2 * kStages + 2 + b); };
-    const uint32_t tmem_holder = base + kOffTmemHolder;
+    auto full_bar = [&](int s) { return base + G::kOffBars + 8u * s; };
+    auto empty_bar = [&](int s) { return base + G::kOffBars + 8u * (G::kStages + s); };
+    auto acc_full_bar = [&](int b) { return base + G::kOffBars + 8u * (2 * G::kStages + b); };
+    auto acc_empty_bar = [&](int b) { return base + G::kOffBars + 8u * (2 * G::kStages + 2 + b); };
+    const uint32_t tmem_holder = base + G::kOffTmemHolder;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < G::kStages; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(acc_full_bar(b), 1);
-            mbar_init(acc_empty_bar(b), 2 * kEpiWarps);
+            mbar_init(acc_empty_bar(b), kCG * kEpiWarps);
         }
         fence_mbar_init_cluster();
     }
@@ -192,13 +218,18 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
         prefetch_tensor_map(&tmap_c);
     }
     if (warp == 1) {
-        tmem_alloc_pair(tmem_holder, kTmemCols);
-        tmem_relinquish_pair();
+        if constexpr (kCG == 2) {
+            tmem_alloc_pair(tmem_holder, G::kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc_one(tmem_holder, G::kTmemCols);
+            tmem_relinquish_one();
+        }
     }
     tc_fence_before_sync();
-    cluster_sync();
+    if constexpr (kCG == 2) cluster_sync(); else __syncthreads();
     tc_fence_after_sync();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemHolder);
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + G::kOffTmemHolder);
 
     bool abort_seen = false;
 
@@ -208,29 +239,35 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
             int stage = 0;
             uint32_t phase = 0;
             bool dropped = false;
-            for (int t = pair; t < p.num_tiles && !abort_seen; t += num_pairs) {
+            for (int t = unit; t < p.num_tiles && !abort_seen; t += num_units) {
                 int tm, tn;
                 tile_coords(p, t, tm, tn);
-                const int a_row = tm * kPairM + static_cast<int>(rank) * kCtaM;
-                const int b_row = tn * kTileN + static_cast<int>(rank) * kCtaN;
+                const int a_row = tm * G::kTileM + static_cast<int>(rank) * kCtaM;
+                const int b_row = tn * G::kTileN + static_cast<int>(rank) * G::kBRows;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!wait_bounded(p, empty_bar(stage), phase ^ 1u, kErrProducerEmpty)) {
                         abort_seen = true;
                         break;
                     }
-                    const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
                     if (rank == 0) {
                         if ((p.flags & kFlagDropArrive) && !dropped) {
                             dropped = true;   // test-only fault: withhold this arrival
                         } else {
-                            mbar_arrive_expect_tx(full_bar(stage), 2u * (kAStageBytes + kBStageBytes));
+                            mbar_arrive_expect_tx(full_bar(stage), G::kExpectBytes);
                         }
                     }
-                    tma_load_2d_pair(base + kOffA + stage * kAStageBytes, &tmap_a, kb * kTileK, a_row,
-                                     leader_full);
-                    tma_load_2d_pair(base + kOffB + stage * kBStageBytes, &tmap_b, kb * kTileK, b_row,
-                                     leader_full);
-                    if (++stage == kStages) {
+                    const uint32_t a_dst = base + G::kOffA + stage * kABytes;
+                    const uint32_t b_dst = base + G::kOffB + stage * G::kBBytes;
+                    if constexpr (kCG == 2) {
+                        // both CTAs' copies complete on the leader's barrier
+                        const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
+                        tma_load_2d_pair(a_dst, &tmap_a, kb * kTileK, a_row, leader_full);
+                        tma_load_2d_pair(b_dst, &tmap_b, kb * kTileK, b_row, leader_full);
+                    } else {
+                        tma_load_2d(a_dst, &tmap_a, kb * kTileK, a_row, full_bar(stage));
+                        tma_load_2d(b_dst, &tmap_b, kb * kTileK, b_row, full_bar(stage));
+                    }
+                    if (++stage == G::kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -240,53 +277,60 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
         if (rank == 0 && lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kPairM, kTileN);
             int stage = 0;
             uint32_t phase = 0;
             int local = 0;
-            for (int t = pair; t < p.num_tiles && !abort_seen; t += num_pairs, ++local) {
+            for (int t = unit; t < p.num_tiles && !abort_seen; t += num_units, ++local) {
                 const int buf = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
-                if (!wait_bounded_cluster(p, acc_empty_bar(buf), acc_phase ^ 1u, kErrMmaAccEmpty)) {
+                const bool acc_free = kCG == 2
+                                          ? wait_bounded_cluster(p, acc_empty_bar(buf), acc_phase ^ 1u, kErrMmaAccEmpty)
+                                          : wait_bounded(p, acc_empty_bar(buf), acc_phase ^ 1u, kErrMmaAccEmpty);
+                if (!acc_free) {
                     abort_seen = true;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + buf * kAccCols;
+                const uint32_t d_tmem = tmem_base + buf * G::kAccCols;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!wait_bounded(p, full_bar(stage), phase, kErrMmaFull)) {
                         abort_seen = true;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint64_t a_desc = smem_desc_kmajor_sw128(base + kOffA + stage * kAStageBytes);
-                    const uint64_t b_desc = smem_desc_kmajor_sw128(base + kOffB + stage * kBStageBytes);
+                    const uint64_t a_desc = smem_desc_kmajor_sw128(base + G::kOffA + stage * kABytes);
+                    const uint64_t b_desc = smem_desc_kmajor_sw128(base + G::kOffB + stage * G::kBBytes);
 #pragma unroll
                     for (int k = 0; k < kTileK / kMmaK; ++k) {
                         // advance 16 bf16 = 32 bytes along K inside the swizzle atom
-                        mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
-                                      (kb | k) != 0 ? 1u : 0u);
+                        const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+                        if constexpr (kCG == 2)
+                            mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, G::kIdesc, acc);
+                        else
+                            mma_bf16_one(d_tmem, a_desc + 2u * k, b_desc + 2u * k, G::kIdesc, acc);
                     }
-                    // free this stage in both CTAs once the MMAs above have read it
-                    mma_commit_pair_mask(empty_bar(stage), 0x3);
-                    if (++stage == kStages) {
+                    // free this stage (in both CTAs of a pair) once the MMAs above have read it
+                    if constexpr (kCG == 2) mma_commit_pair_mask(empty_bar(stage), 0x3);
+                    else mma_commit_one(empty_bar(stage));
+                    if (++stage == G::kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (abort_seen) break;
-                // accumulator complete: hand it to both CTAs' epilogues
-                mma_commit_pair_mask(acc_full_bar(buf), 0x3);
+                // accumulator complete: hand it to the epilogue(s)
+                if constexpr (kCG == 2) mma_commit_pair_mask(acc_full_bar(buf), 0x3);
+                else mma_commit_one(acc_full_bar(buf));
             }
         }
     } else {
         // --------------------------------------------------- epilogue --
         const uint32_t q = warp & 3u;                  // TMEM lane quarter this warp may read
-        const uint32_t epi = base + kOffEpi + (warp - 2) * 2 * kEpiBufBytes;
+        const uint32_t epi = base + G::kOffEpi + (warp - 2) * 2 * kEpiBufBytes;
         const uint32_t swz = (lane >> 1) & 3u;         // 64-byte swizzle of this lane's row
         uint32_t chunk_count = 0;
         int local = 0;
-        for (int t = pair; t < p.num_tiles; t += num_pairs, ++local) {
+        for (int t = unit; t < p.num_tiles; t += num_units, ++local) {
             int tm, tn;
             tile_coords(p, t, tm, tn);
             const int buf = local & 1;
@@ -296,10 +340,10 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 break;
             }
             tc_fence_after_sync();
-            const int row0 = tm * kPairM + static_cast<int>(rank) * kCtaM + static_cast<int>(q) * 32;
-            const uint32_t t_row = tmem_base + ((q * 32u) << 16) + buf * kAccCols;
+            const int row0 = tm * G::kTileM + static_cast<int>(rank) * kCtaM + static_cast<int>(q) * 32;
+            const uint32_t t_row = tmem_base + ((q * 32u) << 16) + buf * G::kAccCols;
 #pragma unroll 1
-            for (int c = 0; c < kTileN / kEpiCols; ++c) {
+            for (int c = 0; c < G::kTileN / kEpiCols; ++c) {
                 uint32_t v[32];
                 if (p.k_blocks > 0) {
                     tmem_load_32cols(t_row + c * kEpiCols, v);
@@ -308,11 +352,14 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = 0u;
                 }
-                if (c == kTileN / kEpiCols - 1) {
+                if (c == G::kTileN / kEpiCols - 1) {
                     // every TMEM read of this accumulator is done: release it to the MMA
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(map_to_cta(acc_empty_bar(buf), 0));
+                    if (lane == 0) {
+                        if constexpr (kCG == 2) mbar_arrive_cluster(map_to_cta(acc_empty_bar(buf), 0));
+                        else mbar_arrive(acc_empty_bar(buf));
+                    }
                 }
                 uint32_t w[16];
 #pragma unroll
@@ -328,7 +375,7 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                  w[4 * j + 2], w[4 * j + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
-                const int col0 = tn * kTileN + c * kEpiCols;
+                const int col0 = tn * G::kTileN + c * kEpiCols;
                 if (lane == 0 && row0 < p.M && col0 < p.n_tma) {
                     tma_store_2d(&tmap_c, sbuf, col0, row0);
                 }
@@ -358,10 +405,11 @@ gemm_bf16_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
     if (abort_seen || aborted(p)) drain_after_abort();
     __syncwarp();
     tc_fence_before_sync();
-    cluster_sync();
+    if constexpr (kCG == 2) cluster_sync(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc_pair(tmem_base, kTmemCols);
+        if constexpr (kCG == 2) tmem_dealloc_pair(tmem_base, G::kTmemCols);
+        else tmem_dealloc_one(tmem_base, G::kTmemCols);
     }
 }
 

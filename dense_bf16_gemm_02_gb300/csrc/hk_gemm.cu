@@ -39,13 +39,48 @@ constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s per bounded wait
 constexpr int kDefaultGroupM = 8;
 
+// -------------------------------------------------------------- variants --
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, hk::GemmParams);
+
+struct Variant {
+    int id;            // value of hk_gemm_config.kernel
+    int cg;            // CTAs per work unit (1 or 2)
+    int tile_m, tile_n;
+    int stages, smem_bytes;
+    KernelFn fn;
+    const char* name;
+};
+
+template <int kCG, int kTileN>
+constexpr Variant make_variant(int id, const char* name) {
+    using G = hk::Geometry<kCG, kTileN>;
+    return Variant{id, kCG, G::kTileM, G::kTileN, G::kStages, G::kSmemBytes, &hk::gemm_bf16_kernel<kCG, kTileN>,
+                   name};
+}
+
+const Variant kVariants[] = {
+    make_variant<2, 256>(HK_KERNEL_PAIR_256x256, "pair 256x256"),
+    make_variant<1, 256>(HK_KERNEL_SINGLE_128x256, "single 128x256"),
+    make_variant<1, 192>(HK_KERNEL_SINGLE_128x192, "single 128x192"),
+    make_variant<1, 128>(HK_KERNEL_SINGLE_128x128, "single 128x128"),
+    make_variant<1, 64>(HK_KERNEL_SINGLE_128x64, "single 128x64"),
+};
+constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
+
+const Variant* find_variant(int id) {
+    for (const Variant& v : kVariants)
+        if (v.id == id) return &v;
+    return nullptr;
+}
+
 // ----------------------------------------------------------- device info --
 
 struct DeviceInfo {
     bool probed = false;
     bool supported = false;
     int sm_count = 0;
-    int max_pairs = 0;             // co-resident 2-CTA clusters of the GEMM kernel
+    int max_units[kNumVariants] = {};   // co-resident work units (pairs or CTAs) per variant
     std::string why;
 };
 
@@ -65,8 +100,8 @@ hk_status device_info(int device, const DeviceInfo** out) {
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device);
         if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "querying the device", e);
-        d.probed = true;
         if (major != 10 || minor != 3) {
+            d.probed = true;
             d.supported = false;
             d.why = "compute capability " + std::to_string(major) + "." + std::to_string(minor) +
                     " (this library is built for 10.3, sm_103a)";
@@ -74,30 +109,33 @@ hk_status device_info(int device, const DeviceInfo** out) {
             int prev = -1;
             cudaGetDevice(&prev);
             if (prev != device) cudaSetDevice(device);
-            e = cudaFuncSetAttribute(hk::gemm_bf16_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     hk::kSmemBytes);
-            int clusters = 0;
-            if (e == cudaSuccess) {
-                cudaLaunchConfig_t cfg = {};
-                cudaLaunchAttribute attr[1];
-                attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = 2;
-                attr[0].val.clusterDim.y = 1;
-                attr[0].val.clusterDim.z = 1;
-                cfg.gridDim = dim3(2 * d.sm_count, 1, 1);
-                cfg.blockDim = dim3(hk::kThreads, 1, 1);
-                cfg.dynamicSmemBytes = hk::kSmemBytes;
-                cfg.attrs = attr;
-                cfg.numAttrs = 1;
-                e = cudaOccupancyMaxActiveClusters(&clusters, hk::gemm_bf16_pair_kernel, &cfg);
+            for (int i = 0; i < kNumVariants && e == cudaSuccess; ++i) {
+                const Variant& v = kVariants[i];
+                e = cudaFuncSetAttribute(v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v.smem_bytes);
+                if (e != cudaSuccess) break;
+                if (v.cg == 2) {
+                    cudaLaunchConfig_t cfg = {};
+                    cudaLaunchAttribute attr[1];
+                    attr[0].id = cudaLaunchAttributeClusterDimension;
+                    attr[0].val.clusterDim.x = 2;
+                    attr[0].val.clusterDim.y = 1;
+                    attr[0].val.clusterDim.z = 1;
+                    cfg.gridDim = dim3(2 * d.sm_count, 1, 1);
+                    cfg.blockDim = dim3(hk::kThreads, 1, 1);
+                    cfg.dynamicSmemBytes = v.smem_bytes;
+                    cfg.attrs = attr;
+                    cfg.numAttrs = 1;
+                    e = cudaOccupancyMaxActiveClusters(&d.max_units[i], v.fn, &cfg);
+                } else {
+                    int per_sm = 0;
+                    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, v.fn, hk::kThreads, v.smem_bytes);
+                    d.max_units[i] = per_sm * d.sm_count;
+                }
             }
             if (prev >= 0 && prev != device) cudaSetDevice(prev);
-            if (e != cudaSuccess) {
-                d.probed = false;
-                return cuda_fail(HK_ERR_CUDA, "configuring the GEMM kernel", e);
-            }
-            d.supported = clusters > 0;
-            d.max_pairs = clusters;
+            if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "configuring the GEMM kernels", e);
+            d.probed = true;
+            d.supported = d.max_units[0] > 0;
             if (!d.supported) d.why = "no 2-CTA cluster of the GEMM kernel fits on the device";
         }
     }
@@ -209,6 +247,7 @@ struct DeviceGuard {
 struct hk_gemm_plan {
     int64_t M, N, K, lda, ldb, ldc;
     int device;
+    const Variant* variant;
     hk::GemmParams params;      // everything but status/launch id
     int grid_ctas;
     hk_gemm_config cfg;
@@ -218,6 +257,33 @@ struct hk_gemm_plan {
 
 namespace {
 
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Fraction of the work-unit slots that the tiles keep busy over all waves.
+double slot_use(int64_t tiles, int64_t slots) {
+    if (tiles <= 0 || slots <= 0) return 0.0;
+    return double(tiles) / double(ceil_div(tiles, slots) * slots);
+}
+
+// Kernel choice: the CTA pair (256-row tiles) whenever there are more than
+// 128 rows; otherwise a single-CTA kernel (128-row tiles) with the tile width
+// that keeps the most SMs busy (ties go to the wider tile, which re-reads A
+// fewer times).
+const Variant* choose_variant(int64_t M, int64_t N, const DeviceInfo* di) {
+    if (M > hk::kCtaM) return &kVariants[0];
+    const Variant* best = nullptr;
+    double best_use = -1.0;
+    for (int i = 1; i < kNumVariants; ++i) {
+        const Variant& v = kVariants[i];
+        const double use = slot_use(ceil_div(M, v.tile_m) * ceil_div(N, v.tile_n), di->max_units[i]);
+        if (use > best_use + 1e-9) {
+            best_use = use;
+            best = &v;
+        }
+    }
+    return best ? best : &kVariants[0];
+}
+
 hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                     int device, const hk_gemm_config* config, const DeviceInfo* di) {
     p->M = M; p->N = N; p->K = K; p->lda = lda; p->ldb = ldb; p->ldc = ldc;
@@ -226,15 +292,23 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     if (config) p->cfg = *config;
     if (p->cfg.split_k > 1) return fail(HK_ERR_INVALID_ARG, "split_k > 1 is not available for this shape");
     if (p->cfg.group_m < 0 || p->cfg.max_clusters < 0) return fail(HK_ERR_INVALID_ARG, "negative config field");
+    const Variant* v = nullptr;
+    if (p->cfg.kernel == HK_KERNEL_AUTO) {
+        v = choose_variant(M, N, di);
+    } else if (!(v = find_variant(p->cfg.kernel))) {
+        return fail(HK_ERR_INVALID_ARG, "unknown kernel id %d", (int)p->cfg.kernel);
+    }
+    p->variant = v;
+    const int vi = static_cast<int>(v - kVariants);
     const int group_m = p->cfg.group_m > 0 ? p->cfg.group_m : kDefaultGroupM;
     hk::GemmParams& g = p->params;
     std::memset(&g, 0, sizeof g);
     g.M = static_cast<int32_t>(M);
     g.N = static_cast<int32_t>(N);
     g.K = static_cast<int32_t>(K);
-    g.tiles_m = static_cast<int32_t>((M + hk::kPairM - 1) / hk::kPairM);
-    g.tiles_n = static_cast<int32_t>((N + hk::kTileN - 1) / hk::kTileN);
-    g.k_blocks = static_cast<int32_t>((K + hk::kTileK - 1) / hk::kTileK);
+    g.tiles_m = static_cast<int32_t>(ceil_div(M, v->tile_m));
+    g.tiles_n = static_cast<int32_t>(ceil_div(N, v->tile_n));
+    g.k_blocks = static_cast<int32_t>(ceil_div(K, hk::kTileK));
     const int64_t tiles = int64_t(g.tiles_m) * g.tiles_n;
     if (tiles > (int64_t(1) << 30)) return fail(HK_ERR_INVALID_ARG, "too many output tiles");
     g.num_tiles = static_cast<int32_t>(tiles);
@@ -243,10 +317,11 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     g.ldc = ldc;
     g.flags = p->cfg.flags;
     g.timeout_ns = p->cfg.timeout_ns ? p->cfg.timeout_ns : kDefaultTimeoutNs;
-    int pairs = di->max_pairs;
-    if (p->cfg.max_clusters > 0 && p->cfg.max_clusters < pairs) pairs = p->cfg.max_clusters;
-    if (pairs > g.num_tiles) pairs = g.num_tiles;
-    p->grid_ctas = 2 * pairs;
+    int units = di->max_units[vi];
+    if (units <= 0) return fail(HK_ERR_UNSUPPORTED_DEVICE, "kernel %s does not fit on the device", v->name);
+    if (p->cfg.max_clusters > 0 && p->cfg.max_clusters < units) units = p->cfg.max_clusters;
+    if (units > g.num_tiles) units = g.num_tiles;
+    p->grid_ctas = v->cg * units;
     return HK_OK;
 }
 
@@ -261,8 +336,10 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
     const int64_t kk = p->K > 0 ? p->K : 8;
     const int64_t lda = p->K > 0 ? p->lda : p->ldc;
     const int64_t ldb = p->K > 0 ? p->ldb : p->ldc;
+    const Variant* v = p->variant;
+    const uint32_t b_rows = static_cast<uint32_t>(v->tile_n / v->cg);
     if ((s = encode_2d(&ta, a_ptr, p->K > 0 ? p->M : 1, kk, lda, hk::kTileK, hk::kCtaM, CU_TENSOR_MAP_SWIZZLE_128B, "A")) != HK_OK) return s;
-    if ((s = encode_2d(&tb, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, hk::kTileK, hk::kCtaN, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != HK_OK) return s;
+    if ((s = encode_2d(&tb, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, hk::kTileK, b_rows, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != HK_OK) return s;
     // the map covers N rounded down to a multiple of 8 (see the epilogue); at
     // least 8 columns so that it stays valid when N < 8 (then it is unused)
     const int64_t n_tma = p->N & ~int64_t(7);
@@ -277,16 +354,16 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(v->cg);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(p->grid_ctas, 1, 1);
     cfg.blockDim = dim3(hk::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = hk::kSmemBytes;
+    cfg.dynamicSmemBytes = v->smem_bytes;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, hk::gemm_bf16_pair_kernel, ta, tb, tc, g);
+    cfg.numAttrs = v->cg > 1 ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, v->fn, ta, tb, tc, g);
     if (e != cudaSuccess) return cuda_fail(HK_ERR_LAUNCH, "launching the GEMM kernel", e);
     return HK_OK;
 }
@@ -346,14 +423,16 @@ hk_status hk_gemm_plan_get_info(const hk_gemm_plan* p, hk_gemm_plan_info* info) 
     if (!p || !info) return fail(HK_ERR_INVALID_ARG, "NULL plan or info");
     std::memset(info, 0, sizeof *info);
     info->M = p->M; info->N = p->N; info->K = p->K;
-    info->tile_m = hk::kPairM; info->tile_n = hk::kTileN; info->tile_k = hk::kTileK;
-    info->stages = hk::kStages;
+    info->tile_m = p->variant->tile_m; info->tile_n = p->variant->tile_n; info->tile_k = hk::kTileK;
+    info->stages = p->variant->stages;
+    info->kernel = p->variant->id;
+    info->ctas_per_unit = p->variant->cg;
     info->num_tiles = p->params.num_tiles;
     info->grid_ctas = (p->M == 0 || p->N == 0) ? 0 : p->grid_ctas;
     info->group_m = p->params.group_m;
     info->split_k = 1;
     info->kernels_per_run = (p->M == 0 || p->N == 0) ? 0 : 1;
-    info->smem_bytes = hk::kSmemBytes;
+    info->smem_bytes = p->variant->smem_bytes;
     info->workspace_bytes = 0;
     return HK_OK;
 }

@@ -23,6 +23,15 @@ HK_ERR_TIMEOUT = 5
 HK_ERR_WORKSPACE = 6
 HK_ERR_CUDA = 7
 
+HK_KERNEL_AUTO = 0
+HK_KERNEL_PAIR_256x256 = 1
+HK_KERNEL_SINGLE_128x256 = 2
+HK_KERNEL_SINGLE_128x192 = 3
+HK_KERNEL_SINGLE_128x128 = 4
+HK_KERNEL_SINGLE_128x64 = 5
+KERNELS = (HK_KERNEL_PAIR_256x256, HK_KERNEL_SINGLE_128x256, HK_KERNEL_SINGLE_128x192,
+           HK_KERNEL_SINGLE_128x128, HK_KERNEL_SINGLE_128x64)
+
 HK_FLAG_NONE = 0x0
 HK_FLAG_FAULT_DROP_ARRIVE = 0x1
 
@@ -35,13 +44,14 @@ EXPORTED = (
 
 class hk_gemm_config(ctypes.Structure):
     _fields_ = [("group_m", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
-                ("split_k", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("split_k", ctypes.c_int32), ("kernel", ctypes.c_int32),
                 ("timeout_ns", ctypes.c_uint64), ("flags", ctypes.c_uint32),
                 ("reserved1", ctypes.c_uint32)]
 
 
 class hk_gemm_plan_info(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("kernel", ctypes.c_int32), ("ctas_per_unit", ctypes.c_int32),
                 ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32), ("tile_k", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("num_tiles", ctypes.c_int32),
                 ("grid_ctas", ctypes.c_int32), ("group_m", ctypes.c_int32),
@@ -167,12 +177,12 @@ class Plan:
     """A plan for one GEMM shape (wraps hk_gemm_plan_*)."""
 
     def __init__(self, M, N, K, lda=None, ldb=None, ldc=None, device=0, group_m=0, max_clusters=0,
-                 split_k=0, timeout_ns=0, flags=0):
+                 split_k=0, timeout_ns=0, flags=0, kernel=0):
         lib = load()
         self._lib = lib
         self.M, self.N, self.K = M, N, K
         cfg = hk_gemm_config(group_m=group_m, max_clusters=max_clusters, split_k=split_k,
-                             timeout_ns=timeout_ns, flags=flags)
+                             timeout_ns=timeout_ns, flags=flags, kernel=kernel)
         handle = ctypes.c_void_p()
         st = lib.hk_gemm_plan_create(ctypes.byref(handle), M, N, K, lda if lda is not None else K,
                                      ldb if ldb is not None else K, ldc if ldc is not None else N,

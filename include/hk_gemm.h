@@ -74,12 +74,22 @@ typedef enum hk_status {
  * HK_ERR_TIMEOUT through the device status word. No GPU fault is caused. */
 #define HK_FLAG_FAULT_DROP_ARRIVE 0x1u
 
+/* Kernel variants (hk_gemm_config.kernel). A "pair" kernel runs on clusters
+ * of two CTAs (tcgen05 cta_group::2) with 256-row output tiles; a "single"
+ * kernel runs one CTA per output tile of 128 rows and suits M <= 128. */
+#define HK_KERNEL_AUTO 0            /* pair 256x256 if M > 128, else the single kernel that keeps most SMs busy */
+#define HK_KERNEL_PAIR_256x256 1
+#define HK_KERNEL_SINGLE_128x256 2
+#define HK_KERNEL_SINGLE_128x192 3
+#define HK_KERNEL_SINGLE_128x128 4
+#define HK_KERNEL_SINGLE_128x64 5
+
 /* Tuning knobs of a plan. Zero in any field selects the default. */
 typedef struct hk_gemm_config {
-    int32_t group_m;        /* grouped rasterisation: height of a group in 256-row tiles (default 8) */
-    int32_t max_clusters;   /* cap on the persistent grid, in CTA pairs (default: all that fit) */
+    int32_t group_m;        /* grouped rasterisation: height of a group in output-tile rows (default 8) */
+    int32_t max_clusters;   /* cap on the persistent grid, in work units (CTA pairs or CTAs; default: all that fit) */
     int32_t split_k;        /* K-split factor (default: chosen by the plan; 1 = none) */
-    int32_t reserved0;
+    int32_t kernel;         /* HK_KERNEL_* (default HK_KERNEL_AUTO) */
     uint64_t timeout_ns;    /* limit of each bounded wait in the kernel (default 1 s) */
     uint32_t flags;         /* HK_FLAG_* */
     uint32_t reserved1;
@@ -88,10 +98,12 @@ typedef struct hk_gemm_config {
 /* What a plan chose (for logging and benchmarks). */
 typedef struct hk_gemm_plan_info {
     int64_t M, N, K;
-    int32_t tile_m, tile_n, tile_k;   /* output tile of one CTA pair and K step */
+    int32_t kernel;                   /* HK_KERNEL_* actually used */
+    int32_t ctas_per_unit;            /* 2 for a pair kernel, 1 for a single-CTA kernel */
+    int32_t tile_m, tile_n, tile_k;   /* output tile of one work unit and K step */
     int32_t stages;                   /* depth of the shared-memory ring */
     int32_t num_tiles;                /* output tiles (times split_k) */
-    int32_t grid_ctas;                /* CTAs launched (2 per cluster) */
+    int32_t grid_ctas;                /* CTAs launched */
     int32_t group_m;
     int32_t split_k;
     int32_t kernels_per_run;          /* kernel launches one run enqueues */

@@ -233,3 +233,60 @@ def test_workload_projection(hk):
 
 def test_workload_skinny(hk):
     _check_workload(hk, "skinny_128x28672x8192")
+
+
+# ------------------------------------------------------ kernel variants --
+
+VARIANT_SHAPES = [(1, 1, 1), (100, 300, 70), (128, 1000, 520), (257, 130, 64), (700, 452, 1000)]
+
+
+def run_plan(hk, A_bits, B_bits, **cfg):
+    import torch
+    M, K = A_bits.shape
+    N = B_bits.shape[0]
+    kp = (-K) % 8
+    A, Astore = to_device(A_bits, cols_pad=kp)
+    B, Bstore = to_device(B_bits, cols_pad=kp + 8)
+    ldc = N + ((-N) % 8) + 8
+    C, Cstore = to_device(np.full((M, N), SENTINEL, dtype=np.uint16), rows_pad=2, cols_pad=ldc - N,
+                          fill=SENTINEL)
+    plan = hk.Plan(M, N, K, lda=Astore.stride(0), ldb=Bstore.stride(0), ldc=Cstore.stride(0), **cfg)
+    info = plan.info()
+    st = plan.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), 0, 0,
+                      int(torch.cuda.current_stream().cuda_stream))
+    assert st == hk.HK_OK, hk.hk_gemm_last_error_string()
+    torch.cuda.synchronize()
+    assert plan.device_status() == hk.HK_OK
+    plan.close()
+    full = to_host(Cstore)
+    guard = full.copy()
+    guard[:M, :N] = SENTINEL
+    assert np.all(guard == SENTINEL), "a write landed outside C"
+    return full[:M, :N], info
+
+
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("M,N,K", VARIANT_SHAPES)
+def test_kernel_variants_integer_bitexact(hk, kernel, M, N, K):
+    A = synth.int_bf16(M, K, 1200 + M)
+    B = synth.int_bf16(N, K, 2200 + N)
+    got, info = run_plan(hk, A, B, kernel=kernel, max_clusters=3)
+    assert info["kernel"] == kernel
+    assert_bitexact(got, oracle.gemm(A, B), f"kernel {kernel} int {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("kernel", [2, 3, 4, 5])
+def test_kernel_variants_normal(hk, kernel):
+    M, N, K = 200, 777, 1500
+    A = synth.normal_bf16(M, K, 31)
+    B = synth.normal_bf16(N, K, 32)
+    got, info = run_plan(hk, A, B, kernel=kernel)
+    assert_close(got, oracle.gemm(A, B), K, 1, 1, f"kernel {kernel}")
+
+
+def test_automatic_kernel_choice(hk):
+    assert hk.Plan(128, 28672, 8192).info()["kernel"] == 3      # 150 tiles of 128x192 ~ one per SM
+    assert hk.Plan(8192, 8192, 8192).info()["kernel"] == 1
+    assert hk.Plan(129, 4096, 4096).info()["kernel"] == 1
+    small = hk.Plan(64, 1024, 1024).info()
+    assert small["kernel"] == 5 and small["ctas_per_unit"] == 1  # 16 tiles: narrowest tiles spread widest
