@@ -295,35 +295,61 @@ def run_hk(args, w):
         clocks = sampler.summary(t_host0, t_host1)
     elapsed_max = max_over_ranks(world, elapsed_ms)
 
-    # ---- end to end: pinned host inputs -> device -> GEMM -> host result
+    # ---- end to end: pinned host inputs -> device -> GEMM -> host result.
+    # Steps are independent GEMMs, so they are pipelined on three streams:
+    # the H2D copy of step i+1 and the D2H copy of step i-1 overlap the GEMM
+    # of step i; device operands are double-buffered.
     A_h = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
     B_h = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    C_h = torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory()
-    e2e_steps = max(3, min(args.steps, 20))
+    C_h = [torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    A_d = [A, torch.empty_like(A)]
+    B_d = [B, torch.empty_like(B)]
+    C_d = [C, torch.empty_like(C)]
+    s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    e2e_steps = max(4, min(args.steps, 30))
 
-    def e2e_step():
-        A.copy_(A_h, non_blocking=True)
-        B.copy_(B_h, non_blocking=True)
-        step()
-        C_h.copy_(C, non_blocking=True)
+    def e2e_run(n):
+        h2d_done = [torch.cuda.Event() for _ in range(2)]
+        comp_done = [None, None]
+        d2h_done = [None, None]
+        for i in range(n):
+            k = i & 1
+            if comp_done[k] is not None:
+                s_h2d.wait_event(comp_done[k])      # the GEMM that read slot k is finished
+            with torch.cuda.stream(s_h2d):
+                A_d[k].copy_(A_h, non_blocking=True)
+                B_d[k].copy_(B_h, non_blocking=True)
+                h2d_done[k].record(s_h2d)
+            stream.wait_event(h2d_done[k])
+            if d2h_done[k] is not None:
+                stream.wait_event(d2h_done[k])      # C of slot k has been copied out
+            st = hk.hk_gemm_bf16(A_d[k].data_ptr(), B_d[k].data_ptr(), C_d[k].data_ptr(), w.M, w.N, w.K, w.K,
+                                 w.K, w.N, sh)
+            if st != hk.HK_OK:
+                raise hk.HKError(st, "hk_gemm_bf16")
+            comp_done[k] = torch.cuda.Event()
+            comp_done[k].record(stream)
+            s_d2h.wait_event(comp_done[k])
+            with torch.cuda.stream(s_d2h):
+                C_h[k].copy_(C_d[k], non_blocking=True)
+                d2h_done[k] = torch.cuda.Event()
+                d2h_done[k].record(s_d2h)
 
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
+    e2e_run(2)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
+    e0.record(s_h2d)
+    e2e_run(e2e_steps)
+    e1.record(s_d2h)
     torch.cuda.synchronize(dev)
     barrier(world)
     e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
-    if not np.array_equal(C_h.view(torch.int16).numpy()[0, :16].view(np.uint16),
+    if not np.array_equal(C_h[(e2e_steps - 1) & 1].view(torch.int16).numpy()[0, :16].view(np.uint16),
                           C.view(torch.int16).cpu().numpy()[0, :16].view(np.uint16)):
         raise RuntimeError("end-to-end result differs from the device result")
+    if hk.hk_gemm_last_device_status(local) != hk.HK_OK:
+        raise RuntimeError("device status after the end-to-end run: " + hk.hk_gemm_last_error_string())
 
     if rank != 0:
         if world > 1:
@@ -371,7 +397,8 @@ def run_hk(args, w):
                      "source_digest": digest},
         "e2e": {"value": flops * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": int(A_h.numel() * 2 + B_h.numel() * 2),
-                "d2h_bytes_per_step": int(C_h.numel() * 2), "steps": e2e_steps},
+                "d2h_bytes_per_step": int(C_h[0].numel() * 2), "steps": e2e_steps,
+                "pipelined": "H2D(i+1) | GEMM(i) | D2H(i-1) on three streams"},
         "gpu_launches": args.steps * int(info["kernels_per_run"]),
         "clocks": clocks,
     }
