@@ -83,7 +83,6 @@ struct Geometry {
     static constexpr int kAccCols = kTileN;                 // TMEM columns per accumulator
     static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);
     static_assert(kTmemCols <= 512, "TMEM");
-    static constexpr uint32_t kExpectBytes = kCG * kStageBytes;   // bytes landing per stage in the cluster
     static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, kTileN);
 };
 
@@ -100,7 +99,12 @@ struct GemmParams {
     int32_t tiles_m, tiles_n;     // output tiles along M and N
     int32_t k_blocks;             // ceil(K / 64)
     int32_t num_tiles;
+    int32_t splits;               // K splits per tile (1: none); work units = num_tiles * splits
     int32_t group_m;
+    int32_t a_rows;               // rows of A each CTA loads per stage (128, or M rounded up to 8 if smaller)
+    uint32_t expect_bytes;        // bytes that land per stage in the cluster (both CTAs of a pair)
+    int64_t n_pad;                // split K: row stride of the partial matrices (tiles_n * tile width)
+    float* partials;              // split K: fp32 partial matrices P[split][M][n_pad]
     int32_t n_tma;                // columns [0, n_tma) of C are written by TMA stores (n_tma = N & ~7)
     int64_t ldc;                  // leading dimension of C (elements), for the ragged tail columns
     uint16_t* c_ptr;              // C, for the columns [n_tma, N) a TMA store cannot bound exactly
@@ -174,6 +178,12 @@ __device__ __forceinline__ bool wait_bounded_warp(const GemmParams& p, uint32_t 
     return ok != 0;
 }
 
+// K blocks [begin, end) of split `s` of `splits` (as even as possible).
+__device__ __forceinline__ void split_range(const GemmParams& p, int s, int& begin, int& end) {
+    begin = static_cast<int>((static_cast<int64_t>(s) * p.k_blocks) / p.splits);
+    end = static_cast<int>((static_cast<int64_t>(s + 1) * p.k_blocks) / p.splits);
+}
+
 __device__ __forceinline__ void drain_after_abort() {
     // let copies and MMAs that were already issued land before teardown
     for (int i = 0; i < 200; ++i) __nanosleep(1000);
@@ -239,12 +249,15 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             int stage = 0;
             uint32_t phase = 0;
             bool dropped = false;
-            for (int t = unit; t < p.num_tiles && !abort_seen; t += num_units) {
-                int tm, tn;
+            const int total = p.num_tiles * p.splits;
+            for (int u = unit; u < total && !abort_seen; u += num_units) {
+                const int t = u / p.splits;
+                int tm, tn, kb_begin, kb_end;
                 tile_coords(p, t, tm, tn);
+                split_range(p, u - t * p.splits, kb_begin, kb_end);
                 const int a_row = tm * G::kTileM + static_cast<int>(rank) * kCtaM;
                 const int b_row = tn * G::kTileN + static_cast<int>(rank) * G::kBRows;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bounded(p, empty_bar(stage), phase ^ 1u, kErrProducerEmpty)) {
                         abort_seen = true;
                         break;
@@ -253,7 +266,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         if ((p.flags & kFlagDropArrive) && !dropped) {
                             dropped = true;   // test-only fault: withhold this arrival
                         } else {
-                            mbar_arrive_expect_tx(full_bar(stage), G::kExpectBytes);
+                            mbar_arrive_expect_tx(full_bar(stage), p.expect_bytes);
                         }
                     }
                     const uint32_t a_dst = base + G::kOffA + stage * kABytes;
@@ -280,7 +293,11 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             int stage = 0;
             uint32_t phase = 0;
             int local = 0;
-            for (int t = unit; t < p.num_tiles && !abort_seen; t += num_units, ++local) {
+            const int total = p.num_tiles * p.splits;
+            for (int u = unit; u < total && !abort_seen; u += num_units, ++local) {
+                const int t = u / p.splits;
+                int kb_begin, kb_end;
+                split_range(p, u - t * p.splits, kb_begin, kb_end);
                 const int buf = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
                 const bool acc_free = kCG == 2
@@ -292,7 +309,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * G::kAccCols;
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bounded(p, full_bar(stage), phase, kErrMmaFull)) {
                         abort_seen = true;
                         break;
@@ -303,7 +320,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
 #pragma unroll
                     for (int k = 0; k < kTileK / kMmaK; ++k) {
                         // advance 16 bf16 = 32 bytes along K inside the swizzle atom
-                        const uint32_t acc = (kb | k) != 0 ? 1u : 0u;
+                        const uint32_t acc = (kb != kb_begin || k != 0) ? 1u : 0u;
                         if constexpr (kCG == 2)
                             mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, G::kIdesc, acc);
                         else
@@ -329,8 +346,47 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         const uint32_t epi = base + G::kOffEpi + (warp - 2) * 2 * kEpiBufBytes;
         const uint32_t swz = (lane >> 1) & 3u;         // 64-byte swizzle of this lane's row
         uint32_t chunk_count = 0;
+
+        // Round 32 fp32 values of this lane's row to bf16 and write them to C
+        // at (row0 + lane, col0): staged through 64-byte-swizzled shared
+        // memory and written by a TMA store; when N is not a multiple of 8
+        // the last (< 8) columns are written with plain stores, since a TMA
+        // store bounds the innermost dimension only to 16-byte granules.
+        auto store_chunk = [&](const uint32_t (&v)[32], int row0, int col0) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2_rn(v[2 * i], v[2 * i + 1]);
+            const uint32_t sbuf = epi + (chunk_count & 1u) * kEpiBufBytes;
+            if (lane == 0) bulk_wait_group_read<1>();   // the store that last used sbuf has read it
+            __syncwarp();
+            const uint32_t row_addr = sbuf + lane * 64u;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ swz) << 4), w[4 * j], w[4 * j + 1],
+                             w[4 * j + 2], w[4 * j + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && row0 < p.M && col0 < p.n_tma) tma_store_2d(&tmap_c, sbuf, col0, row0);
+            if (lane == 0) bulk_commit_group();
+            if (p.N > p.n_tma && col0 + kEpiCols > p.n_tma && col0 < p.N) {
+                const int row = row0 + static_cast<int>(lane);
+                if (row < p.M) {
+                    uint16_t* const crow = p.c_ptr + static_cast<int64_t>(row) * p.ldc;
+#pragma unroll
+                    for (int e = 0; e < kEpiCols; ++e) {   // static indices keep w[] in registers
+                        const int j = col0 + e;
+                        if (j >= p.n_tma && j < p.N)
+                            crow[j] = static_cast<uint16_t>((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
+                    }
+                }
+            }
+            ++chunk_count;
+        };
+
         int local = 0;
-        for (int t = unit; t < p.num_tiles; t += num_units, ++local) {
+        const int total = p.num_tiles * p.splits;
+        for (int u = unit; u < total; u += num_units, ++local) {
+            const int t = u / p.splits;
             int tm, tn;
             tile_coords(p, t, tm, tn);
             const int buf = local & 1;
@@ -340,8 +396,14 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                 break;
             }
             tc_fence_after_sync();
-            const int row0 = tm * G::kTileM + static_cast<int>(rank) * kCtaM + static_cast<int>(q) * 32;
+            const int tile_row = static_cast<int>(rank) * kCtaM + static_cast<int>(q) * 32;   // in the tile
+            const int row0 = tm * G::kTileM + tile_row;
+            const int row = row0 + static_cast<int>(lane);
             const uint32_t t_row = tmem_base + ((q * 32u) << 16) + buf * G::kAccCols;
+            // split K: this lane's row of this split's fp32 partial matrix
+            const int split = u - t * p.splits;
+            float* const part_row =
+                p.partials + (static_cast<int64_t>(split) * p.M + row) * p.n_pad + tn * G::kTileN;
 #pragma unroll 1
             for (int c = 0; c < G::kTileN / kEpiCols; ++c) {
                 uint32_t v[32];
@@ -361,41 +423,15 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         else mbar_arrive(acc_empty_bar(buf));
                     }
                 }
-                uint32_t w[16];
+                if (p.splits == 1) {
+                    store_chunk(v, row0, tn * G::kTileN + c * kEpiCols);
+                } else if (row < p.M) {
+                    float4* dst = reinterpret_cast<float4*>(part_row + c * kEpiCols);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2_rn(v[2 * i], v[2 * i + 1]);
-
-                const uint32_t sbuf = epi + (chunk_count & 1u) * kEpiBufBytes;
-                if (lane == 0) bulk_wait_group_read<1>();   // the store that last used sbuf has read it
-                __syncwarp();
-                const uint32_t row_addr = sbuf + lane * 64u;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ swz) << 4), w[4 * j], w[4 * j + 1],
-                                 w[4 * j + 2], w[4 * j + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                const int col0 = tn * G::kTileN + c * kEpiCols;
-                if (lane == 0 && row0 < p.M && col0 < p.n_tma) {
-                    tma_store_2d(&tmap_c, sbuf, col0, row0);
+                    for (int j = 0; j < 8; ++j)
+                        dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
                 }
-                if (lane == 0) bulk_commit_group();
-                // A TMA store bounds the innermost dimension only to 16-byte
-                // granules, so when N is not a multiple of 8 the last (< 8)
-                // columns are written with plain stores from the registers.
-                if (p.N > p.n_tma && col0 + kEpiCols > p.n_tma && col0 < p.N) {
-                    const int row = row0 + static_cast<int>(lane);
-                    if (row < p.M) {
-                        uint16_t* const crow = p.c_ptr + static_cast<int64_t>(row) * p.ldc;
-#pragma unroll
-                        for (int e = 0; e < kEpiCols; ++e) {   // static indices keep w[] in registers
-                            const int j = col0 + e;
-                            if (j >= p.n_tma && j < p.N)
-                                crow[j] = static_cast<uint16_t>((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
-                        }
-                    }
-                }
-                ++chunk_count;
             }
         }
         if (lane == 0) bulk_wait_group<0>();
@@ -410,6 +446,43 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         tc_fence_after_sync();
         if constexpr (kCG == 2) tmem_dealloc_pair(tmem_base, G::kTmemCols);
         else tmem_dealloc_one(tmem_base, G::kTmemCols);
+    }
+}
+
+// Split K, second pass: C = bf16_rne(P[0] + P[1] + ... + P[splits-1]),
+// summed in this fixed order (so the result does not depend on which split
+// finished first). Each thread handles 8 consecutive columns of one row.
+__global__ void __launch_bounds__(256)
+splitk_reduce_kernel(const float* __restrict__ partials, int32_t splits, int32_t M, int32_t N, int64_t n_pad,
+                     uint16_t* __restrict__ C, int64_t ldc) {
+    const int64_t groups_per_row = (N + 7) / 8;
+    const int64_t total = static_cast<int64_t>(M) * groups_per_row;
+    const int64_t split_stride = static_cast<int64_t>(M) * n_pad;
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row = g / groups_per_row;
+        const int col = static_cast<int>(g - row * groups_per_row) * 8;
+        const float4* src = reinterpret_cast<const float4*>(partials + row * n_pad + col);
+        float4 a = __ldcs(src), b = __ldcs(src + 1);
+#pragma unroll 4
+        for (int sp = 1; sp < splits; ++sp) {
+            const float4* q = reinterpret_cast<const float4*>(partials + sp * split_stride + row * n_pad + col);
+            const float4 x = __ldcs(q), y = __ldcs(q + 1);
+            a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+            b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+        }
+        const uint32_t w0 = pack_bf16x2_rn(__float_as_uint(a.x), __float_as_uint(a.y));
+        const uint32_t w1 = pack_bf16x2_rn(__float_as_uint(a.z), __float_as_uint(a.w));
+        const uint32_t w2 = pack_bf16x2_rn(__float_as_uint(b.x), __float_as_uint(b.y));
+        const uint32_t w3 = pack_bf16x2_rn(__float_as_uint(b.z), __float_as_uint(b.w));
+        uint16_t* dst = C + row * ldc + col;
+        if (col + 8 <= N) {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(w0, w1, w2, w3);   // 16-byte aligned: ldc, col % 8 == 0
+        } else {
+            const uint32_t w[4] = {w0, w1, w2, w3};
+            for (int e = 0; col + e < N; ++e)
+                dst[e] = static_cast<uint16_t>((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
+        }
     }
 }
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -172,10 +173,19 @@ hk_status encode_2d(CUtensorMap* map, const void* ptr, int64_t rows, int64_t col
     return HK_OK;
 }
 
+// Launch ids are unique in the process: the kernel uses them to recognise
+// its own abort flag and its own split-K arrival counters.
+std::atomic<uint32_t> g_next_launch{1};
+
+uint32_t next_launch_id() {
+    uint32_t id = g_next_launch.fetch_add(1, std::memory_order_relaxed);
+    if (id == 0) id = g_next_launch.fetch_add(1, std::memory_order_relaxed);
+    return id;
+}
+
 // Per-device context of the one-shot entry point: its status word.
 struct StatusWord {
     uint32_t* dev = nullptr;                 // [0] error bits, [1] aborted launch id
-    std::atomic<uint32_t> next_launch{1};
 };
 
 std::mutex g_ctx_mutex;
@@ -248,6 +258,8 @@ struct hk_gemm_plan {
     int64_t M, N, K, lda, ldb, ldc;
     int device;
     const Variant* variant;
+    int sm_count;
+    size_t ws_bytes;            // split K: fp32 partial matrices [splits][M][n_pad]
     hk::GemmParams params;      // everything but status/launch id
     int grid_ctas;
     hk_gemm_config cfg;
@@ -265,40 +277,93 @@ double slot_use(int64_t tiles, int64_t slots) {
     return double(tiles) / double(ceil_div(tiles, slots) * slots);
 }
 
-// Kernel choice: the CTA pair (256-row tiles) whenever there are more than
-// 128 rows; otherwise a single-CTA kernel (128-row tiles) with the tile width
-// that keeps the most SMs busy (ties go to the wider tile, which re-reads A
-// fewer times).
-const Variant* choose_variant(int64_t M, int64_t N, const DeviceInfo* di) {
-    if (M > hk::kCtaM) return &kVariants[0];
-    const Variant* best = nullptr;
-    double best_use = -1.0;
-    for (int i = 1; i < kNumVariants; ++i) {
+// Rows of A one CTA loads per stage: 128, or M rounded up to 8 when M is
+// smaller (single-CTA kernels); rows of the smem tile beyond them only feed
+// output rows that are never stored.
+int a_rows_for(const Variant& v, int64_t M) {
+    if (v.cg == 2 || M >= hk::kCtaM) return hk::kCtaM;
+    return static_cast<int>(std::max<int64_t>(8, ceil_div(M, 8) * 8));
+}
+
+// Kernel choice by a small time model. The CTA pair (256-row tiles) serves
+// M > 128, single-CTA kernels (128-row tiles, four widths) M <= 128. K is
+// split only when one wave of tiles leaves work-unit slots idle and a
+// workspace may be used. Estimated time of a candidate = the largest of
+//   streaming: waves × bytes one CTA moves per unit ÷ per-SM copy rate,
+//   HBM:       unique bytes (B, A, C, and split partials written + read) ÷ HBM rate,
+//   tensor:    waves × K-steps per unit × time of one K-step,
+// plus a second-launch overhead when K is split.
+constexpr int kMaxSplits = 16;
+constexpr int kMinKBlocksPerSplit = 8;
+constexpr double kSmBytesPerUs = 65e3;       // one SM's sustained TMA rate from HBM (measured, bytes/µs)
+constexpr double kHbmBytesPerUs = 6.7e6;     // HBM copy rate (bytes/µs)
+constexpr double kKStepUsPair = 0.27;        // 256x256x64 per pair (4 tcgen05.mma)
+constexpr double kSplitOverheadUs = 3.0;
+
+double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int64_t slots, int splits) {
+    const int64_t tiles = ceil_div(M, v.tile_m) * ceil_div(N, v.tile_n);
+    const int64_t units = tiles * splits;
+    const double waves = double(ceil_div(units, slots));
+    const double kb = double(ceil_div(ceil_div(K, hk::kTileK), splits));
+    const double cta_bytes = double(a_rows_for(v, M) + v.tile_n / v.cg) * hk::kTileK * 2 * kb;
+    const double t_stream = waves * cta_bytes / kSmBytesPerUs;
+    const double n_pad = double(ceil_div(N, v.tile_n) * v.tile_n);
+    const double hbm = 2.0 * (N * K + M * K + M * N) + (splits > 1 ? 2.0 * 4.0 * splits * M * n_pad : 0.0);
+    const double t_hbm = hbm / kHbmBytesPerUs;
+    const double t_mma = waves * kb * kKStepUsPair * (double(v.tile_n) / 256.0) * (v.cg == 2 ? 1.0 : 1.0);
+    return std::max(t_stream, std::max(t_hbm, t_mma)) + (splits > 1 ? kSplitOverheadUs : 0.0);
+}
+
+void choose_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo* di, int max_units_cap, bool allow_split,
+                 int forced_kernel, int forced_splits, const Variant** out_v, int* out_s) {
+    const Variant* best_v = nullptr;
+    int best_s = 1;
+    double best_t = 0.0;
+    const int64_t k_blocks = ceil_div(K, hk::kTileK);
+    for (int i = 0; i < kNumVariants; ++i) {
         const Variant& v = kVariants[i];
-        const double use = slot_use(ceil_div(M, v.tile_m) * ceil_div(N, v.tile_n), di->max_units[i]);
-        if (use > best_use + 1e-9) {
-            best_use = use;
-            best = &v;
+        if (forced_kernel != HK_KERNEL_AUTO ? v.id != forced_kernel : ((M > hk::kCtaM) != (v.cg == 2))) continue;
+        int64_t slots = di->max_units[i];
+        if (max_units_cap > 0 && max_units_cap < slots) slots = max_units_cap;
+        const int64_t tiles = ceil_div(M, v.tile_m) * ceil_div(N, v.tile_n);
+        int s_lo = 1, s_hi = 1;
+        if (forced_splits > 0) {
+            s_lo = s_hi = forced_splits;
+        } else if (allow_split && tiles < slots && k_blocks >= 2 * kMinKBlocksPerSplit) {
+            s_hi = static_cast<int>(std::min<int64_t>(kMaxSplits, k_blocks / kMinKBlocksPerSplit));
+        }
+        for (int sp = s_lo; sp <= s_hi; ++sp) {
+            const double t = estimate_us(v, M, N, K, slots, sp);
+            if (!best_v || t < best_t * 0.98) {   // a candidate must win by 2 % (earlier = wider / fewer splits)
+                best_v = &v;
+                best_s = sp;
+                best_t = t;
+            }
         }
     }
-    return best ? best : &kVariants[0];
+    *out_v = best_v ? best_v : &kVariants[0];
+    *out_s = best_v ? best_s : 1;
 }
 
 hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                    int device, const hk_gemm_config* config, const DeviceInfo* di) {
+                    int device, const hk_gemm_config* config, const DeviceInfo* di, bool allow_split) {
     p->M = M; p->N = N; p->K = K; p->lda = lda; p->ldb = ldb; p->ldc = ldc;
     p->device = device;
     std::memset(&p->cfg, 0, sizeof p->cfg);
     if (config) p->cfg = *config;
-    if (p->cfg.split_k > 1) return fail(HK_ERR_INVALID_ARG, "split_k > 1 is not available for this shape");
-    if (p->cfg.group_m < 0 || p->cfg.max_clusters < 0) return fail(HK_ERR_INVALID_ARG, "negative config field");
-    const Variant* v = nullptr;
-    if (p->cfg.kernel == HK_KERNEL_AUTO) {
-        v = choose_variant(M, N, di);
-    } else if (!(v = find_variant(p->cfg.kernel))) {
+    if (p->cfg.group_m < 0 || p->cfg.max_clusters < 0 || p->cfg.split_k < 0)
+        return fail(HK_ERR_INVALID_ARG, "negative config field");
+    if (p->cfg.kernel != HK_KERNEL_AUTO && !find_variant(p->cfg.kernel))
         return fail(HK_ERR_INVALID_ARG, "unknown kernel id %d", (int)p->cfg.kernel);
-    }
+    const int64_t k_blocks_all = ceil_div(K, hk::kTileK);
+    if (p->cfg.split_k > 1 && (p->cfg.split_k > k_blocks_all || p->cfg.split_k > 4096))
+        return fail(HK_ERR_INVALID_ARG, "split_k %d exceeds the %lld K blocks of 64", (int)p->cfg.split_k,
+                    (long long)k_blocks_all);
+    const Variant* v = nullptr;
+    int splits = 1;
+    choose_plan(M, N, K, di, p->cfg.max_clusters, allow_split, p->cfg.kernel, p->cfg.split_k, &v, &splits);
     p->variant = v;
+    p->sm_count = di->sm_count;
     const int vi = static_cast<int>(v - kVariants);
     const int group_m = p->cfg.group_m > 0 ? p->cfg.group_m : kDefaultGroupM;
     hk::GemmParams& g = p->params;
@@ -312,6 +377,12 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     const int64_t tiles = int64_t(g.tiles_m) * g.tiles_n;
     if (tiles > (int64_t(1) << 30)) return fail(HK_ERR_INVALID_ARG, "too many output tiles");
     g.num_tiles = static_cast<int32_t>(tiles);
+    g.splits = splits;
+    if (int64_t(splits) * tiles > (int64_t(1) << 30)) return fail(HK_ERR_INVALID_ARG, "too many work units");
+    g.a_rows = a_rows_for(*v, M);
+    g.expect_bytes = static_cast<uint32_t>(v->cg * (g.a_rows + v->tile_n / v->cg) * hk::kTileK * 2);
+    g.n_pad = int64_t(g.tiles_n) * v->tile_n;
+    p->ws_bytes = splits > 1 ? static_cast<size_t>(splits) * static_cast<size_t>(M) * g.n_pad * 4 : 0;
     g.group_m = group_m;
     g.n_tma = static_cast<int32_t>(N & ~int64_t(7));
     g.ldc = ldc;
@@ -320,12 +391,13 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     int units = di->max_units[vi];
     if (units <= 0) return fail(HK_ERR_UNSUPPORTED_DEVICE, "kernel %s does not fit on the device", v->name);
     if (p->cfg.max_clusters > 0 && p->cfg.max_clusters < units) units = p->cfg.max_clusters;
-    if (units > g.num_tiles) units = g.num_tiles;
+    if (units > g.num_tiles * splits) units = g.num_tiles * splits;
     p->grid_ctas = v->cg * units;
     return HK_OK;
 }
 
-hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const void* B, void* C, cudaStream_t stream) {
+hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const void* B, void* C, void* workspace,
+                 cudaStream_t stream) {
     if (p->M == 0 || p->N == 0) return HK_OK;
     hk_status s = get_encoder();
     if (s != HK_OK) return s;
@@ -338,7 +410,8 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
     const int64_t ldb = p->K > 0 ? p->ldb : p->ldc;
     const Variant* v = p->variant;
     const uint32_t b_rows = static_cast<uint32_t>(v->tile_n / v->cg);
-    if ((s = encode_2d(&ta, a_ptr, p->K > 0 ? p->M : 1, kk, lda, hk::kTileK, hk::kCtaM, CU_TENSOR_MAP_SWIZZLE_128B, "A")) != HK_OK) return s;
+    const uint32_t a_box_rows = static_cast<uint32_t>(p->params.a_rows);
+    if ((s = encode_2d(&ta, a_ptr, p->K > 0 ? p->M : 1, kk, lda, hk::kTileK, a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B, "A")) != HK_OK) return s;
     if ((s = encode_2d(&tb, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, hk::kTileK, b_rows, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != HK_OK) return s;
     // the map covers N rounded down to a multiple of 8 (see the epilogue); at
     // least 8 columns so that it stays valid when N < 8 (then it is unused)
@@ -348,8 +421,8 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
     hk::GemmParams g = p->params;
     g.c_ptr = static_cast<uint16_t*>(C);
     g.status = sw->dev;
-    g.launch_id = sw->next_launch.fetch_add(1, std::memory_order_relaxed);
-    if (g.launch_id == 0) g.launch_id = sw->next_launch.fetch_add(1, std::memory_order_relaxed);
+    g.launch_id = next_launch_id();
+    if (g.splits > 1) g.partials = static_cast<float*>(workspace);
 
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -365,6 +438,14 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
     cfg.numAttrs = v->cg > 1 ? 1 : 0;
     cudaError_t e = cudaLaunchKernelEx(&cfg, v->fn, ta, tb, tc, g);
     if (e != cudaSuccess) return cuda_fail(HK_ERR_LAUNCH, "launching the GEMM kernel", e);
+    if (g.splits > 1) {
+        const int64_t groups = p->M * ceil_div(p->N, 8);
+        const int64_t blocks = std::min<int64_t>(ceil_div(groups, 256), int64_t(p->sm_count) * 8);
+        hk::splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            g.partials, g.splits, g.M, g.N, g.n_pad, g.c_ptr, g.ldc);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(HK_ERR_LAUNCH, "launching the split-K reduction", e);
+    }
     return HK_OK;
 }
 
@@ -398,7 +479,7 @@ hk_status hk_gemm_plan_create(hk_gemm_plan** out, int64_t M, int64_t N, int64_t 
     if ((s = device_info(device, &di)) != HK_OK) return s;
     hk_gemm_plan* p = new (std::nothrow) hk_gemm_plan();
     if (!p) return fail(HK_ERR_INVALID_ARG, "out of host memory");
-    if ((s = fill_plan(p, M, N, K, lda, ldb, ldc, device, config, di)) != HK_OK) {
+    if ((s = fill_plan(p, M, N, K, lda, ldb, ldc, device, config, di, true)) != HK_OK) {
         delete p;
         return s;
     }
@@ -414,10 +495,7 @@ hk_status hk_gemm_plan_create(hk_gemm_plan** out, int64_t M, int64_t N, int64_t 
     return HK_OK;
 }
 
-size_t hk_gemm_plan_workspace_size(const hk_gemm_plan* plan) {
-    (void)plan;
-    return 0;
-}
+size_t hk_gemm_plan_workspace_size(const hk_gemm_plan* plan) { return plan ? plan->ws_bytes : 0; }
 
 hk_status hk_gemm_plan_get_info(const hk_gemm_plan* p, hk_gemm_plan_info* info) {
     if (!p || !info) return fail(HK_ERR_INVALID_ARG, "NULL plan or info");
@@ -430,22 +508,28 @@ hk_status hk_gemm_plan_get_info(const hk_gemm_plan* p, hk_gemm_plan_info* info) 
     info->num_tiles = p->params.num_tiles;
     info->grid_ctas = (p->M == 0 || p->N == 0) ? 0 : p->grid_ctas;
     info->group_m = p->params.group_m;
-    info->split_k = 1;
-    info->kernels_per_run = (p->M == 0 || p->N == 0) ? 0 : 1;
+    info->split_k = p->params.splits;
+    info->kernels_per_run = (p->M == 0 || p->N == 0) ? 0 : (p->params.splits > 1 ? 2 : 1);
     info->smem_bytes = p->variant->smem_bytes;
-    info->workspace_bytes = 0;
+    info->workspace_bytes = p->ws_bytes;
     return HK_OK;
 }
 
 hk_status hk_gemm_plan_run(const hk_gemm_plan* p, const void* A, const void* B, void* C, void* workspace,
                            size_t workspace_bytes, void* stream) {
-    (void)workspace; (void)workspace_bytes;
     if (!p) return fail(HK_ERR_INVALID_ARG, "NULL plan");
     if (p->M == 0 || p->N == 0) return HK_OK;
     hk_status s = check_pointers(A, B, C, p->K);
     if (s != HK_OK) return s;
+    if (p->ws_bytes > 0) {
+        if (!workspace || workspace_bytes < p->ws_bytes)
+            return fail(HK_ERR_WORKSPACE, "the plan needs %zu bytes of workspace, %zu given", p->ws_bytes,
+                        workspace ? workspace_bytes : size_t(0));
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+            return fail(HK_ERR_WORKSPACE, "the workspace must be 256-byte aligned");
+    }
     DeviceGuard guard(p->device);
-    return launch(p, const_cast<StatusWord*>(&p->status), A, B, C, static_cast<cudaStream_t>(stream));
+    return launch(p, const_cast<StatusWord*>(&p->status), A, B, C, workspace, static_cast<cudaStream_t>(stream));
 }
 
 hk_status hk_gemm_plan_device_status(hk_gemm_plan* p) {
@@ -488,9 +572,9 @@ hk_status hk_gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t
         sw = g_ctx[device];
     }
     hk_gemm_plan plan;
-    if ((s = fill_plan(&plan, M, N, K, lda, ldb, ldc, device, nullptr, di)) != HK_OK) return s;
+    if ((s = fill_plan(&plan, M, N, K, lda, ldb, ldc, device, nullptr, di, false)) != HK_OK) return s;
     plan.owns_status = false;
-    return launch(&plan, sw, A, B, C, static_cast<cudaStream_t>(stream));
+    return launch(&plan, sw, A, B, C, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 hk_status hk_gemm_last_device_status(int device) {

@@ -207,8 +207,17 @@ class Plan:
         return self._lib.hk_gemm_plan_run(self._h, A, B, C, workspace, workspace_bytes, stream)
 
     def run(self, A, B, C, workspace=None, stream=None):
-        ws = 0 if workspace is None else workspace.data_ptr()
-        wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        """Run on torch tensors. Without an explicit workspace, one is
+        allocated once (through torch) and kept with the plan."""
+        import torch
+        if workspace is None and self.workspace_size > 0:
+            if getattr(self, "_ws", None) is None:
+                self._ws = torch.empty(self.workspace_size + 256, dtype=torch.uint8, device=A.device)
+            ws = (self._ws.data_ptr() + 255) & ~255
+            wsb = self.workspace_size
+        else:
+            ws = 0 if workspace is None else workspace.data_ptr()
+            wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
         st = self.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), ws, wsb, _stream_handle(stream))
         if st != HK_OK:
             raise HKError(st, "hk_gemm_plan_run")

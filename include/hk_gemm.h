@@ -88,7 +88,8 @@ typedef enum hk_status {
 typedef struct hk_gemm_config {
     int32_t group_m;        /* grouped rasterisation: height of a group in output-tile rows (default 8) */
     int32_t max_clusters;   /* cap on the persistent grid, in work units (CTA pairs or CTAs; default: all that fit) */
-    int32_t split_k;        /* K-split factor (default: chosen by the plan; 1 = none) */
+    int32_t split_k;        /* K splits per output tile (0: chosen by the plan, which splits only when
+                               the tiles do not fill one wave; 1: never; > 1: forced) */
     int32_t kernel;         /* HK_KERNEL_* (default HK_KERNEL_AUTO) */
     uint64_t timeout_ns;    /* limit of each bounded wait in the kernel (default 1 s) */
     uint32_t flags;         /* HK_FLAG_* */
@@ -102,7 +103,7 @@ typedef struct hk_gemm_plan_info {
     int32_t ctas_per_unit;            /* 2 for a pair kernel, 1 for a single-CTA kernel */
     int32_t tile_m, tile_n, tile_k;   /* output tile of one work unit and K step */
     int32_t stages;                   /* depth of the shared-memory ring */
-    int32_t num_tiles;                /* output tiles (times split_k) */
+    int32_t num_tiles;                /* output tiles */
     int32_t grid_ctas;                /* CTAs launched */
     int32_t group_m;
     int32_t split_k;
@@ -130,7 +131,10 @@ hk_status hk_gemm_plan_create(hk_gemm_plan** out, int64_t M, int64_t N, int64_t 
                               int64_t lda, int64_t ldb, int64_t ldc, int device,
                               const hk_gemm_config* config);
 
-/* Bytes of device workspace a run needs (0 when no K split is used). */
+/* Bytes of device workspace a run needs (0 when no K split is used). With
+ * S > 1 splits it holds S fp32 partial matrices (S × M × N', N' = N rounded
+ * up to the tile width); a second kernel sums them in split order
+ * (deterministic) and writes C. */
 size_t hk_gemm_plan_workspace_size(const hk_gemm_plan* plan);
 
 /* Fill *info with what the plan chose. */

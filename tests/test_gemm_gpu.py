@@ -242,6 +242,7 @@ VARIANT_SHAPES = [(1, 1, 1), (100, 300, 70), (128, 1000, 520), (257, 130, 64), (
 
 def run_plan(hk, A_bits, B_bits, **cfg):
     import torch
+    cfg.setdefault("split_k", 1)
     M, K = A_bits.shape
     N = B_bits.shape[0]
     kp = (-K) % 8
@@ -290,3 +291,87 @@ def test_automatic_kernel_choice(hk):
     assert hk.Plan(129, 4096, 4096).info()["kernel"] == 1
     small = hk.Plan(64, 1024, 1024).info()
     assert small["kernel"] == 5 and small["ctas_per_unit"] == 1  # 16 tiles: narrowest tiles spread widest
+
+
+# ----------------------------------------------------------------- split K --
+
+def run_split(hk, A_bits, B_bits, ws_fill=0, runs=1, **cfg):
+    """Plan with (possibly forced) K splits, run `runs` times on one workspace."""
+    import torch
+    M, K = A_bits.shape
+    N = B_bits.shape[0]
+    kp = (-K) % 8
+    A, Astore = to_device(A_bits, cols_pad=kp)
+    B, Bstore = to_device(B_bits, cols_pad=kp)
+    ldc = N + ((-N) % 8)
+    plan = hk.Plan(M, N, K, lda=Astore.stride(0), ldb=Bstore.stride(0), ldc=ldc, **cfg)
+    info = plan.info()
+    ws_bytes = plan.workspace_size
+    ws = torch.full((max(ws_bytes, 1) + 255,), ws_fill, dtype=torch.uint8, device="cuda")
+    ws_ptr = (ws.data_ptr() + 255) & ~255
+    outs = []
+    for _ in range(runs):
+        C, Cstore = to_device(np.full((M, N), SENTINEL, dtype=np.uint16), rows_pad=2, cols_pad=ldc - N,
+                              fill=SENTINEL)
+        st = plan.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), ws_ptr, ws_bytes,
+                          int(torch.cuda.current_stream().cuda_stream))
+        assert st == hk.HK_OK, hk.hk_gemm_last_error_string()
+        torch.cuda.synchronize()
+        assert plan.device_status() == hk.HK_OK
+        full = to_host(Cstore)
+        guard = full.copy()
+        guard[:M, :N] = SENTINEL
+        assert np.all(guard == SENTINEL), "a write landed outside C"
+        outs.append(full[:M, :N])
+    plan.close()
+    return outs, info
+
+
+@pytest.mark.parametrize("kernel,splits,M,N,K", [
+    (1, 2, 300, 200, 1000), (1, 5, 257, 520, 2049), (2, 3, 100, 700, 900), (3, 7, 64, 1000, 2000),
+    (4, 16, 128, 300, 1030), (5, 4, 1, 77, 640), (3, 2, 200, 600, 128)])
+def test_split_k_integer_bitexact(hk, kernel, splits, M, N, K):
+    A = synth.int_bf16(M, K, 1300 + M)
+    B = synth.int_bf16(N, K, 2300 + N)
+    (got,), info = run_split(hk, A, B, kernel=kernel, split_k=splits)
+    assert info["split_k"] == splits and info["workspace_bytes"] > 0
+    assert_bitexact(got, oracle.gemm(A, B), f"kernel {kernel} split {splits} {M}x{N}x{K}")
+
+
+def test_split_k_normal_and_deterministic(hk):
+    M, N, K = 96, 2000, 4096
+    A = synth.normal_bf16(M, K, 41)
+    B = synth.normal_bf16(N, K, 42)
+    outs, info = run_split(hk, A, B, ws_fill=0xFF, runs=3, kernel=3, split_k=6)
+    assert_close(outs[0], oracle.gemm(A, B), K, 1, 1, "split 6")
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+
+
+def test_split_k_automatic_for_small_m(hk):
+    A = synth.normal_bf16(64, 8192, 43)
+    B = synth.normal_bf16(8192, 8192, 44)
+    outs, info = run_split(hk, A, B)
+    assert info["split_k"] > 1 and info["ctas_per_unit"] == 1
+    r, c = synth.sample_positions(64, 8192, 45, count=2048)
+    ref, _ = oracle.gemm_entries(A, B, r, c)
+    assert_close(outs[0][r, c], ref, 8192, 1, 1, "auto split")
+    assert hk.Plan(8192, 8192, 8192).info()["split_k"] == 1          # full waves: never split
+
+
+def test_split_k_workspace_errors(hk):
+    import torch
+    plan = hk.Plan(64, 1024, 4096, split_k=4, kernel=4)
+    need = plan.workspace_size
+    assert need > 0
+    A = torch.zeros((64, 4096), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((1024, 4096), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((64, 1024), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(need + 512, dtype=torch.uint8, device="cuda")
+    base = (ws.data_ptr() + 255) & ~255
+    assert plan.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), 0, 0, 0) == hk.HK_ERR_WORKSPACE
+    assert plan.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), base, need - 1, 0) == hk.HK_ERR_WORKSPACE
+    assert plan.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), base + 16, need, 0) == hk.HK_ERR_WORKSPACE
+    assert plan.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), base, need, 0) == hk.HK_OK
+    torch.cuda.synchronize()
+    assert plan.device_status() == hk.HK_OK
+    plan.close()
