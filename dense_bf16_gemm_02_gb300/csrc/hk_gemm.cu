@@ -588,4 +588,80 @@ hk_status hk_gemm_last_device_status(int device) {
     return read_status(sw, device);
 }
 
+// ------------------------------------------------- no-allocation variant --
+//
+// Some callers cannot allocate device memory when they call a GEMM: code
+// running inside a memory pool or arena that owns every byte of the device,
+// allocator or runtime hooks that must not re-enter cudaMalloc, or services
+// that pre-plan all of their memory at start-up. hk_gemm_bf16_noalloc serves
+// them: its K-split scratch (fp32 partial products) and its status word live
+// in the fixed array below, which is part of the library's device image and
+// stays resident on every device that loads the library until the process
+// exits. The array is shared by all calls on a device and keeps whatever the
+// last call left in it; nothing in it has to start at zero (each call writes
+// every partial it reads, and the kernel recognises its own abort flag by a
+// launch id that is unique in the process). Calls that overlap on the GPU
+// (different streams, or different host threads without ordering) use the
+// same array at the same time and race.
+
+constexpr size_t kNoAllocStatusBytes = 256;                   // status word, padded to keep the partials aligned
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;     // 32 MiB of K-split partials
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocStatusBytes + kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mutex;
+unsigned char* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the fixed array on `device` (the current device). Looked
+// up once per device; the host-side symbol itself is not a device address.
+hk_status noalloc_scratch(int device, unsigned char** out) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[device]) {
+        void* ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "looking up the fixed scratch array", e);
+        g_noalloc_ptr[device] = static_cast<unsigned char*>(ptr);
+    }
+    *out = g_noalloc_ptr[device];
+    return HK_OK;
+}
+
+}  // namespace
+
+hk_status hk_gemm_bf16_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                               int64_t lda, int64_t ldb, int64_t ldc, int32_t split_k, void* stream) {
+    hk_status s = check_shape(M, N, K, lda, ldb, ldc);
+    if (s != HK_OK) return s;
+    if (split_k < 0) return fail(HK_ERR_INVALID_ARG, "split_k must be >= 0");
+    if (M == 0 || N == 0) return HK_OK;
+    if ((s = check_pointers(A, B, C, K)) != HK_OK) return s;
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "cudaGetDevice", e);
+    const DeviceInfo* di = nullptr;
+    if ((s = device_info(device, &di)) != HK_OK) return s;
+    unsigned char* scratch = nullptr;
+    if ((s = noalloc_scratch(device, &scratch)) != HK_OK) return s;
+
+    hk_gemm_config cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.split_k = split_k;
+    hk_gemm_plan plan;
+    if ((s = fill_plan(&plan, M, N, K, lda, ldb, ldc, device, &cfg, di, true)) != HK_OK) return s;
+    if (plan.ws_bytes > kNoAllocScratchBytes) {
+        if (split_k > 0)
+            return fail(HK_ERR_WORKSPACE,
+                        "split_k=%d needs %zu bytes of scratch; the fixed scratch array holds %zu bytes",
+                        (int)split_k, plan.ws_bytes, kNoAllocScratchBytes);
+        cfg.split_k = 1;   // the automatic split does not fit: run without splitting K
+        if ((s = fill_plan(&plan, M, N, K, lda, ldb, ldc, device, &cfg, di, true)) != HK_OK) return s;
+    }
+    plan.owns_status = false;
+    StatusWord sw;
+    sw.dev = reinterpret_cast<uint32_t*>(scratch);
+    return launch(&plan, &sw, A, B, C, scratch + kNoAllocStatusBytes, static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

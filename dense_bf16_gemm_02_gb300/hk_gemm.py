@@ -38,7 +38,7 @@ HK_FLAG_FAULT_DROP_ARRIVE = 0x1
 EXPORTED = (
     "hk_gemm_bf16", "hk_gemm_plan_create", "hk_gemm_plan_workspace_size", "hk_gemm_plan_get_info",
     "hk_gemm_plan_run", "hk_gemm_plan_device_status", "hk_gemm_last_device_status",
-    "hk_gemm_plan_destroy", "hk_status_string", "hk_gemm_last_error_string",
+    "hk_gemm_plan_destroy", "hk_status_string", "hk_gemm_last_error_string", "hk_gemm_bf16_noalloc",
 )
 
 
@@ -106,6 +106,8 @@ def load() -> ctypes.CDLL:
         lib.hk_status_string.restype = ctypes.c_char_p
         lib.hk_gemm_last_error_string.argtypes = []
         lib.hk_gemm_last_error_string.restype = ctypes.c_char_p
+        lib.hk_gemm_bf16_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, ctypes.c_int32, P]
+        lib.hk_gemm_bf16_noalloc.restype = I32
         _lib = lib
         return lib
 
@@ -115,6 +117,12 @@ def load() -> ctypes.CDLL:
 def hk_gemm_bf16(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
                  stream: int = 0) -> int:
     return load().hk_gemm_bf16(A, B, C, M, N, K, lda, ldb, ldc, stream)
+
+
+def hk_gemm_bf16_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+                         split_k: int = 0, stream: int = 0) -> int:
+    """The GEMM that allocates nothing (scratch in a fixed array of the library)."""
+    return load().hk_gemm_bf16_noalloc(A, B, C, M, N, K, lda, ldb, ldc, split_k, stream)
 
 
 def hk_gemm_last_device_status(device: int) -> int:

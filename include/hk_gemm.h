@@ -157,6 +157,34 @@ hk_status hk_gemm_last_device_status(int device);
 
 void hk_gemm_plan_destroy(hk_gemm_plan* plan);
 
+/* GEMM that allocates nothing, for callers that cannot call cudaMalloc when
+ * they run a GEMM (code inside a memory pool or arena that owns all device
+ * memory, allocator or runtime hooks that must not re-enter the allocator,
+ * services that fix their memory at start-up). This entry point has no
+ * counterpart on the HipKittens pages; it exists for those callers.
+ *
+ * Same operation, arguments and errors as hk_gemm_bf16, plus `split_k`
+ * (0: chosen automatically, 1: never split K, > 1: forced). Its K-split
+ * scratch and its status word live in one fixed array inside the library's
+ * device image: 32 MiB of scratch, resident on every device that loads the
+ * library until the process exits. A forced split_k whose fp32 partials
+ * (split_k × M × N rounded up to the tile width × 4 bytes) exceed 32 MiB is
+ * rejected with HK_ERR_WORKSPACE; an automatic split that would not fit is
+ * not taken. The caller provides A, B and C; nothing is allocated, freed or
+ * set up through an allocating library routine.
+ *
+ * The first call on a device looks up the array's device address (once, with
+ * that device current); make that first call before any stream capture.
+ * All calls on a device share the array and it keeps the last call's
+ * contents (nothing in it needs to start at zero). Calls that overlap on the
+ * GPU race on it: order them on one stream or serialise them. A bounded wait
+ * that runs out in this variant ends the kernel early without a status that
+ * can be queried. */
+hk_status hk_gemm_bf16_noalloc(const void* A, const void* B, void* C,
+                               int64_t M, int64_t N, int64_t K,
+                               int64_t lda, int64_t ldb, int64_t ldc,
+                               int32_t split_k, void* stream);
+
 /* Static description of a status code. */
 const char* hk_status_string(hk_status status);
 
