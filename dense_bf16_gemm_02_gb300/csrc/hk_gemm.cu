@@ -271,12 +271,6 @@ namespace {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Fraction of the work-unit slots that the tiles keep busy over all waves.
-double slot_use(int64_t tiles, int64_t slots) {
-    if (tiles <= 0 || slots <= 0) return 0.0;
-    return double(tiles) / double(ceil_div(tiles, slots) * slots);
-}
-
 // Rows of A one CTA loads per stage: 128, or M rounded up to 8 when M is
 // smaller (single-CTA kernels); rows of the smem tile beyond them only feed
 // output rows that are never stored.
