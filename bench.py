@@ -41,8 +41,10 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources whose digest is given; see profiles/.
 MEASURED_TRAFFIC = {
-    "gemm_8192": {"source_digest": "61beb5cc9d56c9de", "bytes_per_launch": 1064003000 + 126472448,
-                  "profile": "profiles/gemm_bf16_pair_kernel_gemm_8192.md"},
+    "gemm_8192": {"source_digest": "a00f76b659ea9f45", "bytes_per_launch": 1077694000 + 127190016,
+                  "profile": "profiles/gemm_bf16_kernel_pair256_gemm_8192.md"},
+    "skinny_128x28672x8192": {"source_digest": "a00f76b659ea9f45", "bytes_per_launch": 471919872 + 6630144,
+                              "profile": "profiles/gemm_bf16_kernel_single128x192_skinny_128x28672x8192.md"},
 }
 
 
