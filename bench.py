@@ -164,6 +164,12 @@ def barrier(world):
         dist.barrier()
 
 
+def replica_value(flops_per_step: float, steps: int, world: int, elapsed_ms_max: float) -> float:
+    """Whole-job TFLOP/s of `world` independent replicas that each ran `steps`
+    GEMMs: the flops of all ranks over the slowest rank's time."""
+    return flops_per_step * steps * world / (elapsed_ms_max / 1e3) / 1e12
+
+
 def max_over_ranks(world, x: float) -> float:
     if world == 1:
         return x
@@ -361,7 +367,7 @@ def run_hk(args, w):
 
     peaks, peaks_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
-    value = flops * args.steps * world / (elapsed_max / 1e3) / 1e12
+    value = replica_value(flops, args.steps, world, elapsed_max)
     mean_launch_ms = statistics.mean(per_launch)
     nbytes = gemm_bytes(w.M, w.N, w.K)
     hbm_bound = flops / nbytes < peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)   # below the roofline knee
@@ -397,7 +403,7 @@ def run_hk(args, w):
                      "kernel": f"gemm_bf16_kernel ({info['tile_m']}x{info['tile_n']}, "
                                f"{info['ctas_per_unit']} CTA(s) per tile)",
                      "source_digest": digest},
-        "e2e": {"value": flops * e2e_steps * world / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+        "e2e": {"value": replica_value(flops, e2e_steps, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(A_h.numel() * 2 + B_h.numel() * 2),
                 "d2h_bytes_per_step": int(C_h[0].numel() * 2), "steps": e2e_steps,
                 "pipelined": "H2D(i+1) | GEMM(i) | D2H(i-1) on three streams"},
