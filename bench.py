@@ -260,14 +260,20 @@ def run_hk(args, w):
     C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
     sh = int(stream.cuda_stream)
-    plan = hk.Plan(w.M, w.N, w.K, device=local)
+    plan = hk.Plan(w.M, w.N, w.K, device=local, group_m=args.group_m, split_k=1)
     info = plan.info()
     flops = gemm_flops(w.M, w.N, w.K)
 
     def step():
-        st = hk.hk_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, w.K, w.K, w.N, sh)
+        if args.group_m:
+            # an explicit schedule goes through a plan (hk_gemm_plan_run)
+            st = plan.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), 0, 0, sh)
+            where = "hk_gemm_plan_run"
+        else:
+            st = hk.hk_gemm_bf16(A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, w.K, w.K, w.N, sh)
+            where = "hk_gemm_bf16"
         if st != hk.HK_OK:
-            raise hk.HKError(st, "hk_gemm_bf16")
+            raise hk.HKError(st, where)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -427,6 +433,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["hk", "reference"], default="hk")
     ap.add_argument("--workload", default="gemm_8192", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--group-m", type=int, default=0,
+                    help="raster group height in tile rows (0: the library default via hk_gemm_bf16)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     w = synth.WORKLOADS[args.workload]
