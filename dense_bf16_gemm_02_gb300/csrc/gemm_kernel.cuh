@@ -105,6 +105,9 @@ struct GemmParams {
     uint32_t expect_bytes;        // bytes that land per stage in the cluster (both CTAs of a pair)
     int64_t n_pad;                // split K: row stride of the partial matrices (tiles_n * tile width)
     float* partials;              // split K: fp32 partial matrices P[split][M][n_pad]
+    int32_t tail_start;           // pair kernel: tiles from here on run as two half-width units (-1: none)
+    int32_t total_units;          // work units of this launch
+    uint32_t expect_bytes_half;   // bytes per stage of a half-width unit
     int32_t n_tma;                // columns [0, n_tma) of C are written by TMA stores (n_tma = N & ~7)
     int64_t ldc;                  // leading dimension of C (elements), for the ragged tail columns
     uint16_t* c_ptr;              // C, for the columns [n_tma, N) a TMA store cannot bound exactly
@@ -184,6 +187,22 @@ __device__ __forceinline__ void split_range(const GemmParams& p, int s, int& beg
     end = static_cast<int>((static_cast<int64_t>(s + 1) * p.k_blocks) / p.splits);
 }
 
+// Work unit u -> tile, K split and half. Units before tail_start are whole
+// tiles (times the K splits); from tail_start on, each tile of the last,
+// partial round of the schedule is run as two units of half its width, so
+// that the round keeps twice as many units busy (half = 0 or 1; -1: whole).
+__device__ __forceinline__ void unit_info(const GemmParams& p, int u, int& t, int& split, int& half) {
+    if (p.tail_start >= 0 && u >= p.tail_start) {
+        t = p.tail_start + ((u - p.tail_start) >> 1);
+        split = 0;
+        half = (u - p.tail_start) & 1;
+    } else {
+        t = u / p.splits;
+        split = u - t * p.splits;
+        half = -1;
+    }
+}
+
 __device__ __forceinline__ void drain_after_abort() {
     // let copies and MMAs that were already issued land before teardown
     for (int i = 0; i < 200; ++i) __nanosleep(1000);
@@ -192,7 +211,8 @@ __device__ __forceinline__ void drain_after_abort() {
 template <int kCG, int kTileN>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                 const __grid_constant__ CUtensorMap tmap_c, const GemmParams p) {
+                 const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_b_half,
+                 const GemmParams p) {
     using G = Geometry<kCG, kTileN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -249,14 +269,20 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             int stage = 0;
             uint32_t phase = 0;
             bool dropped = false;
-            const int total = p.num_tiles * p.splits;
+            const int total = p.total_units;
             for (int u = unit; u < total && !abort_seen; u += num_units) {
-                const int t = u / p.splits;
+                int t, split, half;
+                unit_info(p, u, t, split, half);
                 int tm, tn, kb_begin, kb_end;
                 tile_coords(p, t, tm, tn);
-                split_range(p, u - t * p.splits, kb_begin, kb_end);
+                split_range(p, split, kb_begin, kb_end);
                 const int a_row = tm * G::kTileM + static_cast<int>(rank) * kCtaM;
-                const int b_row = tn * G::kTileN + static_cast<int>(rank) * G::kBRows;
+                const int b_row = half < 0 ? tn * G::kTileN + static_cast<int>(rank) * G::kBRows
+                                           : tn * G::kTileN + half * (G::kTileN / 2) +
+                                                 static_cast<int>(rank) * (G::kBRows / 2);
+                const void* const b_map = half < 0 ? static_cast<const void*>(&tmap_b)
+                                                   : static_cast<const void*>(&tmap_b_half);
+                const uint32_t stage_bytes = half < 0 ? p.expect_bytes : p.expect_bytes_half;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bounded(p, empty_bar(stage), phase ^ 1u, kErrProducerEmpty)) {
                         abort_seen = true;
@@ -266,7 +292,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         if ((p.flags & kFlagDropArrive) && !dropped) {
                             dropped = true;   // test-only fault: withhold this arrival
                         } else {
-                            mbar_arrive_expect_tx(full_bar(stage), p.expect_bytes);
+                            mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
                         }
                     }
                     const uint32_t a_dst = base + G::kOffA + stage * kABytes;
@@ -275,7 +301,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         // both CTAs' copies complete on the leader's barrier
                         const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
                         tma_load_2d_pair(a_dst, &tmap_a, kb * kTileK, a_row, leader_full);
-                        tma_load_2d_pair(b_dst, &tmap_b, kb * kTileK, b_row, leader_full);
+                        tma_load_2d_pair(b_dst, b_map, kb * kTileK, b_row, leader_full);
                     } else {
                         tma_load_2d(a_dst, &tmap_a, kb * kTileK, a_row, full_bar(stage));
                         tma_load_2d(b_dst, &tmap_b, kb * kTileK, b_row, full_bar(stage));
@@ -293,11 +319,13 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             int stage = 0;
             uint32_t phase = 0;
             int local = 0;
-            const int total = p.num_tiles * p.splits;
+            const int total = p.total_units;
             for (int u = unit; u < total && !abort_seen; u += num_units, ++local) {
-                const int t = u / p.splits;
+                int t, split, half;
+                unit_info(p, u, t, split, half);
                 int kb_begin, kb_end;
-                split_range(p, u - t * p.splits, kb_begin, kb_end);
+                split_range(p, split, kb_begin, kb_end);
+                const uint32_t idesc = half < 0 ? G::kIdesc : idesc_bf16_f32(G::kTileM, G::kTileN / 2);
                 const int buf = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
                 const bool acc_free = kCG == 2
@@ -322,9 +350,9 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         // advance 16 bf16 = 32 bytes along K inside the swizzle atom
                         const uint32_t acc = (kb != kb_begin || k != 0) ? 1u : 0u;
                         if constexpr (kCG == 2)
-                            mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, G::kIdesc, acc);
+                            mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
                         else
-                            mma_bf16_one(d_tmem, a_desc + 2u * k, b_desc + 2u * k, G::kIdesc, acc);
+                            mma_bf16_one(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
                     }
                     // free this stage (in both CTAs of a pair) once the MMAs above have read it
                     if constexpr (kCG == 2) mma_commit_pair_mask(empty_bar(stage), 0x3);
@@ -384,11 +412,14 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         };
 
         int local = 0;
-        const int total = p.num_tiles * p.splits;
+        const int total = p.total_units;
         for (int u = unit; u < total; u += num_units, ++local) {
-            const int t = u / p.splits;
+            int t, split, half;
+            unit_info(p, u, t, split, half);
             int tm, tn;
             tile_coords(p, t, tm, tn);
+            const int chunks = (half < 0 ? G::kTileN : G::kTileN / 2) / kEpiCols;
+            const int col_base = tn * G::kTileN + (half < 0 ? 0 : half * (G::kTileN / 2));
             const int buf = local & 1;
             const uint32_t acc_phase = (local >> 1) & 1;
             if (!wait_bounded_warp(p, acc_full_bar(buf), acc_phase, kErrEpiAccFull)) {
@@ -401,11 +432,10 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             const int row = row0 + static_cast<int>(lane);
             const uint32_t t_row = tmem_base + ((q * 32u) << 16) + buf * G::kAccCols;
             // split K: this lane's row of this split's fp32 partial matrix
-            const int split = u - t * p.splits;
             float* const part_row =
                 p.partials + (static_cast<int64_t>(split) * p.M + row) * p.n_pad + tn * G::kTileN;
 #pragma unroll 1
-            for (int c = 0; c < G::kTileN / kEpiCols; ++c) {
+            for (int c = 0; c < chunks; ++c) {
                 uint32_t v[32];
                 if (p.k_blocks > 0) {
                     tmem_load_32cols(t_row + c * kEpiCols, v);
@@ -414,7 +444,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = 0u;
                 }
-                if (c == G::kTileN / kEpiCols - 1) {
+                if (c == chunks - 1) {
                     // every TMEM read of this accumulator is done: release it to the MMA
                     tc_fence_before_sync();
                     __syncwarp();
@@ -424,7 +454,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                     }
                 }
                 if (p.splits == 1) {
-                    store_chunk(v, row0, tn * G::kTileN + c * kEpiCols);
+                    store_chunk(v, row0, col_base + c * kEpiCols);
                 } else if (row < p.M) {
                     float4* dst = reinterpret_cast<float4*>(part_row + c * kEpiCols);
 #pragma unroll

@@ -42,7 +42,7 @@ constexpr int kDefaultGroupM = 8;
 
 // -------------------------------------------------------------- variants --
 
-using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, hk::GemmParams);
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, hk::GemmParams);
 
 struct Variant {
     int id;            // value of hk_gemm_config.kernel
@@ -282,30 +282,41 @@ int a_rows_for(const Variant& v, int64_t M) {
 // Kernel choice by a small time model. The CTA pair (256-row tiles) serves
 // M > 128, single-CTA kernels (128-row tiles, four widths) M <= 128. K is
 // split only when one wave of tiles leaves work-unit slots idle and a
-// workspace may be used. Estimated time of a candidate = the largest of
-//   streaming: waves × bytes one CTA moves per unit ÷ per-SM copy rate,
-//   HBM:       unique bytes (B, A, C, and split partials written + read) ÷ HBM rate,
-//   tensor:    waves × K-steps per unit × time of one K-step,
-// plus a second-launch overhead when K is split.
+// workspace may be used. Estimated time of a candidate:
+//   GEMM   = the largest of
+//              streaming: waves × (bytes one CTA moves per unit ÷ per-SM copy
+//                         rate + pipeline fill), the per-SM rate being the
+//                         bytes the ring keeps in flight ÷ the load latency,
+//                         at most the rate measured with every SM streaming,
+//              HBM:       (A, B, and C or the fp32 partials) ÷ HBM rate,
+//              tensor:    waves × K-steps per unit × time of one K-step;
+//   reduce = (partials read + C written) ÷ HBM rate + launch, when K is split
+//            (it runs after the GEMM, so its time adds).
 constexpr int kMaxSplits = 16;
 constexpr int kMinKBlocksPerSplit = 8;
 constexpr double kSmBytesPerUs = 65e3;       // one SM's sustained TMA rate from HBM (measured, bytes/µs)
+constexpr double kLoadLatencyUs = 2.5;       // TMA load latency under load (measured: in flight ÷ rate)
 constexpr double kHbmBytesPerUs = 6.7e6;     // HBM copy rate (bytes/µs)
 constexpr double kKStepUsPair = 0.27;        // 256x256x64 per pair (4 tcgen05.mma)
-constexpr double kSplitOverheadUs = 3.0;
+constexpr double kFillUs = 1.5;              // filling the ring at the start of a unit
+constexpr double kLaunchUs = 3.0;            // a second kernel launch
 
 double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int64_t slots, int splits) {
     const int64_t tiles = ceil_div(M, v.tile_m) * ceil_div(N, v.tile_n);
     const int64_t units = tiles * splits;
     const double waves = double(ceil_div(units, slots));
     const double kb = double(ceil_div(ceil_div(K, hk::kTileK), splits));
-    const double cta_bytes = double(a_rows_for(v, M) + v.tile_n / v.cg) * hk::kTileK * 2 * kb;
-    const double t_stream = waves * cta_bytes / kSmBytesPerUs;
+    const double stage_bytes = double(a_rows_for(v, M) + v.tile_n / v.cg) * hk::kTileK * 2;
+    const double cta_bytes = stage_bytes * kb;
+    const double sm_rate = std::min(kSmBytesPerUs, stage_bytes * v.stages / kLoadLatencyUs);
+    const double t_stream = waves * (cta_bytes / sm_rate + kFillUs);
     const double n_pad = double(ceil_div(N, v.tile_n) * v.tile_n);
-    const double hbm = 2.0 * (N * K + M * K + M * N) + (splits > 1 ? 2.0 * 4.0 * splits * M * n_pad : 0.0);
-    const double t_hbm = hbm / kHbmBytesPerUs;
-    const double t_mma = waves * kb * kKStepUsPair * (double(v.tile_n) / 256.0) * (v.cg == 2 ? 1.0 : 1.0);
-    return std::max(t_stream, std::max(t_hbm, t_mma)) + (splits > 1 ? kSplitOverheadUs : 0.0);
+    const double partials = splits > 1 ? 4.0 * splits * M * n_pad : 0.0;
+    const double operands = 2.0 * (double(N) * K + double(M) * K);
+    const double t_hbm = (operands + (splits > 1 ? partials : 2.0 * M * N)) / kHbmBytesPerUs;
+    const double t_mma = waves * kb * kKStepUsPair * (double(v.tile_n) / 256.0);
+    const double t_reduce = splits > 1 ? (partials + 2.0 * M * N) / kHbmBytesPerUs + kLaunchUs : 0.0;
+    return std::max(t_stream, std::max(t_hbm, t_mma)) + t_reduce;
 }
 
 void choose_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo* di, int max_units_cap, bool allow_split,
@@ -385,7 +396,21 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     int units = di->max_units[vi];
     if (units <= 0) return fail(HK_ERR_UNSUPPORTED_DEVICE, "kernel %s does not fit on the device", v->name);
     if (p->cfg.max_clusters > 0 && p->cfg.max_clusters < units) units = p->cfg.max_clusters;
-    if (units > g.num_tiles * splits) units = g.num_tiles * splits;
+    // Last partial round of a pair kernel: when its R tiles fill at most half
+    // of the units, each runs as two half-width units (256 x 128), so the
+    // round takes about half as long. No workspace is involved.
+    g.tail_start = -1;
+    g.total_units = g.num_tiles * splits;
+    if (v->cg == 2 && splits == 1 && g.num_tiles > 0 && !(p->cfg.flags & HK_FLAG_NO_TAIL_SPLIT)) {
+        const int64_t rounds = ceil_div(g.num_tiles, units);
+        const int64_t last = g.num_tiles - (rounds - 1) * units;
+        if (2 * last <= units) {
+            g.tail_start = static_cast<int32_t>(g.num_tiles - last);
+            g.total_units = static_cast<int32_t>(g.num_tiles + last);
+        }
+    }
+    g.expect_bytes_half = static_cast<uint32_t>(v->cg * (g.a_rows + v->tile_n / v->cg / 2) * hk::kTileK * 2);
+    if (units > g.total_units) units = g.total_units;
     p->grid_ctas = v->cg * units;
     return HK_OK;
 }
@@ -407,6 +432,8 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
     const uint32_t a_box_rows = static_cast<uint32_t>(p->params.a_rows);
     if ((s = encode_2d(&ta, a_ptr, p->K > 0 ? p->M : 1, kk, lda, hk::kTileK, a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B, "A")) != HK_OK) return s;
     if ((s = encode_2d(&tb, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, hk::kTileK, b_rows, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != HK_OK) return s;
+    CUtensorMap tbh;   // B in boxes of half the rows, for half-width units
+    if ((s = encode_2d(&tbh, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, hk::kTileK, b_rows / 2, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != HK_OK) return s;
     // the map covers N rounded down to a multiple of 8 (see the epilogue); at
     // least 8 columns so that it stays valid when N < 8 (then it is unused)
     const int64_t n_tma = p->N & ~int64_t(7);
@@ -430,7 +457,7 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = v->cg > 1 ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, v->fn, ta, tb, tc, g);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, v->fn, ta, tb, tc, tbh, g);
     if (e != cudaSuccess) return cuda_fail(HK_ERR_LAUNCH, "launching the GEMM kernel", e);
     if (g.splits > 1) {
         const int64_t groups = p->M * ceil_div(p->N, 8);
@@ -506,6 +533,7 @@ hk_status hk_gemm_plan_get_info(const hk_gemm_plan* p, hk_gemm_plan_info* info) 
     info->kernels_per_run = (p->M == 0 || p->N == 0) ? 0 : (p->params.splits > 1 ? 2 : 1);
     info->smem_bytes = p->variant->smem_bytes;
     info->workspace_bytes = p->ws_bytes;
+    info->tail_split_tiles = p->params.tail_start >= 0 ? p->params.num_tiles - p->params.tail_start : 0;
     return HK_OK;
 }
 

@@ -34,6 +34,7 @@ KERNELS = (HK_KERNEL_PAIR_256x256, HK_KERNEL_SINGLE_128x256, HK_KERNEL_SINGLE_12
 
 HK_FLAG_NONE = 0x0
 HK_FLAG_FAULT_DROP_ARRIVE = 0x1
+HK_FLAG_NO_TAIL_SPLIT = 0x2
 
 EXPORTED = (
     "hk_gemm_bf16", "hk_gemm_plan_create", "hk_gemm_plan_workspace_size", "hk_gemm_plan_get_info",
@@ -56,7 +57,8 @@ class hk_gemm_plan_info(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("num_tiles", ctypes.c_int32),
                 ("grid_ctas", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("kernels_per_run", ctypes.c_int32),
-                ("smem_bytes", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t)]
+                ("smem_bytes", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t),
+                ("tail_split_tiles", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -73,6 +73,9 @@ typedef enum hk_status {
  * stage, so the MMA issuer's bounded wait runs out and the call reports
  * HK_ERR_TIMEOUT through the device status word. No GPU fault is caused. */
 #define HK_FLAG_FAULT_DROP_ARRIVE 0x1u
+/* Keep the tiles of the last partial round whole (by default, when they fill
+ * at most half of the CTA pairs, each runs as two 256x128 halves). */
+#define HK_FLAG_NO_TAIL_SPLIT 0x2u
 
 /* Kernel variants (hk_gemm_config.kernel). A "pair" kernel runs on clusters
  * of two CTAs (tcgen05 cta_group::2) with 256-row output tiles; a "single"
@@ -110,6 +113,8 @@ typedef struct hk_gemm_plan_info {
     int32_t kernels_per_run;          /* kernel launches one run enqueues */
     int32_t smem_bytes;               /* dynamic shared memory per CTA */
     size_t workspace_bytes;
+    int32_t tail_split_tiles;         /* tiles of the last round run as two half-width units */
+    int32_t reserved;
 } hk_gemm_plan_info;
 
 typedef struct hk_gemm_plan hk_gemm_plan;

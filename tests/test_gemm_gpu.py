@@ -375,3 +375,35 @@ def test_split_k_workspace_errors(hk):
     torch.cuda.synchronize()
     assert plan.device_status() == hk.HK_OK
     plan.close()
+
+
+# ---------------------------------------------------- tail round split --
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 512), (256, 1024, 640), (512, 1000, 320), (2900, 700, 200),
+                                   (8192, 8192, 128)])
+def test_tail_split_integer_bitexact(hk, M, N, K):
+    """Tiles of the last partial round run as two 256x128 halves."""
+    A = synth.int_bf16(M, K, 1400 + M)
+    B = synth.int_bf16(N, K, 2400 + N)
+    got, info = run_plan(hk, A, B)
+    assert info["kernel"] == 1 and info["tail_split_tiles"] > 0
+    if M * N <= 4096 * 4096:
+        assert_bitexact(got, oracle.gemm(A, B), f"tail split {M}x{N}x{K}")
+    else:
+        r, c = synth.sample_positions(M, N, 77, count=4096)
+        ref, _ = oracle.gemm_entries(A, B, r, c)
+        assert_bitexact(got[r, c], ref, f"tail split {M}x{N}x{K} samples")
+    whole, info2 = run_plan(hk, A, B, flags=hk.HK_FLAG_NO_TAIL_SPLIT if hasattr(hk, "HK_FLAG_NO_TAIL_SPLIT") else 2)
+    assert info2["tail_split_tiles"] == 0
+    assert_bitexact(got, whole, "split vs whole")
+
+
+def test_tail_split_normal_matches_whole_tiles(hk):
+    M, N, K = 1024, 2000, 1000          # 4 x 8 = 32 tiles: all run as halves
+    A = synth.normal_bf16(M, K, 61)
+    B = synth.normal_bf16(N, K, 62)
+    got, info = run_plan(hk, A, B)
+    assert info["tail_split_tiles"] > 0
+    assert_close(got, oracle.gemm(A, B), K, 1, 1, "tail split normal")
+    whole, _ = run_plan(hk, A, B, flags=2)
+    assert_close(got, whole, K, 1, 1, "split vs whole")
