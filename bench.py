@@ -365,6 +365,23 @@ def run_hk(args, w):
     if hk.hk_gemm_last_device_status(local) != hk.HK_OK:
         raise RuntimeError("device status after the end-to-end run: " + hk.hk_gemm_last_error_string())
 
+    # ---- context only: the vendor library on the same GPU and inputs (outside the timed region)
+    cublas = None
+    if rank == 0 and not args.no_cublas_context:
+        for _ in range(3):
+            torch.matmul(A, B.t(), out=C)
+        torch.cuda.synchronize(dev)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_ctx = max(5, min(args.steps, 50))
+        c0.record()
+        for _ in range(n_ctx):
+            torch.matmul(A, B.t(), out=C)
+        c1.record()
+        torch.cuda.synchronize(dev)
+        ms = c0.elapsed_time(c1) / n_ctx
+        cublas = {"value": flops / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_gemm": ms, "launches": n_ctx,
+                  "what": "torch.matmul (cuBLAS) on the same GPU and inputs, timed after ours; context only"}
+
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
@@ -415,6 +432,7 @@ def run_hk(args, w):
                 "pipelined": "H2D(i+1) | GEMM(i) | D2H(i-1) on three streams"},
         "gpu_launches": args.steps * int(info["kernels_per_run"]),
         "clocks": clocks,
+        "context_cublas": cublas,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, A_bits, B_bits)
@@ -433,6 +451,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["hk", "reference"], default="hk")
     ap.add_argument("--workload", default="gemm_8192", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cublas-context", action="store_true")
     ap.add_argument("--group-m", type=int, default=0,
                     help="raster group height in tile rows (0: the library default via hk_gemm_bf16)")
     args = ap.parse_args(argv)

@@ -9,6 +9,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -412,6 +413,10 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     g.expect_bytes_half = static_cast<uint32_t>(v->cg * (g.a_rows + v->tile_n / v->cg / 2) * hk::kTileK * 2);
     if (units > g.total_units) units = g.total_units;
     p->grid_ctas = v->cg * units;
+    if (const char* log = std::getenv("HK_LOG"); log && log[0] == '1')
+        std::fprintf(stderr, "hk_gemm plan: M=%lld N=%lld K=%lld kernel=%s splits=%d tail_tiles=%d grid=%d ctas "
+                     "group_m=%d workspace=%zu B\n", (long long)M, (long long)N, (long long)K, v->name, splits,
+                     g.tail_start >= 0 ? g.num_tiles - g.tail_start : 0, p->grid_ctas, group_m, p->ws_bytes);
     return HK_OK;
 }
 
