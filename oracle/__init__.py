@@ -68,6 +68,14 @@ def _load():
             lib.oracle_gemm_bf16_entries.argtypes = [_P, _P, _P, _I64, _I64, _I64, _P, _P, _I64,
                                                      ctypes.c_int]
             lib.oracle_gemm_bf16_entries.restype = ctypes.c_int
+            lib.oracle_activation.argtypes = [ctypes.c_double, ctypes.c_int]
+            lib.oracle_activation.restype = ctypes.c_double
+            lib.oracle_gemm_bf16_epilogue.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
+                                                      ctypes.c_int, ctypes.c_int]
+            lib.oracle_gemm_bf16_epilogue.restype = ctypes.c_int
+            lib.oracle_gemm_bf16_epilogue_entries.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int,
+                                                              _P, _P, _I64, ctypes.c_int]
+            lib.oracle_gemm_bf16_epilogue_entries.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -151,3 +159,51 @@ def gemm_entries(A: np.ndarray, B: np.ndarray, rows, cols, threads: int = 0) -> 
                                                 A.strides[0] // 2, B.strides[0] // 2,
                                                 _ptr(rows), _ptr(cols), rows.size, int(threads))
     return out, used
+
+
+# ---- fused epilogue: C = RNE_bf16(act(A·Bᵀ + bias)) -----------------------
+ACT_NONE, ACT_RELU, ACT_GELU, ACT_SILU = 0, 1, 2, 3
+
+
+def activation(x: float, act: int) -> float:
+    """The activation in binary64 (0 none, 1 ReLU, 2 GELU with erf, 3 SiLU)."""
+    return float(_load().oracle_activation(float(x), int(act)))
+
+
+def _bias_ptr(bias, N):
+    if bias is None:
+        return None, 0
+    bias = np.ascontiguousarray(np.asarray(bias, dtype=np.uint16))
+    if bias.shape != (N,):
+        raise ValueError("bias must hold N bf16 values")
+    return bias, bias.ctypes.data
+
+
+def gemm_epilogue(A: np.ndarray, B: np.ndarray, bias=None, act: int = ACT_NONE, threads: int = 0) -> np.ndarray:
+    """C = RNE_bf16(act(A·Bᵀ + bias)), bias a length-N bf16 vector or None."""
+    A = _as_bits(A, "A")
+    B = _as_bits(B, "B")
+    M, K = A.shape
+    N = B.shape[0]
+    keep, bptr = _bias_ptr(bias, N)
+    C = np.zeros((M, N), dtype=np.uint16)
+    if M and N:
+        _load().oracle_gemm_bf16_epilogue(_ptr(A), _ptr(B), bptr, _ptr(C), M, N, K, max(A.strides[0] // 2, K),
+                                          max(B.strides[0] // 2, K), N, int(act), int(threads))
+    return C
+
+
+def gemm_epilogue_entries(A: np.ndarray, B: np.ndarray, rows, cols, bias=None, act: int = ACT_NONE,
+                          threads: int = 0) -> np.ndarray:
+    """Entries of RNE_bf16(act(A·Bᵀ + bias)) at (rows[t], cols[t])."""
+    A = _as_bits(A, "A")
+    B = _as_bits(B, "B")
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    keep, bptr = _bias_ptr(bias, B.shape[0])
+    out = np.zeros(rows.size, dtype=np.uint16)
+    if rows.size:
+        _load().oracle_gemm_bf16_epilogue_entries(_ptr(A), _ptr(B), bptr, _ptr(out), A.shape[1],
+                                                  A.strides[0] // 2, B.strides[0] // 2, int(act), _ptr(rows),
+                                                  _ptr(cols), rows.size, int(threads))
+    return out

@@ -89,12 +89,31 @@ double oracle_dot_f64(const uint16_t* A, const uint16_t* B, int64_t K,
     return s;
 }
 
+/* ---- fused epilogue (bias + activation) ----------------------------------
+ * C[i][j] = round_bf16_rne( act( sum_k A[i][k] * B[j][k] + bias[j] ) ), the
+ * bias a bf16 vector of N entries (or none), act one of
+ *   0 none:  x
+ *   1 ReLU:  max(x, 0)
+ *   2 GELU:  x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt(2)))   (the exact, erf form)
+ *   3 SiLU:  x * sigmoid(x) = x / (1 + exp(-x))
+ * all evaluated in binary64 before the single rounding to bf16. */
+double oracle_activation(double x, int act) {
+    switch (act) {
+        case 1: return x > 0.0 ? x : 0.0;
+        case 2: return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+        case 3: return x / (1.0 + exp(-x));
+        default: return x;
+    }
+}
+
 /* ---- threading: a plain static split of a list of work items ---------- */
 
 typedef struct {
     const uint16_t* A;
     const uint16_t* B;
     uint16_t* out;
+    const uint16_t* bias;  /* epilogue: per-column bias (bf16) or NULL */
+    int act;               /* epilogue: activation code */
     int64_t N, K, lda, ldb, ldo;
     const int64_t* rows;   /* entry mode: row index per entry; row mode: row list */
     const int64_t* cols;   /* entry mode only */
@@ -102,17 +121,25 @@ typedef struct {
     int mode;              /* 0: full rows, 1: single entries */
 } work_t;
 
+/* One output entry: the dot product, then (if requested) bias and activation. */
+static uint16_t entry(const work_t* w, int64_t i, int64_t j) {
+    double x = oracle_dot_f64(w->A, w->B, w->K, w->lda, w->ldb, i, j);
+    if (w->bias || w->act) {
+        if (w->bias) x += bf16_bits_to_double(w->bias[j]);
+        x = oracle_activation(x, w->act);
+    }
+    return oracle_round_bf16(x);
+}
+
 static void* worker(void* p) {
     work_t* w = (work_t*)p;
     for (int64_t t = w->begin; t < w->end; ++t) {
         if (w->mode == 0) {
             int64_t i = w->rows ? w->rows[t] : t;
             uint16_t* o = w->out + t * w->ldo;
-            for (int64_t j = 0; j < w->N; ++j)
-                o[j] = oracle_round_bf16(oracle_dot_f64(w->A, w->B, w->K, w->lda, w->ldb, i, j));
+            for (int64_t j = 0; j < w->N; ++j) o[j] = entry(w, i, j);
         } else {
-            w->out[t] = oracle_round_bf16(
-                oracle_dot_f64(w->A, w->B, w->K, w->lda, w->ldb, w->rows[t], w->cols[t]));
+            w->out[t] = entry(w, w->rows[t], w->cols[t]);
         }
     }
     return NULL;
@@ -156,7 +183,7 @@ static int run_parallel(work_t base, int64_t items, int threads) {
 int oracle_gemm_bf16(const uint16_t* A, const uint16_t* B, uint16_t* C,
                      int64_t M, int64_t N, int64_t K,
                      int64_t lda, int64_t ldb, int64_t ldc, int threads) {
-    work_t w = {A, B, C, N, K, lda, ldb, ldc, NULL, NULL, 0, 0, 0};
+    work_t w = {A, B, C, NULL, 0, N, K, lda, ldb, ldc, NULL, NULL, 0, 0, 0};
     return run_parallel(w, M, threads);
 }
 
@@ -165,7 +192,7 @@ int oracle_gemm_bf16(const uint16_t* A, const uint16_t* B, uint16_t* C,
 int oracle_gemm_bf16_rows(const uint16_t* A, const uint16_t* B, uint16_t* out,
                           int64_t N, int64_t K, int64_t lda, int64_t ldb,
                           const int64_t* rows, int64_t nrows, int threads) {
-    work_t w = {A, B, out, N, K, lda, ldb, N, rows, NULL, 0, 0, 0};
+    work_t w = {A, B, out, NULL, 0, N, K, lda, ldb, N, rows, NULL, 0, 0, 0};
     return run_parallel(w, nrows, threads);
 }
 
@@ -174,6 +201,22 @@ int oracle_gemm_bf16_entries(const uint16_t* A, const uint16_t* B, uint16_t* out
                              int64_t K, int64_t lda, int64_t ldb,
                              const int64_t* rows, const int64_t* cols, int64_t count,
                              int threads) {
-    work_t w = {A, B, out, 0, K, lda, ldb, 0, rows, cols, 0, 0, 1};
+    work_t w = {A, B, out, NULL, 0, 0, K, lda, ldb, 0, rows, cols, 0, 0, 1};
+    return run_parallel(w, count, threads);
+}
+
+/* Full GEMM with the fused epilogue: C = round(act(A * B^T + bias)). */
+int oracle_gemm_bf16_epilogue(const uint16_t* A, const uint16_t* B, const uint16_t* bias, uint16_t* C,
+                              int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                              int act, int threads) {
+    work_t w = {A, B, C, bias, act, N, K, lda, ldb, ldc, NULL, NULL, 0, 0, 0};
+    return run_parallel(w, M, threads);
+}
+
+/* Selected entries with the fused epilogue. */
+int oracle_gemm_bf16_epilogue_entries(const uint16_t* A, const uint16_t* B, const uint16_t* bias,
+                                      uint16_t* out, int64_t K, int64_t lda, int64_t ldb, int act,
+                                      const int64_t* rows, const int64_t* cols, int64_t count, int threads) {
+    work_t w = {A, B, out, bias, act, 0, K, lda, ldb, 0, rows, cols, 0, 0, 1};
     return run_parallel(w, count, threads);
 }

@@ -241,3 +241,120 @@ def test_mutants_fail_pins(tmp_path, name):
     mutant = _Lib(str(path_so))
     failures = [p.__name__ for p in PINS if p(mutant) is not None]
     assert failures, f"mutant {name} passed every pin"
+
+
+# ------------------------------------------------------ fused epilogue --
+
+def pin_activation_values(o):
+    """Activation values fixed by mathematics, not by re-typing the formulas:
+    Φ(1) from the normal table, σ(ln 3) = 3/4, the odd-part identities
+    GELU(x) − GELU(−x) = x (Φ(x) + Φ(−x) = 1) and SiLU(x) − SiLU(−x) = x
+    (σ(x) + σ(−x) = 1), ReLU's definition and GELU's limits."""
+    act = o.activation if hasattr(o, "activation") else None
+    if act is None:
+        return "no activation entry"
+    if abs(act(1.0, 2) - 0.8413447460685429) > 1e-15:
+        return "GELU(1) != Φ(1)"
+    if abs(act(np.log(3.0), 3) - 0.75 * np.log(3.0)) > 1e-15:
+        return "SiLU(ln 3) != 3/4 ln 3"
+    for x in (0.3, 1.7, 4.25, 9.0):
+        if abs((act(x, 2) - act(-x, 2)) - x) > 1e-12 or abs((act(x, 3) - act(-x, 3)) - x) > 1e-12:
+            return f"odd-part identity fails at {x}"
+        if act(x, 1) != x or act(-x, 1) != 0.0:
+            return f"ReLU({x})"
+    if abs(act(8.0, 2) - 8.0) > 1e-12 or abs(act(-8.0, 2)) > 1e-12:
+        return "GELU limits"
+    if act(0.0, 2) != 0.0 or act(0.0, 3) != 0.0 or act(2.5, 0) != 2.5:
+        return "activation at 0 / identity"
+    return None
+
+
+def pin_epilogue_gemm(o):
+    """Bias and activation on top of the GEMM: exact rational bias sums on
+    tiny shapes; A = 0 gives RNE(act(bias)); ReLU on integer inputs against
+    int64 arithmetic."""
+    if not hasattr(o, "gemm_epilogue"):
+        return "no epilogue entry"
+    M, N, K = 5, 7, 9
+    A = synth.normal_bf16(M, K, 91)
+    B = synth.normal_bf16(N, K, 92)
+    bias = synth.normal_bf16(1, N, 93, 2.0)[0]
+    want = np.zeros((M, N), dtype=np.uint16)
+    Af = [[bits_to_fraction(int(x)) for x in r] for r in A]
+    Bf = [[bits_to_fraction(int(x)) for x in r] for r in B]
+    for i in range(M):
+        for j in range(N):
+            s = sum(Af[i][k] * Bf[j][k] for k in range(K)) + bits_to_fraction(int(bias[j]))
+            want[i, j] = round_fraction(s)
+    if not np.array_equal(o.gemm_epilogue(A, B, bias, 0), want):
+        return "bias sum is not exact"
+    Z = np.zeros_like(A)
+    for act in (1, 2, 3):
+        got = o.gemm_epilogue(Z, B, bias, act)
+        ref = np.array([round_fraction(Fraction(o.activation(float(bits_to_fraction(int(b))), act))) for b in bias],
+                       dtype=np.uint16)
+        if not np.array_equal(got[0], ref) or not np.all(got == got[0]):
+            return f"A = 0 with act {act}"
+    Ai, Bi = synth.int_bf16(6, 40, 94), synth.int_bf16(8, 40, 95)
+    bi = synth.int_bf16(1, 8, 96)[0]
+    ref = synth.bf16_bits_to_f32(Ai).astype(np.int64) @ synth.bf16_bits_to_f32(Bi).astype(np.int64).T
+    ref = np.maximum(ref + synth.bf16_bits_to_f32(bi).astype(np.int64), 0)
+    want = np.array([[round_fraction(Fraction(int(v))) for v in r] for r in ref], dtype=np.uint16)
+    if not np.array_equal(o.gemm_epilogue(Ai, Bi, bi, 1), want):
+        return "ReLU on integers"
+    return None
+
+
+@pytest.mark.parametrize("pin", [pin_activation_values, pin_epilogue_gemm], ids=lambda p: p.__name__)
+def test_epilogue_pin(oracle_lib, pin):
+    assert pin(oracle_lib) is None
+
+
+EPILOGUE_MUTANTS = {
+    "bias_by_row": ("if (w->bias) x += bf16_bits_to_double(w->bias[j]);",
+                    "if (w->bias) x += bf16_bits_to_double(w->bias[i % 5]);"),
+    "gelu_no_sqrt2": ("case 2: return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
+                      "case 2: return 0.5 * x * (1.0 + erf(x));"),
+    "silu_sign": ("case 3: return x / (1.0 + exp(-x));", "case 3: return x / (1.0 + exp(x));"),
+    "relu_leaky": ("case 1: return x > 0.0 ? x : 0.0;", "case 1: return x > 0.0 ? x : 0.01 * x;"),
+    "act_before_bias": ("        if (w->bias) x += bf16_bits_to_double(w->bias[j]);\n        x = oracle_activation(x, w->act);",
+                        "        x = oracle_activation(x, w->act);\n        if (w->bias) x += bf16_bits_to_double(w->bias[j]);"),
+}
+
+
+class _EpiLib(_Lib):
+    def __init__(self, path):
+        super().__init__(path)
+        P, I = ctypes.c_void_p, ctypes.c_int64
+        self.lib.oracle_activation.argtypes = [ctypes.c_double, ctypes.c_int]
+        self.lib.oracle_activation.restype = ctypes.c_double
+        self.lib.oracle_gemm_bf16_epilogue.argtypes = [P, P, P, P, I, I, I, I, I, I, ctypes.c_int, ctypes.c_int]
+
+    def activation(self, x, act):
+        return float(self.lib.oracle_activation(float(x), int(act)))
+
+    def gemm_epilogue(self, A, B, bias, act):
+        A = np.ascontiguousarray(A, dtype=np.uint16)
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        bias = np.ascontiguousarray(bias, dtype=np.uint16)
+        M, K = A.shape
+        N = B.shape[0]
+        C = np.zeros((M, N), dtype=np.uint16)
+        self.lib.oracle_gemm_bf16_epilogue(A.ctypes.data, B.ctypes.data, bias.ctypes.data, C.ctypes.data, M, N,
+                                           K, K, K, N, act, 1)
+        return C
+
+
+@pytest.mark.parametrize("name", sorted(EPILOGUE_MUTANTS))
+def test_epilogue_mutants_fail_pins(tmp_path, name):
+    src = open(os.path.join(ROOT, "oracle", "gemm_ref.c")).read()
+    old, new = EPILOGUE_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    path_c = tmp_path / f"{name}.c"
+    path_so = tmp_path / f"{name}.so"
+    path_c.write_text(src.replace(old, new))
+    subprocess.run(["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                    "-D_GNU_SOURCE", str(path_c), "-o", str(path_so), "-lm"], check=True)
+    mutant = _EpiLib(str(path_so))
+    assert pin_activation_values(mutant) is not None or pin_epilogue_gemm(mutant) is not None, \
+        f"mutant {name} passed the epilogue pins"
