@@ -264,7 +264,19 @@ def run_hk(args, w):
     info = plan.info()
     flops = gemm_flops(w.M, w.N, w.K)
 
+    act = {"none": 0, "bias": 0, "bias_relu": 1, "bias_gelu": 2, "bias_silu": 3}[args.epilogue]
+    bias_t = None
+    if args.epilogue != "none":
+        bias_bits = synth.normal_bf16(1, w.N, 4000 + w.wid, 1.0)[0]
+        bias_t = torch.from_numpy(bias_bits.view(np.int16)).to(dev)
+
     def step():
+        if bias_t is not None:
+            st = hk.hk_gemm_bf16_epilogue(A.data_ptr(), B.data_ptr(), C.data_ptr(), bias_t.data_ptr(), w.M, w.N,
+                                          w.K, w.K, w.K, w.N, act, sh)
+            if st != hk.HK_OK:
+                raise hk.HKError(st, "hk_gemm_bf16_epilogue")
+            return
         if args.group_m:
             # an explicit schedule goes through a plan (hk_gemm_plan_run)
             st = plan.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), 0, 0, sh)
@@ -412,6 +424,7 @@ def run_hk(args, w):
         "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(workload_config(w), parallelism="replicas" if world > 1 else "single GPU",
+                       epilogue=args.epilogue,
                        tile=f"{info['tile_m']}x{info['tile_n']}x{info['tile_k']} per "
                             f"{'CTA pair' if info['ctas_per_unit'] == 2 else 'CTA'}",
                        stages=info["stages"], grid_ctas=info["grid_ctas"], group_m=info["group_m"]),
@@ -452,6 +465,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="gemm_8192", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cublas-context", action="store_true")
+    ap.add_argument("--epilogue", default="none", choices=["none", "bias", "bias_relu", "bias_gelu", "bias_silu"],
+                    help="fused epilogue of each step (hk_gemm_bf16_epilogue)")
     ap.add_argument("--group-m", type=int, default=0,
                     help="raster group height in tile rows (0: the library default via hk_gemm_bf16)")
     args = ap.parse_args(argv)

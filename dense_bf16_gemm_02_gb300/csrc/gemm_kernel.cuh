@@ -105,6 +105,8 @@ struct GemmParams {
     uint32_t expect_bytes;        // bytes that land per stage in the cluster (both CTAs of a pair)
     int64_t n_pad;                // split K: row stride of the partial matrices (tiles_n * tile width)
     float* partials;              // split K: fp32 partial matrices P[split][M][n_pad]
+    const uint16_t* bias;         // fused epilogue: per-column bf16 bias (N values) or null
+    int32_t act;                  // fused epilogue: 0 none, 1 ReLU, 2 GELU (erf), 3 SiLU
     int32_t tail_start;           // pair kernel: tiles from here on run as two half-width units (-1: none)
     int32_t total_units;          // work units of this launch
     uint32_t expect_bytes_half;   // bytes per stage of a half-width unit
@@ -179,6 +181,45 @@ __device__ __forceinline__ bool wait_bounded_warp(const GemmParams& p, uint32_t 
     if (ok) (void)mbar_try_wait(bar, parity);
     __syncwarp();
     return ok != 0;
+}
+
+// Fused epilogue on one fp32 accumulator value: + bias, then the activation.
+__device__ __forceinline__ float epilogue_op(float x, float bias, int act) {
+    x += bias;
+    switch (act) {
+        case 1: return fmaxf(x, 0.0f);
+        case 2: return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));   // x·Φ(x)
+        case 3: return x / (1.0f + expf(-x));                                  // x·σ(x)
+        default: return x;
+    }
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
+    return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+
+// Apply the fused epilogue to 32 accumulator values of columns col0..col0+31.
+__device__ __forceinline__ void apply_epilogue(const GemmParams& p, uint32_t (&v)[32], int col0) {
+    float b[32];
+    if (p.bias != nullptr && col0 + 32 <= p.N) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.bias + col0);   // 64-byte aligned chunk
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 x = __ldg(src + q);
+            const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                b[8 * q + 2 * h] = bf16_bits_to_float(static_cast<uint16_t>(w4[h] & 0xFFFFu));
+                b[8 * q + 2 * h + 1] = bf16_bits_to_float(static_cast<uint16_t>(w4[h] >> 16));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            b[e] = (p.bias != nullptr && col0 + e < p.N) ? bf16_bits_to_float(p.bias[col0 + e]) : 0.0f;
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(epilogue_op(__uint_as_float(v[e]), b[e], p.act));
 }
 
 // K blocks [begin, end) of split `s` of `splits` (as even as possible).
@@ -380,7 +421,8 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         // memory and written by a TMA store; when N is not a multiple of 8
         // the last (< 8) columns are written with plain stores, since a TMA
         // store bounds the innermost dimension only to 16-byte granules.
-        auto store_chunk = [&](const uint32_t (&v)[32], int row0, int col0) {
+        auto store_chunk = [&](uint32_t (&v)[32], int row0, int col0) {
+            if (p.bias != nullptr || p.act != 0) apply_epilogue(p, v, col0);
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2_rn(v[2 * i], v[2 * i + 1]);
@@ -479,12 +521,13 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     }
 }
 
-// Split K, second pass: C = bf16_rne(P[0] + P[1] + ... + P[splits-1]),
-// summed in this fixed order (so the result does not depend on which split
-// finished first). Each thread handles 8 consecutive columns of one row.
+// Split K, second pass: C = bf16_rne(act(P[0] + P[1] + ... + P[splits-1] +
+// bias)), summed in this fixed order (so the result does not depend on
+// which split finished first). Each thread handles 8 consecutive columns of
+// one row.
 __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float* __restrict__ partials, int32_t splits, int32_t M, int32_t N, int64_t n_pad,
-                     uint16_t* __restrict__ C, int64_t ldc) {
+                     uint16_t* __restrict__ C, int64_t ldc, const uint16_t* __restrict__ bias, int32_t act) {
     const int64_t groups_per_row = (N + 7) / 8;
     const int64_t total = static_cast<int64_t>(M) * groups_per_row;
     const int64_t split_stride = static_cast<int64_t>(M) * n_pad;
@@ -500,6 +543,15 @@ splitk_reduce_kernel(const float* __restrict__ partials, int32_t splits, int32_t
             const float4 x = __ldcs(q), y = __ldcs(q + 1);
             a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
             b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+        }
+        if (bias != nullptr || act != 0) {
+            float bb[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) bb[e] = (bias != nullptr && col + e < N) ? bf16_bits_to_float(bias[col + e]) : 0.0f;
+            a.x = epilogue_op(a.x, bb[0], act); a.y = epilogue_op(a.y, bb[1], act);
+            a.z = epilogue_op(a.z, bb[2], act); a.w = epilogue_op(a.w, bb[3], act);
+            b.x = epilogue_op(b.x, bb[4], act); b.y = epilogue_op(b.y, bb[5], act);
+            b.z = epilogue_op(b.z, bb[6], act); b.w = epilogue_op(b.w, bb[7], act);
         }
         const uint32_t w0 = pack_bf16x2_rn(__float_as_uint(a.x), __float_as_uint(a.y));
         const uint32_t w1 = pack_bf16x2_rn(__float_as_uint(a.z), __float_as_uint(a.w));

@@ -359,6 +359,7 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     if (config) p->cfg = *config;
     if (p->cfg.group_m < 0 || p->cfg.max_clusters < 0 || p->cfg.split_k < 0)
         return fail(HK_ERR_INVALID_ARG, "negative config field");
+    if (p->cfg.activation > HK_ACT_SILU) return fail(HK_ERR_INVALID_ARG, "unknown activation %u", p->cfg.activation);
     if (p->cfg.kernel != HK_KERNEL_AUTO && !find_variant(p->cfg.kernel))
         return fail(HK_ERR_INVALID_ARG, "unknown kernel id %d", (int)p->cfg.kernel);
     const int64_t k_blocks_all = ceil_div(K, hk::kTileK);
@@ -393,6 +394,7 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     g.n_tma = static_cast<int32_t>(N & ~int64_t(7));
     g.ldc = ldc;
     g.flags = p->cfg.flags;
+    g.act = static_cast<int32_t>(p->cfg.activation);
     g.timeout_ns = p->cfg.timeout_ns ? p->cfg.timeout_ns : kDefaultTimeoutNs;
     int units = di->max_units[vi];
     if (units <= 0) return fail(HK_ERR_UNSUPPORTED_DEVICE, "kernel %s does not fit on the device", v->name);
@@ -421,7 +423,7 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
 }
 
 hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const void* B, void* C, void* workspace,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, const void* bias = nullptr) {
     if (p->M == 0 || p->N == 0) return HK_OK;
     hk_status s = get_encoder();
     if (s != HK_OK) return s;
@@ -446,6 +448,7 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
 
     hk::GemmParams g = p->params;
     g.c_ptr = static_cast<uint16_t*>(C);
+    g.bias = static_cast<const uint16_t*>(bias);
     g.status = sw->dev;
     g.launch_id = next_launch_id();
     if (g.splits > 1) g.partials = static_cast<float*>(workspace);
@@ -468,7 +471,7 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
         const int64_t groups = p->M * ceil_div(p->N, 8);
         const int64_t blocks = std::min<int64_t>(ceil_div(groups, 256), int64_t(p->sm_count) * 8);
         hk::splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            g.partials, g.splits, g.M, g.N, g.n_pad, g.c_ptr, g.ldc);
+            g.partials, g.splits, g.M, g.N, g.n_pad, g.c_ptr, g.ldc, g.bias, g.act);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(HK_ERR_LAUNCH, "launching the split-K reduction", e);
     }
@@ -613,6 +616,63 @@ hk_status hk_gemm_last_device_status(int device) {
     }
     if (!sw) return HK_OK;
     return read_status(sw, device);
+}
+
+hk_status hk_gemm_plan_run_epilogue(const hk_gemm_plan* p, const void* A, const void* B, void* C, const void* bias,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+    if (!p) return fail(HK_ERR_INVALID_ARG, "NULL plan");
+    if (p->M == 0 || p->N == 0) return HK_OK;
+    hk_status s = check_pointers(A, B, C, p->K);
+    if (s != HK_OK) return s;
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 15u))
+        return fail(HK_ERR_MISALIGNED, "the bias vector must be 16-byte aligned");
+    if (p->ws_bytes > 0) {
+        if (!workspace || workspace_bytes < p->ws_bytes)
+            return fail(HK_ERR_WORKSPACE, "the plan needs %zu bytes of workspace, %zu given", p->ws_bytes,
+                        workspace ? workspace_bytes : size_t(0));
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+            return fail(HK_ERR_WORKSPACE, "the workspace must be 256-byte aligned");
+    }
+    DeviceGuard guard(p->device);
+    return launch(p, const_cast<StatusWord*>(&p->status), A, B, C, workspace, static_cast<cudaStream_t>(stream),
+                  bias);
+}
+
+hk_status hk_gemm_bf16_epilogue(const void* A, const void* B, void* C, const void* bias, int64_t M, int64_t N,
+                                int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int32_t activation, void* stream) {
+    hk_status s = check_shape(M, N, K, lda, ldb, ldc);
+    if (s != HK_OK) return s;
+    if (activation < 0 || activation > HK_ACT_SILU) return fail(HK_ERR_INVALID_ARG, "unknown activation %d", (int)activation);
+    if (M == 0 || N == 0) return HK_OK;
+    if ((s = check_pointers(A, B, C, K)) != HK_OK) return s;
+    if (bias && (reinterpret_cast<uintptr_t>(bias) & 15u))
+        return fail(HK_ERR_MISALIGNED, "the bias vector must be 16-byte aligned");
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "cudaGetDevice", e);
+    const DeviceInfo* di = nullptr;
+    if ((s = device_info(device, &di)) != HK_OK) return s;
+    StatusWord* sw = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_ctx_mutex);
+        if (!g_ctx[device]) {
+            StatusWord* w = new (std::nothrow) StatusWord();
+            if (!w) return fail(HK_ERR_INVALID_ARG, "out of host memory");
+            if ((s = alloc_status(w)) != HK_OK) {
+                delete w;
+                return s;
+            }
+            g_ctx[device] = w;
+        }
+        sw = g_ctx[device];
+    }
+    hk_gemm_config cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.activation = static_cast<uint32_t>(activation);
+    hk_gemm_plan plan;
+    if ((s = fill_plan(&plan, M, N, K, lda, ldb, ldc, device, &cfg, di, false)) != HK_OK) return s;
+    plan.owns_status = false;
+    return launch(&plan, sw, A, B, C, nullptr, static_cast<cudaStream_t>(stream), bias);
 }
 
 // ------------------------------------------------- no-allocation variant --

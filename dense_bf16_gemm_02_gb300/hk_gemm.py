@@ -32,6 +32,11 @@ HK_KERNEL_SINGLE_128x64 = 5
 KERNELS = (HK_KERNEL_PAIR_256x256, HK_KERNEL_SINGLE_128x256, HK_KERNEL_SINGLE_128x192,
            HK_KERNEL_SINGLE_128x128, HK_KERNEL_SINGLE_128x64)
 
+HK_ACT_NONE = 0
+HK_ACT_RELU = 1
+HK_ACT_GELU = 2
+HK_ACT_SILU = 3
+
 HK_FLAG_NONE = 0x0
 HK_FLAG_FAULT_DROP_ARRIVE = 0x1
 HK_FLAG_NO_TAIL_SPLIT = 0x2
@@ -40,6 +45,7 @@ EXPORTED = (
     "hk_gemm_bf16", "hk_gemm_plan_create", "hk_gemm_plan_workspace_size", "hk_gemm_plan_get_info",
     "hk_gemm_plan_run", "hk_gemm_plan_device_status", "hk_gemm_last_device_status",
     "hk_gemm_plan_destroy", "hk_status_string", "hk_gemm_last_error_string", "hk_gemm_bf16_noalloc",
+    "hk_gemm_bf16_epilogue", "hk_gemm_plan_run_epilogue",
 )
 
 
@@ -47,7 +53,7 @@ class hk_gemm_config(ctypes.Structure):
     _fields_ = [("group_m", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("kernel", ctypes.c_int32),
                 ("timeout_ns", ctypes.c_uint64), ("flags", ctypes.c_uint32),
-                ("reserved1", ctypes.c_uint32)]
+                ("activation", ctypes.c_uint32)]
 
 
 class hk_gemm_plan_info(ctypes.Structure):
@@ -108,6 +114,10 @@ def load() -> ctypes.CDLL:
         lib.hk_status_string.restype = ctypes.c_char_p
         lib.hk_gemm_last_error_string.argtypes = []
         lib.hk_gemm_last_error_string.restype = ctypes.c_char_p
+        lib.hk_gemm_bf16_epilogue.argtypes = [P, P, P, P, I64, I64, I64, I64, I64, I64, ctypes.c_int32, P]
+        lib.hk_gemm_bf16_epilogue.restype = I32
+        lib.hk_gemm_plan_run_epilogue.argtypes = [P, P, P, P, P, P, ctypes.c_size_t, P]
+        lib.hk_gemm_plan_run_epilogue.restype = I32
         lib.hk_gemm_bf16_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, ctypes.c_int32, P]
         lib.hk_gemm_bf16_noalloc.restype = I32
         _lib = lib
@@ -119,6 +129,12 @@ def load() -> ctypes.CDLL:
 def hk_gemm_bf16(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
                  stream: int = 0) -> int:
     return load().hk_gemm_bf16(A, B, C, M, N, K, lda, ldb, ldc, stream)
+
+
+def hk_gemm_bf16_epilogue(A: int, B: int, C: int, bias: int, M: int, N: int, K: int, lda: int, ldb: int,
+                          ldc: int, activation: int = 0, stream: int = 0) -> int:
+    """C = bf16(act(A·Bᵀ + bias)) (bias: device pointer or 0)."""
+    return load().hk_gemm_bf16_epilogue(A, B, C, bias or None, M, N, K, lda, ldb, ldc, activation, stream)
 
 
 def hk_gemm_bf16_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
@@ -187,12 +203,12 @@ class Plan:
     """A plan for one GEMM shape (wraps hk_gemm_plan_*)."""
 
     def __init__(self, M, N, K, lda=None, ldb=None, ldc=None, device=0, group_m=0, max_clusters=0,
-                 split_k=0, timeout_ns=0, flags=0, kernel=0):
+                 split_k=0, timeout_ns=0, flags=0, kernel=0, activation=0):
         lib = load()
         self._lib = lib
         self.M, self.N, self.K = M, N, K
         cfg = hk_gemm_config(group_m=group_m, max_clusters=max_clusters, split_k=split_k,
-                             timeout_ns=timeout_ns, flags=flags, kernel=kernel)
+                             timeout_ns=timeout_ns, flags=flags, kernel=kernel, activation=activation)
         handle = ctypes.c_void_p()
         st = lib.hk_gemm_plan_create(ctypes.byref(handle), M, N, K, lda if lda is not None else K,
                                      ldb if ldb is not None else K, ldc if ldc is not None else N,
@@ -232,6 +248,11 @@ class Plan:
         if st != HK_OK:
             raise HKError(st, "hk_gemm_plan_run")
         return C
+
+    def run_epilogue_raw(self, A: int, B: int, C: int, bias: int = 0, workspace: int = 0, workspace_bytes: int = 0,
+                         stream: int = 0) -> int:
+        return self._lib.hk_gemm_plan_run_epilogue(self._h, A, B, C, bias or None, workspace, workspace_bytes,
+                                                   stream)
 
     def device_status(self) -> int:
         return int(self._lib.hk_gemm_plan_device_status(self._h))

@@ -77,6 +77,12 @@ typedef enum hk_status {
  * at most half of the CTA pairs, each runs as two 256x128 halves). */
 #define HK_FLAG_NO_TAIL_SPLIT 0x2u
 
+/* Fused epilogue activations: C = bf16(act(A·Bᵀ + bias)). */
+#define HK_ACT_NONE 0
+#define HK_ACT_RELU 1               /* max(x, 0) */
+#define HK_ACT_GELU 2               /* x·Φ(x) = 0.5·x·(1 + erf(x/√2)) */
+#define HK_ACT_SILU 3               /* x·σ(x) = x / (1 + e^(−x)) */
+
 /* Kernel variants (hk_gemm_config.kernel). A "pair" kernel runs on clusters
  * of two CTAs (tcgen05 cta_group::2) with 256-row output tiles; a "single"
  * kernel runs one CTA per output tile of 128 rows and suits M <= 128. */
@@ -96,7 +102,7 @@ typedef struct hk_gemm_config {
     int32_t kernel;         /* HK_KERNEL_* (default HK_KERNEL_AUTO) */
     uint64_t timeout_ns;    /* limit of each bounded wait in the kernel (default 1 s) */
     uint32_t flags;         /* HK_FLAG_* */
-    uint32_t reserved1;
+    uint32_t activation;    /* fused epilogue activation, HK_ACT_* (used by hk_gemm_plan_run_epilogue) */
 } hk_gemm_config;
 
 /* What a plan chose (for logging and benchmarks). */
@@ -151,6 +157,24 @@ hk_status hk_gemm_plan_get_info(const hk_gemm_plan* plan, hk_gemm_plan_info* inf
  * another run that can overlap this one. The call allocates nothing. */
 hk_status hk_gemm_plan_run(const hk_gemm_plan* plan, const void* A, const void* B, void* C,
                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* GEMM with a fused epilogue (a "next" step the survey lists after the plain
+ * GEMM; the HipKittens pages fuse nothing into their GEMM):
+ *     C[i,j] = bf16_rne( act( Σ_k A[i,k]·B[j,k] + bias[j] ) )
+ * computed in fp32 (accumulator + bias, then the activation) before the one
+ * rounding. `bias` is a device vector of N bf16 values, 16-byte aligned, or
+ * NULL (no bias); `activation` is an HK_ACT_* code (HK_ERR_INVALID_ARG
+ * otherwise). Everything else as hk_gemm_bf16. */
+hk_status hk_gemm_bf16_epilogue(const void* A, const void* B, void* C, const void* bias,
+                                int64_t M, int64_t N, int64_t K,
+                                int64_t lda, int64_t ldb, int64_t ldc,
+                                int32_t activation, void* stream);
+
+/* Plan form: the activation is hk_gemm_config.activation of the plan; the
+ * bias (or NULL) is given per run. Otherwise as hk_gemm_plan_run. */
+hk_status hk_gemm_plan_run_epilogue(const hk_gemm_plan* plan, const void* A, const void* B, void* C,
+                                    const void* bias, void* workspace, size_t workspace_bytes,
+                                    void* stream);
 
 /* Synchronise the plan's device and read-and-clear its status word:
  * HK_OK, or HK_ERR_TIMEOUT if a bounded wait ran out in any run since the

@@ -407,3 +407,80 @@ def test_tail_split_normal_matches_whole_tiles(hk):
     assert_close(got, oracle.gemm(A, B), K, 1, 1, "tail split normal")
     whole, _ = run_plan(hk, A, B, flags=2)
     assert_close(got, whole, K, 1, 1, "split vs whole")
+
+
+# --------------------------------------------------------- fused epilogue --
+
+def run_epilogue(hk, A_bits, B_bits, bias_bits, act, split_k=None, kernel=0):
+    import torch
+    M, K = A_bits.shape
+    N = B_bits.shape[0]
+    kp = (-K) % 8
+    A, Astore = to_device(A_bits, cols_pad=kp)
+    B, Bstore = to_device(B_bits, cols_pad=kp)
+    ldc = N + ((-N) % 8)
+    C, Cstore = to_device(np.full((M, N), SENTINEL, dtype=np.uint16), rows_pad=1, cols_pad=ldc - N,
+                          fill=SENTINEL)
+    bias_t = None
+    if bias_bits is not None:
+        bias_t = torch.from_numpy(np.ascontiguousarray(bias_bits).view(np.int16)).to("cuda")
+    bptr = bias_t.data_ptr() if bias_t is not None else 0
+    stream = int(torch.cuda.current_stream().cuda_stream)
+    if split_k is None:
+        st = hk.hk_gemm_bf16_epilogue(A.data_ptr(), B.data_ptr(), C.data_ptr(), bptr, M, N, K, Astore.stride(0),
+                                      Bstore.stride(0), Cstore.stride(0), act, stream)
+    else:
+        plan = hk.Plan(M, N, K, lda=Astore.stride(0), ldb=Bstore.stride(0), ldc=Cstore.stride(0),
+                       split_k=split_k, kernel=kernel, activation=act)
+        ws = torch.zeros(max(plan.workspace_size, 1) + 256, dtype=torch.uint8, device="cuda")
+        st = plan.run_epilogue_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), bptr, (ws.data_ptr() + 255) & ~255,
+                                   plan.workspace_size, stream)
+    assert st == hk.HK_OK, hk.hk_gemm_last_error_string()
+    torch.cuda.synchronize()
+    full = to_host(Cstore)
+    guard = full.copy()
+    guard[:M, :N] = SENTINEL
+    assert np.all(guard == SENTINEL), "a write landed outside C"
+    return full[:M, :N]
+
+
+@pytest.mark.parametrize("act", [0, 1, 2, 3])
+@pytest.mark.parametrize("with_bias", [False, True])
+@pytest.mark.parametrize("M,N,K", [(300, 517, 200), (64, 1000, 640), (1024, 768, 1536)])
+def test_epilogue_normal(hk, act, with_bias, M, N, K):
+    A = synth.normal_bf16(M, K, 1500 + M)
+    B = synth.normal_bf16(N, K, 2500 + N)
+    bias = synth.normal_bf16(1, N, 3500 + N, 4.0)[0] if with_bias else None
+    got = run_epilogue(hk, A, B, bias, act)
+    ref = oracle.gemm_epilogue(A, B, bias, act)
+    assert_close(got, ref, K, 1, 1, f"act {act} bias {with_bias} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(257, 300, 128), (128, 2050, 96)])
+def test_epilogue_relu_integer_bitexact(hk, M, N, K):
+    A = synth.int_bf16(M, K, 1600 + M)
+    B = synth.int_bf16(N, K, 2600 + N)
+    bias = synth.int_bf16(1, N, 3600 + N)[0]
+    got = run_epilogue(hk, A, B, bias, 1)
+    assert_bitexact(got, oracle.gemm_epilogue(A, B, bias, 1), "relu + bias integer")
+
+
+@pytest.mark.parametrize("act", [1, 2, 3])
+def test_epilogue_in_split_k_reduction(hk, act):
+    M, N, K = 64, 1200, 4096
+    A = synth.normal_bf16(M, K, 71)
+    B = synth.normal_bf16(N, K, 72)
+    bias = synth.normal_bf16(1, N, 73, 2.0)[0]
+    got = run_epilogue(hk, A, B, bias, act, split_k=4, kernel=4)
+    assert_close(got, oracle.gemm_epilogue(A, B, bias, act), K, 1, 1, f"split-K act {act}")
+
+
+def test_epilogue_argument_errors(hk):
+    import torch
+    A = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    bias = torch.zeros(80, dtype=torch.bfloat16, device="cuda")
+    assert hk.hk_gemm_bf16_epilogue(A.data_ptr(), A.data_ptr(), C.data_ptr(), bias.data_ptr() + 2, 64, 64, 64,
+                                    64, 64, 64, 1, 0) == hk.HK_ERR_MISALIGNED
+    assert hk.hk_gemm_bf16_epilogue(A.data_ptr(), A.data_ptr(), C.data_ptr(), bias.data_ptr(), 64, 64, 64,
+                                    64, 64, 64, 7, 0) == hk.HK_ERR_INVALID_ARG
