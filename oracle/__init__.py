@@ -76,6 +76,14 @@ def _load():
             lib.oracle_gemm_bf16_epilogue_entries.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int,
                                                               _P, _P, _I64, ctypes.c_int]
             lib.oracle_gemm_bf16_epilogue_entries.restype = ctypes.c_int
+            lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_double.restype = ctypes.c_double
+            lib.oracle_gemm_fp8e4m3.argtypes = [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, ctypes.c_double,
+                                                ctypes.c_int]
+            lib.oracle_gemm_fp8e4m3.restype = ctypes.c_int
+            lib.oracle_gemm_fp8e4m3_entries.argtypes = [_P, _P, _P, _I64, _I64, _I64, ctypes.c_double, _P, _P,
+                                                        _I64, ctypes.c_int]
+            lib.oracle_gemm_fp8e4m3_entries.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -206,4 +214,48 @@ def gemm_epilogue_entries(A: np.ndarray, B: np.ndarray, rows, cols, bias=None, a
         _load().oracle_gemm_bf16_epilogue_entries(_ptr(A), _ptr(B), bptr, _ptr(out), A.shape[1],
                                                   A.strides[0] // 2, B.strides[0] // 2, int(act), _ptr(rows),
                                                   _ptr(cols), rows.size, int(threads))
+    return out
+
+
+# ---- FP8 (E4M3) GEMM with per-tensor scales ------------------------------
+
+def e4m3_value(code: int) -> float:
+    """Exact value of an E4M3 byte (NaN for S.1111.111)."""
+    return float(_load().oracle_e4m3_to_double(int(code) & 0xFF))
+
+
+def _as_bytes(x: np.ndarray, name: str) -> np.ndarray:
+    if x.dtype != np.uint8 or x.ndim != 2:
+        raise TypeError(f"{name} must be a 2-D uint8 array of E4M3 codes")
+    if x.shape[1] > 1 and x.strides[1] != 1:
+        raise ValueError(f"{name} must have a unit stride along K")
+    return x
+
+
+def gemm_fp8(A: np.ndarray, B: np.ndarray, scale_a: float = 1.0, scale_b: float = 1.0,
+             threads: int = 0) -> np.ndarray:
+    """C = RNE_bf16(sa·sb·A·Bᵀ) for E4M3 codes A (M×K), B (N×K); sa, sb are float32 values."""
+    A = _as_bytes(A, "A")
+    B = _as_bytes(B, "B")
+    M, K = A.shape
+    N = B.shape[0]
+    C = np.zeros((M, N), dtype=np.uint16)
+    scale = float(np.float32(scale_a)) * float(np.float32(scale_b))
+    if M and N:
+        _load().oracle_gemm_fp8e4m3(_ptr(A), _ptr(B), _ptr(C), M, N, K, max(A.strides[0], K), max(B.strides[0], K),
+                                    N, scale, int(threads))
+    return C
+
+
+def gemm_fp8_entries(A: np.ndarray, B: np.ndarray, rows, cols, scale_a: float = 1.0, scale_b: float = 1.0,
+                     threads: int = 0) -> np.ndarray:
+    A = _as_bytes(A, "A")
+    B = _as_bytes(B, "B")
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    out = np.zeros(rows.size, dtype=np.uint16)
+    scale = float(np.float32(scale_a)) * float(np.float32(scale_b))
+    if rows.size:
+        _load().oracle_gemm_fp8e4m3_entries(_ptr(A), _ptr(B), _ptr(out), A.shape[1], A.strides[0], B.strides[0],
+                                            scale, _ptr(rows), _ptr(cols), rows.size, int(threads))
     return out

@@ -220,3 +220,89 @@ int oracle_gemm_bf16_epilogue_entries(const uint16_t* A, const uint16_t* B, cons
     work_t w = {A, B, out, bias, act, 0, K, lda, ldb, 0, rows, cols, 0, 0, 1};
     return run_parallel(w, count, threads);
 }
+
+/* ---- FP8 (E4M3) GEMM with per-tensor scales ------------------------------
+ * C[i][j] = round_bf16_rne( sa * sb * sum_k e4m3(A[i][k]) * e4m3(B[j][k]) )
+ * (the FP8 GEMM row of the HipKittens "L2" detail page's §3 "Target
+ * operation" table: 8-bit inputs, FP32 accumulation, bf16 output; here with
+ * one scale per operand tensor). E4M3 (the OCP 8-bit format): 1 sign bit, 4
+ * exponent bits with bias 7, 3 fraction bits; exponent field 0 encodes
+ * subnormals m/8 * 2^-6; S.1111.111 is NaN; there is no infinity; the largest
+ * finite magnitude is 1.75 * 2^8 = 448. Every E4M3 value and every product
+ * of two is exact in binary64. */
+double oracle_e4m3_to_double(uint8_t b) {
+    int s = (b >> 7) & 1, e = (b >> 3) & 0xF, m = b & 7;
+    double v;
+    if (e == 0xF && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+typedef struct {
+    const uint8_t* A;
+    const uint8_t* B;
+    uint16_t* out;
+    int64_t N, K, lda, ldb, ldo;
+    const int64_t* rows;
+    const int64_t* cols;
+    int64_t begin, end;
+    int mode;
+    double scale;
+} work8_t;
+
+static uint16_t entry8(const work8_t* w, int64_t i, int64_t j) {
+    const uint8_t* a = w->A + i * w->lda;
+    const uint8_t* b = w->B + j * w->ldb;
+    double s = 0.0;
+    for (int64_t k = 0; k < w->K; ++k) s += oracle_e4m3_to_double(a[k]) * oracle_e4m3_to_double(b[k]);
+    return oracle_round_bf16(w->scale * s);
+}
+
+static void* worker8(void* p) {
+    work8_t* w = (work8_t*)p;
+    for (int64_t t = w->begin; t < w->end; ++t) {
+        if (w->mode == 0) {
+            int64_t i = w->rows ? w->rows[t] : t;
+            uint16_t* o = w->out + t * w->ldo;
+            for (int64_t j = 0; j < w->N; ++j) o[j] = entry8(w, i, j);
+        } else {
+            w->out[t] = entry8(w, w->rows[t], w->cols[t]);
+        }
+    }
+    return NULL;
+}
+
+static int run_parallel8(work8_t base, int64_t items, int threads) {
+    threads = resolve_threads(threads, items);
+    pthread_t tid[256];
+    int joined[256];
+    work8_t w[256];
+    for (int t = 0; t < threads; ++t) {
+        w[t] = base;
+        w[t].begin = items * t / threads;
+        w[t].end = items * (t + 1) / threads;
+        joined[t] = 0;
+        if (t == threads - 1) worker8(&w[t]);
+        else if (pthread_create(&tid[t], NULL, worker8, &w[t]) == 0) joined[t] = 1;
+        else worker8(&w[t]);
+    }
+    for (int t = 0; t < threads - 1; ++t)
+        if (joined[t]) pthread_join(tid[t], NULL);
+    return threads;
+}
+
+/* Full FP8 GEMM; `scale` = sa * sb (taken in binary64). */
+int oracle_gemm_fp8e4m3(const uint8_t* A, const uint8_t* B, uint16_t* C, int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldc, double scale, int threads) {
+    work8_t w = {A, B, C, N, K, lda, ldb, ldc, NULL, NULL, 0, 0, 0, scale};
+    return run_parallel8(w, M, threads);
+}
+
+/* Selected entries of the FP8 GEMM. */
+int oracle_gemm_fp8e4m3_entries(const uint8_t* A, const uint8_t* B, uint16_t* out, int64_t K, int64_t lda,
+                                int64_t ldb, double scale, const int64_t* rows, const int64_t* cols,
+                                int64_t count, int threads) {
+    work8_t w = {A, B, out, 0, K, lda, ldb, 0, rows, cols, 0, 0, 1, scale};
+    return run_parallel8(w, count, threads);
+}

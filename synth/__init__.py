@@ -14,7 +14,9 @@ shapes of the same operation):
   round-to-nearest-even on the float32 bit pattern;
 * integer entries: ``integers(-4, 5)`` (uniform on {-4..4}), exact in bf16;
 * seeds: A = 1000 + workload id, B = 2000 + workload id (integer variant 1100+,
-  2100+), sample positions 3000 + workload id.
+  2100+), sample positions 3000 + workload id;
+* FP8 workloads: the same normal draws rounded to E4M3 codes (nearest value,
+  ties to the even code, saturating at ±448).
 """
 from __future__ import annotations
 
@@ -45,6 +47,21 @@ WORKLOADS = {
     "skinny_128x28672x8192": Workload("skinny_128x28672x8192", 6, 128, 28672, 8192, 0.02, False),
 }
 
+# FP8 (E4M3) workloads: operands N(0,1) rounded to E4M3, per-tensor scales
+# (the FP8 GEMM of the pages, headline shape 8192^3).
+FP8_WORKLOADS = {
+    "fp8_gemm_8192": Workload("fp8_gemm_8192", 7, 8192, 8192, 8192, 1.0, True),
+    "fp8_gemm_256": Workload("fp8_gemm_256", 8, 256, 256, 256, 1.0, False),
+}
+FP8_SCALES = (0.5, 0.25)   # scale_a, scale_b of the FP8 workloads
+
+
+def operands_fp8(w: Workload, integer: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """(A, B) E4M3 codes for an FP8 workload."""
+    if integer:
+        return int_e4m3(w.M, w.K, 1100 + w.wid), int_e4m3(w.N, w.K, 2100 + w.wid)
+    return (normal_e4m3(w.M, w.K, 1000 + w.wid, w.scale), normal_e4m3(w.N, w.K, 2000 + w.wid, w.scale))
+
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """float32 -> bf16 bit patterns, round-to-nearest-even on the low 16 bits.
@@ -59,6 +76,52 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
     """bf16 bit patterns -> float32 values (exact)."""
     return (np.asarray(h, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _e4m3_table():
+    """Non-negative finite E4M3 values for codes 0x00..0x7E (ascending)."""
+    codes = np.arange(0x7F, dtype=np.int64)
+    e = codes >> 3
+    m = codes & 7
+    vals = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    return vals
+
+
+_E4M3 = _e4m3_table()
+
+
+def f32_to_e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """float32 -> E4M3 codes: nearest representable value, ties to the even
+    code, magnitudes above 448 saturate to 448."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), _E4M3[-1])
+    hi = np.clip(np.searchsorted(_E4M3, a, side="left"), 0, len(_E4M3) - 1)
+    lo = np.clip(hi - 1, 0, len(_E4M3) - 1)
+    dlo = np.abs(a - _E4M3[lo])
+    dhi = np.abs(_E4M3[hi] - a)
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    sign = (np.signbit(x) & (pick != 0)).astype(np.int64) << 7
+    return (pick | sign).astype(np.uint8)
+
+
+def normal_e4m3(rows: int, cols: int, seed: int, scale: float = 1.0) -> np.ndarray:
+    """rows×cols E4M3 codes of N(0,1)·scale, drawn row-major from PCG64(seed)."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    out = np.empty(rows * cols, dtype=np.uint8)
+    s = np.float32(scale)
+    for off in range(0, rows * cols, _CHUNK):
+        n = min(_CHUNK, rows * cols - off)
+        x = g.standard_normal(n, dtype=np.float32)
+        if scale != 1.0:
+            x *= s
+        out[off:off + n] = f32_to_e4m3_codes(x)
+    return out.reshape(rows, cols)
+
+
+def int_e4m3(rows: int, cols: int, seed: int, lo: int = -4, hi: int = 4) -> np.ndarray:
+    """rows×cols E4M3 codes of integers uniform on {lo..hi} (exact in E4M3)."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    return f32_to_e4m3_codes(g.integers(lo, hi + 1, size=(rows, cols)).astype(np.float32))
 
 
 def normal_bf16(rows: int, cols: int, seed: int, scale: float = 1.0) -> np.ndarray:

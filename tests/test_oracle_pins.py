@@ -218,7 +218,8 @@ def test_empty_k_gives_zero(oracle_lib):
 MUTANTS = {
     "dropped_last_term": ("for (int64_t k = 0; k < K; ++k) s +=", "for (int64_t k = 0; k + 1 < K; ++k) s +="),
     "transposed_B": ("const uint16_t* b = B + j * ldb;", "const uint16_t* b = B + j;"),
-    "swapped_index": ("int64_t i = w->rows ? w->rows[t] : t;", "int64_t i = w->rows ? w->rows[t] : (t + 1) % (w->end);"),
+    "swapped_index": ("for (int64_t j = 0; j < w->N; ++j) o[j] = entry(w, i, j);",
+                      "for (int64_t j = 0; j < w->N; ++j) o[j] = entry(w, (i + 1) % w->end, j);"),
     "ties_away": ("if (fmod(fl, 2.0) != 0.0) n = fl + 1.0;", "n = fl + 1.0;"),
     "truncation": ("if (frac > 0.5) {", "if (frac > 2.0) {"),
     "sign_error": ("s += bf16_bits_to_double(a[k]) * bf16_bits_to_double(b[k]);",
@@ -358,3 +359,127 @@ def test_epilogue_mutants_fail_pins(tmp_path, name):
     mutant = _EpiLib(str(path_so))
     assert pin_activation_values(mutant) is not None or pin_epilogue_gemm(mutant) is not None, \
         f"mutant {name} passed the epilogue pins"
+
+
+# ------------------------------------------------------------ FP8 (E4M3) --
+
+def pin_e4m3_decode(o):
+    """All 256 E4M3 codes against PyTorch's float8_e4m3fn (a library routine),
+    plus the format's documented landmarks: 448 = largest (0x7E), 2^-6 =
+    smallest normal (0x08), 2^-9 = smallest subnormal (0x01), 1.0 = 0x38,
+    NaN = 0x7F / 0xFF."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([o.e4m3_value(int(c)) for c in codes])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    if not same.all():
+        return f"decode differs at codes {np.nonzero(~same)[0][:5].tolist()}"
+    marks = {0x7E: 448.0, 0x08: 2.0 ** -6, 0x01: 2.0 ** -9, 0x38: 1.0, 0xB8: -1.0}
+    for c, v in marks.items():
+        if o.e4m3_value(c) != v:
+            return f"landmark {c:#x}"
+    if not (np.isnan(o.e4m3_value(0x7F)) and np.isnan(o.e4m3_value(0xFF))):
+        return "NaN codes"
+    return None
+
+
+def _exact_fp8_gemm(o, A, B, sa, sb):
+    val = {c: Fraction(o.e4m3_value(c)) for c in range(256) if not np.isnan(o.e4m3_value(c))}
+    scale = Fraction(float(np.float32(sa))) * Fraction(float(np.float32(sb)))
+    M, K = A.shape
+    N = B.shape[0]
+    C = np.zeros((M, N), dtype=np.uint16)
+    for i in range(M):
+        for j in range(N):
+            C[i, j] = round_fraction(scale * sum(val[int(A[i, k])] * val[int(B[j, k])] for k in range(K)))
+    return C
+
+
+def pin_fp8_gemm(o):
+    """Exact rational FP8 GEMMs on tiny shapes (power-of-two and general
+    float32 scales), integer inputs against int64, and the closed form
+    A ≡ a, B ≡ b ⇒ C ≡ RNE(K·a·b·sa·sb)."""
+    if not hasattr(o, "gemm_fp8"):
+        return "no FP8 entry"
+    for seed, (M, N, K, sa, sb) in enumerate([(3, 4, 5, 1.0, 1.0), (6, 5, 17, 0.5, 0.25), (4, 7, 33, 0.3, 1.7)]):
+        A = synth.normal_e4m3(M, K, 600 + seed, 2.0)
+        B = synth.normal_e4m3(N, K, 700 + seed, 3.0)
+        if not np.array_equal(o.gemm_fp8(A, B, sa, sb), _exact_fp8_gemm(o, A, B, sa, sb)):
+            return f"exact FP8 GEMM {(M, N, K, sa, sb)}"
+    Ai, Bi = synth.int_e4m3(9, 64, 801), synth.int_e4m3(7, 64, 802)
+    dec = np.vectorize(o.e4m3_value)
+    ref = dec(Ai).astype(np.int64) @ dec(Bi).astype(np.int64).T
+    want = np.array([[round_fraction(Fraction(int(v))) for v in r] for r in ref], dtype=np.uint16)
+    if not np.array_equal(o.gemm_fp8(Ai, Bi), want):
+        return "integer FP8 GEMM"
+    a, b = 0x3A, 0xC4          # 1.25 and -3.0
+    A = np.full((2, 100), a, dtype=np.uint8)
+    B = np.full((3, 100), b, dtype=np.uint8)
+    want = round_fraction(Fraction(100) * Fraction(1.25) * Fraction(-3) * Fraction(0.5) * Fraction(0.25))
+    if not np.all(o.gemm_fp8(A, B, 0.5, 0.25) == want):
+        return "closed form"
+    return None
+
+
+@pytest.mark.parametrize("pin", [pin_e4m3_decode, pin_fp8_gemm], ids=lambda p: p.__name__)
+def test_fp8_pin(oracle_lib, pin):
+    assert pin(oracle_lib) is None
+
+
+def test_e4m3_generator_matches_library_rounding():
+    import torch
+    g = np.random.Generator(np.random.PCG64(9))
+    x = (g.standard_normal(50000) * np.exp2(g.integers(-12, 8, 50000))).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = synth.f32_to_e4m3_codes(x)
+    zero = (want & 0x7F) == 0
+    assert np.array_equal(got[~zero], want[~zero]) and np.all((got[zero] & 0x7F) == 0)
+
+
+FP8_MUTANTS = {
+    "bias8": ("else v = ldexp(1.0 + (double)m / 8.0, e - 7);", "else v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "subnormal_exp": ("if (e == 0) v = ldexp((double)m / 8.0, -6);", "if (e == 0) v = ldexp((double)m / 8.0, -7);"),
+    "no_nan": ("if (e == 0xF && m == 7) return NAN;", "if (e == 0xF && m == 8) return NAN;"),
+    "scale_dropped": ("return oracle_round_bf16(w->scale * s);", "return oracle_round_bf16(s);"),
+    "mantissa_bits": ("int s = (b >> 7) & 1, e = (b >> 3) & 0xF, m = b & 7;",
+                      "int s = (b >> 7) & 1, e = (b >> 2) & 0x1F, m = b & 3;"),
+}
+
+
+class _Fp8Lib(_Lib):
+    def __init__(self, path):
+        super().__init__(path)
+        P, I = ctypes.c_void_p, ctypes.c_int64
+        self.lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        self.lib.oracle_e4m3_to_double.restype = ctypes.c_double
+        self.lib.oracle_gemm_fp8e4m3.argtypes = [P, P, P, I, I, I, I, I, I, ctypes.c_double, ctypes.c_int]
+
+    def e4m3_value(self, c):
+        return float(self.lib.oracle_e4m3_to_double(int(c) & 0xFF))
+
+    def gemm_fp8(self, A, B, sa=1.0, sb=1.0):
+        A = np.ascontiguousarray(A, dtype=np.uint8)
+        B = np.ascontiguousarray(B, dtype=np.uint8)
+        M, K = A.shape
+        N = B.shape[0]
+        C = np.zeros((M, N), dtype=np.uint16)
+        self.lib.oracle_gemm_fp8e4m3(A.ctypes.data, B.ctypes.data, C.ctypes.data, M, N, K, K, K, N,
+                                     float(np.float32(sa)) * float(np.float32(sb)), 1)
+        return C
+
+
+@pytest.mark.parametrize("name", sorted(FP8_MUTANTS))
+def test_fp8_mutants_fail_pins(tmp_path, name):
+    src = open(os.path.join(ROOT, "oracle", "gemm_ref.c")).read()
+    old, new = FP8_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    path_c = tmp_path / f"{name}.c"
+    path_so = tmp_path / f"{name}.so"
+    path_c.write_text(src.replace(old, new))
+    subprocess.run(["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                    "-D_GNU_SOURCE", str(path_c), "-o", str(path_so), "-lm"], check=True)
+    mutant = _Fp8Lib(str(path_so))
+    assert pin_e4m3_decode(mutant) is not None or pin_fp8_gemm(mutant) is not None, \
+        f"mutant {name} passed the FP8 pins"
