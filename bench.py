@@ -182,10 +182,29 @@ def max_over_ranks(world, x: float) -> float:
 
 # --------------------------------------------------------- CPU oracle --
 
+ALL_WORKLOADS = {**synth.WORKLOADS, **synth.FP8_WORKLOADS}
+
+
+def is_fp8(w) -> bool:
+    return w.name in synth.FP8_WORKLOADS
+
+
+def operands_of(w):
+    return synth.operands_fp8(w) if is_fp8(w) else synth.operands(w)
+
+
 def oracle_rows_timed(A, B, rows) -> tuple[float, int]:
     import oracle
     t0 = time.perf_counter()
-    _, used = oracle.gemm_rows(A, B, rows)
+    if A.dtype == np.uint8:      # FP8 operands: full rows as entries
+        N = B.shape[0]
+        rr = np.repeat(np.asarray(rows, dtype=np.int64), N)
+        cc = np.tile(np.arange(N, dtype=np.int64), len(rows))
+        sa, sb = synth.FP8_SCALES
+        oracle.gemm_fp8_entries(A, B, rr, cc, sa, sb)
+        used = os.cpu_count() or 1
+    else:
+        _, used = oracle.gemm_rows(A, B, rows)
     return time.perf_counter() - t0, used
 
 
@@ -208,7 +227,7 @@ def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    A, B = synth.operands(w)
+    A, B = operands_of(w)
     probe = np.arange(min(64, w.M), dtype=np.int64)
     t, _ = oracle_rows_timed(A, B, probe)
     per_row = max(t / len(probe), 1e-6)
@@ -236,12 +255,17 @@ def run_reference(args, w):
 
 
 def workload_config(w) -> dict:
-    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
-            "layout": "A MxK row-major, B NxK row-major, C MxN row-major (C = A·Bᵀ)",
-            "values": f"N(0,1)·{w.scale} rounded to bf16, seeds {1000 + w.wid}/{2000 + w.wid}",
-            "l2": "no flush: inputs larger than L2 (A+B = %d MiB > 126 MiB)" % ((w.M + w.N) * w.K * 2 >> 20)
-            if (w.M + w.N) * w.K * 2 > 126 << 20 else "inputs smaller than L2 (warm L2)",
-            "accumulate": "fp32", "output": "bf16"}
+    elem = 1 if is_fp8(w) else 2
+    cfg = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+           "layout": "A MxK row-major, B NxK row-major, C MxN row-major (C = A·Bᵀ)",
+           "values": f"N(0,1)·{w.scale} rounded to {'E4M3' if elem == 1 else 'bf16'}, "
+                     f"seeds {1000 + w.wid}/{2000 + w.wid}",
+           "l2": "no flush: inputs larger than L2 (A+B = %d MiB > 126 MiB)" % ((w.M + w.N) * w.K * elem >> 20)
+           if (w.M + w.N) * w.K * elem > 126 << 20 else "inputs smaller than L2 (warm L2)",
+           "accumulate": "fp32", "output": "bf16"}
+    if elem == 1:
+        cfg["scales"] = list(synth.FP8_SCALES)
+    return cfg
 
 
 # ---------------------------------------------------------------- GPU arm --
@@ -254,13 +278,20 @@ def run_hk(args, w):
     dev = torch.device("cuda", local)
     import dense_bf16_gemm_02_gb300 as hk
 
-    A_bits, B_bits = synth.operands(w)
-    A = torch.from_numpy(A_bits.view(np.int16)).to(dev).view(torch.bfloat16)
-    B = torch.from_numpy(B_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    fp8 = is_fp8(w)
+    A_bits, B_bits = operands_of(w)
+    if fp8:
+        A = torch.from_numpy(A_bits).to(dev)
+        B = torch.from_numpy(B_bits).to(dev)
+    else:
+        A = torch.from_numpy(A_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        B = torch.from_numpy(B_bits.view(np.int16)).to(dev).view(torch.bfloat16)
     C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.Stream(device=dev)
     sh = int(stream.cuda_stream)
-    plan = hk.Plan(w.M, w.N, w.K, device=local, group_m=args.group_m, split_k=1)
+    sa, sb = synth.FP8_SCALES
+    plan = hk.Plan(w.M, w.N, w.K, device=local, group_m=args.group_m, split_k=1,
+                   input_type=hk.HK_INPUT_E4M3 if fp8 else hk.HK_INPUT_BF16, alpha=sa * sb if fp8 else 0.0)
     info = plan.info()
     flops = gemm_flops(w.M, w.N, w.K)
 
@@ -271,6 +302,12 @@ def run_hk(args, w):
         bias_t = torch.from_numpy(bias_bits.view(np.int16)).to(dev)
 
     def step():
+        if fp8:
+            st = hk.hk_gemm_fp8_e4m3(A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, w.K, w.K, w.N, sa, sb,
+                                     sh)
+            if st != hk.HK_OK:
+                raise hk.HKError(st, "hk_gemm_fp8_e4m3")
+            return
         if bias_t is not None:
             st = hk.hk_gemm_bf16_epilogue(A.data_ptr(), B.data_ptr(), C.data_ptr(), bias_t.data_ptr(), w.M, w.N,
                                           w.K, w.K, w.K, w.N, act, sh)
@@ -325,8 +362,12 @@ def run_hk(args, w):
     # Steps are independent GEMMs, so they are pipelined on three streams:
     # the H2D copy of step i+1 and the D2H copy of step i-1 overlap the GEMM
     # of step i; device operands are double-buffered.
-    A_h = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    B_h = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    if fp8:
+        A_h = torch.from_numpy(A_bits).pin_memory()
+        B_h = torch.from_numpy(B_bits).pin_memory()
+    else:
+        A_h = torch.from_numpy(A_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        B_h = torch.from_numpy(B_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
     C_h = [torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     A_d = [A, torch.empty_like(A)]
     B_d = [B, torch.empty_like(B)]
@@ -349,10 +390,14 @@ def run_hk(args, w):
             stream.wait_event(h2d_done[k])
             if d2h_done[k] is not None:
                 stream.wait_event(d2h_done[k])      # C of slot k has been copied out
-            st = hk.hk_gemm_bf16(A_d[k].data_ptr(), B_d[k].data_ptr(), C_d[k].data_ptr(), w.M, w.N, w.K, w.K,
-                                 w.K, w.N, sh)
+            if fp8:
+                st = hk.hk_gemm_fp8_e4m3(A_d[k].data_ptr(), B_d[k].data_ptr(), C_d[k].data_ptr(), w.M, w.N, w.K,
+                                         w.K, w.K, w.N, sa, sb, sh)
+            else:
+                st = hk.hk_gemm_bf16(A_d[k].data_ptr(), B_d[k].data_ptr(), C_d[k].data_ptr(), w.M, w.N, w.K, w.K,
+                                     w.K, w.N, sh)
             if st != hk.HK_OK:
-                raise hk.HKError(st, "hk_gemm_bf16")
+                raise hk.HKError(st, "GEMM")
             comp_done[k] = torch.cuda.Event()
             comp_done[k].record(stream)
             s_d2h.wait_event(comp_done[k])
@@ -380,19 +425,31 @@ def run_hk(args, w):
     # ---- context only: the vendor library on the same GPU and inputs (outside the timed region)
     cublas = None
     if rank == 0 and not args.no_cublas_context:
-        for _ in range(3):
-            torch.matmul(A, B.t(), out=C)
-        torch.cuda.synchronize(dev)
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_ctx = max(5, min(args.steps, 50))
-        c0.record()
-        for _ in range(n_ctx):
-            torch.matmul(A, B.t(), out=C)
-        c1.record()
-        torch.cuda.synchronize(dev)
-        ms = c0.elapsed_time(c1) / n_ctx
-        cublas = {"value": flops / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_gemm": ms, "launches": n_ctx,
-                  "what": "torch.matmul (cuBLAS) on the same GPU and inputs, timed after ours; context only"}
+        try:
+            if fp8:
+                A8, B8 = A.view(torch.float8_e4m3fn), B.view(torch.float8_e4m3fn)
+                s_a = torch.tensor(sa, dtype=torch.float32, device=dev)
+                s_b = torch.tensor(sb, dtype=torch.float32, device=dev)
+                lib_call = lambda: torch._scaled_mm(A8, B8.t(), scale_a=s_a, scale_b=s_b, out_dtype=torch.bfloat16)
+                what = "torch._scaled_mm (cuBLASLt FP8) on the same GPU and inputs, timed after ours; context only"
+            else:
+                lib_call = lambda: torch.matmul(A, B.t(), out=C)
+                what = "torch.matmul (cuBLAS) on the same GPU and inputs, timed after ours; context only"
+            for _ in range(3):
+                lib_call()
+            torch.cuda.synchronize(dev)
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n_ctx = max(5, min(args.steps, 50))
+            c0.record()
+            for _ in range(n_ctx):
+                lib_call()
+            c1.record()
+            torch.cuda.synchronize(dev)
+            ms = c0.elapsed_time(c1) / n_ctx
+            cublas = {"value": flops / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_gemm": ms, "launches": n_ctx,
+                      "what": what}
+        except Exception as exc:   # context only: never fails the bench
+            cublas = {"unavailable": str(exc)[:200]}
 
     if rank != 0:
         if world > 1:
@@ -401,10 +458,10 @@ def run_hk(args, w):
         return 0
 
     peaks, peaks_src = load_peaks()
-    peak = float(peaks["bf16_tflops"])
+    peak = float(peaks["bf16_tflops"]) * (2.0 if fp8 else 1.0)   # FP8: bf16 measured × nominal ratio 4.5/2.25
     value = replica_value(flops, args.steps, world, elapsed_max)
     mean_launch_ms = statistics.mean(per_launch)
-    nbytes = gemm_bytes(w.M, w.N, w.K)
+    nbytes = gemm_bytes(w.M, w.N, w.K) if not fp8 else float(w.M * w.K + w.N * w.K + 2 * w.M * w.N)
     hbm_bound = flops / nbytes < peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)   # below the roofline knee
     if hbm_bound:
         bound, rf_unit, rf_peak = "hbm", "GB/s", float(peaks["hbm_gbs"])
@@ -413,7 +470,8 @@ def run_hk(args, w):
     else:
         bound, rf_unit, rf_peak = "tensor", UNIT, peak
         achieved = flops / (mean_launch_ms / 1e3) / 1e12
-        peak_source = f"bf16_tflops (burst) of {peaks_src}"
+        peak_source = (f"bf16_tflops (burst) of {peaks_src} × 2 (nominal fp8/bf16 ratio)" if fp8
+                       else f"bf16_tflops (burst) of {peaks_src}")
     digest = kernel_source_digest()
     traffic = None
     tr = MEASURED_TRAFFIC.get(w.name)
@@ -422,7 +480,7 @@ def run_hk(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic",
         "config": dict(workload_config(w), parallelism="replicas" if world > 1 else "single GPU",
                        epilogue=args.epilogue,
                        tile=f"{info['tile_m']}x{info['tile_n']}x{info['tile_k']} per "
@@ -433,14 +491,14 @@ def run_hk(args, w):
                      "frac": achieved / rf_peak, "traffic": traffic,
                      "peak_source": peak_source,
                      "algorithmic_flops_per_launch": flops,
-                     "algorithmic_bytes_per_launch": gemm_bytes(w.M, w.N, w.K),
+                     "algorithmic_bytes_per_launch": nbytes,
                      "mean_launch_ms": mean_launch_ms, "p10_launch_ms": float(np.percentile(per_launch, 10)),
                      "p90_launch_ms": float(np.percentile(per_launch, 90)),
                      "kernel": f"gemm_bf16_kernel ({info['tile_m']}x{info['tile_n']}, "
                                f"{info['ctas_per_unit']} CTA(s) per tile)",
                      "source_digest": digest},
         "e2e": {"value": replica_value(flops, e2e_steps, world, e2e_ms), "unit": UNIT,
-                "h2d_bytes_per_step": int(A_h.numel() * 2 + B_h.numel() * 2),
+                "h2d_bytes_per_step": int(A_h.numel() * A_h.element_size() + B_h.numel() * B_h.element_size()),
                 "d2h_bytes_per_step": int(C_h[0].numel() * 2), "steps": e2e_steps,
                 "pipelined": "H2D(i+1) | GEMM(i) | D2H(i-1) on three streams"},
         "gpu_launches": args.steps * int(info["kernels_per_run"]),
@@ -462,7 +520,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["hk", "reference"], default="hk")
-    ap.add_argument("--workload", default="gemm_8192", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="gemm_8192", choices=sorted(ALL_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cublas-context", action="store_true")
     ap.add_argument("--epilogue", default="none", choices=["none", "bias", "bias_relu", "bias_gelu", "bias_silu"],
@@ -471,7 +529,7 @@ def main(argv=None):
                     help="raster group height in tile rows (0: the library default via hk_gemm_bf16)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
-    w = synth.WORKLOADS[args.workload]
+    w = ALL_WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
     return run_hk(args, w)

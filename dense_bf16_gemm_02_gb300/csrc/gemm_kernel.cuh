@@ -42,9 +42,10 @@
 namespace hk {
 
 constexpr int kCtaM = 128;           // rows of C (and of A) per CTA
-constexpr int kTileK = 64;           // K per pipeline stage (one 128-byte swizzle row)
-constexpr int kMmaK = 16;            // K per tcgen05.mma
-constexpr int kABytes = kCtaM * kTileK * 2;        // 16 KiB of A per stage per CTA
+constexpr int kRowBytes = 128;       // bytes of K per stage and row: one 128-byte swizzle row
+constexpr int kTileK = 64;           // bf16 elements of K per stage (FP8: 128)
+constexpr int kMmaKBytes = 32;       // bytes of K per tcgen05.mma (bf16 K=16, FP8 K=32)
+constexpr int kABytes = kCtaM * kRowBytes;         // 16 KiB of A per stage per CTA
 constexpr int kEpiCols = 32;                        // columns per epilogue store
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBufBytes = 32 * kEpiCols * 2;     // 32 rows × 64 B
@@ -58,7 +59,7 @@ constexpr int pow2_at_least(int x) {
 }
 
 // Compile-time geometry of one kernel instance.
-template <int kCG, int kTileN_>
+template <int kCG, int kTileN_, bool kFp8 = false>
 struct Geometry {
     static_assert(kCG == 1 || kCG == 2, "one CTA or a CTA pair");
     static_assert(kTileN_ % (16 * kCG) == 0 && kTileN_ >= 32 && kTileN_ <= 256, "MMA N");
@@ -66,7 +67,8 @@ struct Geometry {
     static constexpr int kTileN = kTileN_;                  // columns of C per tile (MMA N)
     static constexpr int kBRows = kTileN / kCG;             // rows of B each CTA loads per stage
     static_assert(kBRows % 8 == 0, "B rows fill whole 8-row swizzle atoms");
-    static constexpr int kBBytes = kBRows * kTileK * 2;
+    static constexpr int kBBytes = kBRows * kRowBytes;
+    static constexpr int kKElems = kFp8 ? 128 : 64;        // K elements per stage
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kFixed = kEpiWarps * 2 * kEpiBufBytes + 256 + 1024;   // epilogue, barriers, alignment
     static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
@@ -83,7 +85,9 @@ struct Geometry {
     static constexpr int kAccCols = kTileN;                 // TMEM columns per accumulator
     static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);
     static_assert(kTmemCols <= 512, "TMEM");
-    static constexpr uint32_t kIdesc = idesc_bf16_f32(kTileM, kTileN);
+    static constexpr uint32_t kIdesc = kFp8 ? idesc_e4m3_f32(kTileM, kTileN) : idesc_bf16_f32(kTileM, kTileN);
+    static constexpr uint32_t kIdescHalf =
+        kFp8 ? idesc_e4m3_f32(kTileM, kTileN / 2) : idesc_bf16_f32(kTileM, kTileN / 2);
 };
 
 // error bits written to the status word when a bounded wait runs out
@@ -105,6 +109,7 @@ struct GemmParams {
     uint32_t expect_bytes;        // bytes that land per stage in the cluster (both CTAs of a pair)
     int64_t n_pad;                // split K: row stride of the partial matrices (tiles_n * tile width)
     float* partials;              // split K: fp32 partial matrices P[split][M][n_pad]
+    float alpha;                  // scale of the accumulator (FP8: scale_a * scale_b; bf16: 1)
     const uint16_t* bias;         // fused epilogue: per-column bf16 bias (N values) or null
     int32_t act;                  // fused epilogue: 0 none, 1 ReLU, 2 GELU (erf), 3 SiLU
     int32_t tail_start;           // pair kernel: tiles from here on run as two half-width units (-1: none)
@@ -200,6 +205,11 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
 
 // Apply the fused epilogue to 32 accumulator values of columns col0..col0+31.
 __device__ __forceinline__ void apply_epilogue(const GemmParams& p, uint32_t (&v)[32], int col0) {
+    if (p.alpha != 1.0f) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * p.alpha);
+    }
+    if (p.bias == nullptr && p.act == 0) return;
     float b[32];
     if (p.bias != nullptr && col0 + 32 <= p.N) {
         const uint4* src = reinterpret_cast<const uint4*>(p.bias + col0);   // 64-byte aligned chunk
@@ -249,12 +259,12 @@ __device__ __forceinline__ void drain_after_abort() {
     for (int i = 0; i < 200; ++i) __nanosleep(1000);
 }
 
-template <int kCG, int kTileN>
+template <int kCG, int kTileN, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                  const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_b_half,
                  const GemmParams p) {
-    using G = Geometry<kCG, kTileN>;
+    using G = Geometry<kCG, kTileN, kFp8>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -341,11 +351,11 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                     if constexpr (kCG == 2) {
                         // both CTAs' copies complete on the leader's barrier
                         const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
-                        tma_load_2d_pair(a_dst, &tmap_a, kb * kTileK, a_row, leader_full);
-                        tma_load_2d_pair(b_dst, b_map, kb * kTileK, b_row, leader_full);
+                        tma_load_2d_pair(a_dst, &tmap_a, kb * G::kKElems, a_row, leader_full);
+                        tma_load_2d_pair(b_dst, b_map, kb * G::kKElems, b_row, leader_full);
                     } else {
-                        tma_load_2d(a_dst, &tmap_a, kb * kTileK, a_row, full_bar(stage));
-                        tma_load_2d(b_dst, &tmap_b, kb * kTileK, b_row, full_bar(stage));
+                        tma_load_2d(a_dst, &tmap_a, kb * G::kKElems, a_row, full_bar(stage));
+                        tma_load_2d(b_dst, b_map, kb * G::kKElems, b_row, full_bar(stage));
                     }
                     if (++stage == G::kStages) {
                         stage = 0;
@@ -366,7 +376,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                 unit_info(p, u, t, split, half);
                 int kb_begin, kb_end;
                 split_range(p, split, kb_begin, kb_end);
-                const uint32_t idesc = half < 0 ? G::kIdesc : idesc_bf16_f32(G::kTileM, G::kTileN / 2);
+                const uint32_t idesc = half < 0 ? G::kIdesc : G::kIdescHalf;
                 const int buf = local & 1;
                 const uint32_t acc_phase = (local >> 1) & 1;
                 const bool acc_free = kCG == 2
@@ -387,11 +397,15 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                     const uint64_t a_desc = smem_desc_kmajor_sw128(base + G::kOffA + stage * kABytes);
                     const uint64_t b_desc = smem_desc_kmajor_sw128(base + G::kOffB + stage * G::kBBytes);
 #pragma unroll
-                    for (int k = 0; k < kTileK / kMmaK; ++k) {
-                        // advance 16 bf16 = 32 bytes along K inside the swizzle atom
+                    for (int k = 0; k < kRowBytes / kMmaKBytes; ++k) {
+                        // advance 32 bytes along K inside the swizzle atom (16 bf16 or 32 FP8)
                         const uint32_t acc = (kb != kb_begin || k != 0) ? 1u : 0u;
-                        if constexpr (kCG == 2)
+                        if constexpr (kCG == 2 && kFp8)
+                            mma_f8_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
+                        else if constexpr (kCG == 2)
                             mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
+                        else if constexpr (kFp8)
+                            mma_f8_one(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
                         else
                             mma_bf16_one(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
                     }
@@ -422,7 +436,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         // the last (< 8) columns are written with plain stores, since a TMA
         // store bounds the innermost dimension only to 16-byte granules.
         auto store_chunk = [&](uint32_t (&v)[32], int row0, int col0) {
-            if (p.bias != nullptr || p.act != 0) apply_epilogue(p, v, col0);
+            if (p.bias != nullptr || p.act != 0 || p.alpha != 1.0f) apply_epilogue(p, v, col0);
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2_rn(v[2 * i], v[2 * i + 1]);
@@ -527,7 +541,8 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
 // one row.
 __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float* __restrict__ partials, int32_t splits, int32_t M, int32_t N, int64_t n_pad,
-                     uint16_t* __restrict__ C, int64_t ldc, const uint16_t* __restrict__ bias, int32_t act) {
+                     uint16_t* __restrict__ C, int64_t ldc, const uint16_t* __restrict__ bias, int32_t act,
+                     float alpha) {
     const int64_t groups_per_row = (N + 7) / 8;
     const int64_t total = static_cast<int64_t>(M) * groups_per_row;
     const int64_t split_stride = static_cast<int64_t>(M) * n_pad;
@@ -543,6 +558,10 @@ splitk_reduce_kernel(const float* __restrict__ partials, int32_t splits, int32_t
             const float4 x = __ldcs(q), y = __ldcs(q + 1);
             a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
             b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+        }
+        if (alpha != 1.0f) {
+            a.x *= alpha; a.y *= alpha; a.z *= alpha; a.w *= alpha;
+            b.x *= alpha; b.y *= alpha; b.z *= alpha; b.w *= alpha;
         }
         if (bias != nullptr || act != 0) {
             float bb[8];

@@ -9,6 +9,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -50,29 +51,36 @@ struct Variant {
     int cg;            // CTAs per work unit (1 or 2)
     int tile_m, tile_n;
     int stages, smem_bytes;
+    bool fp8;          // E4M3 operands (else bf16)
+    int k_elems;       // K elements per pipeline stage
     KernelFn fn;
     const char* name;
 };
 
-template <int kCG, int kTileN>
+template <int kCG, int kTileN, bool kFp8>
 constexpr Variant make_variant(int id, const char* name) {
-    using G = hk::Geometry<kCG, kTileN>;
-    return Variant{id, kCG, G::kTileM, G::kTileN, G::kStages, G::kSmemBytes, &hk::gemm_bf16_kernel<kCG, kTileN>,
-                   name};
+    using G = hk::Geometry<kCG, kTileN, kFp8>;
+    return Variant{id, kCG, G::kTileM, G::kTileN, G::kStages, G::kSmemBytes, kFp8, G::kKElems,
+                   &hk::gemm_bf16_kernel<kCG, kTileN, kFp8>, name};
 }
 
 const Variant kVariants[] = {
-    make_variant<2, 256>(HK_KERNEL_PAIR_256x256, "pair 256x256"),
-    make_variant<1, 256>(HK_KERNEL_SINGLE_128x256, "single 128x256"),
-    make_variant<1, 192>(HK_KERNEL_SINGLE_128x192, "single 128x192"),
-    make_variant<1, 128>(HK_KERNEL_SINGLE_128x128, "single 128x128"),
-    make_variant<1, 64>(HK_KERNEL_SINGLE_128x64, "single 128x64"),
+    make_variant<2, 256, false>(HK_KERNEL_PAIR_256x256, "pair 256x256"),
+    make_variant<1, 256, false>(HK_KERNEL_SINGLE_128x256, "single 128x256"),
+    make_variant<1, 192, false>(HK_KERNEL_SINGLE_128x192, "single 128x192"),
+    make_variant<1, 128, false>(HK_KERNEL_SINGLE_128x128, "single 128x128"),
+    make_variant<1, 64, false>(HK_KERNEL_SINGLE_128x64, "single 128x64"),
+    make_variant<2, 256, true>(HK_KERNEL_PAIR_256x256, "fp8 pair 256x256"),
+    make_variant<1, 256, true>(HK_KERNEL_SINGLE_128x256, "fp8 single 128x256"),
+    make_variant<1, 192, true>(HK_KERNEL_SINGLE_128x192, "fp8 single 128x192"),
+    make_variant<1, 128, true>(HK_KERNEL_SINGLE_128x128, "fp8 single 128x128"),
+    make_variant<1, 64, true>(HK_KERNEL_SINGLE_128x64, "fp8 single 128x64"),
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
-const Variant* find_variant(int id) {
+const Variant* find_variant(int id, bool fp8) {
     for (const Variant& v : kVariants)
-        if (v.id == id) return &v;
+        if (v.id == id && v.fp8 == fp8) return &v;
     return nullptr;
 }
 
@@ -137,7 +145,7 @@ hk_status device_info(int device, const DeviceInfo** out) {
             if (prev >= 0 && prev != device) cudaSetDevice(prev);
             if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "configuring the GEMM kernels", e);
             d.probed = true;
-            d.supported = d.max_units[0] > 0;
+            d.supported = d.max_units[0] > 0;   // the bf16 pair kernel
             if (!d.supported) d.why = "no 2-CTA cluster of the GEMM kernel fits on the device";
         }
     }
@@ -162,12 +170,14 @@ hk_status get_encoder() {
 // 2-D bf16 tensor map over a row-major (rows × cols, leading dimension ld)
 // matrix with box (box_cols × box_rows).
 hk_status encode_2d(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
-                    uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle, const char* name) {
+                    uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle, const char* name,
+                    bool bytes = false) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * (bytes ? 1u : 2u)};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t elem_strides[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+    CUresult r = g_encode(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void*>(ptr), dims, strides, box,
                           elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(HK_ERR_INVALID_ARG, "encoding the tensor map of %s failed (CUresult %d)", name, (int)r);
@@ -306,14 +316,15 @@ double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int64_t sl
     const int64_t tiles = ceil_div(M, v.tile_m) * ceil_div(N, v.tile_n);
     const int64_t units = tiles * splits;
     const double waves = double(ceil_div(units, slots));
-    const double kb = double(ceil_div(ceil_div(K, hk::kTileK), splits));
-    const double stage_bytes = double(a_rows_for(v, M) + v.tile_n / v.cg) * hk::kTileK * 2;
+    const double kb = double(ceil_div(ceil_div(K, v.k_elems), splits));
+    const double elem = v.fp8 ? 1.0 : 2.0;
+    const double stage_bytes = double(a_rows_for(v, M) + v.tile_n / v.cg) * hk::kRowBytes;
     const double cta_bytes = stage_bytes * kb;
     const double sm_rate = std::min(kSmBytesPerUs, stage_bytes * v.stages / kLoadLatencyUs);
     const double t_stream = waves * (cta_bytes / sm_rate + kFillUs);
     const double n_pad = double(ceil_div(N, v.tile_n) * v.tile_n);
     const double partials = splits > 1 ? 4.0 * splits * M * n_pad : 0.0;
-    const double operands = 2.0 * (double(N) * K + double(M) * K);
+    const double operands = elem * (double(N) * K + double(M) * K);
     const double t_hbm = (operands + (splits > 1 ? partials : 2.0 * M * N)) / kHbmBytesPerUs;
     const double t_mma = waves * kb * kKStepUsPair * (double(v.tile_n) / 256.0);
     const double t_reduce = splits > 1 ? (partials + 2.0 * M * N) / kHbmBytesPerUs + kLaunchUs : 0.0;
@@ -321,14 +332,15 @@ double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int64_t sl
 }
 
 void choose_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo* di, int max_units_cap, bool allow_split,
-                 int forced_kernel, int forced_splits, const Variant** out_v, int* out_s) {
+                 int forced_kernel, int forced_splits, bool fp8, const Variant** out_v, int* out_s) {
     const Variant* best_v = nullptr;
     int best_s = 1;
     double best_t = 0.0;
-    const int64_t k_blocks = ceil_div(K, hk::kTileK);
     for (int i = 0; i < kNumVariants; ++i) {
         const Variant& v = kVariants[i];
+        if (v.fp8 != fp8) continue;
         if (forced_kernel != HK_KERNEL_AUTO ? v.id != forced_kernel : ((M > hk::kCtaM) != (v.cg == 2))) continue;
+        const int64_t k_blocks = ceil_div(K, v.k_elems);
         int64_t slots = di->max_units[i];
         if (max_units_cap > 0 && max_units_cap < slots) slots = max_units_cap;
         const int64_t tiles = ceil_div(M, v.tile_m) * ceil_div(N, v.tile_n);
@@ -347,12 +359,13 @@ void choose_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo* di, int max_
             }
         }
     }
-    *out_v = best_v ? best_v : &kVariants[0];
+    *out_v = best_v ? best_v : find_variant(HK_KERNEL_PAIR_256x256, fp8);
     *out_s = best_v ? best_s : 1;
 }
 
 hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                    int device, const hk_gemm_config* config, const DeviceInfo* di, bool allow_split) {
+                    int device, const hk_gemm_config* config, const DeviceInfo* di, bool allow_split,
+                    bool fp8 = false, float alpha = 1.0f) {
     p->M = M; p->N = N; p->K = K; p->lda = lda; p->ldb = ldb; p->ldc = ldc;
     p->device = device;
     std::memset(&p->cfg, 0, sizeof p->cfg);
@@ -360,15 +373,24 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     if (p->cfg.group_m < 0 || p->cfg.max_clusters < 0 || p->cfg.split_k < 0)
         return fail(HK_ERR_INVALID_ARG, "negative config field");
     if (p->cfg.activation > HK_ACT_SILU) return fail(HK_ERR_INVALID_ARG, "unknown activation %u", p->cfg.activation);
-    if (p->cfg.kernel != HK_KERNEL_AUTO && !find_variant(p->cfg.kernel))
+    if (p->cfg.input_type != HK_INPUT_BF16 && p->cfg.input_type != HK_INPUT_E4M3)
+        return fail(HK_ERR_INVALID_ARG, "unknown input type %d", (int)p->cfg.input_type);
+    if (config) {   // a plan's own element type and scale
+        fp8 = p->cfg.input_type == HK_INPUT_E4M3;
+        if (p->cfg.alpha != 0.0f) alpha = p->cfg.alpha;
+        if (!std::isfinite(alpha)) return fail(HK_ERR_INVALID_ARG, "alpha must be finite");
+        if (fp8 && ((lda % 16) || (ldb % 16)))
+            return fail(HK_ERR_MISALIGNED, "FP8 leading dimensions must be multiples of 16 elements");
+    }
+    if (p->cfg.kernel != HK_KERNEL_AUTO && !find_variant(p->cfg.kernel, fp8))
         return fail(HK_ERR_INVALID_ARG, "unknown kernel id %d", (int)p->cfg.kernel);
-    const int64_t k_blocks_all = ceil_div(K, hk::kTileK);
+    const int64_t k_blocks_all = ceil_div(K, fp8 ? 128 : hk::kTileK);
     if (p->cfg.split_k > 1 && (p->cfg.split_k > k_blocks_all || p->cfg.split_k > 4096))
         return fail(HK_ERR_INVALID_ARG, "split_k %d exceeds the %lld K blocks of 64", (int)p->cfg.split_k,
                     (long long)k_blocks_all);
     const Variant* v = nullptr;
     int splits = 1;
-    choose_plan(M, N, K, di, p->cfg.max_clusters, allow_split, p->cfg.kernel, p->cfg.split_k, &v, &splits);
+    choose_plan(M, N, K, di, p->cfg.max_clusters, allow_split, p->cfg.kernel, p->cfg.split_k, fp8, &v, &splits);
     p->variant = v;
     p->sm_count = di->sm_count;
     const int vi = static_cast<int>(v - kVariants);
@@ -380,14 +402,15 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     g.K = static_cast<int32_t>(K);
     g.tiles_m = static_cast<int32_t>(ceil_div(M, v->tile_m));
     g.tiles_n = static_cast<int32_t>(ceil_div(N, v->tile_n));
-    g.k_blocks = static_cast<int32_t>(ceil_div(K, hk::kTileK));
+    g.k_blocks = static_cast<int32_t>(ceil_div(K, v->k_elems));
+    g.alpha = alpha;
     const int64_t tiles = int64_t(g.tiles_m) * g.tiles_n;
     if (tiles > (int64_t(1) << 30)) return fail(HK_ERR_INVALID_ARG, "too many output tiles");
     g.num_tiles = static_cast<int32_t>(tiles);
     g.splits = splits;
     if (int64_t(splits) * tiles > (int64_t(1) << 30)) return fail(HK_ERR_INVALID_ARG, "too many work units");
     g.a_rows = a_rows_for(*v, M);
-    g.expect_bytes = static_cast<uint32_t>(v->cg * (g.a_rows + v->tile_n / v->cg) * hk::kTileK * 2);
+    g.expect_bytes = static_cast<uint32_t>(v->cg * (g.a_rows + v->tile_n / v->cg) * hk::kRowBytes);
     g.n_pad = int64_t(g.tiles_n) * v->tile_n;
     p->ws_bytes = splits > 1 ? static_cast<size_t>(splits) * static_cast<size_t>(M) * g.n_pad * 4 : 0;
     g.group_m = group_m;
@@ -412,7 +435,7 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
             g.total_units = static_cast<int32_t>(g.num_tiles + last);
         }
     }
-    g.expect_bytes_half = static_cast<uint32_t>(v->cg * (g.a_rows + v->tile_n / v->cg / 2) * hk::kTileK * 2);
+    g.expect_bytes_half = static_cast<uint32_t>(v->cg * (g.a_rows + v->tile_n / v->cg / 2) * hk::kRowBytes);
     if (units > g.total_units) units = g.total_units;
     p->grid_ctas = v->cg * units;
     if (const char* log = std::getenv("HK_LOG"); log && log[0] == '1')
@@ -429,18 +452,20 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
     if (s != HK_OK) return s;
     CUtensorMap ta, tb, tc;
     // A with K == 0 is never read; give the map a valid 1-column shape over C's memory
+    const Variant* v = p->variant;
+    const bool bytes = v->fp8;               // FP8 operands: 1-byte elements
     const void* a_ptr = p->K > 0 ? A : C;
     const void* b_ptr = p->K > 0 ? B : C;
-    const int64_t kk = p->K > 0 ? p->K : 8;
-    const int64_t lda = p->K > 0 ? p->lda : p->ldc;
-    const int64_t ldb = p->K > 0 ? p->ldb : p->ldc;
-    const Variant* v = p->variant;
+    const int64_t kk = p->K > 0 ? p->K : (bytes ? 16 : 8);
+    const int64_t lda = p->K > 0 ? p->lda : (bytes ? 2 * p->ldc : p->ldc);
+    const int64_t ldb = p->K > 0 ? p->ldb : (bytes ? 2 * p->ldc : p->ldc);
     const uint32_t b_rows = static_cast<uint32_t>(v->tile_n / v->cg);
     const uint32_t a_box_rows = static_cast<uint32_t>(p->params.a_rows);
-    if ((s = encode_2d(&ta, a_ptr, p->K > 0 ? p->M : 1, kk, lda, hk::kTileK, a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B, "A")) != HK_OK) return s;
-    if ((s = encode_2d(&tb, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, hk::kTileK, b_rows, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != HK_OK) return s;
+    const uint32_t box_k = static_cast<uint32_t>(v->k_elems);
+    if ((s = encode_2d(&ta, a_ptr, p->K > 0 ? p->M : 1, kk, lda, box_k, a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B, "A", bytes)) != HK_OK) return s;
+    if ((s = encode_2d(&tb, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, box_k, b_rows, CU_TENSOR_MAP_SWIZZLE_128B, "B", bytes)) != HK_OK) return s;
     CUtensorMap tbh;   // B in boxes of half the rows, for half-width units
-    if ((s = encode_2d(&tbh, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, hk::kTileK, b_rows / 2, CU_TENSOR_MAP_SWIZZLE_128B, "B")) != HK_OK) return s;
+    if ((s = encode_2d(&tbh, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, box_k, b_rows / 2, CU_TENSOR_MAP_SWIZZLE_128B, "B", bytes)) != HK_OK) return s;
     // the map covers N rounded down to a multiple of 8 (see the epilogue); at
     // least 8 columns so that it stays valid when N < 8 (then it is unused)
     const int64_t n_tma = p->N & ~int64_t(7);
@@ -471,7 +496,7 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
         const int64_t groups = p->M * ceil_div(p->N, 8);
         const int64_t blocks = std::min<int64_t>(ceil_div(groups, 256), int64_t(p->sm_count) * 8);
         hk::splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            g.partials, g.splits, g.M, g.N, g.n_pad, g.c_ptr, g.ldc, g.bias, g.act);
+            g.partials, g.splits, g.M, g.N, g.n_pad, g.c_ptr, g.ldc, g.bias, g.act, g.alpha);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(HK_ERR_LAUNCH, "launching the split-K reduction", e);
     }
@@ -530,7 +555,7 @@ hk_status hk_gemm_plan_get_info(const hk_gemm_plan* p, hk_gemm_plan_info* info) 
     if (!p || !info) return fail(HK_ERR_INVALID_ARG, "NULL plan or info");
     std::memset(info, 0, sizeof *info);
     info->M = p->M; info->N = p->N; info->K = p->K;
-    info->tile_m = p->variant->tile_m; info->tile_n = p->variant->tile_n; info->tile_k = hk::kTileK;
+    info->tile_m = p->variant->tile_m; info->tile_n = p->variant->tile_n; info->tile_k = p->variant->k_elems;
     info->stages = p->variant->stages;
     info->kernel = p->variant->id;
     info->ctas_per_unit = p->variant->cg;
@@ -673,6 +698,45 @@ hk_status hk_gemm_bf16_epilogue(const void* A, const void* B, void* C, const voi
     if ((s = fill_plan(&plan, M, N, K, lda, ldb, ldc, device, &cfg, di, false)) != HK_OK) return s;
     plan.owns_status = false;
     return launch(&plan, sw, A, B, C, nullptr, static_cast<cudaStream_t>(stream), bias);
+}
+
+hk_status hk_gemm_fp8_e4m3(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                           int64_t ldb, int64_t ldc, float scale_a, float scale_b, void* stream) {
+    // bf16 rules for C; for the 1-byte operands the TMA stride rule asks for
+    // leading dimensions that are multiples of 16 elements
+    hk_status s = check_shape(M, N, K, lda, ldb, ldc);
+    if (s != HK_OK) return s;
+    if ((lda % 16) || (ldb % 16))
+        return fail(HK_ERR_MISALIGNED, "FP8 leading dimensions must be multiples of 16 elements (lda=%lld ldb=%lld)",
+                    (long long)lda, (long long)ldb);
+    if (!std::isfinite(scale_a) || !std::isfinite(scale_b))
+        return fail(HK_ERR_INVALID_ARG, "FP8 scales must be finite");
+    if (M == 0 || N == 0) return HK_OK;
+    if ((s = check_pointers(A, B, C, K)) != HK_OK) return s;
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "cudaGetDevice", e);
+    const DeviceInfo* di = nullptr;
+    if ((s = device_info(device, &di)) != HK_OK) return s;
+    StatusWord* sw = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_ctx_mutex);
+        if (!g_ctx[device]) {
+            StatusWord* w = new (std::nothrow) StatusWord();
+            if (!w) return fail(HK_ERR_INVALID_ARG, "out of host memory");
+            if ((s = alloc_status(w)) != HK_OK) {
+                delete w;
+                return s;
+            }
+            g_ctx[device] = w;
+        }
+        sw = g_ctx[device];
+    }
+    hk_gemm_plan plan;
+    const float alpha = static_cast<float>(static_cast<double>(scale_a) * static_cast<double>(scale_b));
+    if ((s = fill_plan(&plan, M, N, K, lda, ldb, ldc, device, nullptr, di, false, true, alpha)) != HK_OK) return s;
+    plan.owns_status = false;
+    return launch(&plan, sw, A, B, C, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------- no-allocation variant --

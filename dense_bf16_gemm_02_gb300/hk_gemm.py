@@ -37,6 +37,9 @@ HK_ACT_RELU = 1
 HK_ACT_GELU = 2
 HK_ACT_SILU = 3
 
+HK_INPUT_BF16 = 0
+HK_INPUT_E4M3 = 1
+
 HK_FLAG_NONE = 0x0
 HK_FLAG_FAULT_DROP_ARRIVE = 0x1
 HK_FLAG_NO_TAIL_SPLIT = 0x2
@@ -45,7 +48,7 @@ EXPORTED = (
     "hk_gemm_bf16", "hk_gemm_plan_create", "hk_gemm_plan_workspace_size", "hk_gemm_plan_get_info",
     "hk_gemm_plan_run", "hk_gemm_plan_device_status", "hk_gemm_last_device_status",
     "hk_gemm_plan_destroy", "hk_status_string", "hk_gemm_last_error_string", "hk_gemm_bf16_noalloc",
-    "hk_gemm_bf16_epilogue", "hk_gemm_plan_run_epilogue",
+    "hk_gemm_bf16_epilogue", "hk_gemm_plan_run_epilogue", "hk_gemm_fp8_e4m3",
 )
 
 
@@ -53,7 +56,7 @@ class hk_gemm_config(ctypes.Structure):
     _fields_ = [("group_m", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("kernel", ctypes.c_int32),
                 ("timeout_ns", ctypes.c_uint64), ("flags", ctypes.c_uint32),
-                ("activation", ctypes.c_uint32)]
+                ("activation", ctypes.c_uint32), ("input_type", ctypes.c_int32), ("alpha", ctypes.c_float)]
 
 
 class hk_gemm_plan_info(ctypes.Structure):
@@ -118,6 +121,8 @@ def load() -> ctypes.CDLL:
         lib.hk_gemm_bf16_epilogue.restype = I32
         lib.hk_gemm_plan_run_epilogue.argtypes = [P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.hk_gemm_plan_run_epilogue.restype = I32
+        lib.hk_gemm_fp8_e4m3.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, ctypes.c_float, ctypes.c_float, P]
+        lib.hk_gemm_fp8_e4m3.restype = I32
         lib.hk_gemm_bf16_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, ctypes.c_int32, P]
         lib.hk_gemm_bf16_noalloc.restype = I32
         _lib = lib
@@ -135,6 +140,12 @@ def hk_gemm_bf16_epilogue(A: int, B: int, C: int, bias: int, M: int, N: int, K: 
                           ldc: int, activation: int = 0, stream: int = 0) -> int:
     """C = bf16(act(A·Bᵀ + bias)) (bias: device pointer or 0)."""
     return load().hk_gemm_bf16_epilogue(A, B, C, bias or None, M, N, K, lda, ldb, ldc, activation, stream)
+
+
+def hk_gemm_fp8_e4m3(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
+                     scale_a: float = 1.0, scale_b: float = 1.0, stream: int = 0) -> int:
+    """C (bf16) = (scale_a·scale_b)·A·Bᵀ for E4M3 operands A (M×K), B (N×K)."""
+    return load().hk_gemm_fp8_e4m3(A, B, C, M, N, K, lda, ldb, ldc, scale_a, scale_b, stream)
 
 
 def hk_gemm_bf16_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
@@ -203,12 +214,13 @@ class Plan:
     """A plan for one GEMM shape (wraps hk_gemm_plan_*)."""
 
     def __init__(self, M, N, K, lda=None, ldb=None, ldc=None, device=0, group_m=0, max_clusters=0,
-                 split_k=0, timeout_ns=0, flags=0, kernel=0, activation=0):
+                 split_k=0, timeout_ns=0, flags=0, kernel=0, activation=0, input_type=0, alpha=0.0):
         lib = load()
         self._lib = lib
         self.M, self.N, self.K = M, N, K
         cfg = hk_gemm_config(group_m=group_m, max_clusters=max_clusters, split_k=split_k,
-                             timeout_ns=timeout_ns, flags=flags, kernel=kernel, activation=activation)
+                             timeout_ns=timeout_ns, flags=flags, kernel=kernel, activation=activation,
+                             input_type=input_type, alpha=alpha)
         handle = ctypes.c_void_p()
         st = lib.hk_gemm_plan_create(ctypes.byref(handle), M, N, K, lda if lda is not None else K,
                                      ldb if ldb is not None else K, ldc if ldc is not None else N,

@@ -103,7 +103,12 @@ typedef struct hk_gemm_config {
     uint64_t timeout_ns;    /* limit of each bounded wait in the kernel (default 1 s) */
     uint32_t flags;         /* HK_FLAG_* */
     uint32_t activation;    /* fused epilogue activation, HK_ACT_* (used by hk_gemm_plan_run_epilogue) */
+    int32_t input_type;     /* HK_INPUT_BF16 (default) or HK_INPUT_E4M3 (1-byte operands, ld multiples of 16) */
+    float alpha;            /* scale applied to the fp32 accumulator before rounding (0: 1.0) */
 } hk_gemm_config;
+
+#define HK_INPUT_BF16 0
+#define HK_INPUT_E4M3 1
 
 /* What a plan chose (for logging and benchmarks). */
 typedef struct hk_gemm_plan_info {
@@ -175,6 +180,21 @@ hk_status hk_gemm_bf16_epilogue(const void* A, const void* B, void* C, const voi
 hk_status hk_gemm_plan_run_epilogue(const hk_gemm_plan* plan, const void* A, const void* B, void* C,
                                     const void* bias, void* workspace, size_t workspace_bytes,
                                     void* stream);
+
+/* FP8 GEMM (the pages' second GEMM: 8-bit floating-point inputs, FP32
+ * accumulation, bf16 output), with one scale per operand tensor:
+ *     C[i,j] = bf16_rne( (scale_a·scale_b) · Σ_k e4m3(A[i,k])·e4m3(B[j,k]) )
+ * A (M×K) and B (N×K) hold E4M3 codes (1 sign, 4 exponent bits with bias 7,
+ * 3 fraction bits; no infinities; largest magnitude 448), row-major,
+ * K-contiguous; C is bf16 as in hk_gemm_bf16. lda and ldb are in elements
+ * (= bytes) and must be multiples of 16, ldc a multiple of 8 (else
+ * HK_ERR_MISALIGNED); scale_a·scale_b is formed in double and rounded once
+ * to float. The products accumulate in fp32 on the tensor cores
+ * (tcgen05.mma kind::f8f6f4). Block-scaled MXFP8 is not provided. */
+hk_status hk_gemm_fp8_e4m3(const void* A, const void* B, void* C,
+                           int64_t M, int64_t N, int64_t K,
+                           int64_t lda, int64_t ldb, int64_t ldc,
+                           float scale_a, float scale_b, void* stream);
 
 /* Synchronise the plan's device and read-and-clear its status word:
  * HK_OK, or HK_ERR_TIMEOUT if a bounded wait ran out in any run since the

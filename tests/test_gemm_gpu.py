@@ -484,3 +484,67 @@ def test_epilogue_argument_errors(hk):
                                     64, 64, 64, 1, 0) == hk.HK_ERR_MISALIGNED
     assert hk.hk_gemm_bf16_epilogue(A.data_ptr(), A.data_ptr(), C.data_ptr(), bias.data_ptr(), 64, 64, 64,
                                     64, 64, 64, 7, 0) == hk.HK_ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------ FP8 (E4M3) --
+
+def run_fp8(hk, A_codes, B_codes, sa=1.0, sb=1.0):
+    import torch
+    M, K = A_codes.shape
+    N = B_codes.shape[0]
+    kp = (-K) % 16
+    def dev(x, pad):
+        st = np.zeros((x.shape[0], x.shape[1] + pad), dtype=np.uint8)
+        st[:, :x.shape[1]] = x
+        return torch.from_numpy(st).to("cuda")
+    A, B = dev(A_codes, kp), dev(B_codes, kp + 16)
+    ldc = N + ((-N) % 8)
+    C, Cstore = to_device(np.full((M, N), SENTINEL, dtype=np.uint16), rows_pad=1, cols_pad=ldc - N, fill=SENTINEL)
+    st = hk.hk_gemm_fp8_e4m3(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, A.stride(0), B.stride(0),
+                             Cstore.stride(0), sa, sb, int(torch.cuda.current_stream().cuda_stream))
+    assert st == hk.HK_OK, hk.hk_gemm_last_error_string()
+    torch.cuda.synchronize()
+    assert hk.hk_gemm_last_device_status(torch.cuda.current_device()) == hk.HK_OK
+    full = to_host(Cstore)
+    guard = full.copy()
+    guard[:M, :N] = SENTINEL
+    assert np.all(guard == SENTINEL), "a write landed outside C"
+    return full[:M, :N]
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (256, 256, 128), (300, 517, 200), (64, 1000, 640), (1000, 1300, 1000),
+                                   (2048, 2048, 2048)])
+def test_fp8_integer_bitexact(hk, M, N, K):
+    A = synth.int_e4m3(M, K, 1700 + M)
+    B = synth.int_e4m3(N, K, 2700 + N)
+    got = run_fp8(hk, A, B, 0.5, 0.25)
+    assert_bitexact(got, oracle.gemm_fp8(A, B, 0.5, 0.25), f"fp8 int {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (300, 517, 200), (128, 4096, 4096), (1500, 700, 1900)])
+def test_fp8_normal(hk, M, N, K):
+    A = synth.normal_e4m3(M, K, 1800 + M)
+    B = synth.normal_e4m3(N, K, 2800 + N)
+    sa, sb = synth.FP8_SCALES
+    got = run_fp8(hk, A, B, sa, sb)
+    assert_close(got, oracle.gemm_fp8(A, B, sa, sb), K, sa, sb, f"fp8 {M}x{N}x{K}")
+
+
+def test_fp8_workload_8192(hk):
+    w = synth.FP8_WORKLOADS["fp8_gemm_8192"]
+    A, B = synth.operands_fp8(w)
+    sa, sb = synth.FP8_SCALES
+    got = run_fp8(hk, A, B, sa, sb)
+    r, c = synth.sample_positions(w.M, w.N, 3000 + w.wid)
+    ref = oracle.gemm_fp8_entries(A, B, r, c, sa, sb)
+    assert_close(got[r, c], ref, w.K, sa, sb, "fp8 8192^3 samples")
+
+
+def test_fp8_argument_errors(hk):
+    import torch
+    A = torch.zeros((64, 64), dtype=torch.uint8, device="cuda")
+    C = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    assert hk.hk_gemm_fp8_e4m3(A.data_ptr(), A.data_ptr(), C.data_ptr(), 64, 64, 40, 40, 64, 64, 1.0, 1.0, 0) == \
+        hk.HK_ERR_MISALIGNED
+    assert hk.hk_gemm_fp8_e4m3(A.data_ptr(), A.data_ptr(), C.data_ptr(), 64, 64, 64, 64, 64, 64,
+                               float("inf"), 1.0, 0) == hk.HK_ERR_INVALID_ARG
