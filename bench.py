@@ -41,6 +41,8 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources whose digest is given; see profiles/.
 MEASURED_TRAFFIC = {
+    "fp8_gemm_8192": {"source_digest": "65485f133f7bc8ea", "bytes_per_launch": 341788416 + 116316928,
+                      "profile": "profiles/gemm_fp8_kernel_pair256_fp8_gemm_8192.md"},
     "gemm_8192": {"source_digest": "a00f76b659ea9f45", "bytes_per_launch": 1077694000 + 127190016,
                   "profile": "profiles/gemm_bf16_kernel_pair256_gemm_8192.md"},
     "skinny_128x28672x8192": {"source_digest": "a00f76b659ea9f45", "bytes_per_launch": 471919872 + 6630144,
