@@ -548,3 +548,54 @@ def test_fp8_argument_errors(hk):
         hk.HK_ERR_MISALIGNED
     assert hk.hk_gemm_fp8_e4m3(A.data_ptr(), A.data_ptr(), C.data_ptr(), 64, 64, 64, 64, 64, 64,
                                float("inf"), 1.0, 0) == hk.HK_ERR_INVALID_ARG
+
+
+# ------------------------------------------------ graphs and concurrency --
+
+def test_cuda_graph_capture_and_replay(hk):
+    """After its first call on a device, hk_gemm_bf16 enqueues only a kernel
+    launch, so a sequence of GEMMs can be captured into a CUDA graph and
+    replayed."""
+    import torch
+    A = synth.int_bf16(512, 640, 11)
+    B = synth.int_bf16(768, 640, 12)
+    At, _ = to_device(A)
+    Bt, _ = to_device(B)
+    C = torch.empty((512, 768), dtype=torch.bfloat16, device="cuda")
+    hk.gemm(At, Bt, out=C)                  # first call: per-device set-up outside the capture
+    torch.cuda.synchronize()
+    C.zero_()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            hk.gemm(At, Bt, out=C)
+    torch.cuda.synchronize()
+    C.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert_bitexact(to_host(C), oracle.gemm(A, B), "graph replay")
+    assert hk.hk_gemm_last_device_status(torch.cuda.current_device()) == hk.HK_OK
+
+
+def test_concurrent_streams_with_different_plans(hk):
+    """Persistent GEMMs of different shapes on two streams at once: no
+    kernel waits on another, so they can share the SMs in any order."""
+    import torch
+    shapes = [(2048, 2048, 1024), (128, 8192, 2048)]
+    ops, outs, refs = [], [], []
+    for i, (M, N, K) in enumerate(shapes):
+        A = synth.int_bf16(M, K, 20 + i)
+        B = synth.int_bf16(N, K, 30 + i)
+        ops.append((to_device(A)[0], to_device(B)[0]))
+        refs.append(oracle.gemm(A, B))
+    streams = [torch.cuda.Stream() for _ in shapes]
+    torch.cuda.synchronize()
+    for rep in range(4):
+        for (At, Bt), s in zip(ops, streams):
+            with torch.cuda.stream(s):
+                outs.append(hk.gemm(At, Bt))
+    torch.cuda.synchronize()
+    for i, C in enumerate(outs):
+        assert_bitexact(to_host(C), refs[i % 2], f"stream {i % 2} rep {i // 2}")
+    assert hk.hk_gemm_last_device_status(torch.cuda.current_device()) == hk.HK_OK
