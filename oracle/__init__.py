@@ -11,9 +11,14 @@ second operand used transposed as in the "ABt" GEMM of §7/§9.2:
 
     C[i, j] = RNE_bf16( Σ_k  A[i, k] · B[j, k] )      (sum in binary64)
 
+It also holds the fused-epilogue GEMM (bias + activation), the FP8 (E4M3)
+GEMM with per-tensor scales, and the attention forward of the same page's
+"MHA fwd" / "GQA fwd" rows (softmax(Q·Kᵀ/√D)·V, bf16 in and out).
+
 This module only marshals numpy arrays of bf16 bit patterns (``uint16``) to
 that C code. Every function here is pinned by ``tests/test_oracle_pins.py``
-against exact rational arithmetic, closed forms and invariants.
+and ``tests/test_oracle_attention_pins.py`` against exact rational
+arithmetic, closed forms and invariants.
 """
 from __future__ import annotations
 
@@ -84,6 +89,9 @@ def _load():
             lib.oracle_gemm_fp8e4m3_entries.argtypes = [_P, _P, _P, _I64, _I64, _I64, ctypes.c_double, _P, _P,
                                                         _I64, ctypes.c_int]
             lib.oracle_gemm_fp8e4m3_entries.restype = ctypes.c_int
+            lib.oracle_attention_fwd.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, ctypes.c_int,
+                                                 _I64, _I64, ctypes.c_int]
+            lib.oracle_attention_fwd.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -259,3 +267,28 @@ def gemm_fp8_entries(A: np.ndarray, B: np.ndarray, rows, cols, scale_a: float = 
         _load().oracle_gemm_fp8e4m3_entries(_ptr(A), _ptr(B), _ptr(out), A.shape[1], A.strides[0], B.strides[0],
                                             scale, _ptr(rows), _ptr(cols), rows.size, int(threads))
     return out
+
+
+# ---- attention forward (GQA) ---------------------------------------------
+
+def attention_fwd(Q: np.ndarray, K: np.ndarray, V: np.ndarray, causal: bool = False, rows=None,
+                  threads: int = 0, with_lse: bool = False):
+    """O = softmax(Q·Kᵀ/√D)·V per (batch, head), GQA head groups, bf16 bits in
+    and out; Q [B, Hq, S, D], K and V [B, Hkv, S, D]. ``rows`` = (begin, end)
+    of the flattened (b, h, i) rows to compute (others stay 0). With
+    ``with_lse`` also returns the float64 log-sum-exp of each row's scaled
+    scores, shape [B, Hq, S] (NaN where not computed)."""
+    for name, x in (("Q", Q), ("K", K), ("V", V)):
+        if x.dtype != np.uint16 or x.ndim != 4 or not x.flags.c_contiguous:
+            raise TypeError(f"{name} must be a contiguous 4-D uint16 array of bf16 bits")
+    B, Hq, S, D = Q.shape
+    Hkv = K.shape[1]
+    if K.shape != (B, Hkv, S, D) or V.shape != K.shape or Hq % Hkv:
+        raise ValueError("shapes do not form a GQA attention")
+    O = np.zeros_like(Q)
+    lse = np.full((B, Hq, S), np.nan) if with_lse else None
+    r0, r1 = (0, B * Hq * S) if rows is None else rows
+    if r1 > r0:
+        _load().oracle_attention_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse) if with_lse else None,
+                                     B, Hq, Hkv, S, D, int(bool(causal)), int(r0), int(r1), int(threads))
+    return (O, lse) if with_lse else O

@@ -22,6 +22,9 @@
  * round-to-nearest-even written out from the IEEE 754 definition (no detour
  * through binary32, so there is no double rounding).
  *
+ * The file also holds the fused-epilogue and FP8 variants of the GEMM and the
+ * attention forward (GQA) of the same page; each section states its source.
+ *
  * Build: plain C99, no -ffast-math, -ffp-contract=off (a fused multiply-add
  * would not change these exact products, but the flag keeps the arithmetic
  * literally what is written here).
@@ -305,4 +308,83 @@ int oracle_gemm_fp8e4m3_entries(const uint8_t* A, const uint8_t* B, uint16_t* ou
                                 int64_t count, int threads) {
     work8_t w = {A, B, out, 0, K, lda, ldb, 0, rows, cols, 0, 0, 1, scale};
     return run_parallel8(w, count, threads);
+}
+
+/* ---- attention forward (GQA) ----------------------------------------------
+ * The pages' second workload (HipKittens "L2" detail page, §3 "Target
+ * operation" table, rows MHA / GQA fwd: Q [B, Hq, S, D], K and V
+ * [B, Hkv, S, D], O [B, Hq, S, D], bf16 in, FP32 accumulate, bf16 out; §5
+ * "Numerical considerations": softmax with temperature sqrt(1/D)):
+ *     O[b,h,i,:] = round_bf16( sum_j P[i,j] V[b,g,j,:] ),
+ *     P[i,:] = softmax_j( (Q[b,h,i,:] . K[b,g,j,:]) / sqrt(D) ),  g = h / (Hq/Hkv),
+ * with j <= i when causal. Written as the definition: the scores in binary64,
+ * the softmax as exp(s_j - max_j s) / sum (the shift by the maximum changes
+ * nothing mathematically and keeps exp finite), one rounding at the end.
+ * The log-sum-exp of each row's scaled scores, ln sum_j exp(s_j), which the
+ * pages' forward kernel also stores for the backward pass (§9.3 "Attention
+ * forward", epilogue), is written to lse when it is not NULL. */
+typedef struct {
+    const uint16_t *Q, *K, *V;
+    uint16_t* O;
+    double* lse;
+    int64_t B, Hq, Hkv, S, D;
+    int causal;
+    int64_t begin, end;   /* range of (b, h, i) rows */
+} attn_t;
+
+static void* attn_worker(void* p) {
+    attn_t* w = (attn_t*)p;
+    double* s = (double*)malloc(sizeof(double) * (size_t)w->S);
+    double* o = (double*)malloc(sizeof(double) * (size_t)w->D);
+    const double scale = 1.0 / sqrt((double)w->D);
+    const int64_t group = w->Hq / w->Hkv;
+    for (int64_t r = w->begin; r < w->end; ++r) {
+        const int64_t i = r % w->S, h = (r / w->S) % w->Hq, b = r / (w->S * w->Hq), g = h / group;
+        const uint16_t* q = w->Q + ((b * w->Hq + h) * w->S + i) * w->D;
+        const uint16_t* kb = w->K + (b * w->Hkv + g) * w->S * w->D;
+        const uint16_t* vb = w->V + (b * w->Hkv + g) * w->S * w->D;
+        const int64_t n = w->causal ? i + 1 : w->S;
+        double mx = -INFINITY;
+        for (int64_t j = 0; j < n; ++j) {
+            double d = 0.0;
+            for (int64_t t = 0; t < w->D; ++t) d += bf16_bits_to_double(q[t]) * bf16_bits_to_double(kb[j * w->D + t]);
+            s[j] = d * scale;
+            if (s[j] > mx) mx = s[j];
+        }
+        double sum = 0.0;
+        for (int64_t j = 0; j < n; ++j) { s[j] = exp(s[j] - mx); sum += s[j]; }
+        for (int64_t t = 0; t < w->D; ++t) o[t] = 0.0;
+        for (int64_t j = 0; j < n; ++j)
+            for (int64_t t = 0; t < w->D; ++t) o[t] += s[j] * bf16_bits_to_double(vb[j * w->D + t]);
+        uint16_t* out = w->O + ((b * w->Hq + h) * w->S + i) * w->D;
+        for (int64_t t = 0; t < w->D; ++t) out[t] = oracle_round_bf16(o[t] / sum);
+        if (w->lse) w->lse[r] = mx + log(sum);
+    }
+    free(s);
+    free(o);
+    return NULL;
+}
+
+/* O = attention(Q, K, V) for the rows [row_begin, row_end) of the flattened
+ * (b, h, i) index (all rows: 0, B*Hq*S). Returns the number of threads used. */
+int oracle_attention_fwd(const uint16_t* Q, const uint16_t* K, const uint16_t* V, uint16_t* O, double* lse,
+                         int64_t B, int64_t Hq, int64_t Hkv, int64_t S, int64_t D, int causal,
+                         int64_t row_begin, int64_t row_end, int threads) {
+    const int64_t items = row_end - row_begin;
+    threads = resolve_threads(threads, items);
+    pthread_t tid[256];
+    int joined[256];
+    attn_t w[256];
+    for (int t = 0; t < threads; ++t) {
+        attn_t a = {Q, K, V, O, lse, B, Hq, Hkv, S, D, causal, row_begin + items * t / threads,
+                    row_begin + items * (t + 1) / threads};
+        w[t] = a;
+        joined[t] = 0;
+        if (t == threads - 1) attn_worker(&w[t]);
+        else if (pthread_create(&tid[t], NULL, attn_worker, &w[t]) == 0) joined[t] = 1;
+        else attn_worker(&w[t]);
+    }
+    for (int t = 0; t < threads - 1; ++t)
+        if (joined[t]) pthread_join(tid[t], NULL);
+    return threads;
 }

@@ -16,7 +16,11 @@ shapes of the same operation):
 * seeds: A = 1000 + workload id, B = 2000 + workload id (integer variant 1100+,
   2100+), sample positions 3000 + workload id;
 * FP8 workloads: the same normal draws rounded to E4M3 codes (nearest value,
-  ties to the even code, saturating at ±448).
+  ties to the even code, saturating at ±448);
+* attention workloads (the pages' GQA forward of §5 Fig. 7: batch 16, 64
+  query heads, 8 KV heads, head dim 64 or 128, prefill lengths 1k-8k):
+  Q, K, V entries N(0,1) rounded to bf16, laid out [B, H, S, D], seeds
+  Q = 4000 + id, K = 5000 + id, V = 6000 + id.
 """
 from __future__ import annotations
 
@@ -54,6 +58,36 @@ FP8_WORKLOADS = {
     "fp8_gemm_256": Workload("fp8_gemm_256", 8, 256, 256, 256, 1.0, False),
 }
 FP8_SCALES = (0.5, 0.25)   # scale_a, scale_b of the FP8 workloads
+
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    name: str
+    wid: int
+    B: int
+    Hq: int
+    Hkv: int
+    S: int
+    D: int
+    causal: bool
+    sampled: bool   # oracle checks sampled rows rather than every row
+
+
+ATTN_WORKLOADS = {
+    "attn_gqa_b16_s4096_d128": AttnWorkload("attn_gqa_b16_s4096_d128", 20, 16, 64, 8, 4096, 128, False, True),
+    "attn_gqa_b16_s4096_d128_causal": AttnWorkload("attn_gqa_b16_s4096_d128_causal", 21, 16, 64, 8, 4096, 128,
+                                                   True, True),
+    "attn_gqa_b16_s4096_d64": AttnWorkload("attn_gqa_b16_s4096_d64", 22, 16, 64, 8, 4096, 64, False, True),
+    "attn_gqa_small": AttnWorkload("attn_gqa_small", 23, 2, 8, 2, 300, 128, False, False),
+}
+
+
+def attn_operands(w: AttnWorkload) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """(Q, K, V) bf16 bits for an attention workload, shapes [B, H, S, D]."""
+    Q = normal_bf16(w.B * w.Hq * w.S, w.D, 4000 + w.wid).reshape(w.B, w.Hq, w.S, w.D)
+    K = normal_bf16(w.B * w.Hkv * w.S, w.D, 5000 + w.wid).reshape(w.B, w.Hkv, w.S, w.D)
+    V = normal_bf16(w.B * w.Hkv * w.S, w.D, 6000 + w.wid).reshape(w.B, w.Hkv, w.S, w.D)
+    return Q, K, V
 
 
 def operands_fp8(w: Workload, integer: bool = False) -> tuple[np.ndarray, np.ndarray]:
