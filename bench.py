@@ -516,13 +516,262 @@ def run_hk(args, w):
     return 0
 
 
+# ------------------------------------------------- attention forward --
+
+ATTN_METRIC = "GQA attention forward TFLOPS at 1 GB300 and % of dense-BF16 tensor peak"
+
+
+def attn_flops(w) -> float:
+    """Algorithmic flops of one attention forward: Q·Kᵀ and P·V, 2·D flops
+    each per visible (query, key) pair; S² pairs per head, S(S+1)/2 causal."""
+    pairs = w.S * (w.S + 1) / 2 if w.causal else float(w.S) * w.S
+    return 4.0 * w.B * w.Hq * w.D * pairs
+
+
+def attn_bytes(w) -> float:
+    """Algorithmic bytes: read Q, K, V once, write O once (bf16)."""
+    return 2.0 * w.D * w.S * w.B * (2 * w.Hq + 2 * w.Hkv)
+
+
+def attn_config(w) -> dict:
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": w.causal,
+            "layout": "Q, O [B, Hq, S, D]; K, V [B, Hkv, S, D]; bf16 row-major",
+            "values": f"N(0,1) rounded to bf16, seeds {4000 + w.wid}/{5000 + w.wid}/{6000 + w.wid}",
+            "l2": "no flush: Q alone is %d MiB > 126 MiB" % (w.B * w.Hq * w.S * w.D * 2 >> 20)
+            if w.B * w.Hq * w.S * w.D * 2 > 126 << 20 else "inputs smaller than L2 (warm L2)",
+            "softmax_scale": "1/sqrt(D)", "accumulate": "fp32", "output": "bf16"}
+
+
+def oracle_attn_rows_timed(Q, K, V, w, rows) -> tuple[float, int]:
+    """The oracle on `rows` (query rows of head (0, 0)); returns (seconds, threads)."""
+    import oracle
+    q1, k1, v1 = (np.ascontiguousarray(x[:1, :1]) for x in (Q, K, V))
+    t0 = time.perf_counter()
+    oracle.attention_fwd(q1, k1, v1, causal=w.causal, rows=(0, rows))
+    return time.perf_counter() - t0, min(os.cpu_count() or 1, rows)
+
+
+def attn_row_flops(w, rows: int) -> float:
+    pairs = rows * (rows + 1) / 2 if w.causal else float(rows) * w.S
+    return 4.0 * w.D * pairs
+
+
+def attn_cpu_sample(w, Q, K, V, budget_s: float) -> tuple[float, int, int, float]:
+    rows = min(w.S, 64)
+    t, _ = oracle_attn_rows_timed(Q, K, V, w, rows)
+    rate = attn_row_flops(w, rows) / max(t, 1e-6)
+    while rows < w.S and attn_row_flops(w, min(w.S, rows * 2)) / rate < budget_s:
+        rows = min(w.S, rows * 2)
+    t, used = oracle_attn_rows_timed(Q, K, V, w, rows)
+    return attn_row_flops(w, rows) / t / 1e12, used, rows, t
+
+
+def run_reference_attn(args, w):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    Q, K, V = synth.attn_operands(w)
+    per_step = 120.0 / (args.steps + args.warmup)
+    _, _, rows, _ = attn_cpu_sample(w, Q, K, V, per_step)
+    for _ in range(args.warmup):
+        oracle_attn_rows_timed(Q, K, V, w, rows)
+    total, used = 0.0, 0
+    for _ in range(args.steps):
+        dt, used = oracle_attn_rows_timed(Q, K, V, w, rows)
+        total += dt
+    value = attn_row_flops(w, rows) * args.steps / total / 1e12
+    line = {
+        "impl": "reference", "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": attn_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": f"query rows 0..{rows - 1} of head (0,0) per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_attn(args, w):
+    import torch
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import dense_bf16_gemm_02_gb300 as hk
+
+    Qb, Kb, Vb = synth.attn_operands(w)
+    to_dev = lambda x: torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    Q, K, V = to_dev(Qb), to_dev(Kb), to_dev(Vb)
+    O = torch.empty_like(Q)
+    lse = torch.empty((w.B, w.Hq, w.S), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = int(stream.cuda_stream)
+    flops = attn_flops(w)
+
+    def launch(q, k, v, o):
+        st = hk.hk_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B, w.Hq,
+                                 w.Hkv, w.S, w.D, int(w.causal), sh)
+        if st != hk.HK_OK:
+            raise hk.HKError(st, "hk_attention_fwd")
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            launch(Q, K, V, O)
+    torch.cuda.synchronize(dev)
+    if hk.hk_gemm_last_device_status(local) != hk.HK_OK:
+        raise RuntimeError("device status after warm-up: " + hk.hk_gemm_last_error_string())
+
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    with torch.cuda.stream(stream):
+        events[0].record(stream)
+        for i in range(args.steps):
+            launch(Q, K, V, O)
+            events[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    barrier(world)
+    elapsed_ms = events[0].elapsed_time(events[-1])
+    per_launch = [events[i].elapsed_time(events[i + 1]) for i in range(args.steps)]
+    if hk.hk_gemm_last_device_status(local) != hk.HK_OK:
+        raise RuntimeError("device status after timing: " + hk.hk_gemm_last_error_string())
+    clocks = None
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+        clocks = sampler.summary(t_host0, t_host1)
+    elapsed_max = max_over_ranks(world, elapsed_ms)
+
+    # ---- end to end: pinned host Q, K, V -> device -> attention -> O to pinned host,
+    # pipelined on three streams with double-buffered device tensors
+    Q_h, K_h, V_h = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (Qb, Kb, Vb))
+    O_h = [torch.empty(Q.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    Q_d, K_d, V_d, O_d = [Q, torch.empty_like(Q)], [K, torch.empty_like(K)], [V, torch.empty_like(V)], \
+        [O, torch.empty_like(O)]
+    s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    e2e_steps = max(4, min(args.steps, 12))
+
+    def e2e_run(n):
+        h2d_done = [torch.cuda.Event() for _ in range(2)]
+        comp_done, d2h_done = [None, None], [None, None]
+        for i in range(n):
+            k = i & 1
+            if comp_done[k] is not None:
+                s_h2d.wait_event(comp_done[k])
+            with torch.cuda.stream(s_h2d):
+                Q_d[k].copy_(Q_h, non_blocking=True)
+                K_d[k].copy_(K_h, non_blocking=True)
+                V_d[k].copy_(V_h, non_blocking=True)
+                h2d_done[k].record(s_h2d)
+            stream.wait_event(h2d_done[k])
+            if d2h_done[k] is not None:
+                stream.wait_event(d2h_done[k])
+            launch(Q_d[k], K_d[k], V_d[k], O_d[k])
+            comp_done[k] = torch.cuda.Event()
+            comp_done[k].record(stream)
+            s_d2h.wait_event(comp_done[k])
+            with torch.cuda.stream(s_d2h):
+                O_h[k].copy_(O_d[k], non_blocking=True)
+                d2h_done[k] = torch.cuda.Event()
+                d2h_done[k].record(s_d2h)
+
+    e2e_run(2)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(s_h2d)
+    e2e_run(e2e_steps)
+    e1.record(s_d2h)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
+    if not np.array_equal(O_h[(e2e_steps - 1) & 1].view(torch.int16).numpy()[0, 0, :4],
+                          O.view(torch.int16).cpu().numpy()[0, 0, :4]):
+        raise RuntimeError("end-to-end result differs from the device result")
+
+    # ---- context only: PyTorch's fused attention on the same GPU and inputs
+    sdpa = None
+    if rank == 0 and not args.no_cublas_context:
+        try:
+            import torch.nn.functional as F
+            call = lambda: F.scaled_dot_product_attention(Q, K, V, is_causal=w.causal, enable_gqa=True)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize(dev)
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n_ctx = max(3, min(args.steps, 20))
+            c0.record()
+            for _ in range(n_ctx):
+                call()
+            c1.record()
+            torch.cuda.synchronize(dev)
+            ms = c0.elapsed_time(c1) / n_ctx
+            sdpa = {"value": flops / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_call": ms, "launches": n_ctx,
+                    "what": "torch scaled_dot_product_attention (enable_gqa) on the same GPU and inputs, "
+                            "timed after ours; context only"}
+        except Exception as exc:
+            sdpa = {"unavailable": str(exc)[:200]}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+    peaks, peaks_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    value = replica_value(flops, args.steps, world, elapsed_max)
+    mean_launch_ms = statistics.mean(per_launch)
+    achieved = flops / (mean_launch_ms / 1e3) / 1e12
+    digest = kernel_source_digest()
+    tr = MEASURED_TRAFFIC.get(w.name)
+    traffic = tr["bytes_per_launch"] if tr and tr.get("source_digest") == digest else None
+    h2d = int(sum(x.numel() * 2 for x in (Q_h, K_h, V_h)))
+    line = {
+        "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(attn_config(w), parallelism="replicas" if world > 1 else "single GPU",
+                       tile="2x128 query rows per CTA, 128-key blocks"),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"bf16_tflops (burst) of {peaks_src}",
+                     "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": attn_bytes(w),
+                     "mean_launch_ms": mean_launch_ms, "p10_launch_ms": float(np.percentile(per_launch, 10)),
+                     "p90_launch_ms": float(np.percentile(per_launch, 90)),
+                     "kernel": f"attn_fwd_kernel<{w.D}>", "source_digest": digest},
+        "e2e": {"value": replica_value(flops, e2e_steps, world, e2e_ms), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": int(O_h[0].numel() * 2), "steps": e2e_steps,
+                "pipelined": "H2D(i+1) | attention(i) | D2H(i-1) on three streams"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "context_sdpa": sdpa,
+    }
+    if not args.no_cpu_baseline:
+        v, used, rows, t = attn_cpu_sample(w, Qb, Kb, Vb, 15.0)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": used, "kind": "oracle",
+                                "sample": f"query rows 0..{rows - 1} of head (0,0) (fp64 C oracle, {t:.1f} s)"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["hk", "reference"], default="hk")
-    ap.add_argument("--workload", default="gemm_8192", choices=sorted(ALL_WORKLOADS))
+    ap.add_argument("--workload", default="gemm_8192", choices=sorted(ALL_WORKLOADS) + sorted(synth.ATTN_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cublas-context", action="store_true")
     ap.add_argument("--epilogue", default="none", choices=["none", "bias", "bias_relu", "bias_gelu", "bias_silu"],
@@ -531,6 +780,9 @@ def main(argv=None):
                     help="raster group height in tile rows (0: the library default via hk_gemm_bf16)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
+    if args.workload in synth.ATTN_WORKLOADS:
+        w = synth.ATTN_WORKLOADS[args.workload]
+        return run_reference_attn(args, w) if args.impl == "reference" else run_attn(args, w)
     w = ALL_WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

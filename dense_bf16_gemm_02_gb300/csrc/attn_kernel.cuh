@@ -1,0 +1,418 @@
+// Attention forward (MHA / GQA)  O = softmax(Q·Kᵀ/√D)·V  for sm_103a.
+//
+// The operation is the pages' second workload (HipKittens "L2" detail page,
+// §3 "Target operation" table, rows "MHA fwd" / "GQA fwd": Q [B, Hq, S, D],
+// K and V [B, Hkv, S, D], bf16 in, FP32 accumulation, bf16 out; §5
+// "Numerical considerations": online softmax in base 2 with temperature
+// sqrt(1/D)·log2(e); §9.3: QKᵀ, row max, exp2, row sum, rescale of the
+// running output, P·V, then a final 1/l and the log-sum-exp per row).
+// The pages' kernel is an 8-wave ping-pong on AMD matrix cores. This one is
+// a Blackwell design:
+//
+//  * one CTA owns two 128-row query tiles of one (batch, query head); both
+//    tiles share every K/V block that a TMA producer warp streams through a
+//    shared-memory ring (128 keys per block, 128-byte swizzle);
+//  * one thread issues tcgen05.mma: S_t = Q_t·K_jᵀ (M=128, N=128, K=D) into
+//    Tensor Memory, then O_t += P_t·V_j (M=128, N=D, K=128) with P_t read
+//    from Tensor Memory and V_j read from shared memory in MN-major form,
+//    so that neither P nor a transposed V ever touches shared memory;
+//  * two softmax warpgroups, one per query tile, each thread owning one row:
+//    tcgen05.ld of the row of S, masking, row max, exp2 on the special
+//    function unit, row sum, bf16 P written back over the row of S with
+//    tcgen05.st; while one tile is in softmax the tensor core works on the
+//    other (the Blackwell counterpart of the pages' ping-pong);
+//  * the running output is rescaled only when a row's maximum grows by more
+//    than 2^8 (the result is the same softmax: P and l share the stale
+//    maximum), and the rescale is done in Tensor Memory by the row's thread;
+//  * the epilogue multiplies by 1/l, rounds to bf16 (RNE) and stores each
+//    row directly; the log-sum-exp goes to an optional fp32 array.
+//
+// Each KV head's K and V are read by Hq/Hkv query heads; CTAs are numbered
+// head-fastest so the heads of a group run together and share K/V in L2.
+// Every mbarrier wait is bounded like the GEMM's: a wait that runs out
+// records an error in the device status word, the CTA drains and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace hk {
+namespace attn {
+
+constexpr int kTileQ = 128;         // query rows per tile (MMA M)
+constexpr int kTiles = 2;           // query tiles per CTA
+constexpr int kBlockKV = 128;       // keys per K/V block
+constexpr int kThreads = 320;       // warps 0-3 softmax tile 0, 4-7 softmax tile 1, 8 TMA, 9 MMA
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
+constexpr int kSmemLimit = 232448;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
+
+constexpr uint32_t kErrTmaEmpty = 1u << 8;
+constexpr uint32_t kErrMmaKv = 1u << 9;
+constexpr uint32_t kErrMmaP = 1u << 10;
+constexpr uint32_t kErrMmaO = 1u << 11;
+constexpr uint32_t kErrSoftmaxS = 1u << 12;
+constexpr uint32_t kErrEpilogueO = 1u << 13;
+
+constexpr uint32_t kFlagDropArrive = 0x1u;
+
+template <int kD>
+struct AttnGeometry {
+    static_assert(kD == 64 || kD == 128, "head dimension 64 or 128");
+    static constexpr int kChunks = kD / 64;                   // 128-byte column chunks per row
+    static constexpr int kChunkBytes = 128 * 128;             // 128 rows × 128 B (one TMA box)
+    static constexpr int kTileBytes = kChunks * kChunkBytes;  // one Q tile, one K block or one V block
+    static constexpr int kQBytes = kTiles * kTileBytes;
+    static constexpr int kSlotsFit = (kSmemLimit - kQBytes - 2048) / kTileBytes;
+    static constexpr int kSlots = kSlotsFit > 8 ? 8 : kSlotsFit;   // K/V ring (K_j and V_j alternate)
+    static_assert(kSlots >= 4, "K/V ring too shallow");
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = kQBytes;
+    static constexpr int kOffBars = kOffKV + kSlots * kTileBytes;
+    // q_full, kv_full[kSlots], kv_empty[kSlots], s_full[2], p_full[2], o_done[2]
+    static constexpr int kNumBars = 1 + 2 * kSlots + 6;
+    static constexpr int kOffTmemHolder = kOffBars + kNumBars * 8;
+    static constexpr int kSmemBytes = kOffTmemHolder + 16 + 1024;
+    static_assert(kSmemBytes <= kSmemLimit, "shared memory");
+    // TMEM columns: O_0, O_1 (kD each), then S_0, S_1 (128 each; P_t overlays S_t)
+    static constexpr int kColO = 0;
+    static constexpr int kColS = 2 * kD;
+    static constexpr int kTmemCols = 512;
+    static constexpr uint32_t kIdescS = idesc_bf16_f32(kTileQ, kBlockKV);
+    static constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileQ, kD) | (1u << 16);   // B (V) MN-major
+};
+
+struct AttnParams {
+    int32_t B, Hq, Hkv, S;
+    int32_t causal;
+    int32_t q_pairs;          // ceil(S / 256): CTAs per (batch, query head)
+    int32_t kv_blocks;        // ceil(S / 128)
+    float scale_log2;         // log2(e) / sqrt(D)
+    uint16_t* O;              // [B, Hq, S, D] bf16
+    float* lse;               // [B, Hq, S] natural-log sum of exp of the scaled scores, or null
+    uint32_t* status;         // [0]: error bits (sticky), [1]: launch id that aborted
+    uint32_t launch_id;
+    uint32_t flags;
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ bool attn_aborted(const AttnParams& p) {
+    return *reinterpret_cast<volatile uint32_t*>(p.status + 1) == p.launch_id;
+}
+
+__device__ __noinline__ bool attn_wait_slow(const AttnParams& p, uint32_t bar, uint32_t parity, uint32_t code) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (attn_aborted(p)) return false;
+            if (global_timer_ns() - t0 > p.timeout_ns) {
+                atomicOr(p.status, code);
+                atomicExch(p.status + 1, p.launch_id);
+                __threadfence();
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool attn_wait(const AttnParams& p, uint32_t bar, uint32_t parity, uint32_t code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return attn_wait_slow(p, bar, parity, code);
+}
+
+// Lane 0 waits; the verdict is broadcast and every lane then observes the
+// completed phase itself.
+__device__ __forceinline__ bool attn_wait_warp(const AttnParams& p, uint32_t bar, uint32_t parity, uint32_t code) {
+    uint32_t ok = 0;
+    if (lane_id() == 0) ok = attn_wait(p, bar, parity, code) ? 1u : 0u;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) (void)mbar_try_wait(bar, parity);
+    __syncwarp();
+    return ok != 0;
+}
+
+// K/V blocks query tile `row0` needs: all of them, or (causal) those up to
+// the block holding the tile's last row. 0 for a tile entirely past S.
+__device__ __forceinline__ int tile_blocks(const AttnParams& p, int row0) {
+    if (row0 >= p.S) return 0;
+    if (!p.causal) return p.kv_blocks;
+    const int last = row0 / kBlockKV + 1;
+    return last < p.kv_blocks ? last : p.kv_blocks;
+}
+
+template <int kD>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
+    using G = AttnGeometry<kD>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* const smem = smem_raw + (base - raw);
+
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = lane_id();
+
+    // CTA -> (query-row pair, batch·head); heads fastest, so the query heads
+    // of one KV group run side by side. Causal: the longest rows first.
+    const int bh_count = p.B * p.Hq;
+    const int slot_q = static_cast<int>(blockIdx.x) / bh_count;
+    const int bh = static_cast<int>(blockIdx.x) - slot_q * bh_count;
+    const int qp = p.causal ? p.q_pairs - 1 - slot_q : slot_q;
+    const int b = bh / p.Hq;
+    const int h = bh - b * p.Hq;
+    const int kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
+    const int q0 = qp * (kTiles * kTileQ);
+    const int n_t0 = tile_blocks(p, q0), n_t1 = tile_blocks(p, q0 + kTileQ);
+    auto n_t = [&](int t) { return t ? n_t1 : n_t0; };
+    const int n_all = n_t0 > n_t1 ? n_t0 : n_t1;
+
+    const uint32_t q_full = base + G::kOffBars;
+    auto kv_full = [&](int s) { return base + G::kOffBars + 8u * (1 + s); };
+    auto kv_empty = [&](int s) { return base + G::kOffBars + 8u * (1 + G::kSlots + s); };
+    auto s_full = [&](int t) { return base + G::kOffBars + 8u * (1 + 2 * G::kSlots + t); };
+    auto p_full = [&](int t) { return base + G::kOffBars + 8u * (3 + 2 * G::kSlots + t); };
+    auto o_done = [&](int t) { return base + G::kOffBars + 8u * (5 + 2 * G::kSlots + t); };
+    auto slot_addr = [&](int s) { return base + G::kOffKV + static_cast<uint32_t>(s) * G::kTileBytes; };
+    const uint32_t tmem_holder = base + G::kOffTmemHolder;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < G::kSlots; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
+        for (int t = 0; t < kTiles; ++t) {
+            mbar_init(s_full(t), 1);
+            mbar_init(p_full(t), 4 * 32);
+            mbar_init(o_done(t), 1);
+        }
+        fence_mbar_init_cluster();
+    }
+    if (warp == kWarpTma && lane == 0) {
+        prefetch_tensor_map(&tmap_q);
+        prefetch_tensor_map(&tmap_k);
+        prefetch_tensor_map(&tmap_v);
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc_one(tmem_holder, G::kTmemCols);
+        tmem_relinquish_one();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(smem + G::kOffTmemHolder);
+    bool abort_seen = false;
+
+    if (warp == kWarpTma) {
+        // ------------------------------------------------ TMA producer --
+        if (lane == 0 && n_all > 0) {
+            const int tiles = n_t1 > 0 ? 2 : 1;
+            mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(tiles * G::kTileBytes));
+            for (int t = 0; t < tiles; ++t)
+                for (int c = 0; c < G::kChunks; ++c)
+                    tma_load_3d(base + G::kOffQ + t * G::kTileBytes + c * G::kChunkBytes, &tmap_q, c * 64,
+                                q0 + t * kTileQ, bh, q_full);
+            for (int u = 0; u < 2 * n_all && !abort_seen; ++u) {
+                const int s = u % G::kSlots;
+                const uint32_t parity = ((u / G::kSlots) & 1) ^ 1;
+                if (!attn_wait(p, kv_empty(s), parity, kErrTmaEmpty)) {
+                    abort_seen = true;
+                    break;
+                }
+                if ((p.flags & kFlagDropArrive) && u == 0) continue;   // test hook: never fill slot 0
+                const CUtensorMap* map = (u & 1) ? &tmap_v : &tmap_k;
+                mbar_arrive_expect_tx(kv_full(s), G::kTileBytes);
+                for (int c = 0; c < G::kChunks; ++c)
+                    tma_load_3d(slot_addr(s) + c * G::kChunkBytes, map, c * 64, (u >> 1) * kBlockKV, kvh,
+                                kv_full(s));
+            }
+        }
+    } else if (warp == kWarpMma) {
+        // --------------------------------------------------- MMA issue --
+        if (lane == 0 && n_all > 0) {
+            auto wait = [&](uint32_t bar, uint32_t parity, uint32_t code) {
+                if (abort_seen) return false;
+                if (!attn_wait(p, bar, parity, code)) abort_seen = true;
+                return !abort_seen;
+            };
+            auto kv_slot = [&](int u) { return u % G::kSlots; };
+            auto kv_parity = [&](int u) { return static_cast<uint32_t>((u / G::kSlots) & 1); };
+            const uint32_t q_base = base + G::kOffQ;
+            auto issue_s = [&](int t, int u) {   // S_t = Q_t · K_uᵀ
+                const uint32_t qa = q_base + t * G::kTileBytes;
+                const uint32_t ka = slot_addr(kv_slot(u));
+                const uint32_t d = tmem_base + G::kColS + t * kBlockKV;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
+                    mma_bf16_one(d, smem_desc_kmajor_sw128(qa + off), smem_desc_kmajor_sw128(ka + off), G::kIdescS,
+                                 kk > 0 ? 1u : 0u);
+                }
+                mma_commit_one(s_full(t));
+            };
+            auto issue_pv = [&](int t, int u, bool first) {   // O_t += P_t · V_u
+                const uint32_t va = slot_addr(kv_slot(u));
+                const uint32_t d = tmem_base + G::kColO + t * kD;
+                const uint32_t a = tmem_base + G::kColS + t * kBlockKV;
+#pragma unroll
+                for (int kk = 0; kk < kBlockKV / 16; ++kk)
+                    mma_bf16_ts_one(d, a + kk * 8, smem_desc_mnmajor_sw128(va + kk * 2048, G::kChunkBytes),
+                                    G::kIdescPV, (first && kk == 0) ? 0u : 1u);
+                mma_commit_one(o_done(t));
+            };
+
+            if (wait(q_full, 0, kErrMmaKv) && wait(kv_full(kv_slot(0)), kv_parity(0), kErrMmaKv)) {
+                tc_fence_after_sync();
+                for (int t = 0; t < kTiles; ++t)
+                    if (n_t(t) > 0) issue_s(t, 0);
+                mma_commit_one(kv_empty(kv_slot(0)));
+            }
+            for (int j = 0; j < n_all && !abort_seen; ++j) {
+                const int uv = 2 * j + 1, uk = 2 * j + 2;
+                if (!wait(kv_full(kv_slot(uv)), kv_parity(uv), kErrMmaKv)) break;
+                tc_fence_after_sync();
+                bool k_next = false;
+                for (int t = 0; t < kTiles && !abort_seen; ++t) {
+                    if (j < n_t(t)) {
+                        if (!wait(p_full(t), j & 1, kErrMmaP)) break;
+                        tc_fence_after_sync();
+                        issue_pv(t, uv, j == 0);
+                    }
+                    if (j + 1 < n_t(t)) {
+                        if (!k_next) {
+                            if (!wait(kv_full(kv_slot(uk)), kv_parity(uk), kErrMmaKv)) break;
+                            k_next = true;
+                        }
+                        // P_t overlays S_t: the next S_t waits until this P_t·V has been read
+                        if (!wait(o_done(t), j & 1, kErrMmaO)) break;
+                        tc_fence_after_sync();
+                        issue_s(t, uk);
+                    }
+                }
+                if (abort_seen) break;
+                mma_commit_one(kv_empty(kv_slot(uv)));
+                if (k_next) mma_commit_one(kv_empty(kv_slot(uk)));
+            }
+        }
+    } else {
+        // ------------------------------------------ softmax warpgroups --
+        const int t = static_cast<int>(warp) >> 2;
+        const uint32_t quarter = warp & 3u;
+        const int r = static_cast<int>(quarter * 32 + lane);
+        const int q = q0 + t * kTileQ + r;              // this thread's query row
+        const uint32_t lane_off = (quarter * 32u) << 16;
+        const uint32_t s_addr = tmem_base + lane_off + G::kColS + t * kBlockKV;
+        const uint32_t o_addr = tmem_base + lane_off + G::kColO + t * kD;
+        const int n = n_t(t);
+        const int key_end = p.causal ? (q + 1 < p.S ? q + 1 : p.S) : p.S;   // keys [0, key_end) are visible
+        const float c = p.scale_log2;
+        float m = 0.0f;   // running max of the scaled scores (log2 units) used for P
+        float l = 0.0f;   // running sum of P
+        for (int j = 0; j < n; ++j) {
+            if (!attn_wait_warp(p, s_full(t), j & 1, kErrSoftmaxS)) {
+                abort_seen = true;
+                break;
+            }
+            tc_fence_after_sync();
+            uint32_t v[128];
+            tmem_load_32cols_at<0>(s_addr + 0, v);
+            tmem_load_32cols_at<32>(s_addr + 32, v);
+            tmem_load_32cols_at<64>(s_addr + 64, v);
+            tmem_load_32cols_at<96>(s_addr + 96, v);
+            tmem_wait_ld();
+            const int lim = key_end - j * kBlockKV;     // visible columns of this block
+            if (lim < kBlockKV) {
+#pragma unroll
+                for (int e = 0; e < 128; ++e)
+                    if (e >= lim) v[e] = __float_as_uint(-INFINITY);
+            }
+            float mx = __uint_as_float(v[0]);
+#pragma unroll
+            for (int e = 1; e < 128; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+            const float m_blk = mx * c;
+            float alpha = 1.0f;
+            if (j == 0) {
+                m = m_blk;
+            } else if (m_blk > m + kRescaleThreshold) {
+                alpha = ex2_approx(m - m_blk);
+                m = m_blk;
+                l *= alpha;
+            }
+            // P = 2^(s·c - m) in bf16 over the first 64 columns of the row of S
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(v[64 * half + 2 * e]), c, -m));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(v[64 * half + 2 * e + 1]), c, -m));
+                    l += p0 + p1;
+                    pk[e] = pack_bf16x2_rn(__float_as_uint(p0), __float_as_uint(p1));
+                }
+                tmem_store_32cols(s_addr + 32 * half, pk);
+            }
+            // rescale the running output (warp-wide when any row of the warp needs it)
+            if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+                for (int cc = 0; cc < kD / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_load_32cols(o_addr + 32 * cc, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_store_32cols(o_addr + 32 * cc, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            mbar_arrive(p_full(t));
+        }
+        // ------------------------------------------------------ epilogue --
+        if (!abort_seen && n > 0) {
+            if (!attn_wait_warp(p, o_done(t), (n - 1) & 1, kErrEpilogueO)) {
+                abort_seen = true;
+            } else {
+                tc_fence_after_sync();
+                const float inv_l = 1.0f / l;
+                uint16_t* out = p.O + (static_cast<int64_t>(bh) * p.S + q) * kD;
+#pragma unroll
+                for (int cc = 0; cc < kD / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_load_32cols(o_addr + 32 * cc, o);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack_bf16x2_rn(__float_as_uint(__uint_as_float(o[2 * e]) * inv_l),
+                                               __float_as_uint(__uint_as_float(o[2 * e + 1]) * inv_l));
+                    if (q < p.S) {
+#pragma unroll
+                        for (int w = 0; w < 4; ++w)
+                            st_global_v4(out + 32 * cc + 8 * w, pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                    }
+                }
+                if (p.lse != nullptr && q < p.S)
+                    p.lse[static_cast<int64_t>(bh) * p.S + q] = (m + log2f(l)) * 0.69314718055994531f;
+            }
+        }
+    }
+
+    if (abort_seen || attn_aborted(p)) {
+        // let copies and MMAs that were already issued land before teardown
+        for (int i = 0; i < 200; ++i) __nanosleep(1000);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after_sync();
+        tmem_dealloc_one(tmem_base, G::kTmemCols);
+    }
+}
+
+}  // namespace attn
+}  // namespace hk

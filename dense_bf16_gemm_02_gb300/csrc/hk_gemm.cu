@@ -18,6 +18,7 @@
 
 #include "../../include/hk_gemm.h"
 #include "gemm_kernel.cuh"
+#include "host_internal.h"
 
 namespace {
 
@@ -504,6 +505,49 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
 }
 
 }  // namespace
+
+namespace hk_host {
+
+hk_status set_error(hk_status s, const char* msg) {
+    g_last_error = msg;
+    return s;
+}
+
+hk_status status_word(int device, uint32_t** out) {
+    if (device < 0 || device >= kMaxDevices) return fail(HK_ERR_INVALID_ARG, "device %d out of range", device);
+    std::lock_guard<std::mutex> lock(g_ctx_mutex);
+    if (!g_ctx[device]) {
+        StatusWord* w = new (std::nothrow) StatusWord();
+        if (!w) return fail(HK_ERR_INVALID_ARG, "out of host memory");
+        hk_status s = alloc_status(w);
+        if (s != HK_OK) {
+            delete w;
+            return s;
+        }
+        g_ctx[device] = w;
+    }
+    *out = g_ctx[device]->dev;
+    return HK_OK;
+}
+
+hk_status check_device(int device, int* sm_count) {
+    const DeviceInfo* di = nullptr;
+    hk_status s = device_info(device, &di);
+    if (s != HK_OK) return s;
+    *sm_count = di->sm_count;
+    return HK_OK;
+}
+
+hk_status tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
+    hk_status s = get_encoder();
+    if (s != HK_OK) return s;
+    *out = g_encode;
+    return HK_OK;
+}
+
+uint32_t next_launch_id() { return ::next_launch_id(); }
+
+}  // namespace hk_host
 
 extern "C" {
 

@@ -312,6 +312,24 @@ __device__ __forceinline__ void tmem_load_32cols(uint32_t taddr, uint32_t (&v)[3
         : "r"(taddr));
 }
 
+// The same into v[kOff .. kOff+31] of a larger register array.
+template <int kOff, int kN>
+__device__ __forceinline__ void tmem_load_32cols_at(uint32_t taddr, uint32_t (&v)[kN]) {
+    static_assert(kOff + 32 <= kN, "range");
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[kOff + 0]), "=r"(v[kOff + 1]), "=r"(v[kOff + 2]), "=r"(v[kOff + 3]), "=r"(v[kOff + 4]),
+          "=r"(v[kOff + 5]), "=r"(v[kOff + 6]), "=r"(v[kOff + 7]), "=r"(v[kOff + 8]), "=r"(v[kOff + 9]),
+          "=r"(v[kOff + 10]), "=r"(v[kOff + 11]), "=r"(v[kOff + 12]), "=r"(v[kOff + 13]), "=r"(v[kOff + 14]),
+          "=r"(v[kOff + 15]), "=r"(v[kOff + 16]), "=r"(v[kOff + 17]), "=r"(v[kOff + 18]), "=r"(v[kOff + 19]),
+          "=r"(v[kOff + 20]), "=r"(v[kOff + 21]), "=r"(v[kOff + 22]), "=r"(v[kOff + 23]), "=r"(v[kOff + 24]),
+          "=r"(v[kOff + 25]), "=r"(v[kOff + 26]), "=r"(v[kOff + 27]), "=r"(v[kOff + 28]), "=r"(v[kOff + 29]),
+          "=r"(v[kOff + 30]), "=r"(v[kOff + 31])
+        : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -334,6 +352,58 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) 
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// 3-D tiled TMA load into this CTA's shared memory (coordinates innermost
+// first), completing on `bar` with complete_tx.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] · B[smem]ᵀ on one CTA, kind::f16: the A operand is
+// read from Tensor Memory (one row per lane, two bf16 per 32-bit column).
+__device__ __forceinline__ void mma_bf16_ts_one(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Warp-collective registers -> TMEM: lane l of the warp writes TMEM lane
+// (taddr.lane + l), 32 consecutive 32-bit columns starting at taddr.col.
+__device__ __forceinline__ void tmem_store_32cols(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 2^x on the special-function unit (approximate; -inf -> +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void st_global_v4(void* ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
 // ------------------------------------------------- tcgen05 descriptors --
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
@@ -347,6 +417,20 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
     d |= static_cast<uint64_t>(1u) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// Shared-memory matrix descriptor for an MN-major operand tile written by
+// TMA with 128-byte swizzling: rows of 64 bf16 along MN (128 B), one row per
+// K index, 8-row (8 K) swizzle atoms of 1024 B (stride byte offset), and
+// further 64-element MN groups `mn_group_bytes` apart (leading byte offset).
+__device__ __forceinline__ uint64_t smem_desc_mnmajor_sw128(uint32_t saddr, uint32_t mn_group_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((mn_group_bytes >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>(1024u >> 4) << 32;
     d |= static_cast<uint64_t>(1u) << 46;
     d |= static_cast<uint64_t>(2u) << 61;

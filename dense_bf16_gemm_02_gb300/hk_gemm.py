@@ -49,6 +49,7 @@ EXPORTED = (
     "hk_gemm_plan_run", "hk_gemm_plan_device_status", "hk_gemm_last_device_status",
     "hk_gemm_plan_destroy", "hk_status_string", "hk_gemm_last_error_string", "hk_gemm_bf16_noalloc",
     "hk_gemm_bf16_epilogue", "hk_gemm_plan_run_epilogue", "hk_gemm_fp8_e4m3",
+    "hk_attention_fwd", "hk_attention_fwd_ex",
 )
 
 
@@ -125,6 +126,11 @@ def load() -> ctypes.CDLL:
         lib.hk_gemm_fp8_e4m3.restype = I32
         lib.hk_gemm_bf16_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, ctypes.c_int32, P]
         lib.hk_gemm_bf16_noalloc.restype = I32
+        lib.hk_attention_fwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I32, P]
+        lib.hk_attention_fwd.restype = I32
+        lib.hk_attention_fwd_ex.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I32, ctypes.c_uint32,
+                                            ctypes.c_uint64, P]
+        lib.hk_attention_fwd_ex.restype = I32
         _lib = lib
         return lib
 
@@ -152,6 +158,18 @@ def hk_gemm_bf16_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: in
                          split_k: int = 0, stream: int = 0) -> int:
     """The GEMM that allocates nothing (scratch in a fixed array of the library)."""
     return load().hk_gemm_bf16_noalloc(A, B, C, M, N, K, lda, ldb, ldc, split_k, stream)
+
+
+def hk_attention_fwd(Q: int, K: int, V: int, O: int, lse: int, B: int, Hq: int, Hkv: int, S: int, D: int,
+                     causal: int = 0, stream: int = 0) -> int:
+    """O = softmax(Q·Kᵀ/√D)·V (GQA; Q, O [B,Hq,S,D], K, V [B,Hkv,S,D] bf16; lse fp32 [B,Hq,S] or 0)."""
+    return load().hk_attention_fwd(Q, K, V, O, lse or None, B, Hq, Hkv, S, D, int(causal), stream)
+
+
+def hk_attention_fwd_ex(Q: int, K: int, V: int, O: int, lse: int, B: int, Hq: int, Hkv: int, S: int, D: int,
+                        causal: int = 0, flags: int = 0, timeout_ns: int = 0, stream: int = 0) -> int:
+    return load().hk_attention_fwd_ex(Q, K, V, O, lse or None, B, Hq, Hkv, S, D, int(causal), flags,
+                                      timeout_ns, stream)
 
 
 def hk_gemm_last_device_status(device: int) -> int:
@@ -208,6 +226,30 @@ def gemm(A, B, out=None, stream=None):
     if st != HK_OK:
         raise HKError(st, "hk_gemm_bf16")
     return out
+
+
+def attention(q, k, v, causal: bool = False, return_lse: bool = False, out=None, stream=None):
+    """softmax(q·kᵀ/√D)·v for contiguous bf16 CUDA tensors q [B, Hq, S, D] and
+    k, v [B, Hkv, S, D] (Hkv divides Hq; D 64 or 128). Returns o [B, Hq, S, D]
+    (and the fp32 log-sum-exp [B, Hq, S] with ``return_lse``)."""
+    import torch
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        if (not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4
+                or not t.is_contiguous()):
+            raise TypeError(f"{name} must be a contiguous 4-D bfloat16 CUDA tensor")
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, S, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, Hkv, S, D] with q's B, S and D")
+    if out is None:
+        out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device) if return_lse else None
+    st = hk_attention_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                          lse.data_ptr() if lse is not None else 0, B, Hq, Hkv, S, D, int(causal),
+                          _stream_handle(stream))
+    if st != HK_OK:
+        raise HKError(st, "hk_attention_fwd")
+    return (out, lse) if return_lse else out
 
 
 class Plan:

@@ -201,7 +201,8 @@ hk_status hk_gemm_fp8_e4m3(const void* A, const void* B, void* C,
  * last read. */
 hk_status hk_gemm_plan_device_status(hk_gemm_plan* plan);
 
-/* The same for the calls hk_gemm_bf16 made on `device`. */
+/* The same for the calls of the one-shot entry points (hk_gemm_bf16,
+ * hk_gemm_bf16_epilogue, hk_gemm_fp8_e4m3, hk_attention_fwd) on `device`. */
 hk_status hk_gemm_last_device_status(int device);
 
 void hk_gemm_plan_destroy(hk_gemm_plan* plan);
@@ -233,6 +234,40 @@ hk_status hk_gemm_bf16_noalloc(const void* A, const void* B, void* C,
                                int64_t M, int64_t N, int64_t K,
                                int64_t lda, int64_t ldb, int64_t ldc,
                                int32_t split_k, void* stream);
+
+/* Attention forward, MHA or GQA (the pages' second workload: HipKittens "L2"
+ * detail page, §3 "Target operation" table, rows "MHA fwd" / "GQA fwd";
+ * §5 "Numerical considerations" and §9.3 for the online softmax with
+ * temperature sqrt(1/D)):
+ *
+ *     O[b,h,i,:] = bf16_rne( Σ_j P[i,j] · V[b,g,j,:] ),
+ *     P[i,:]     = softmax_j( Q[b,h,i,:]·K[b,g,j,:] / sqrt(D) ),
+ *     g = h / (Hq / Hkv)  (consecutive query heads share a KV head),
+ *
+ * over the keys j < S, or j ≤ i when `causal` is non-zero. Q·Kᵀ and P·V run
+ * on the tensor cores (bf16 operands, fp32 accumulation); P is rounded to
+ * bf16 before P·V and the row sums use the unrounded fp32 P; exp is the
+ * hardware base-2 exponential. `lse`, when not NULL, receives per row the
+ * natural-log sum ln Σ_j exp(Q·K/sqrt(D)) in fp32, [B, Hq, S].
+ *
+ * Layout: Q and O are [B, Hq, S, D], K and V are [B, Hkv, S, D], contiguous
+ * row-major bf16 device arrays (16-byte aligned, else HK_ERR_MISALIGNED);
+ * lse is a 4-byte-aligned fp32 device array or NULL. O must not overlap the
+ * inputs. D must be 64 or 128, Hkv ≥ 1 must divide Hq, and B·Hq·S must stay
+ * below 2^31 (else HK_ERR_INVALID_ARG). B, Hq or S equal to 0: HK_OK,
+ * nothing launched. Asynchronous on `stream`; a bounded wait that runs out
+ * is reported by hk_gemm_last_device_status(device). */
+hk_status hk_attention_fwd(const void* Q, const void* K, const void* V, void* O, float* lse,
+                           int64_t B, int64_t Hq, int64_t Hkv, int64_t S, int64_t D,
+                           int32_t causal, void* stream);
+
+/* The same with test and tuning controls: `flags` takes
+ * HK_FLAG_FAULT_DROP_ARRIVE (the producer never fills the first K/V slot,
+ * so a bounded wait runs out and the status word reports HK_ERR_TIMEOUT),
+ * `timeout_ns` bounds each wait (0: 1 s). */
+hk_status hk_attention_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* lse,
+                              int64_t B, int64_t Hq, int64_t Hkv, int64_t S, int64_t D,
+                              int32_t causal, uint32_t flags, uint64_t timeout_ns, void* stream);
 
 /* Static description of a status code. */
 const char* hk_status_string(hk_status status);

@@ -79,6 +79,26 @@ def test_host_validation_without_gpu(lib):
     lib.hk_gemm_plan_destroy(None)
 
 
+def test_attention_host_validation_without_gpu(lib):
+    from dense_bf16_gemm_02_gb300 import hk_gemm as h
+    P = 1 << 20
+    att = lib.hk_attention_fwd
+    # empty problems: nothing launched
+    assert att(None, None, None, None, None, 0, 8, 2, 128, 128, 0, None) == h.HK_OK
+    assert att(None, None, None, None, None, 2, 8, 2, 0, 64, 1, None) == h.HK_OK
+    # head dimension, head grouping, negative sizes, size limit
+    assert att(P, P, P, P, None, 1, 8, 2, 128, 96, 0, None) == h.HK_ERR_INVALID_ARG
+    assert b"head dimension" in lib.hk_gemm_last_error_string()
+    assert att(P, P, P, P, None, 1, 8, 3, 128, 128, 0, None) == h.HK_ERR_INVALID_ARG
+    assert att(P, P, P, P, None, 1, 8, 0, 128, 128, 0, None) == h.HK_ERR_INVALID_ARG
+    assert att(P, P, P, P, None, -1, 8, 2, 128, 128, 0, None) == h.HK_ERR_INVALID_ARG
+    assert att(P, P, P, P, None, 1 << 16, 64, 8, 1 << 16, 128, 0, None) == h.HK_ERR_INVALID_ARG
+    # null and misaligned pointers
+    assert att(None, P, P, P, None, 1, 8, 2, 128, 128, 0, None) == h.HK_ERR_INVALID_ARG
+    assert att(P, P, P + 8, P, None, 1, 8, 2, 128, 128, 0, None) == h.HK_ERR_MISALIGNED
+    assert att(P, P, P, P, P + 2, 1, 8, 2, 128, 128, 0, None) == h.HK_ERR_MISALIGNED
+
+
 def test_product_path_has_no_oracle_or_fallback():
     """The CUDA package never imports the oracle and has no CPU path."""
     pkg = os.path.join(ROOT, "dense_bf16_gemm_02_gb300")
