@@ -331,9 +331,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 for (int e = 0; e < 128; ++e)
                     if (e >= lim) v[e] = __float_as_uint(-INFINITY);
             }
-            float mx = __uint_as_float(v[0]);
+            // row max: eight independent chains of three-input maxima, then a tree
+            float acc[8];
 #pragma unroll
-            for (int e = 1; e < 128; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+            for (int k = 0; k < 8; ++k) {
+                const int e0 = 16 * k;
+                float a = fmax3(__uint_as_float(v[e0]), __uint_as_float(v[e0 + 1]), __uint_as_float(v[e0 + 2]));
+#pragma unroll
+                for (int e = 3; e < 15; e += 2)
+                    a = fmax3(a, __uint_as_float(v[e0 + e]), __uint_as_float(v[e0 + e + 1]));
+                acc[k] = fmaxf(a, __uint_as_float(v[e0 + 15]));
+            }
+            const float mx = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
+                                   fmaxf(acc[6], acc[7]));
             const float m_blk = mx * c;
             float alpha = 1.0f;
             if (j == 0) {
@@ -343,18 +353,32 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 m = m_blk;
                 l *= alpha;
             }
-            // P = 2^(s·c - m) in bf16 over the first 64 columns of the row of S
+            // P = 2^(s·c - m) in bf16 over the first 64 columns of the row of S;
+            // the scale-and-shift and the row sum run on packed pairs
+            const uint64_t c2 = f32x2(c, c);
+            const uint64_t nm2 = f32x2(-m, -m);
+            uint64_t sum2[4] = {0, 0, 0, 0};
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(v[64 * half + 2 * e]), c, -m));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(v[64 * half + 2 * e + 1]), c, -m));
-                    l += p0 + p1;
+                    const int i = 64 * half + 2 * e;
+                    const uint64_t x = ffma2(f32x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), c2, nm2);
+                    float x0, x1;
+                    f32x2_split(x, x0, x1);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
+                    sum2[e & 3] = fadd2(sum2[e & 3], f32x2(p0, p1));
                     pk[e] = pack_bf16x2_rn(__float_as_uint(p0), __float_as_uint(p1));
                 }
                 tmem_store_32cols(s_addr + 32 * half, pk);
+            }
+            {
+                const uint64_t s01 = fadd2(fadd2(sum2[0], sum2[1]), fadd2(sum2[2], sum2[3]));
+                float lo, hi;
+                f32x2_split(s01, lo, hi);
+                l += lo + hi;
             }
             // rescale the running output (warp-wide when any row of the warp needs it)
             if (__any_sync(0xffffffffu, alpha != 1.0f)) {
