@@ -13,14 +13,18 @@
 //    tiles share every K/V block that a TMA producer warp streams through a
 //    shared-memory ring (128 keys per block, 128-byte swizzle);
 //  * one thread issues tcgen05.mma: S_t = Q_t·K_jᵀ (M=128, N=128, K=D) into
-//    Tensor Memory, then O_t += P_t·V_j (M=128, N=D, K=128) with P_t read
-//    from Tensor Memory and V_j read from shared memory in MN-major form,
-//    so that neither P nor a transposed V ever touches shared memory;
+//    Tensor Memory, and O_t += P_t·V_j (M=128, N=D, K=128) with P_t and V_j
+//    (MN-major, so V is never transposed) read from shared memory;
 //  * two softmax warpgroups, one per query tile, each thread owning one row:
-//    tcgen05.ld of the row of S, masking, row max, exp2 on the special
-//    function unit, row sum, bf16 P written back over the row of S with
-//    tcgen05.st; while one tile is in softmax the tensor core works on the
-//    other (the Blackwell counterpart of the pages' ping-pong);
+//    tcgen05.ld of the row of S, then at once a "S read" signal, so that the
+//    MMA thread computes S_t for the next block while this one is still in
+//    masking, row max, exp2 on the special function unit and row sum; the
+//    bf16 P goes to shared memory (128-byte swizzled, the layout the MMA
+//    reads). The softmax of a tile therefore never waits for its own P·V,
+//    and the tensor core alternates between the two tiles (the Blackwell
+//    counterpart of the pages' ping-pong);
+//  * K/V blocks are streamed in the order the MMAs consume them (K of the
+//    next block ahead of V of the current one);
 //  * the running output is rescaled only when a row's maximum grows by more
 //    than 2^8 (the result is the same softmax: P and l share the stale
 //    maximum), and the rescale is done in Tensor Memory by the row's thread;
@@ -66,24 +70,31 @@ struct AttnGeometry {
     static constexpr int kChunkBytes = 128 * 128;             // 128 rows × 128 B (one TMA box)
     static constexpr int kTileBytes = kChunks * kChunkBytes;  // one Q tile, one K block or one V block
     static constexpr int kQBytes = kTiles * kTileBytes;
-    static constexpr int kSlotsFit = (kSmemLimit - kQBytes - 2048) / kTileBytes;
-    static constexpr int kSlots = kSlotsFit > 8 ? 8 : kSlotsFit;   // K/V ring (K_j and V_j alternate)
-    static_assert(kSlots >= 4, "K/V ring too shallow");
+    static constexpr int kPBytes = kTileQ * kBlockKV * 2;     // bf16 P of one tile (two 64-key chunks)
+    static constexpr int kSlotsFit = (kSmemLimit - kQBytes - kTiles * kPBytes - 2048) / kTileBytes;
+    static constexpr int kSlots = kSlotsFit > 8 ? 8 : kSlotsFit;   // K/V ring
+    static_assert(kSlots >= 3, "K/V ring too shallow");
     static constexpr int kOffQ = 0;
-    static constexpr int kOffKV = kQBytes;
+    static constexpr int kOffP = kQBytes;
+    static constexpr int kOffKV = kOffP + kTiles * kPBytes;
     static constexpr int kOffBars = kOffKV + kSlots * kTileBytes;
-    // q_full, kv_full[kSlots], kv_empty[kSlots], s_full[2], p_full[2], o_done[2]
-    static constexpr int kNumBars = 1 + 2 * kSlots + 6;
+    // q_full, kv_full[kSlots], kv_empty[kSlots], s_full[2], s_free[2], p_full[2], o_done[2]
+    static constexpr int kNumBars = 1 + 2 * kSlots + 8;
     static constexpr int kOffTmemHolder = kOffBars + kNumBars * 8;
     static constexpr int kSmemBytes = kOffTmemHolder + 16 + 1024;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
-    // TMEM columns: O_0, O_1 (kD each), then S_0, S_1 (128 each; P_t overlays S_t)
+    // TMEM columns: O_0, O_1 (kD each), then S_0, S_1 (128 each)
     static constexpr int kColO = 0;
     static constexpr int kColS = 2 * kD;
     static constexpr int kTmemCols = 512;
     static constexpr uint32_t kIdescS = idesc_bf16_f32(kTileQ, kBlockKV);
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileQ, kD) | (1u << 16);   // B (V) MN-major
 };
+
+// Ring position of each K/V block in the order the MMAs use them:
+// K_0, then (K_{j+1}, V_j) for j = 0 .. n-2, then V_{n-1}.
+__device__ __forceinline__ int pos_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int pos_v(int j, int n) { return j + 1 < n ? 2 * j + 2 : 2 * n - 1; }
 
 struct AttnParams {
     int32_t B, Hq, Hkv, S;
@@ -103,25 +114,43 @@ __device__ __forceinline__ bool attn_aborted(const AttnParams& p) {
     return *reinterpret_cast<volatile uint32_t*>(p.status + 1) == p.launch_id;
 }
 
-__device__ __noinline__ bool attn_wait_slow(const AttnParams& p, uint32_t bar, uint32_t parity, uint32_t code) {
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (attn_aborted(p)) return false;
-            if (global_timer_ns() - t0 > p.timeout_ns) {
-                atomicOr(p.status, code);
-                atomicExch(p.status + 1, p.launch_id);
-                __threadfence();
-                return false;
-            }
-        }
-    }
+// Bounded waits. On the S -> softmax -> P·V chain a wait polls with
+// non-suspending probes: a suspended mbarrier wait was measured to resume
+// several hundred cycles after its phase completed. The TMA producer, whose
+// waits are off that chain, lets the hardware suspend it instead, so that it
+// takes no issue slots from the softmax warps. The polling loop is inline (an
+// out-of-line call would save and restore the caller's live registers through
+// local memory on every wait); the clock is read every 4096 probes (or after
+// each suspension), and only a wait that has lasted 20 µs calls out to check
+// the launch's abort flag (a global load) and the time limit.
+enum class Wait { kPoll, kPollCluster, kSuspend };
+
+// Returns true when the wait must give up (this launch was aborted, or the
+// time limit ran out; then it records `code` and aborts the launch).
+__device__ __noinline__ bool attn_wait_expired(const AttnParams& p, uint64_t waited_ns, uint32_t code) {
+    if (attn_aborted(p)) return true;
+    if (waited_ns <= p.timeout_ns) return false;
+    atomicOr(p.status, code);
+    atomicExch(p.status + 1, p.launch_id);
+    __threadfence();
+    return true;
 }
 
-__device__ __forceinline__ bool attn_wait(const AttnParams& p, uint32_t bar, uint32_t parity, uint32_t code) {
-    if (mbar_try_wait(bar, parity)) return true;
-    return attn_wait_slow(p, bar, parity, code);
+__device__ __forceinline__ bool attn_wait(const AttnParams& p, uint32_t bar, uint32_t parity, uint32_t code,
+                                          Wait mode = Wait::kPoll) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 1;; ++it) {
+        bool done;
+        if (mode == Wait::kSuspend) done = mbar_try_wait_suspend(bar, parity, 20000);
+        else if (mode == Wait::kPollCluster) done = mbar_test_wait_cluster(bar, parity);
+        else done = mbar_test_wait(bar, parity);
+        if (done) return true;
+        if (mode == Wait::kSuspend || (it & 4095u) == 0) {
+            const uint64_t now = global_timer_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 >= 20000 && attn_wait_expired(p, now - t0, code)) return false;
+        }
+    }
 }
 
 // Lane 0 waits; the verdict is broadcast and every lane then observes the
@@ -130,7 +159,7 @@ __device__ __forceinline__ bool attn_wait_warp(const AttnParams& p, uint32_t bar
     uint32_t ok = 0;
     if (lane_id() == 0) ok = attn_wait(p, bar, parity, code) ? 1u : 0u;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) (void)mbar_try_wait(bar, parity);
+    if (ok) (void)mbar_test_wait(bar, parity);
     __syncwarp();
     return ok != 0;
 }
@@ -175,8 +204,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     auto kv_full = [&](int s) { return base + G::kOffBars + 8u * (1 + s); };
     auto kv_empty = [&](int s) { return base + G::kOffBars + 8u * (1 + G::kSlots + s); };
     auto s_full = [&](int t) { return base + G::kOffBars + 8u * (1 + 2 * G::kSlots + t); };
-    auto p_full = [&](int t) { return base + G::kOffBars + 8u * (3 + 2 * G::kSlots + t); };
-    auto o_done = [&](int t) { return base + G::kOffBars + 8u * (5 + 2 * G::kSlots + t); };
+    auto s_free = [&](int t) { return base + G::kOffBars + 8u * (3 + 2 * G::kSlots + t); };
+    auto p_full = [&](int t) { return base + G::kOffBars + 8u * (5 + 2 * G::kSlots + t); };
+    auto o_done = [&](int t) { return base + G::kOffBars + 8u * (7 + 2 * G::kSlots + t); };
+    auto p_smem = [&](int t) { return base + G::kOffP + static_cast<uint32_t>(t) * G::kPBytes; };
     auto slot_addr = [&](int s) { return base + G::kOffKV + static_cast<uint32_t>(s) * G::kTileBytes; };
     const uint32_t tmem_holder = base + G::kOffTmemHolder;
 
@@ -188,6 +219,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         }
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(s_full(t), 1);
+            mbar_init(s_free(t), 4 * 32);
             mbar_init(p_full(t), 4 * 32);
             mbar_init(o_done(t), 1);
         }
@@ -220,16 +252,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             for (int u = 0; u < 2 * n_all && !abort_seen; ++u) {
                 const int s = u % G::kSlots;
                 const uint32_t parity = ((u / G::kSlots) & 1) ^ 1;
-                if (!attn_wait(p, kv_empty(s), parity, kErrTmaEmpty)) {
+                if (!attn_wait(p, kv_empty(s), parity, kErrTmaEmpty, Wait::kSuspend)) {
                     abort_seen = true;
                     break;
                 }
                 if ((p.flags & kFlagDropArrive) && u == 0) continue;   // test hook: never fill slot 0
-                const CUtensorMap* map = (u & 1) ? &tmap_v : &tmap_k;
+                // position u of the consumption order: K_0, (K_{j+1}, V_j)..., V_{n-1}
+                bool is_k;
+                int blk;
+                if (u == 0) {
+                    is_k = true;
+                    blk = 0;
+                } else if (u - 1 < 2 * (n_all - 1)) {
+                    is_k = ((u - 1) & 1) == 0;
+                    blk = is_k ? (u - 1) / 2 + 1 : (u - 1) / 2;
+                } else {
+                    is_k = false;
+                    blk = n_all - 1;
+                }
                 mbar_arrive_expect_tx(kv_full(s), G::kTileBytes);
                 for (int c = 0; c < G::kChunks; ++c)
-                    tma_load_3d(slot_addr(s) + c * G::kChunkBytes, map, c * 64, (u >> 1) * kBlockKV, kvh,
-                                kv_full(s));
+                    tma_load_3d(slot_addr(s) + c * G::kChunkBytes, is_k ? &tmap_k : &tmap_v, c * 64, blk * kBlockKV,
+                                kvh, kv_full(s));
             }
         }
     } else if (warp == kWarpMma) {
@@ -258,11 +302,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             auto issue_pv = [&](int t, int u, bool first) {   // O_t += P_t · V_u
                 const uint32_t va = slot_addr(kv_slot(u));
                 const uint32_t d = tmem_base + G::kColO + t * kD;
-                const uint32_t a = tmem_base + G::kColS + t * kBlockKV;
+                const uint32_t pa = p_smem(t);
 #pragma unroll
                 for (int kk = 0; kk < kBlockKV / 16; ++kk)
-                    mma_bf16_ts_one(d, a + kk * 8, smem_desc_mnmajor_sw128(va + kk * 2048, G::kChunkBytes),
-                                    G::kIdescPV, (first && kk == 0) ? 0u : 1u);
+                    mma_bf16_one(d, smem_desc_kmajor_sw128(pa + (kk >> 2) * G::kChunkBytes + (kk & 3) * 32),
+                                 smem_desc_mnmajor(va + kk * 2048, 128, G::kChunkBytes), G::kIdescPV,
+                                 (first && kk == 0) ? 0u : 1u);
                 mma_commit_one(o_done(t));
             };
 
@@ -273,30 +318,32 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 mma_commit_one(kv_empty(kv_slot(0)));
             }
             for (int j = 0; j < n_all && !abort_seen; ++j) {
-                const int uv = 2 * j + 1, uk = 2 * j + 2;
+                // S for block j+1, as soon as each tile's softmax has read its S of block j
+                if (j + 1 < n_all) {
+                    const int uk = pos_k(j + 1);
+                    if (!wait(kv_full(kv_slot(uk)), kv_parity(uk), kErrMmaKv)) break;
+                    for (int t = 0; t < kTiles && !abort_seen; ++t) {
+                        if (j + 1 < n_t(t)) {
+                            if (!wait(s_free(t), j & 1, kErrMmaP)) break;
+                            tc_fence_after_sync();
+                            issue_s(t, uk);
+                        }
+                    }
+                    if (abort_seen) break;
+                    mma_commit_one(kv_empty(kv_slot(uk)));
+                }
+                // P·V for block j, as each tile's P lands in shared memory
+                const int uv = pos_v(j, n_all);
                 if (!wait(kv_full(kv_slot(uv)), kv_parity(uv), kErrMmaKv)) break;
-                tc_fence_after_sync();
-                bool k_next = false;
                 for (int t = 0; t < kTiles && !abort_seen; ++t) {
                     if (j < n_t(t)) {
                         if (!wait(p_full(t), j & 1, kErrMmaP)) break;
                         tc_fence_after_sync();
                         issue_pv(t, uv, j == 0);
                     }
-                    if (j + 1 < n_t(t)) {
-                        if (!k_next) {
-                            if (!wait(kv_full(kv_slot(uk)), kv_parity(uk), kErrMmaKv)) break;
-                            k_next = true;
-                        }
-                        // P_t overlays S_t: the next S_t waits until this P_t·V has been read
-                        if (!wait(o_done(t), j & 1, kErrMmaO)) break;
-                        tc_fence_after_sync();
-                        issue_s(t, uk);
-                    }
                 }
                 if (abort_seen) break;
                 mma_commit_one(kv_empty(kv_slot(uv)));
-                if (k_next) mma_commit_one(kv_empty(kv_slot(uk)));
             }
         }
     } else {
@@ -325,6 +372,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             tmem_load_32cols_at<64>(s_addr + 64, v);
             tmem_load_32cols_at<96>(s_addr + 96, v);
             tmem_wait_ld();
+            // S is in registers: the MMA thread may compute the next block's S here
+            tc_fence_before_sync();
+            mbar_arrive(s_free(t));
             const int lim = key_end - j * kBlockKV;     // visible columns of this block
             if (lim < kBlockKV) {
 #pragma unroll
@@ -353,26 +403,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 m = m_blk;
                 l *= alpha;
             }
-            // P = 2^(s·c - m) in bf16 over the first 64 columns of the row of S;
-            // the scale-and-shift and the row sum run on packed pairs
+            // P = 2^(s·c - m) in bf16; the scale-and-shift and the row sum run on packed pairs
             const uint64_t c2 = f32x2(c, c);
             const uint64_t nm2 = f32x2(-m, -m);
             uint64_t sum2[4] = {0, 0, 0, 0};
+            uint32_t pk[64];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int i = 64 * half + 2 * e;
-                    const uint64_t x = ffma2(f32x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), c2, nm2);
-                    float x0, x1;
-                    f32x2_split(x, x0, x1);
-                    const float p0 = ex2_approx(x0);
-                    const float p1 = ex2_approx(x1);
-                    sum2[e & 3] = fadd2(sum2[e & 3], f32x2(p0, p1));
-                    pk[e] = pack_bf16x2_rn(__float_as_uint(p0), __float_as_uint(p1));
-                }
-                tmem_store_32cols(s_addr + 32 * half, pk);
+            for (int e = 0; e < 64; ++e) {
+                const uint64_t x = ffma2(f32x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), c2, nm2);
+                float x0, x1;
+                f32x2_split(x, x0, x1);
+                const float p0 = ex2_approx(x0);
+                const float p1 = ex2_approx(x1);
+                sum2[e & 3] = fadd2(sum2[e & 3], f32x2(p0, p1));
+                pk[e] = pack_bf16x2_rn(__float_as_uint(p0), __float_as_uint(p1));
             }
             {
                 const uint64_t s01 = fadd2(fadd2(sum2[0], sum2[1]), fadd2(sum2[2], sum2[3]));
@@ -380,6 +424,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 f32x2_split(s01, lo, hi);
                 l += lo + hi;
             }
+            // P·V of the previous block must be done before its P is overwritten and O rescaled
+            if (j > 0 && !attn_wait_warp(p, o_done(t), (j - 1) & 1, kErrEpilogueO)) {
+                abort_seen = true;
+                break;
+            }
+            tc_fence_after_sync();
             // rescale the running output (warp-wide when any row of the warp needs it)
             if (__any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
@@ -391,8 +441,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
                     tmem_store_32cols(o_addr + 32 * cc, o);
                 }
+                tmem_wait_st();
             }
-            tmem_wait_st();
+            // this row of P into the 128-byte-swizzled K-major tile the MMA reads:
+            // keys [64 h, 64 h + 64) in chunk h, 16-byte unit x of row r at unit x ^ (r % 8)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t row = p_smem(t) + hh * G::kChunkBytes + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+                for (int x = 0; x < 8; ++x)
+                    st_shared_v4(row + ((static_cast<uint32_t>(x) ^ (static_cast<uint32_t>(r) & 7u)) << 4),
+                                 pk[32 * hh + 4 * x], pk[32 * hh + 4 * x + 1], pk[32 * hh + 4 * x + 2],
+                                 pk[32 * hh + 4 * x + 3]);
+            }
+            fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(p_full(t));
         }

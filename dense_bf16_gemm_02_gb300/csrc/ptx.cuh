@@ -78,6 +78,59 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// One non-blocking probe of phase `parity` (never suspends the thread: a
+// suspended mbarrier wait was measured to resume several hundred cycles after
+// the phase completed, a probe loop sees it within tens of cycles).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// One probe that may suspend the thread for up to `hint_ns` nanoseconds while
+// the phase is incomplete; the thread resumes as soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_try_wait_suspend_cluster(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // The same with acquire at cluster scope, for barriers that threads of the
 // peer CTA arrive on.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -363,6 +416,29 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
+// 3-D tiled TMA load into this CTA's shared memory whose completion is
+// signalled on `cluster_bar`, which may live in either CTA of the pair.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                 uint32_t cluster_bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(cluster_bar)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] · B[smem]ᵀ on the CTA pair, kind::f16: each CTA's
+// Tensor Memory supplies its 128 rows of A (two bf16 per 32-bit column).
+__device__ __forceinline__ void mma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= A[tmem] · B[smem]ᵀ on one CTA, kind::f16: the A operand is
 // read from Tensor Memory (one row per lane, two bf16 per 32-bit column).
 __device__ __forceinline__ void mma_bf16_ts_one(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -461,16 +537,17 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
 }
 
 // Shared-memory matrix descriptor for an MN-major operand tile written by
-// TMA with 128-byte swizzling: rows of 64 bf16 along MN (128 B), one row per
-// K index, 8-row (8 K) swizzle atoms of 1024 B (stride byte offset), and
-// further 64-element MN groups `mn_group_bytes` apart (leading byte offset).
-__device__ __forceinline__ uint64_t smem_desc_mnmajor_sw128(uint32_t saddr, uint32_t mn_group_bytes) {
+// TMA with 128- or 64-byte swizzling (`row_bytes` 128 or 64): one row of
+// row_bytes per K index, 8-row (8 K) swizzle atoms of 8·row_bytes bytes
+// (stride byte offset) and further MN groups of row_bytes `mn_group_bytes`
+// apart (leading byte offset). Swizzle mode 2 = 128-byte, 4 = 64-byte.
+__device__ __forceinline__ uint64_t smem_desc_mnmajor(uint32_t saddr, uint32_t row_bytes, uint32_t mn_group_bytes) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
     d |= static_cast<uint64_t>((mn_group_bytes >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>((8u * row_bytes) >> 4) << 32;
     d |= static_cast<uint64_t>(1u) << 46;
-    d |= static_cast<uint64_t>(2u) << 61;
+    d |= static_cast<uint64_t>(row_bytes == 128 ? 2u : 4u) << 61;
     return d;
 }
 
