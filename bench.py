@@ -50,10 +50,18 @@ MEASURED_TRAFFIC = {
 }
 
 
-def kernel_source_digest() -> str:
+KERNEL_SOURCES = {
+    "gemm": ("gemm_kernel.cuh", "ptx.cuh", "hk_gemm.cu"),
+    "attention": ("attn_kernel.cuh", "ptx.cuh", "hk_attention.cu", "host_internal.h"),
+}
+
+
+def kernel_source_digest(kind: str = "gemm") -> str:
+    """Digest of the sources one kernel is built from (a stored ncu traffic
+    figure is valid only while they are unchanged)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_bf16_gemm_02_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kind]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
@@ -729,7 +737,7 @@ def run_attn(args, w):
     value = replica_value(flops, args.steps, world, elapsed_max)
     mean_launch_ms = statistics.mean(per_launch)
     achieved = flops / (mean_launch_ms / 1e3) / 1e12
-    digest = kernel_source_digest()
+    digest = kernel_source_digest("attention")
     tr = MEASURED_TRAFFIC.get(w.name)
     traffic = tr["bytes_per_launch"] if tr and tr.get("source_digest") == digest else None
     h2d = int(sum(x.numel() * 2 for x in (Q_h, K_h, V_h)))

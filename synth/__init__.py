@@ -79,6 +79,7 @@ ATTN_WORKLOADS = {
                                                    True, True),
     "attn_gqa_b16_s4096_d64": AttnWorkload("attn_gqa_b16_s4096_d64", 22, 16, 64, 8, 4096, 64, False, True),
     "attn_gqa_small": AttnWorkload("attn_gqa_small", 23, 2, 8, 2, 300, 128, False, False),
+    "attn_gqa_b2_s4096_d128": AttnWorkload("attn_gqa_b2_s4096_d128", 24, 2, 64, 8, 4096, 128, False, True),
 }
 
 
