@@ -47,6 +47,11 @@ MEASURED_TRAFFIC = {
                   "profile": "profiles/gemm_bf16_kernel_pair256_gemm_8192.md"},
     "skinny_128x28672x8192": {"source_digest": "a00f76b659ea9f45", "bytes_per_launch": 471919872 + 6630144,
                               "profile": "profiles/gemm_bf16_kernel_single128x192_skinny_128x28672x8192.md"},
+    # attention: captured at B2 (one launch); the B16 figure scales it by 8 (traffic grows with B)
+    "attn_gqa_b2_s4096_d128": {"source_digest": "1e2a0b2668de68b3", "bytes_per_launch": 184536832 + 122917632,
+                               "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
+    "attn_gqa_b16_s4096_d128": {"source_digest": "1e2a0b2668de68b3", "bytes_per_launch": 8 * (184536832 + 122917632),
+                                "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
 }
 
 
