@@ -48,7 +48,7 @@ namespace attn {
 constexpr int kTileQ = 128;         // query rows per tile (MMA M)
 constexpr int kTiles = 2;           // query tiles per CTA
 constexpr int kBlockKV = 128;       // keys per K/V block
-constexpr int kThreads = 320;       // warps 0-3 softmax tile 0, 4-7 softmax tile 1, 8 TMA, 9 MMA
+constexpr int kThreads = 352;       // warps 0-3 softmax tile 0, 4-7 softmax tile 1, 8 TMA, 9-10 MMA
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
 constexpr int kSmemLimit = 232448;
@@ -215,7 +215,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         mbar_init(q_full, 1);
         for (int s = 0; s < G::kSlots; ++s) {
             mbar_init(kv_full(s), 1);
-            mbar_init(kv_empty(s), 1);
+            mbar_init(kv_empty(s), n_t1 > 0 ? 2 : 1);   // one commit per active tile
         }
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(s_full(t), 1);
@@ -276,9 +276,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                 kvh, kv_full(s));
             }
         }
-    } else if (warp == kWarpMma) {
-        // --------------------------------------------------- MMA issue --
-        if (lane == 0 && n_all > 0) {
+    } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+        // ------------------------------------------- MMA issue, one warp per tile --
+        // A tcgen05.mma holds its issuing thread for about the time it
+        // computes; with one issuer per tile, each issuer's barrier waits and
+        // commits overlap the other tile's MMAs. A K/V slot is released when
+        // the issuers of every active tile have committed on it.
+        const int t = static_cast<int>(warp) - kWarpMma;
+        const int n = n_t(t);
+        if (lane == 0 && n > 0) {
             auto wait = [&](uint32_t bar, uint32_t parity, uint32_t code) {
                 if (abort_seen) return false;
                 if (!attn_wait(p, bar, parity, code)) abort_seen = true;
@@ -286,63 +292,46 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             };
             auto kv_slot = [&](int u) { return u % G::kSlots; };
             auto kv_parity = [&](int u) { return static_cast<uint32_t>((u / G::kSlots) & 1); };
-            const uint32_t q_base = base + G::kOffQ;
-            auto issue_s = [&](int t, int u) {   // S_t = Q_t · K_uᵀ
-                const uint32_t qa = q_base + t * G::kTileBytes;
+            const uint32_t qa = base + G::kOffQ + t * G::kTileBytes;
+            const uint32_t s_tmem = tmem_base + G::kColS + t * kBlockKV;
+            const uint32_t o_tmem = tmem_base + G::kColO + t * kD;
+            const uint32_t pa = p_smem(t);
+            auto issue_s = [&](int u) {   // S_t = Q_t · K_uᵀ
                 const uint32_t ka = slot_addr(kv_slot(u));
-                const uint32_t d = tmem_base + G::kColS + t * kBlockKV;
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-                    mma_bf16_one(d, smem_desc_kmajor_sw128(qa + off), smem_desc_kmajor_sw128(ka + off), G::kIdescS,
-                                 kk > 0 ? 1u : 0u);
+                    mma_bf16_one(s_tmem, smem_desc_kmajor_sw128(qa + off), smem_desc_kmajor_sw128(ka + off),
+                                 G::kIdescS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit_one(s_full(t));
+                mma_commit_one(kv_empty(kv_slot(u)));
             };
-            auto issue_pv = [&](int t, int u, bool first) {   // O_t += P_t · V_u
-                const uint32_t va = slot_addr(kv_slot(u));
-                const uint32_t d = tmem_base + G::kColO + t * kD;
-                const uint32_t pa = p_smem(t);
-#pragma unroll
-                for (int kk = 0; kk < kBlockKV / 16; ++kk)
-                    mma_bf16_one(d, smem_desc_kmajor_sw128(pa + (kk >> 2) * G::kChunkBytes + (kk & 3) * 32),
-                                 smem_desc_mnmajor(va + kk * 2048, 128, G::kChunkBytes), G::kIdescPV,
-                                 (first && kk == 0) ? 0u : 1u);
-                mma_commit_one(o_done(t));
-            };
-
             if (wait(q_full, 0, kErrMmaKv) && wait(kv_full(kv_slot(0)), kv_parity(0), kErrMmaKv)) {
                 tc_fence_after_sync();
-                for (int t = 0; t < kTiles; ++t)
-                    if (n_t(t) > 0) issue_s(t, 0);
-                mma_commit_one(kv_empty(kv_slot(0)));
+                issue_s(0);
             }
-            for (int j = 0; j < n_all && !abort_seen; ++j) {
-                // S for block j+1, as soon as each tile's softmax has read its S of block j
-                if (j + 1 < n_all) {
+            for (int j = 0; j < n && !abort_seen; ++j) {
+                // S for block j+1, once this tile's softmax has read its S of block j
+                if (j + 1 < n) {
                     const int uk = pos_k(j + 1);
                     if (!wait(kv_full(kv_slot(uk)), kv_parity(uk), kErrMmaKv)) break;
-                    for (int t = 0; t < kTiles && !abort_seen; ++t) {
-                        if (j + 1 < n_t(t)) {
-                            if (!wait(s_free(t), j & 1, kErrMmaP)) break;
-                            tc_fence_after_sync();
-                            issue_s(t, uk);
-                        }
-                    }
-                    if (abort_seen) break;
-                    mma_commit_one(kv_empty(kv_slot(uk)));
+                    if (!wait(s_free(t), j & 1, kErrMmaP)) break;
+                    tc_fence_after_sync();
+                    issue_s(uk);
                 }
-                // P·V for block j, as each tile's P lands in shared memory
+                // O_t += P_t · V_j once P_t is in shared memory
                 const int uv = pos_v(j, n_all);
                 if (!wait(kv_full(kv_slot(uv)), kv_parity(uv), kErrMmaKv)) break;
-                for (int t = 0; t < kTiles && !abort_seen; ++t) {
-                    if (j < n_t(t)) {
-                        if (!wait(p_full(t), j & 1, kErrMmaP)) break;
-                        tc_fence_after_sync();
-                        issue_pv(t, uv, j == 0);
-                    }
-                }
-                if (abort_seen) break;
+                if (!wait(p_full(t), j & 1, kErrMmaP)) break;
+                tc_fence_after_sync();
+                const uint32_t va = slot_addr(kv_slot(uv));
+#pragma unroll
+                for (int kk = 0; kk < kBlockKV / 16; ++kk)
+                    mma_bf16_one(o_tmem, smem_desc_kmajor_sw128(pa + (kk >> 2) * G::kChunkBytes + (kk & 3) * 32),
+                                 smem_desc_mnmajor(va + kk * 2048, 128, G::kChunkBytes), G::kIdescPV,
+                                 (j == 0 && kk == 0) ? 0u : 1u);
+                mma_commit_one(o_done(t));
                 mma_commit_one(kv_empty(kv_slot(uv)));
             }
         }
