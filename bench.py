@@ -43,14 +43,14 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 MEASURED_TRAFFIC = {
     "fp8_gemm_8192": {"source_digest": "65485f133f7bc8ea", "bytes_per_launch": 341788416 + 116316928,
                       "profile": "profiles/gemm_fp8_kernel_pair256_fp8_gemm_8192.md"},
-    "gemm_8192": {"source_digest": "a00f76b659ea9f45", "bytes_per_launch": 1077694000 + 127190016,
+    "gemm_8192": {"source_digest": "ec8f7a99b9ec3031", "bytes_per_launch": 1082111000 + 127698432,
                   "profile": "profiles/gemm_bf16_kernel_pair256_gemm_8192.md"},
-    "skinny_128x28672x8192": {"source_digest": "a00f76b659ea9f45", "bytes_per_launch": 471919872 + 6630144,
+    "skinny_128x28672x8192": {"source_digest": "ec8f7a99b9ec3031", "bytes_per_launch": 471968000 + 3932160,
                               "profile": "profiles/gemm_bf16_kernel_single128x192_skinny_128x28672x8192.md"},
     # attention: captured at B2 (one launch); the B16 figure scales it by 8 (traffic grows with B)
-    "attn_gqa_b2_s4096_d128": {"source_digest": "1e2a0b2668de68b3", "bytes_per_launch": 184536832 + 122917632,
+    "attn_gqa_b2_s4096_d128": {"source_digest": "d7a38284885b41be", "bytes_per_launch": 185660416 + 124675328,
                                "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
-    "attn_gqa_b16_s4096_d128": {"source_digest": "1e2a0b2668de68b3", "bytes_per_launch": 8 * (184536832 + 122917632),
+    "attn_gqa_b16_s4096_d128": {"source_digest": "d7a38284885b41be", "bytes_per_launch": 8 * (185660416 + 124675328),
                                 "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
 }
 
