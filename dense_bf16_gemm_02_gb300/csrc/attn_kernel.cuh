@@ -70,7 +70,10 @@ struct AttnGeometry {
     static constexpr int kChunkBytes = 128 * 128;             // 128 rows × 128 B (one TMA box)
     static constexpr int kTileBytes = kChunks * kChunkBytes;  // one Q tile, one K block or one V block
     static constexpr int kQBytes = kTiles * kTileBytes;
-    static constexpr int kPBytes = kTileQ * kBlockKV * 2;     // bf16 P of one tile (two 64-key chunks)
+    // bf16 P of a tile: in its own TMEM columns when they fit (D = 64), else in
+    // shared memory as two 64-key chunks (D = 128: O and S fill the TMEM)
+    static constexpr bool kPInTmem = kD == 64;
+    static constexpr int kPBytes = kPInTmem ? 0 : kTileQ * kBlockKV * 2;
     static constexpr int kSlotsFit = (kSmemLimit - kQBytes - kTiles * kPBytes - 2048) / kTileBytes;
     static constexpr int kSlots = kSlotsFit > 8 ? 8 : kSlotsFit;   // K/V ring
     static_assert(kSlots >= 3, "K/V ring too shallow");
@@ -83,9 +86,12 @@ struct AttnGeometry {
     static constexpr int kOffTmemHolder = kOffBars + kNumBars * 8;
     static constexpr int kSmemBytes = kOffTmemHolder + 16 + 1024;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
-    // TMEM columns: O_0, O_1 (kD each), then S_0, S_1 (128 each)
+    // TMEM columns: O_0, O_1 (kD each), then S_0, S_1 (128 each), then (D = 64)
+    // P_0, P_1 (64 each: two bf16 per column)
     static constexpr int kColO = 0;
     static constexpr int kColS = 2 * kD;
+    static constexpr int kColP = 2 * kD + 2 * kBlockKV;
+    static_assert(!kPInTmem || kColP + 2 * (kBlockKV / 2) <= 512, "TMEM");
     static constexpr int kTmemCols = 512;
     static constexpr uint32_t kIdescS = idesc_bf16_f32(kTileQ, kBlockKV);
     static constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileQ, kD) | (1u << 16);   // B (V) MN-major
@@ -296,6 +302,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             const uint32_t s_tmem = tmem_base + G::kColS + t * kBlockKV;
             const uint32_t o_tmem = tmem_base + G::kColO + t * kD;
             const uint32_t pa = p_smem(t);
+            const uint32_t p_tmem = tmem_base + G::kColP + t * (kBlockKV / 2);
             auto issue_s = [&](int u) {   // S_t = Q_t · K_uᵀ
                 const uint32_t ka = slot_addr(kv_slot(u));
 #pragma unroll
@@ -327,10 +334,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 tc_fence_after_sync();
                 const uint32_t va = slot_addr(kv_slot(uv));
 #pragma unroll
-                for (int kk = 0; kk < kBlockKV / 16; ++kk)
-                    mma_bf16_one(o_tmem, smem_desc_kmajor_sw128(pa + (kk >> 2) * G::kChunkBytes + (kk & 3) * 32),
-                                 smem_desc_mnmajor(va + kk * 2048, 128, G::kChunkBytes), G::kIdescPV,
-                                 (j == 0 && kk == 0) ? 0u : 1u);
+                for (int kk = 0; kk < kBlockKV / 16; ++kk) {
+                    const uint64_t vdesc = smem_desc_mnmajor(va + kk * 2048, 128, G::kChunkBytes);
+                    const uint32_t acc = (j == 0 && kk == 0) ? 0u : 1u;
+                    if constexpr (G::kPInTmem)
+                        mma_bf16_ts_one(o_tmem, p_tmem + kk * 8, vdesc, G::kIdescPV, acc);
+                    else
+                        mma_bf16_one(o_tmem, smem_desc_kmajor_sw128(pa + (kk >> 2) * G::kChunkBytes + (kk & 3) * 32),
+                                     vdesc, G::kIdescPV, acc);
+                }
                 mma_commit_one(o_done(t));
                 mma_commit_one(kv_empty(kv_slot(uv)));
             }
@@ -432,18 +444,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 }
                 tmem_wait_st();
             }
-            // this row of P into the 128-byte-swizzled K-major tile the MMA reads:
-            // keys [64 h, 64 h + 64) in chunk h, 16-byte unit x of row r at unit x ^ (r % 8)
+            if constexpr (G::kPInTmem) {
+                // this row of P into the tile's own TMEM columns
+                const uint32_t p_addr = tmem_base + lane_off + G::kColP + t * (kBlockKV / 2);
+                tmem_store_32cols(p_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+                tmem_store_32cols(p_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+                tmem_wait_st();
+            } else {
+                // this row of P into the 128-byte-swizzled K-major tile the MMA reads:
+                // keys [64 h, 64 h + 64) in chunk h, 16-byte unit x of row r at unit x ^ (r % 8)
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const uint32_t row = p_smem(t) + hh * G::kChunkBytes + static_cast<uint32_t>(r) * 128u;
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint32_t row = p_smem(t) + hh * G::kChunkBytes + static_cast<uint32_t>(r) * 128u;
 #pragma unroll
-                for (int x = 0; x < 8; ++x)
-                    st_shared_v4(row + ((static_cast<uint32_t>(x) ^ (static_cast<uint32_t>(r) & 7u)) << 4),
-                                 pk[32 * hh + 4 * x], pk[32 * hh + 4 * x + 1], pk[32 * hh + 4 * x + 2],
-                                 pk[32 * hh + 4 * x + 3]);
+                    for (int x = 0; x < 8; ++x)
+                        st_shared_v4(row + ((static_cast<uint32_t>(x) ^ (static_cast<uint32_t>(r) & 7u)) << 4),
+                                     pk[32 * hh + 4 * x], pk[32 * hh + 4 * x + 1], pk[32 * hh + 4 * x + 2],
+                                     pk[32 * hh + 4 * x + 3]);
+                }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(p_full(t));
         }

@@ -404,6 +404,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] · B[smem]ᵀ on one CTA, kind::f16: the A operand is
+// read from Tensor Memory (one row per lane, two bf16 per 32-bit column).
+__device__ __forceinline__ void mma_bf16_ts_one(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Warp-collective registers -> TMEM: lane l of the warp writes TMEM lane
 // (taddr.lane + l), 32 consecutive 32-bit columns starting at taddr.col.
 __device__ __forceinline__ void tmem_store_32cols(uint32_t taddr, const uint32_t (&v)[32]) {
