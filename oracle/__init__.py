@@ -89,6 +89,14 @@ def _load():
             lib.oracle_gemm_fp8e4m3_entries.argtypes = [_P, _P, _P, _I64, _I64, _I64, ctypes.c_double, _P, _P,
                                                         _I64, ctypes.c_int]
             lib.oracle_gemm_fp8e4m3_entries.restype = ctypes.c_int
+            lib.oracle_ue8m0_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_ue8m0_to_double.restype = ctypes.c_double
+            lib.oracle_gemm_mxfp8.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
+                                              ctypes.c_int]
+            lib.oracle_gemm_mxfp8.restype = ctypes.c_int
+            lib.oracle_gemm_mxfp8_entries.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _P, _P,
+                                                      _I64, ctypes.c_int]
+            lib.oracle_gemm_mxfp8_entries.restype = ctypes.c_int
             lib.oracle_attention_fwd.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, ctypes.c_int,
                                                  _I64, _I64, ctypes.c_int]
             lib.oracle_attention_fwd.restype = ctypes.c_int
@@ -266,6 +274,50 @@ def gemm_fp8_entries(A: np.ndarray, B: np.ndarray, rows, cols, scale_a: float = 
     if rows.size:
         _load().oracle_gemm_fp8e4m3_entries(_ptr(A), _ptr(B), _ptr(out), A.shape[1], A.strides[0], B.strides[0],
                                             scale, _ptr(rows), _ptr(cols), rows.size, int(threads))
+    return out
+
+
+# ---- MXFP8 GEMM ------------------------------------------------------------
+
+def ue8m0_value(code: int) -> float:
+    """Value of a UE8M0 scale byte: 2^(E-127), NaN for 255."""
+    return float(_load().oracle_ue8m0_to_double(int(code) & 0xFF))
+
+
+def _mx_args(A, B, SA, SB):
+    A = _as_bytes(A, "A")
+    B = _as_bytes(B, "B")
+    M, K = A.shape
+    N = B.shape[0]
+    if K % 32:
+        raise ValueError("K must be a multiple of the block size 32")
+    for x, rows, name in ((SA, M, "SA"), (SB, N, "SB")):
+        if x.dtype != np.uint8 or x.shape != (rows, K // 32) or (x.shape[1] > 1 and x.strides[1] != 1):
+            raise TypeError(f"{name} must be a uint8 array of shape ({rows}, K/32) with unit stride")
+    return A, B, M, N, K
+
+
+def gemm_mxfp8(A: np.ndarray, B: np.ndarray, SA: np.ndarray, SB: np.ndarray, threads: int = 0) -> np.ndarray:
+    """C = RNE_bf16(Σ_b SA·SB·Σ_block A·B) for E4M3 codes A (M×K), B (N×K) and
+    UE8M0 block scales SA (M×K/32), SB (N×K/32)."""
+    A, B, M, N, K = _mx_args(A, B, SA, SB)
+    C = np.zeros((M, N), dtype=np.uint16)
+    if M and N:
+        _load().oracle_gemm_mxfp8(_ptr(A), _ptr(B), _ptr(SA), _ptr(SB), _ptr(C), M, N, K, max(A.strides[0], K),
+                                  max(B.strides[0], K), max(SA.strides[0], K // 32), max(SB.strides[0], K // 32), N,
+                                  int(threads))
+    return C
+
+
+def gemm_mxfp8_entries(A, B, SA, SB, rows, cols, threads: int = 0) -> np.ndarray:
+    A, B, M, N, K = _mx_args(A, B, SA, SB)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
+    out = np.zeros(rows.size, dtype=np.uint16)
+    if rows.size:
+        _load().oracle_gemm_mxfp8_entries(_ptr(A), _ptr(B), _ptr(SA), _ptr(SB), _ptr(out), K, A.strides[0],
+                                          B.strides[0], max(SA.strides[0], K // 32), max(SB.strides[0], K // 32),
+                                          _ptr(rows), _ptr(cols), rows.size, int(threads))
     return out
 
 

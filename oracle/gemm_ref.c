@@ -310,6 +310,96 @@ int oracle_gemm_fp8e4m3_entries(const uint8_t* A, const uint8_t* B, uint16_t* ou
     return run_parallel8(w, count, threads);
 }
 
+/* ---- MXFP8 GEMM (E4M3 blocks of 32 with UE8M0 scales) --------------------
+ * The FP8 GEMM row of the HipKittens "L2" detail page's §3 "Target
+ * operation" table is an MXFP8 product: FP8 (E4M3) operands whose K dimension
+ * is cut into blocks of 32 consecutive elements, each block of each row
+ * carrying one shared scale, FP32 accumulation, here a bf16 output. The scale
+ * byte is UE8M0 (the OCP MX format's 8-bit unsigned exponent): value
+ * 2^(E - 127), E = 255 is NaN. With KB = K / 32 blocks:
+ *   C[i][j] = round_bf16_rne( sum_b SA[i][b] * SB[j][b] * sum_{k in block b} A[i][k] * B[j][k] ).
+ * Each block sum of 32 exact products is exact in binary64 (the products span
+ * fewer than 53 bits of exponent and mantissa); the scales are powers of two;
+ * the sum over blocks runs in binary64 in increasing b; one rounding. */
+double oracle_ue8m0_to_double(uint8_t e) {
+    if (e == 255) return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
+typedef struct {
+    const uint8_t *A, *B, *SA, *SB;
+    uint16_t* out;
+    int64_t N, K, lda, ldb, ldsa, ldsb, ldo;
+    const int64_t* rows;
+    const int64_t* cols;
+    int64_t begin, end;
+    int mode;
+} workmx_t;
+
+static uint16_t entry_mx(const workmx_t* w, int64_t i, int64_t j) {
+    const uint8_t* a = w->A + i * w->lda;
+    const uint8_t* b = w->B + j * w->ldb;
+    const uint8_t* sa = w->SA + i * w->ldsa;
+    const uint8_t* sb = w->SB + j * w->ldsb;
+    double s = 0.0;
+    for (int64_t blk = 0; blk < w->K / 32; ++blk) {
+        double d = 0.0;
+        for (int64_t k = 32 * blk; k < 32 * blk + 32; ++k)
+            d += oracle_e4m3_to_double(a[k]) * oracle_e4m3_to_double(b[k]);
+        s += oracle_ue8m0_to_double(sa[blk]) * oracle_ue8m0_to_double(sb[blk]) * d;
+    }
+    return oracle_round_bf16(s);
+}
+
+static void* worker_mx(void* p) {
+    workmx_t* w = (workmx_t*)p;
+    for (int64_t t = w->begin; t < w->end; ++t) {
+        if (w->mode == 0) {
+            uint16_t* o = w->out + t * w->ldo;
+            for (int64_t j = 0; j < w->N; ++j) o[j] = entry_mx(w, t, j);
+        } else {
+            w->out[t] = entry_mx(w, w->rows[t], w->cols[t]);
+        }
+    }
+    return NULL;
+}
+
+static int run_parallel_mx(workmx_t base, int64_t items, int threads) {
+    threads = resolve_threads(threads, items);
+    pthread_t tid[256];
+    int joined[256];
+    workmx_t w[256];
+    for (int t = 0; t < threads; ++t) {
+        w[t] = base;
+        w[t].begin = items * t / threads;
+        w[t].end = items * (t + 1) / threads;
+        joined[t] = 0;
+        if (t == threads - 1) worker_mx(&w[t]);
+        else if (pthread_create(&tid[t], NULL, worker_mx, &w[t]) == 0) joined[t] = 1;
+        else worker_mx(&w[t]);
+    }
+    for (int t = 0; t < threads - 1; ++t)
+        if (joined[t]) pthread_join(tid[t], NULL);
+    return threads;
+}
+
+/* Full MXFP8 GEMM; K must be a multiple of 32; SA is M x K/32 (row stride
+ * ldsa bytes), SB is N x K/32 (ldsb). */
+int oracle_gemm_mxfp8(const uint8_t* A, const uint8_t* B, const uint8_t* SA, const uint8_t* SB, uint16_t* C,
+                      int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldsa, int64_t ldsb,
+                      int64_t ldc, int threads) {
+    workmx_t w = {A, B, SA, SB, C, N, K, lda, ldb, ldsa, ldsb, ldc, NULL, NULL, 0, 0, 0};
+    return run_parallel_mx(w, M, threads);
+}
+
+/* Selected entries of the MXFP8 GEMM. */
+int oracle_gemm_mxfp8_entries(const uint8_t* A, const uint8_t* B, const uint8_t* SA, const uint8_t* SB,
+                              uint16_t* out, int64_t K, int64_t lda, int64_t ldb, int64_t ldsa, int64_t ldsb,
+                              const int64_t* rows, const int64_t* cols, int64_t count, int threads) {
+    workmx_t w = {A, B, SA, SB, out, 0, K, lda, ldb, ldsa, ldsb, 0, rows, cols, 0, 0, 1};
+    return run_parallel_mx(w, count, threads);
+}
+
 /* ---- attention forward (GQA) ----------------------------------------------
  * The pages' second workload (HipKittens "L2" detail page, §3 "Target
  * operation" table, rows MHA / GQA fwd: Q [B, Hq, S, D], K and V
