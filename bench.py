@@ -529,6 +529,220 @@ def run_hk(args, w):
     return 0
 
 
+# ------------------------------------------------------------- MXFP8 GEMM --
+
+MX_METRIC = "MXFP8 GEMM TFLOPS at 1 GB300 and % of dense-FP8 tensor peak"
+
+
+def mx_config(w) -> dict:
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+            "layout": "A MxK, B NxK E4M3 row-major; SFA Mx(K/32), SFB Nx(K/32) UE8M0; C MxN bf16 (C = A·Bᵀ)",
+            "values": f"E4M3 of N(0,1), seeds {1000 + w.wid}/{2000 + w.wid}; scales uniform 2^-3..2^3, "
+                      f"seeds {3100 + w.wid}/{3200 + w.wid}",
+            "l2": "no flush: inputs larger than L2 (A+B = %d MiB > 126 MiB)" % ((w.M + w.N) * w.K >> 20)
+            if (w.M + w.N) * w.K > 126 << 20 else "inputs smaller than L2 (warm L2)",
+            "block": 32, "accumulate": "fp32", "output": "bf16", "tile": "128x192 per CTA"}
+
+
+def oracle_mx_rows_timed(A, B, SA, SB, rows) -> tuple[float, int]:
+    import oracle
+    N = B.shape[0]
+    rr = np.repeat(np.asarray(rows, dtype=np.int64), N)
+    cc = np.tile(np.arange(N, dtype=np.int64), len(rows))
+    t0 = time.perf_counter()
+    oracle.gemm_mxfp8_entries(A, B, SA, SB, rr, cc)
+    return time.perf_counter() - t0, os.cpu_count() or 1
+
+
+def run_reference_mx(args, w):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    A, B, SA, SB = synth.operands_mx(w)
+    t, _ = oracle_mx_rows_timed(A, B, SA, SB, [0])
+    rows_per_step = int(max(1, min(64, 120.0 / (args.steps + args.warmup) / max(t, 1e-6))))
+    rows = np.arange(rows_per_step, dtype=np.int64)
+    for _ in range(args.warmup):
+        oracle_mx_rows_timed(A, B, SA, SB, rows)
+    total, used = 0.0, 0
+    for _ in range(args.steps):
+        dt, used = oracle_mx_rows_timed(A, B, SA, SB, rows)
+        total += dt
+    value = gemm_flops(rows_per_step, w.N, w.K) * args.steps / total / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": MX_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": mx_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": f"{rows_per_step} full rows of C per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+    return 0
+
+
+def run_mx(args, w):
+    import torch
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import dense_bf16_gemm_02_gb300 as hk
+
+    Ab, Bb, SAb, SBb = synth.operands_mx(w)
+    A, B, SA, SB = (torch.from_numpy(x).to(dev) for x in (Ab, Bb, SAb, SBb))
+    C = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=dev)
+    nbytes = hk.hk_gemm_mxfp8_workspace_size(w.M, w.N, w.K)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = int(stream.cuda_stream)
+    flops = gemm_flops(w.M, w.N, w.K)
+    kb = w.K // 32
+
+    def launch(a, b, sa, sb, c):
+        st = hk.hk_gemm_mxfp8(a.data_ptr(), b.data_ptr(), sa.data_ptr(), sb.data_ptr(), c.data_ptr(), w.M, w.N, w.K,
+                              w.K, w.K, kb, kb, w.N, ws.data_ptr(), nbytes, sh)
+        if st != hk.HK_OK:
+            raise hk.HKError(st, "hk_gemm_mxfp8")
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            launch(A, B, SA, SB, C)
+    torch.cuda.synchronize(dev)
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    with torch.cuda.stream(stream):
+        events[0].record(stream)
+        for i in range(args.steps):
+            launch(A, B, SA, SB, C)
+            events[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    barrier(world)
+    elapsed_ms = events[0].elapsed_time(events[-1])
+    per_launch = [events[i].elapsed_time(events[i + 1]) for i in range(args.steps)]
+    if hk.hk_gemm_last_device_status(local) != hk.HK_OK:
+        raise RuntimeError("device status after timing: " + hk.hk_gemm_last_error_string())
+    clocks = None
+    if sampler:
+        time.sleep(0.15)
+        sampler.stop()
+        clocks = sampler.summary(t_host0, t_host1)
+    elapsed_max = max_over_ranks(world, elapsed_ms)
+
+    # end to end: pinned host A, B, scales -> device -> GEMM -> C to pinned host (three streams)
+    hosts = [torch.from_numpy(x).pin_memory() for x in (Ab, Bb, SAb, SBb)]
+    devs = [[A, torch.empty_like(A)], [B, torch.empty_like(B)], [SA, torch.empty_like(SA)], [SB, torch.empty_like(SB)]]
+    C_d = [C, torch.empty_like(C)]
+    C_h = [torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    e2e_steps = max(4, min(args.steps, 30))
+
+    def e2e_run(n):
+        h2d_done = [torch.cuda.Event() for _ in range(2)]
+        comp_done, d2h_done = [None, None], [None, None]
+        for i in range(n):
+            k = i & 1
+            if comp_done[k] is not None:
+                s_h2d.wait_event(comp_done[k])
+            with torch.cuda.stream(s_h2d):
+                for h, d in zip(hosts, devs):
+                    d[k].copy_(h, non_blocking=True)
+                h2d_done[k].record(s_h2d)
+            stream.wait_event(h2d_done[k])
+            if d2h_done[k] is not None:
+                stream.wait_event(d2h_done[k])
+            launch(devs[0][k], devs[1][k], devs[2][k], devs[3][k], C_d[k])
+            comp_done[k] = torch.cuda.Event()
+            comp_done[k].record(stream)
+            s_d2h.wait_event(comp_done[k])
+            with torch.cuda.stream(s_d2h):
+                C_h[k].copy_(C_d[k], non_blocking=True)
+                d2h_done[k] = torch.cuda.Event()
+                d2h_done[k].record(s_d2h)
+
+    e2e_run(2)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(s_h2d)
+    e2e_run(e2e_steps)
+    e1.record(s_d2h)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1))
+
+    ctx = None
+    if rank == 0 and not args.no_cublas_context:
+        try:   # cuBLASLt block-scaled FP8 through torch, if this torch exposes it
+            a8, b8 = A.view(torch.float8_e4m3fn), B.view(torch.float8_e4m3fn)
+            sa8, sb8 = SA.view(torch.float8_e8m0fnu), SB.view(torch.float8_e8m0fnu)
+            call = lambda: torch._scaled_mm(a8, b8.t(), scale_a=sa8, scale_b=sb8, out_dtype=torch.bfloat16)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize(dev)
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record()
+            for _ in range(20):
+                call()
+            c1.record()
+            torch.cuda.synchronize(dev)
+            ms = c0.elapsed_time(c1) / 20
+            ctx = {"value": flops / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_gemm": ms,
+                   "what": "torch._scaled_mm with e8m0 block scales (cuBLASLt) on the same GPU and inputs; context only"}
+        except Exception as exc:
+            ctx = {"unavailable": str(exc)[:200]}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+    peaks, peaks_src = load_peaks()
+    peak = float(peaks["bf16_tflops"]) * 2.0
+    value = replica_value(flops, args.steps, world, elapsed_max)
+    mean_launch_ms = statistics.mean(per_launch)
+    achieved = flops / (mean_launch_ms / 1e3) / 1e12
+    digest = kernel_source_digest("gemm")
+    tr = MEASURED_TRAFFIC.get(w.name)
+    traffic = tr["bytes_per_launch"] if tr and tr.get("source_digest") == digest else None
+    line = {
+        "metric": MX_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 (mx)", "data": "synthetic",
+        "config": dict(mx_config(w), parallelism="replicas" if world > 1 else "single GPU"),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+                     "traffic": traffic,
+                     "peak_source": f"bf16_tflops (burst) of {peaks_src} × 2 (nominal fp8/bf16 ratio)",
+                     "algorithmic_flops_per_launch": flops,
+                     "algorithmic_bytes_per_launch": float(w.M * w.K + w.N * w.K + (w.M + w.N) * kb + 2 * w.M * w.N),
+                     "mean_launch_ms": mean_launch_ms, "p10_launch_ms": float(np.percentile(per_launch, 10)),
+                     "p90_launch_ms": float(np.percentile(per_launch, 90)),
+                     "kernel": "mx_scale_blocks_kernel + gemm_bf16_kernel<1, 192, fp8, mx>", "source_digest": digest},
+        "e2e": {"value": replica_value(flops, e2e_steps, world, e2e_ms), "unit": UNIT,
+                "h2d_bytes_per_step": int(sum(h.numel() for h in hosts)), "d2h_bytes_per_step": int(C_h[0].numel() * 2),
+                "steps": e2e_steps, "pipelined": "H2D(i+1) | GEMM(i) | D2H(i-1) on three streams"},
+        "gpu_launches": args.steps * 2,
+        "clocks": clocks,
+        "context_cublaslt": ctx,
+    }
+    if not args.no_cpu_baseline:
+        t, used = oracle_mx_rows_timed(Ab, Bb, SAb, SBb, np.arange(2))
+        rows = int(max(1, min(w.M, 15.0 / max(t / 2, 1e-6))))
+        t, used = oracle_mx_rows_timed(Ab, Bb, SAb, SBb, np.arange(rows))
+        line["cpu_baseline"] = {"value": gemm_flops(rows, w.N, w.K) / t / 1e12, "unit": UNIT, "cores": used,
+                                "kind": "oracle", "sample": f"rows 0..{rows - 1} of C (fp64 C oracle, {t:.1f} s)"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 # ------------------------------------------------- attention forward --
 
 ATTN_METRIC = "GQA attention forward TFLOPS at 1 GB300 and % of dense-BF16 tensor peak"
@@ -784,7 +998,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["hk", "reference"], default="hk")
-    ap.add_argument("--workload", default="gemm_8192", choices=sorted(ALL_WORKLOADS) + sorted(synth.ATTN_WORKLOADS))
+    ap.add_argument("--workload", default="gemm_8192",
+                    choices=sorted(ALL_WORKLOADS) + sorted(synth.ATTN_WORKLOADS) + sorted(synth.MX_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cublas-context", action="store_true")
     ap.add_argument("--epilogue", default="none", choices=["none", "bias", "bias_relu", "bias_gelu", "bias_silu"],
@@ -793,6 +1008,9 @@ def main(argv=None):
                     help="raster group height in tile rows (0: the library default via hk_gemm_bf16)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
+    if args.workload in synth.MX_WORKLOADS:
+        w = synth.MX_WORKLOADS[args.workload]
+        return run_reference_mx(args, w) if args.impl == "reference" else run_mx(args, w)
     if args.workload in synth.ATTN_WORKLOADS:
         w = synth.ATTN_WORKLOADS[args.workload]
         return run_reference_attn(args, w) if args.impl == "reference" else run_attn(args, w)

@@ -58,10 +58,12 @@ constexpr int pow2_at_least(int x) {
     return r;
 }
 
-// Compile-time geometry of one kernel instance.
-template <int kCG, int kTileN_, bool kFp8 = false>
+// Compile-time geometry of one kernel instance. kMx: block-scaled FP8
+// (MXFP8, one UE8M0 scale per 32 K elements).
+template <int kCG, int kTileN_, bool kFp8 = false, bool kMx = false>
 struct Geometry {
     static_assert(kCG == 1 || kCG == 2, "one CTA or a CTA pair");
+    static_assert(!kMx || kFp8, "block scales come with FP8 operands");
     static_assert(kTileN_ % (16 * kCG) == 0 && kTileN_ >= 32 && kTileN_ <= 256, "MMA N");
     static constexpr int kTileM = kCtaM * kCG;              // rows of C per tile
     static constexpr int kTileN = kTileN_;                  // columns of C per tile (MMA N)
@@ -69,23 +71,33 @@ struct Geometry {
     static_assert(kBRows % 8 == 0, "B rows fill whole 8-row swizzle atoms");
     static constexpr int kBBytes = kBRows * kRowBytes;
     static constexpr int kKElems = kFp8 ? 128 : 64;        // K elements per stage
-    static constexpr int kStageBytes = kABytes + kBBytes;
+    // MXFP8: per stage one 512-byte scale block for the CTA's 128 A rows and
+    // one per 128 B rows of the whole tile (scale blocks of 32 rows × 16
+    // bytes, see tmem_cp_128x16b; in a pair each CTA holds all B scales)
+    static constexpr int kSfbAtoms = (kTileN + 127) / 128;
+    static constexpr int kSfBytes = kMx ? 512 * (1 + kSfbAtoms) : 0;
+    static constexpr int kSfCols = kMx ? 4 * (1 + kSfbAtoms) : 0;   // TMEM columns per stage
+    static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
     static constexpr int kFixed = kEpiWarps * 2 * kEpiBufBytes + 256 + 1024;   // epilogue, barriers, alignment
     static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
     static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
     static_assert(kStages >= 3, "pipeline too shallow");
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kABytes;
-    static constexpr int kOffEpi = kOffB + kStages * kBBytes;
+    static constexpr int kOffSf = kOffB + kStages * kBBytes;
+    static constexpr int kOffEpi = kOffSf + kStages * kSfBytes;
     static constexpr int kOffBars = kOffEpi + kEpiWarps * 2 * kEpiBufBytes;
     static constexpr int kNumBars = 2 * kStages + 4;        // full[S], empty[S], acc_full[2], acc_empty[2]
     static constexpr int kOffTmemHolder = kOffBars + kNumBars * 8;
     static constexpr int kSmemBytes = kOffTmemHolder + 16 + 1024;   // + slack for aligning the base
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
     static constexpr int kAccCols = kTileN;                 // TMEM columns per accumulator
-    static constexpr int kTmemCols = pow2_at_least(2 * kAccCols);
+    static constexpr int kColSf = 2 * kAccCols;             // MXFP8: scale ring, kSfCols per stage
+    static constexpr int kTmemCols = pow2_at_least(2 * kAccCols + kStages * kSfCols);
     static_assert(kTmemCols <= 512, "TMEM");
-    static constexpr uint32_t kIdesc = kFp8 ? idesc_e4m3_f32(kTileM, kTileN) : idesc_bf16_f32(kTileM, kTileN);
+    static constexpr uint32_t kIdesc = kMx    ? idesc_mxf8_f32(kTileM, kTileN)
+                                       : kFp8 ? idesc_e4m3_f32(kTileM, kTileN)
+                                              : idesc_bf16_f32(kTileM, kTileN);
     static constexpr uint32_t kIdescHalf =
         kFp8 ? idesc_e4m3_f32(kTileM, kTileN / 2) : idesc_bf16_f32(kTileM, kTileN / 2);
 };
@@ -122,6 +134,10 @@ struct GemmParams {
     uint32_t launch_id;
     uint32_t flags;
     uint64_t timeout_ns;
+    // MXFP8: scale blocks arranged per (tile, K stage) by mx_scale_blocks_kernel,
+    // read through a tensor map over the buffer as rows of 16 bytes (one
+    // 512-byte block = 32 rows); A blocks from row 0, B blocks from sf_b_row
+    int64_t sf_b_row;
 };
 
 // Grouped rasterisation: tiles are numbered so that group_m consecutive tile
@@ -259,12 +275,12 @@ __device__ __forceinline__ void drain_after_abort() {
     for (int i = 0; i < 200; ++i) __nanosleep(1000);
 }
 
-template <int kCG, int kTileN, bool kFp8>
+template <int kCG, int kTileN, bool kFp8, bool kMx = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                  const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_b_half,
                  const GemmParams p) {
-    using G = Geometry<kCG, kTileN, kFp8>;
+    using G = Geometry<kCG, kTileN, kFp8, kMx>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -357,6 +373,23 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         tma_load_2d(a_dst, &tmap_a, kb * G::kKElems, a_row, full_bar(stage));
                         tma_load_2d(b_dst, b_map, kb * G::kKElems, b_row, full_bar(stage));
                     }
+                    if constexpr (kMx) {   // this stage's scale blocks (tensor map in the half-B slot)
+                        const uint32_t sf_dst = base + G::kOffSf + stage * G::kSfBytes;
+                        const int64_t a_group = static_cast<int64_t>(tm) * kCG + rank;   // 128-row group
+                        const int a_row_sf = static_cast<int>((a_group * p.k_blocks + kb) * 32);
+                        const int b_row_sf = static_cast<int>(
+                            p.sf_b_row + (static_cast<int64_t>(tn) * p.k_blocks + kb) * (32 * G::kSfbAtoms));
+                        if constexpr (kCG == 2) {
+                            const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
+                            tma_load_2d_pair(sf_dst, &tmap_b_half, 0, a_row_sf, leader_full);
+                            for (int q = 0; q < G::kSfbAtoms; ++q)
+                                tma_load_2d_pair(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 32 * q, leader_full);
+                        } else {
+                            tma_load_2d(sf_dst, &tmap_b_half, 0, a_row_sf, full_bar(stage));
+                            for (int q = 0; q < G::kSfbAtoms; ++q)
+                                tma_load_2d(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 32 * q, full_bar(stage));
+                        }
+                    }
                     if (++stage == G::kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -396,18 +429,43 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                     tc_fence_after_sync();
                     const uint64_t a_desc = smem_desc_kmajor_sw128(base + G::kOffA + stage * kABytes);
                     const uint64_t b_desc = smem_desc_kmajor_sw128(base + G::kOffB + stage * G::kBBytes);
+                    if constexpr (kMx) {
+                        // scale blocks of this stage -> its slot of the TMEM scale ring (a copy
+                        // followed by MMAs of the same thread needs no wait in between)
+                        const uint32_t sf_src = base + G::kOffSf + stage * G::kSfBytes;
+                        const uint32_t sf_tmem = tmem_base + G::kColSf + stage * G::kSfCols;
 #pragma unroll
-                    for (int k = 0; k < kRowBytes / kMmaKBytes; ++k) {
-                        // advance 32 bytes along K inside the swizzle atom (16 bf16 or 32 FP8)
-                        const uint32_t acc = (kb != kb_begin || k != 0) ? 1u : 0u;
-                        if constexpr (kCG == 2 && kFp8)
-                            mma_f8_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
-                        else if constexpr (kCG == 2)
-                            mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
-                        else if constexpr (kFp8)
-                            mma_f8_one(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
-                        else
-                            mma_bf16_one(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
+                        for (int q = 0; q < 1 + G::kSfbAtoms; ++q) {
+                            if constexpr (kCG == 2)
+                                tmem_cp_128x16b_pair(sf_tmem + 4 * q, smem_desc_plain(sf_src + 512 * q, 16, 128));
+                            else
+                                tmem_cp_128x16b(sf_tmem + 4 * q, smem_desc_plain(sf_src + 512 * q, 16, 128));
+                        }
+#pragma unroll
+                        for (int k = 0; k < kRowBytes / kMmaKBytes; ++k) {
+                            const uint32_t acc = (kb != kb_begin || k != 0) ? 1u : 0u;
+                            // scale block k of the 4 in this stage: byte k of each scale word
+                            const uint32_t id = idesc | (static_cast<uint32_t>(k) << 4) |
+                                                (static_cast<uint32_t>(k) << 29);
+                            if constexpr (kCG == 2)
+                                mma_mxf8_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, id, sf_tmem, sf_tmem + 4, acc);
+                            else
+                                mma_mxf8_one(d_tmem, a_desc + 2u * k, b_desc + 2u * k, id, sf_tmem, sf_tmem + 4, acc);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < kRowBytes / kMmaKBytes; ++k) {
+                            // advance 32 bytes along K inside the swizzle atom (16 bf16 or 32 FP8)
+                            const uint32_t acc = (kb != kb_begin || k != 0) ? 1u : 0u;
+                            if constexpr (kCG == 2 && kFp8)
+                                mma_f8_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
+                            else if constexpr (kCG == 2)
+                                mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
+                            else if constexpr (kFp8)
+                                mma_f8_one(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
+                            else
+                                mma_bf16_one(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, acc);
+                        }
                     }
                     // free this stage (in both CTAs of a pair) once the MMAs above have read it
                     if constexpr (kCG == 2) mma_commit_pair_mask(empty_bar(stage), 0x3);
@@ -584,6 +642,55 @@ splitk_reduce_kernel(const float* __restrict__ partials, int32_t splits, int32_t
             for (int e = 0; col + e < N; ++e)
                 dst[e] = static_cast<uint16_t>((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
         }
+    }
+}
+
+// MXFP8 scale blocks. The caller's scales are row-major, one byte per 32 K
+// elements (sa: M × kb_total, row stride ldsa; sb: N × kb_total, ldsb). The
+// kernel needs, per (tile, 128-element K stage), 512-byte blocks whose byte
+// r·16 + q·4 + j holds the scale of row 32·q + r (of a 128-row group) and K
+// block 4·stage + j: one block per 128-row group of A and `b_groups` blocks
+// for the B rows of an N tile of `tile_n` rows. Rows or K blocks outside the
+// matrix get 0 (2^-127; the operands there are zero). One thread writes one
+// 16-byte line r of a block (4 rows × the 4 scales of the stage); the lines
+// of a block are consecutive, so a warp's stores are contiguous.
+__global__ void mx_scale_blocks_kernel(const uint8_t* __restrict__ sa, int64_t ldsa, const uint8_t* __restrict__ sb,
+                                       int64_t ldsb, int M, int N, int kb_total, int tiles_m, int tiles_n,
+                                       int k_blocks, int tile_n, int b_groups, uint8_t* __restrict__ out_a,
+                                       uint8_t* __restrict__ out_b) {
+    const int64_t lines_a = static_cast<int64_t>(tiles_m) * k_blocks * 32;
+    const int64_t lines_b = static_cast<int64_t>(tiles_n) * k_blocks * 32 * b_groups;
+    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < lines_a + lines_b;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const bool is_a = idx < lines_a;
+        const int64_t i = is_a ? idx : idx - lines_a;            // line index within its region
+        const int lines_per_tile = 32 * (is_a ? 1 : b_groups);   // lines of one (tile, stage)
+        const int64_t atom = i / lines_per_tile;
+        const int line = static_cast<int>(i - atom * lines_per_tile);
+        const int tile = static_cast<int>(atom / k_blocks);
+        const int stage = static_cast<int>(atom - static_cast<int64_t>(tile) * k_blocks);
+        const int group = line >> 5, r = line & 31;
+        const uint8_t* src = is_a ? sa : sb;
+        const int64_t ld = is_a ? ldsa : ldsb;
+        const int rows = is_a ? M : N;
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int local = 128 * group + 32 * q + r;
+            const int row = is_a ? 128 * tile + local : tile_n * tile + local;
+            uint32_t v = 0;
+            if ((is_a || local < tile_n) && row < rows) {
+                const uint8_t* p = src + static_cast<int64_t>(row) * ld;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int blk = 4 * stage + j;
+                    if (blk < kb_total) v |= static_cast<uint32_t>(p[blk]) << (8 * j);
+                }
+            }
+            w[q] = v;
+        }
+        uint8_t* dst = (is_a ? out_a : out_b) + i * 16;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 

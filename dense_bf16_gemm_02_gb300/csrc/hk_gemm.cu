@@ -53,16 +53,18 @@ struct Variant {
     int tile_m, tile_n;
     int stages, smem_bytes;
     bool fp8;          // E4M3 operands (else bf16)
+    bool mx;           // block-scaled E4M3 (MXFP8); never chosen automatically
     int k_elems;       // K elements per pipeline stage
+    int sf_bytes;      // MXFP8: bytes of scale blocks per stage and CTA
     KernelFn fn;
     const char* name;
 };
 
-template <int kCG, int kTileN, bool kFp8>
+template <int kCG, int kTileN, bool kFp8, bool kMx = false>
 constexpr Variant make_variant(int id, const char* name) {
-    using G = hk::Geometry<kCG, kTileN, kFp8>;
-    return Variant{id, kCG, G::kTileM, G::kTileN, G::kStages, G::kSmemBytes, kFp8, G::kKElems,
-                   &hk::gemm_bf16_kernel<kCG, kTileN, kFp8>, name};
+    using G = hk::Geometry<kCG, kTileN, kFp8, kMx>;
+    return Variant{id, kCG, G::kTileM, G::kTileN, G::kStages, G::kSmemBytes, kFp8, kMx, G::kKElems, G::kSfBytes,
+                   &hk::gemm_bf16_kernel<kCG, kTileN, kFp8, kMx>, name};
 }
 
 const Variant kVariants[] = {
@@ -76,12 +78,17 @@ const Variant kVariants[] = {
     make_variant<1, 192, true>(HK_KERNEL_SINGLE_128x192, "fp8 single 128x192"),
     make_variant<1, 128, true>(HK_KERNEL_SINGLE_128x128, "fp8 single 128x128"),
     make_variant<1, 64, true>(HK_KERNEL_SINGLE_128x64, "fp8 single 128x64"),
+    make_variant<1, 192, true, true>(HK_KERNEL_SINGLE_128x192, "mxfp8 single 128x192"),
+    make_variant<2, 192, true, true>(HK_KERNEL_PAIR_256x256, "mxfp8 pair 256x192"),
 };
+constexpr int kMxTileN = 192;   // N of both MXFP8 tiles (one CTA: 128x192, a pair: 256x192)
+using GeomMx = hk::Geometry<1, kMxTileN, true, true>;
+static_assert(GeomMx::kSfbAtoms == hk::Geometry<2, kMxTileN, true, true>::kSfbAtoms, "one scale layout");
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
-const Variant* find_variant(int id, bool fp8) {
+const Variant* find_variant(int id, bool fp8, bool mx = false) {
     for (const Variant& v : kVariants)
-        if (v.id == id && v.fp8 == fp8) return &v;
+        if (v.id == id && v.fp8 == fp8 && v.mx == mx) return &v;
     return nullptr;
 }
 
@@ -339,7 +346,7 @@ void choose_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo* di, int max_
     double best_t = 0.0;
     for (int i = 0; i < kNumVariants; ++i) {
         const Variant& v = kVariants[i];
-        if (v.fp8 != fp8) continue;
+        if (v.fp8 != fp8 || v.mx) continue;
         if (forced_kernel != HK_KERNEL_AUTO ? v.id != forced_kernel : ((M > hk::kCtaM) != (v.cg == 2))) continue;
         const int64_t k_blocks = ceil_div(K, v.k_elems);
         int64_t slots = di->max_units[i];
@@ -447,7 +454,8 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
 }
 
 hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const void* B, void* C, void* workspace,
-                 cudaStream_t stream, const void* bias = nullptr) {
+                 cudaStream_t stream, const void* bias = nullptr, const void* mx_scales = nullptr,
+                 size_t mx_scale_bytes = 0) {
     if (p->M == 0 || p->N == 0) return HK_OK;
     hk_status s = get_encoder();
     if (s != HK_OK) return s;
@@ -465,8 +473,15 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
     const uint32_t box_k = static_cast<uint32_t>(v->k_elems);
     if ((s = encode_2d(&ta, a_ptr, p->K > 0 ? p->M : 1, kk, lda, box_k, a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B, "A", bytes)) != HK_OK) return s;
     if ((s = encode_2d(&tb, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, box_k, b_rows, CU_TENSOR_MAP_SWIZZLE_128B, "B", bytes)) != HK_OK) return s;
-    CUtensorMap tbh;   // B in boxes of half the rows, for half-width units
-    if ((s = encode_2d(&tbh, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, box_k, b_rows / 2, CU_TENSOR_MAP_SWIZZLE_128B, "B", bytes)) != HK_OK) return s;
+    CUtensorMap tbh;   // B in boxes of half the rows, for half-width units (MXFP8: the scale blocks)
+    if (v->mx && mx_scales != nullptr) {
+        // prearranged scale blocks as rows of 16 bytes, one 512-byte block = 32 rows
+        if ((s = encode_2d(&tbh, mx_scales, static_cast<int64_t>(mx_scale_bytes / 16), 16, 16, 16, 32,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, "MXFP8 scales", true)) != HK_OK)
+            return s;
+    } else if ((s = encode_2d(&tbh, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, box_k, b_rows / 2, CU_TENSOR_MAP_SWIZZLE_128B, "B", bytes)) != HK_OK) {
+        return s;
+    }
     // the map covers N rounded down to a multiple of 8 (see the epilogue); at
     // least 8 columns so that it stays valid when N < 8 (then it is unused)
     const int64_t n_tma = p->N & ~int64_t(7);
@@ -781,6 +796,119 @@ hk_status hk_gemm_fp8_e4m3(const void* A, const void* B, void* C, int64_t M, int
     if ((s = fill_plan(&plan, M, N, K, lda, ldb, ldc, device, nullptr, di, false, true, alpha)) != HK_OK) return s;
     plan.owns_status = false;
     return launch(&plan, sw, A, B, C, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------- MXFP8 --
+
+namespace {
+
+struct MxLayout {
+    int64_t tiles_m, tiles_n, k_blocks;
+    size_t a_bytes, b_offset, total;
+};
+
+// A scale blocks per 128-row group (a pair tile covers two groups, so their
+// count is rounded up to even when the pair kernel runs: M > 128).
+MxLayout mx_layout(int64_t M, int64_t N, int64_t K) {
+    MxLayout l;
+    l.tiles_m = M <= hk::kCtaM ? 1 : 2 * ceil_div(M, 2 * hk::kCtaM);
+    l.tiles_n = ceil_div(N, kMxTileN);
+    l.k_blocks = ceil_div(K, 128);
+    l.a_bytes = static_cast<size_t>(l.tiles_m * l.k_blocks * 512);
+    l.b_offset = (l.a_bytes + 255) & ~size_t(255);
+    l.total = l.b_offset + static_cast<size_t>(l.tiles_n * l.k_blocks * 512 * GeomMx::kSfbAtoms);
+    return l;
+}
+
+}  // namespace
+
+size_t hk_gemm_mxfp8_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return mx_layout(M, N, K).total;
+}
+
+hk_status hk_gemm_mxfp8(const void* A, const void* B, const void* SFA, const void* SFB, void* C, int64_t M,
+                        int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldc,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    hk_status s = check_shape(M, N, K, lda, ldb, ldc);
+    if (s != HK_OK) return s;
+    if (K % 32) return fail(HK_ERR_INVALID_ARG, "K=%lld is not a multiple of the scale block 32", (long long)K);
+    if ((lda % 16) || (ldb % 16))
+        return fail(HK_ERR_MISALIGNED, "FP8 leading dimensions must be multiples of 16 elements (lda=%lld ldb=%lld)",
+                    (long long)lda, (long long)ldb);
+    if (K > 0 && (ldsfa < K / 32 || ldsfb < K / 32))
+        return fail(HK_ERR_INVALID_ARG, "scale leading dimensions must be at least K/32 (ldsfa=%lld ldsfb=%lld)",
+                    (long long)ldsfa, (long long)ldsfb);
+    if (M == 0 || N == 0) return HK_OK;
+    if ((s = check_pointers(A, B, C, K)) != HK_OK) return s;
+    if (K > 0 && (!SFA || !SFB)) return fail(HK_ERR_INVALID_ARG, "null scale pointer");
+    const MxLayout lay = mx_layout(M, N, K);
+    if (K > 0) {
+        if (!workspace || workspace_bytes < lay.total)
+            return fail(HK_ERR_WORKSPACE, "MXFP8 workspace of %zu bytes needed (got %zu)", lay.total, workspace_bytes);
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+            return fail(HK_ERR_WORKSPACE, "MXFP8 workspace must be 256-byte aligned");
+    }
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "cudaGetDevice", e);
+    const DeviceInfo* di = nullptr;
+    if ((s = device_info(device, &di)) != HK_OK) return s;
+    uint32_t* status = nullptr;
+    if ((s = hk_host::status_word(device, &status)) != HK_OK) return s;
+    StatusWord sw{status};
+    // one CTA with 128x192 tiles for M <= 128, else CTA pairs with 256x192 tiles
+    const bool pair = M > hk::kCtaM;
+    const Variant* v = find_variant(pair ? HK_KERNEL_PAIR_256x256 : HK_KERNEL_SINGLE_128x192, true, true);
+    const int vi = static_cast<int>(v - kVariants);
+    int units = di->max_units[vi];
+    if (units <= 0) return fail(HK_ERR_UNSUPPORTED_DEVICE, "kernel %s does not fit on the device", v->name);
+    hk_gemm_plan plan;
+    plan.M = M; plan.N = N; plan.K = K; plan.lda = lda; plan.ldb = ldb; plan.ldc = ldc;
+    plan.device = device;
+    std::memset(&plan.cfg, 0, sizeof plan.cfg);
+    plan.variant = v;
+    plan.sm_count = di->sm_count;
+    plan.ws_bytes = 0;
+    plan.owns_status = false;
+    hk::GemmParams& g = plan.params;
+    std::memset(&g, 0, sizeof g);
+    g.M = static_cast<int32_t>(M);
+    g.N = static_cast<int32_t>(N);
+    g.K = static_cast<int32_t>(K);
+    g.tiles_m = static_cast<int32_t>(ceil_div(M, v->tile_m));
+    g.tiles_n = static_cast<int32_t>(ceil_div(N, v->tile_n));
+    g.k_blocks = static_cast<int32_t>(ceil_div(K, v->k_elems));
+    g.alpha = 1.0f;
+    const int64_t tiles = int64_t(g.tiles_m) * g.tiles_n;
+    if (tiles > (int64_t(1) << 30)) return fail(HK_ERR_INVALID_ARG, "too many output tiles");
+    g.num_tiles = static_cast<int32_t>(tiles);
+    g.splits = 1;
+    g.group_m = kDefaultGroupM;
+    g.a_rows = a_rows_for(*v, M);
+    g.expect_bytes = static_cast<uint32_t>(v->cg * ((g.a_rows + v->tile_n / v->cg) * hk::kRowBytes + v->sf_bytes));
+    g.n_pad = int64_t(g.tiles_n) * v->tile_n;
+    g.n_tma = static_cast<int32_t>(N & ~int64_t(7));
+    g.ldc = ldc;
+    g.timeout_ns = kDefaultTimeoutNs;
+    g.tail_start = -1;
+    g.total_units = g.num_tiles;
+    if (units > g.total_units) units = g.total_units;
+    plan.grid_ctas = v->cg * units;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (K > 0) {
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        g.sf_b_row = static_cast<int64_t>(lay.b_offset / 16);
+        const int64_t lines = static_cast<int64_t>(lay.total - lay.b_offset + lay.a_bytes) / 16;
+        const int64_t blocks = std::min<int64_t>(ceil_div(lines, 256), int64_t(di->sm_count) * 16);
+        hk::mx_scale_blocks_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+            static_cast<const uint8_t*>(SFA), ldsfa, static_cast<const uint8_t*>(SFB), ldsfb, static_cast<int>(M),
+            static_cast<int>(N), static_cast<int>(K / 32), static_cast<int>(lay.tiles_m), static_cast<int>(lay.tiles_n),
+            static_cast<int>(lay.k_blocks), kMxTileN, GeomMx::kSfbAtoms, ws, ws + lay.b_offset);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(HK_ERR_LAUNCH, "launching the MXFP8 scale arrangement", e);
+    }
+    return launch(&plan, &sw, A, B, C, nullptr, st, nullptr, K > 0 ? workspace : nullptr, lay.total);
 }
 
 // ------------------------------------------------- no-allocation variant --

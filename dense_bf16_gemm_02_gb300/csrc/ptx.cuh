@@ -319,6 +319,49 @@ __device__ __forceinline__ void mma_f8_one(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// Block-scaled FP8 MMA on one CTA (kind::mxf8f6f4, one UE8M0 scale per 32
+// K elements): D[tmem] (+)= (A·sfa)[smem] · (B·sfb)[smem]ᵀ, with the scale
+// factors read from Tensor Memory at sfa_tmem / sfb_tmem (which byte of each
+// 32-bit scale word is used is selected in the instruction descriptor).
+__device__ __forceinline__ void mma_mxf8_one(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// The CTA-pair form: issued by the leader, it runs in both CTAs of the pair,
+// each copying from its own shared memory to its own TMEM at the same offsets
+// (measured). Each CTA then applies its own A rows' scales and reads the B
+// scales of all N columns from its own TMEM (so every CTA holds all of them).
+__device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_cp_128x16b_pair(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+// Copy a 32-row × 16-byte block (512 bytes, described by `desc`) from shared
+// memory to 4 consecutive TMEM columns at `taddr`, once per 32-lane quarter
+// (32x128b.warpx4). Measured end to end: when byte r·16 + q·4 + j of the block
+// holds the scale of row 32·q + r and K block j, the block-scaled MMA that
+// reads its scales at `taddr` applies them to the 128 rows of its operand.
+__device__ __forceinline__ void tmem_cp_128x16b(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
 // Arrive (once) on `cluster_bar` when every tcgen05 operation this thread
 // issued before has completed.
 __device__ __forceinline__ void mma_commit_pair(uint32_t cluster_bar) {
@@ -516,6 +559,17 @@ __device__ __forceinline__ uint64_t smem_desc_mnmajor(uint32_t saddr, uint32_t r
     return d;
 }
 
+// Shared-memory descriptor of a non-swizzled block: leading byte offset
+// `lbo`, stride byte offset `sbo`, descriptor version 1, no swizzle.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;
+}
+
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16 (bits
 // 7-9 = 1), B bf16 (bits 10-12 = 1), both K-major (bits 15, 16 = 0),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
@@ -528,6 +582,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
 // 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t m, uint32_t n) {
     return (1u << 4) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with block scales: A and B in E4M3
+// (format code 0), both K-major, N >> 3 in bits 17-22, UE8M0 scale type (bit
+// 23), M >> 4 in bits 24-28; the scale-factor ids (bits 4-5 for B, 29-30 for
+// A) are or-ed in per MMA (scale block j of the 4 in a 32-bit scale word).
+__host__ __device__ constexpr uint32_t idesc_mxf8_f32(uint32_t m, uint32_t n) {
+    return ((n >> 3) << 17) | (1u << 23) | ((m >> 4) << 24);
 }
 
 }  // namespace hk

@@ -49,7 +49,7 @@ EXPORTED = (
     "hk_gemm_plan_run", "hk_gemm_plan_device_status", "hk_gemm_last_device_status",
     "hk_gemm_plan_destroy", "hk_status_string", "hk_gemm_last_error_string", "hk_gemm_bf16_noalloc",
     "hk_gemm_bf16_epilogue", "hk_gemm_plan_run_epilogue", "hk_gemm_fp8_e4m3",
-    "hk_attention_fwd", "hk_attention_fwd_ex",
+    "hk_attention_fwd", "hk_attention_fwd_ex", "hk_gemm_mxfp8", "hk_gemm_mxfp8_workspace_size",
 )
 
 
@@ -126,6 +126,10 @@ def load() -> ctypes.CDLL:
         lib.hk_gemm_fp8_e4m3.restype = I32
         lib.hk_gemm_bf16_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, ctypes.c_int32, P]
         lib.hk_gemm_bf16_noalloc.restype = I32
+        lib.hk_gemm_mxfp8.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I64, I64, I64, P, ctypes.c_size_t, P]
+        lib.hk_gemm_mxfp8.restype = I32
+        lib.hk_gemm_mxfp8_workspace_size.argtypes = [I64, I64, I64]
+        lib.hk_gemm_mxfp8_workspace_size.restype = ctypes.c_size_t
         lib.hk_attention_fwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I32, P]
         lib.hk_attention_fwd.restype = I32
         lib.hk_attention_fwd_ex.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I32, ctypes.c_uint32,
@@ -158,6 +162,17 @@ def hk_gemm_bf16_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: in
                          split_k: int = 0, stream: int = 0) -> int:
     """The GEMM that allocates nothing (scratch in a fixed array of the library)."""
     return load().hk_gemm_bf16_noalloc(A, B, C, M, N, K, lda, ldb, ldc, split_k, stream)
+
+
+def hk_gemm_mxfp8(A: int, B: int, SFA: int, SFB: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                  ldsfa: int, ldsfb: int, ldc: int, workspace: int, workspace_bytes: int, stream: int = 0) -> int:
+    """C (bf16) = block-scaled A·Bᵀ: E4M3 A (M×K), B (N×K), UE8M0 scales per 32 K elements."""
+    return load().hk_gemm_mxfp8(A, B, SFA, SFB, C, M, N, K, lda, ldb, ldsfa, ldsfb, ldc, workspace or None,
+                                workspace_bytes, stream)
+
+
+def hk_gemm_mxfp8_workspace_size(M: int, N: int, K: int) -> int:
+    return int(load().hk_gemm_mxfp8_workspace_size(M, N, K))
 
 
 def hk_attention_fwd(Q: int, K: int, V: int, O: int, lse: int, B: int, Hq: int, Hkv: int, S: int, D: int,

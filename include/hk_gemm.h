@@ -196,13 +196,38 @@ hk_status hk_gemm_fp8_e4m3(const void* A, const void* B, void* C,
                            int64_t lda, int64_t ldb, int64_t ldc,
                            float scale_a, float scale_b, void* stream);
 
+/* MXFP8 GEMM (the pages' FP8 GEMM row: MXFP8 inputs, FP32 accumulation; a
+ * bf16 output here): E4M3 operands whose K dimension is cut into blocks of 32
+ * elements, each block of each row scaled by one UE8M0 byte E (value
+ * 2^(E-127); 255 is NaN, as in the OCP MX format):
+ *     C[i,j] = bf16_rne( Σ_b 2^(SFA[i,b]-127)·2^(SFB[j,b]-127)·Σ_{k in block b} A[i,k]·B[j,k] )
+ * A (M×K) and B (N×K) hold E4M3 codes as in hk_gemm_fp8_e4m3 (lda, ldb
+ * multiples of 16); SFA (M × K/32) and SFB (N × K/32) hold the scale bytes,
+ * row-major with row strides ldsfa, ldsfb ≥ K/32 (bytes, any alignment); C is
+ * bf16 as in hk_gemm_bf16. K must be a multiple of 32 (else
+ * HK_ERR_INVALID_ARG). The products accumulate in fp32 on the tensor cores
+ * (tcgen05.mma kind::mxf8f6f4 with block scales, 128×192 tiles on one CTA).
+ * `workspace` (device memory, 256-byte aligned, caller-owned, at least
+ * hk_gemm_mxfp8_workspace_size(M, N, K) bytes, else HK_ERR_WORKSPACE)
+ * receives the scales rearranged per tile and K stage by a small kernel
+ * that runs first on `stream`; calls that overlap on the GPU must not share
+ * it. Errors and asynchrony as hk_gemm_bf16. */
+hk_status hk_gemm_mxfp8(const void* A, const void* B, const void* SFA, const void* SFB, void* C,
+                        int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldc,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace hk_gemm_mxfp8 needs for this shape (0 when M, N or K is 0). */
+size_t hk_gemm_mxfp8_workspace_size(int64_t M, int64_t N, int64_t K);
+
 /* Synchronise the plan's device and read-and-clear its status word:
  * HK_OK, or HK_ERR_TIMEOUT if a bounded wait ran out in any run since the
  * last read. */
 hk_status hk_gemm_plan_device_status(hk_gemm_plan* plan);
 
 /* The same for the calls of the one-shot entry points (hk_gemm_bf16,
- * hk_gemm_bf16_epilogue, hk_gemm_fp8_e4m3, hk_attention_fwd) on `device`. */
+ * hk_gemm_bf16_epilogue, hk_gemm_fp8_e4m3, hk_gemm_mxfp8, hk_attention_fwd)
+ * on `device`. */
 hk_status hk_gemm_last_device_status(int device);
 
 void hk_gemm_plan_destroy(hk_gemm_plan* plan);

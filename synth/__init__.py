@@ -59,6 +59,25 @@ FP8_WORKLOADS = {
 }
 FP8_SCALES = (0.5, 0.25)   # scale_a, scale_b of the FP8 workloads
 
+# MXFP8 workloads: E4M3 operands N(0,1) and UE8M0 block scales (one per 32 K
+# elements) uniform on [124, 130], i.e. 2^-3 .. 2^3, seeds 3100/3200 + id.
+MX_WORKLOADS = {
+    "mxfp8_gemm_8192": Workload("mxfp8_gemm_8192", 9, 8192, 8192, 8192, 1.0, True),
+    "mxfp8_gemm_256": Workload("mxfp8_gemm_256", 10, 256, 256, 256, 1.0, False),
+}
+
+
+def mx_scales(rows: int, blocks: int, seed: int, lo: int = 124, hi: int = 130) -> np.ndarray:
+    """rows × blocks UE8M0 scale bytes uniform on {lo..hi}."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    return g.integers(lo, hi + 1, size=(rows, blocks)).astype(np.uint8)
+
+
+def operands_mx(w: Workload) -> tuple[np.ndarray, np.ndarray, np.ndarray, np.ndarray]:
+    """(A, B, SA, SB) for an MXFP8 workload."""
+    A, B = normal_e4m3(w.M, w.K, 1000 + w.wid), normal_e4m3(w.N, w.K, 2000 + w.wid)
+    return A, B, mx_scales(w.M, w.K // 32, 3100 + w.wid), mx_scales(w.N, w.K // 32, 3200 + w.wid)
+
 
 @dataclass(frozen=True)
 class AttnWorkload:
