@@ -135,8 +135,9 @@ struct GemmParams {
     uint32_t flags;
     uint64_t timeout_ns;
     // MXFP8: scale blocks arranged per (tile, K stage) by mx_scale_blocks_kernel,
-    // read through a tensor map over the buffer as rows of 16 bytes (one
-    // 512-byte block = 32 rows); A blocks from row 0, B blocks from sf_b_row
+    // read through a tensor map over the buffer as rows of 256 bytes (one
+    // 512-byte block = 2 rows, so one TMA copy moves it in two row requests);
+    // A blocks from row 0, B blocks from row sf_b_row
     int64_t sf_b_row;
 };
 
@@ -376,18 +377,18 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                     if constexpr (kMx) {   // this stage's scale blocks (tensor map in the half-B slot)
                         const uint32_t sf_dst = base + G::kOffSf + stage * G::kSfBytes;
                         const int64_t a_group = static_cast<int64_t>(tm) * kCG + rank;   // 128-row group
-                        const int a_row_sf = static_cast<int>((a_group * p.k_blocks + kb) * 32);
+                        const int a_row_sf = static_cast<int>((a_group * p.k_blocks + kb) * 2);
                         const int b_row_sf = static_cast<int>(
-                            p.sf_b_row + (static_cast<int64_t>(tn) * p.k_blocks + kb) * (32 * G::kSfbAtoms));
+                            p.sf_b_row + (static_cast<int64_t>(tn) * p.k_blocks + kb) * (2 * G::kSfbAtoms));
                         if constexpr (kCG == 2) {
                             const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
                             tma_load_2d_pair(sf_dst, &tmap_b_half, 0, a_row_sf, leader_full);
                             for (int q = 0; q < G::kSfbAtoms; ++q)
-                                tma_load_2d_pair(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 32 * q, leader_full);
+                                tma_load_2d_pair(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 2 * q, leader_full);
                         } else {
                             tma_load_2d(sf_dst, &tmap_b_half, 0, a_row_sf, full_bar(stage));
                             for (int q = 0; q < G::kSfbAtoms; ++q)
-                                tma_load_2d(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 32 * q, full_bar(stage));
+                                tma_load_2d(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 2 * q, full_bar(stage));
                         }
                     }
                     if (++stage == G::kStages) {

@@ -475,8 +475,8 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
     if ((s = encode_2d(&tb, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, box_k, b_rows, CU_TENSOR_MAP_SWIZZLE_128B, "B", bytes)) != HK_OK) return s;
     CUtensorMap tbh;   // B in boxes of half the rows, for half-width units (MXFP8: the scale blocks)
     if (v->mx && mx_scales != nullptr) {
-        // prearranged scale blocks as rows of 16 bytes, one 512-byte block = 32 rows
-        if ((s = encode_2d(&tbh, mx_scales, static_cast<int64_t>(mx_scale_bytes / 16), 16, 16, 16, 32,
+        // prearranged scale blocks as rows of 256 bytes, one 512-byte block = 2 rows
+        if ((s = encode_2d(&tbh, mx_scales, static_cast<int64_t>(mx_scale_bytes / 256), 256, 256, 256, 2,
                            CU_TENSOR_MAP_SWIZZLE_NONE, "MXFP8 scales", true)) != HK_OK)
             return s;
     } else if ((s = encode_2d(&tbh, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, box_k, b_rows / 2, CU_TENSOR_MAP_SWIZZLE_128B, "B", bytes)) != HK_OK) {
@@ -898,7 +898,7 @@ hk_status hk_gemm_mxfp8(const void* A, const void* B, const void* SFA, const voi
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (K > 0) {
         uint8_t* ws = static_cast<uint8_t*>(workspace);
-        g.sf_b_row = static_cast<int64_t>(lay.b_offset / 16);
+        g.sf_b_row = static_cast<int64_t>(lay.b_offset / 256);
         const int64_t lines = static_cast<int64_t>(lay.total - lay.b_offset + lay.a_bytes) / 16;
         const int64_t blocks = std::min<int64_t>(ceil_div(lines, 256), int64_t(di->sm_count) * 16);
         hk::mx_scale_blocks_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
