@@ -541,7 +541,8 @@ def mx_config(w) -> dict:
                       f"seeds {3100 + w.wid}/{3200 + w.wid}",
             "l2": "no flush: inputs larger than L2 (A+B = %d MiB > 126 MiB)" % ((w.M + w.N) * w.K >> 20)
             if (w.M + w.N) * w.K > 126 << 20 else "inputs smaller than L2 (warm L2)",
-            "block": 32, "accumulate": "fp32", "output": "bf16", "tile": "128x192 per CTA"}
+            "block": 32, "accumulate": "fp32", "output": "bf16",
+            "tile": "256x256 per CTA pair (M > 128; 128x192 per CTA otherwise)"}
 
 
 def oracle_mx_rows_timed(A, B, SA, SB, rows) -> tuple[float, int]:
@@ -722,7 +723,7 @@ def run_mx(args, w):
                      "algorithmic_bytes_per_launch": float(w.M * w.K + w.N * w.K + (w.M + w.N) * kb + 2 * w.M * w.N),
                      "mean_launch_ms": mean_launch_ms, "p10_launch_ms": float(np.percentile(per_launch, 10)),
                      "p90_launch_ms": float(np.percentile(per_launch, 90)),
-                     "kernel": "mx_scale_blocks_kernel + gemm_bf16_kernel<1, 192, fp8, mx>", "source_digest": digest},
+                     "kernel": ("mx_scale_blocks_kernel + gemm_bf16_kernel<2, 256, fp8, mx>" if w.M > 128 else "mx_scale_blocks_kernel + gemm_bf16_kernel<1, 192, fp8, mx>"), "source_digest": digest},
         "e2e": {"value": replica_value(flops, e2e_steps, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(sum(h.numel() for h in hosts)), "d2h_bytes_per_step": int(C_h[0].numel() * 2),
                 "steps": e2e_steps, "pipelined": "H2D(i+1) | GEMM(i) | D2H(i-1) on three streams"},

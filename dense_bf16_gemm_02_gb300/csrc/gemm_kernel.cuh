@@ -92,8 +92,14 @@ struct Geometry {
     static constexpr int kSmemBytes = kOffTmemHolder + 16 + 1024;   // + slack for aligning the base
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
     static constexpr int kAccCols = kTileN;                 // TMEM columns per accumulator
-    static constexpr int kColSf = 2 * kAccCols;             // MXFP8: scale ring, kSfCols per stage
-    static constexpr int kTmemCols = pow2_at_least(2 * kAccCols + kStages * kSfCols);
+    // Two accumulators (the epilogue of one tile overlaps the MMAs of the
+    // next) unless they and the scale ring do not fit TMEM's 512 columns: the
+    // 256-wide block-scaled tile keeps one, which its epilogue reads whole
+    // into registers before it stores anything, so the MMAs wait only for
+    // the TMEM reads.
+    static constexpr int kAccBufs = 2 * kAccCols + kStages * kSfCols <= 512 ? 2 : 1;
+    static constexpr int kColSf = kAccBufs * kAccCols;      // MXFP8: scale ring, kSfCols per stage
+    static constexpr int kTmemCols = pow2_at_least(kAccBufs * kAccCols + kStages * kSfCols);
     static_assert(kTmemCols <= 512, "TMEM");
     static constexpr uint32_t kIdesc = kMx    ? idesc_mxf8_f32(kTileM, kTileN)
                                        : kFp8 ? idesc_e4m3_f32(kTileM, kTileN)
@@ -411,8 +417,8 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                 int kb_begin, kb_end;
                 split_range(p, split, kb_begin, kb_end);
                 const uint32_t idesc = half < 0 ? G::kIdesc : G::kIdescHalf;
-                const int buf = local & 1;
-                const uint32_t acc_phase = (local >> 1) & 1;
+                const int buf = G::kAccBufs == 2 ? (local & 1) : 0;
+                const uint32_t acc_phase = G::kAccBufs == 2 ? ((local >> 1) & 1) : (local & 1);
                 const bool acc_free = kCG == 2
                                           ? wait_bounded_cluster(p, acc_empty_bar(buf), acc_phase ^ 1u, kErrMmaAccEmpty)
                                           : wait_bounded(p, acc_empty_bar(buf), acc_phase ^ 1u, kErrMmaAccEmpty);
@@ -494,11 +500,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         // memory and written by a TMA store; when N is not a multiple of 8
         // the last (< 8) columns are written with plain stores, since a TMA
         // store bounds the innermost dimension only to 16-byte granules.
-        auto store_chunk = [&](uint32_t (&v)[32], int row0, int col0) {
-            if (p.bias != nullptr || p.act != 0 || p.alpha != 1.0f) apply_epilogue(p, v, col0);
-            uint32_t w[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2_rn(v[2 * i], v[2 * i + 1]);
+        auto store_packed = [&](const uint32_t (&w)[16], int row0, int col0) {
             const uint32_t sbuf = epi + (chunk_count & 1u) * kEpiBufBytes;
             if (lane == 0) bulk_wait_group_read<1>();   // the store that last used sbuf has read it
             __syncwarp();
@@ -525,6 +527,13 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             }
             ++chunk_count;
         };
+        auto store_chunk = [&](uint32_t (&v)[32], int row0, int col0) {
+            if (p.bias != nullptr || p.act != 0 || p.alpha != 1.0f) apply_epilogue(p, v, col0);
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2_rn(v[2 * i], v[2 * i + 1]);
+            store_packed(w, row0, col0);
+        };
 
         int local = 0;
         const int total = p.total_units;
@@ -535,8 +544,8 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             tile_coords(p, t, tm, tn);
             const int chunks = (half < 0 ? G::kTileN : G::kTileN / 2) / kEpiCols;
             const int col_base = tn * G::kTileN + (half < 0 ? 0 : half * (G::kTileN / 2));
-            const int buf = local & 1;
-            const uint32_t acc_phase = (local >> 1) & 1;
+            const int buf = G::kAccBufs == 2 ? (local & 1) : 0;
+            const uint32_t acc_phase = G::kAccBufs == 2 ? ((local >> 1) & 1) : (local & 1);
             if (!wait_bounded_warp(p, acc_full_bar(buf), acc_phase, kErrEpiAccFull)) {
                 abort_seen = true;
                 break;
@@ -549,6 +558,38 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             // split K: this lane's row of this split's fp32 partial matrix
             float* const part_row =
                 p.partials + (static_cast<int64_t>(split) * p.M + row) * p.n_pad + tn * G::kTileN;
+            if constexpr (G::kAccBufs == 1) {
+                // one accumulator: read all of it (as bf16 pairs), release it, then store.
+                // Such tiles never split K, never come in halves and have no fused epilogue.
+                constexpr int kChunks = G::kTileN / kEpiCols;
+                uint32_t w[kChunks][16];
+#pragma unroll
+                for (int c = 0; c < kChunks; c += 2) {
+                    uint32_t v0[32], v1[32];
+                    if (p.k_blocks > 0) {
+                        tmem_load_32cols(t_row + c * kEpiCols, v0);
+                        tmem_load_32cols(t_row + (c + 1) * kEpiCols, v1);
+                        tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v0[i] = v1[i] = 0u;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        w[c][i] = pack_bf16x2_rn(v0[2 * i], v0[2 * i + 1]);
+                        w[c + 1][i] = pack_bf16x2_rn(v1[2 * i], v1[2 * i + 1]);
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (kCG == 2) mbar_arrive_cluster(map_to_cta(acc_empty_bar(buf), 0));
+                    else mbar_arrive(acc_empty_bar(buf));
+                }
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) store_packed(w[c], row0, col_base + c * kEpiCols);
+                continue;
+            }
 #pragma unroll 1
             for (int c = 0; c < chunks; ++c) {
                 uint32_t v[32];
@@ -652,28 +693,31 @@ splitk_reduce_kernel(const float* __restrict__ partials, int32_t splits, int32_t
 // r·16 + q·4 + j holds the scale of row 32·q + r (of a 128-row group) and K
 // block 4·stage + j: one block per 128-row group of A and `b_groups` blocks
 // for the B rows of an N tile of `tile_n` rows. Rows or K blocks outside the
-// matrix get 0 (2^-127; the operands there are zero). One thread writes one
-// 16-byte line r of a block (4 rows × the 4 scales of the stage); the lines
-// of a block are consecutive, so a warp's stores are contiguous.
+// matrix get 0 (2^-127; the operands there are zero). A CTA of 32·b_groups
+// threads builds one (tile, stage) atom per step: A atoms first, then B
+// atoms; thread `line` writes the 16-byte line r = line % 32 of block
+// line / 32 (4 rows × the 4 scales of the stage), so a warp's stores are one
+// contiguous 512-byte block. `words`: every row's 4 scales of a stage are one
+// aligned 32-bit word (scale pointers and strides multiples of 4, kb_total a
+// multiple of 4), read with one load instead of four.
 __global__ void mx_scale_blocks_kernel(const uint8_t* __restrict__ sa, int64_t ldsa, const uint8_t* __restrict__ sb,
                                        int64_t ldsb, int M, int N, int kb_total, int tiles_m, int tiles_n,
-                                       int k_blocks, int tile_n, int b_groups, uint8_t* __restrict__ out_a,
+                                       int k_blocks, int tile_n, int b_groups, int words, uint8_t* __restrict__ out_a,
                                        uint8_t* __restrict__ out_b) {
-    const int64_t lines_a = static_cast<int64_t>(tiles_m) * k_blocks * 32;
-    const int64_t lines_b = static_cast<int64_t>(tiles_n) * k_blocks * 32 * b_groups;
-    for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < lines_a + lines_b;
-         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const bool is_a = idx < lines_a;
-        const int64_t i = is_a ? idx : idx - lines_a;            // line index within its region
-        const int lines_per_tile = 32 * (is_a ? 1 : b_groups);   // lines of one (tile, stage)
-        const int64_t atom = i / lines_per_tile;
-        const int line = static_cast<int>(i - atom * lines_per_tile);
-        const int tile = static_cast<int>(atom / k_blocks);
-        const int stage = static_cast<int>(atom - static_cast<int64_t>(tile) * k_blocks);
-        const int group = line >> 5, r = line & 31;
+    const int64_t atoms_a = static_cast<int64_t>(tiles_m) * k_blocks;
+    const int64_t atoms = atoms_a + static_cast<int64_t>(tiles_n) * k_blocks;
+    const int line = static_cast<int>(threadIdx.x);
+    const int group = line >> 5, r = line & 31;
+    for (int64_t atom = blockIdx.x; atom < atoms; atom += gridDim.x) {
+        const bool is_a = atom < atoms_a;
+        if (is_a && group > 0) continue;   // an A atom is one block (32 lines)
+        const int64_t a_local = is_a ? atom : atom - atoms_a;
+        const int tile = static_cast<int>(a_local / k_blocks);
+        const int stage = static_cast<int>(a_local - static_cast<int64_t>(tile) * k_blocks);
         const uint8_t* src = is_a ? sa : sb;
         const int64_t ld = is_a ? ldsa : ldsb;
         const int rows = is_a ? M : N;
+        const int blk0 = 4 * stage;
         uint32_t w[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -682,15 +726,18 @@ __global__ void mx_scale_blocks_kernel(const uint8_t* __restrict__ sa, int64_t l
             uint32_t v = 0;
             if ((is_a || local < tile_n) && row < rows) {
                 const uint8_t* p = src + static_cast<int64_t>(row) * ld;
+                if (words) {
+                    v = __ldg(reinterpret_cast<const uint32_t*>(p + blk0));
+                } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int blk = 4 * stage + j;
-                    if (blk < kb_total) v |= static_cast<uint32_t>(p[blk]) << (8 * j);
+                    for (int j = 0; j < 4; ++j)
+                        if (blk0 + j < kb_total) v |= static_cast<uint32_t>(__ldg(p + blk0 + j)) << (8 * j);
                 }
             }
             w[q] = v;
         }
-        uint8_t* dst = (is_a ? out_a : out_b) + i * 16;
+        const int64_t out_line = is_a ? atom * 32 + line : a_local * (32 * b_groups) + line;
+        uint8_t* dst = (is_a ? out_a : out_b) + out_line * 16;
         *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }

@@ -79,11 +79,17 @@ const Variant kVariants[] = {
     make_variant<1, 128, true>(HK_KERNEL_SINGLE_128x128, "fp8 single 128x128"),
     make_variant<1, 64, true>(HK_KERNEL_SINGLE_128x64, "fp8 single 128x64"),
     make_variant<1, 192, true, true>(HK_KERNEL_SINGLE_128x192, "mxfp8 single 128x192"),
-    make_variant<2, 192, true, true>(HK_KERNEL_PAIR_256x256, "mxfp8 pair 256x192"),
+    make_variant<2, 256, true, true>(HK_KERNEL_PAIR_256x256, "mxfp8 pair 256x256"),
 };
-constexpr int kMxTileN = 192;   // N of both MXFP8 tiles (one CTA: 128x192, a pair: 256x192)
-using GeomMx = hk::Geometry<1, kMxTileN, true, true>;
-static_assert(GeomMx::kSfbAtoms == hk::Geometry<2, kMxTileN, true, true>::kSfbAtoms, "one scale layout");
+// N of the MXFP8 tiles: one CTA 128x192 (two TMEM accumulators), a pair
+// 256x256 (one accumulator, see Geometry::kAccBufs)
+constexpr int kMxTileNSingle = 192;
+constexpr int kMxTileNPair = 256;
+using GeomMxSingle = hk::Geometry<1, kMxTileNSingle, true, true>;
+using GeomMxPair = hk::Geometry<2, kMxTileNPair, true, true>;
+static_assert(GeomMxSingle::kSfbAtoms == GeomMxPair::kSfbAtoms, "one scale layout");
+static_assert(GeomMxPair::kAccBufs == 1 && GeomMxSingle::kAccBufs == 2, "MXFP8 accumulator buffering");
+constexpr int kMxSfbAtoms = GeomMxPair::kSfbAtoms;
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
 const Variant* find_variant(int id, bool fp8, bool mx = false) {
@@ -804,6 +810,7 @@ namespace {
 
 struct MxLayout {
     int64_t tiles_m, tiles_n, k_blocks;
+    int tile_n;   // N of the tile the kernel for this M uses
     size_t a_bytes, b_offset, total;
 };
 
@@ -812,11 +819,12 @@ struct MxLayout {
 MxLayout mx_layout(int64_t M, int64_t N, int64_t K) {
     MxLayout l;
     l.tiles_m = M <= hk::kCtaM ? 1 : 2 * ceil_div(M, 2 * hk::kCtaM);
-    l.tiles_n = ceil_div(N, kMxTileN);
+    l.tile_n = M <= hk::kCtaM ? kMxTileNSingle : kMxTileNPair;
+    l.tiles_n = ceil_div(N, l.tile_n);
     l.k_blocks = ceil_div(K, 128);
     l.a_bytes = static_cast<size_t>(l.tiles_m * l.k_blocks * 512);
     l.b_offset = (l.a_bytes + 255) & ~size_t(255);
-    l.total = l.b_offset + static_cast<size_t>(l.tiles_n * l.k_blocks * 512 * GeomMx::kSfbAtoms);
+    l.total = l.b_offset + static_cast<size_t>(l.tiles_n * l.k_blocks * 512 * kMxSfbAtoms);
     return l;
 }
 
@@ -857,9 +865,11 @@ hk_status hk_gemm_mxfp8(const void* A, const void* B, const void* SFA, const voi
     uint32_t* status = nullptr;
     if ((s = hk_host::status_word(device, &status)) != HK_OK) return s;
     StatusWord sw{status};
-    // one CTA with 128x192 tiles for M <= 128, else CTA pairs with 256x192 tiles
+    // one CTA with 128x192 tiles for M <= 128, else CTA pairs with 256x256 tiles
     const bool pair = M > hk::kCtaM;
     const Variant* v = find_variant(pair ? HK_KERNEL_PAIR_256x256 : HK_KERNEL_SINGLE_128x192, true, true);
+    if (v == nullptr || v->tile_n != lay.tile_n)
+        return fail(HK_ERR_INVALID_ARG, "no MXFP8 kernel with the %d-column tiles of the scale layout", lay.tile_n);
     const int vi = static_cast<int>(v - kVariants);
     int units = di->max_units[vi];
     if (units <= 0) return fail(HK_ERR_UNSUPPORTED_DEVICE, "kernel %s does not fit on the device", v->name);
@@ -899,12 +909,14 @@ hk_status hk_gemm_mxfp8(const void* A, const void* B, const void* SFA, const voi
     if (K > 0) {
         uint8_t* ws = static_cast<uint8_t*>(workspace);
         g.sf_b_row = static_cast<int64_t>(lay.b_offset / 256);
-        const int64_t lines = static_cast<int64_t>(lay.total - lay.b_offset + lay.a_bytes) / 16;
-        const int64_t blocks = std::min<int64_t>(ceil_div(lines, 256), int64_t(di->sm_count) * 16);
-        hk::mx_scale_blocks_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        const int64_t atoms = (lay.tiles_m + lay.tiles_n) * lay.k_blocks;
+        const int64_t blocks = std::min<int64_t>(atoms, int64_t(di->sm_count) * 32);
+        const bool words = (K % 128) == 0 && (ldsfa % 4) == 0 && (ldsfb % 4) == 0 &&
+                           (reinterpret_cast<uintptr_t>(SFA) & 3u) == 0 && (reinterpret_cast<uintptr_t>(SFB) & 3u) == 0;
+        hk::mx_scale_blocks_kernel<<<static_cast<unsigned>(blocks), 32 * kMxSfbAtoms, 0, st>>>(
             static_cast<const uint8_t*>(SFA), ldsfa, static_cast<const uint8_t*>(SFB), ldsfb, static_cast<int>(M),
             static_cast<int>(N), static_cast<int>(K / 32), static_cast<int>(lay.tiles_m), static_cast<int>(lay.tiles_n),
-            static_cast<int>(lay.k_blocks), kMxTileN, GeomMx::kSfbAtoms, ws, ws + lay.b_offset);
+            static_cast<int>(lay.k_blocks), lay.tile_n, kMxSfbAtoms, words ? 1 : 0, ws, ws + lay.b_offset);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(HK_ERR_LAUNCH, "launching the MXFP8 scale arrangement", e);
     }

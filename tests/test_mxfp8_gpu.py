@@ -119,7 +119,7 @@ def test_mx_workload_sampled(hk, oracle):
     w = synth.MX_WORKLOADS["mxfp8_gemm_8192"]
     A, B, SA, SB = synth.operands_mx(w)
     got = run_mx(hk, A, B, SA, SB)
-    r, c = synth.sample_positions(w.M, w.N, 3000 + w.wid, count=2048, tile_m=128, tile_n=192)
+    r, c = synth.sample_positions(w.M, w.N, 3000 + w.wid, count=2048, tile_m=128, tile_n=256)
     want = oracle.gemm_mxfp8_entries(A, B, SA, SB, r, c)
     g = synth.bf16_bits_to_f32(got[r, c]).astype(np.float64)
     ref = synth.bf16_bits_to_f32(want).astype(np.float64)
@@ -127,6 +127,41 @@ def test_mx_workload_sampled(hk, oracle):
     tol = 2.0 ** -7 * np.abs(ref) + 2.0 ** -16 * 64 * w.K * 0.7
     bad = np.abs(g - ref) > tol
     assert not bad.any(), f"{int(bad.sum())} sampled entries outside tolerance"
+
+
+@pytest.mark.parametrize("lds,offset", [((12, 16), (0, 0)), ((13, 8), (0, 0)), ((8, 8), (1, 3))],
+                         ids=["padded_words", "odd_stride", "odd_offset"])
+def test_mx_strided_scales(hk, oracle, lds, offset):
+    """Scale arrays with row strides above K/32 and at odd byte offsets: the
+    arrangement reads them with 4-byte loads only when every row's scales of a
+    stage are an aligned word, else byte by byte; both must give the oracle's
+    result exactly (integer data)."""
+    import torch
+    M, N, K = 300, 260, 256
+    kb = K // 32
+    A, B = synth.int_e4m3(M, K, 2300), synth.int_e4m3(N, K, 2400)
+    SA, SB = synth.mx_scales(M, kb, 2500, 126, 128), synth.mx_scales(N, kb, 2600, 126, 128)
+
+    def placed(S, ld, off):
+        buf = torch.full((S.shape[0] * ld + off + 16,), 255, dtype=torch.uint8)   # 255 (NaN) in the padding
+        view = buf[off:off + S.shape[0] * ld].view(S.shape[0], ld)
+        view[:, :kb] = torch.from_numpy(S)
+        return buf.to("cuda"), off
+
+    (sa_buf, oa), (sb_buf, ob) = placed(SA, lds[0], offset[0]), placed(SB, lds[1], offset[1])
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to("cuda")
+    a, b = dev(A), dev(B)
+    ldc = N + (-N) % 8
+    c = torch.full((M, ldc), float("nan"), dtype=torch.bfloat16, device="cuda")
+    nbytes = hk.hk_gemm_mxfp8_workspace_size(M, N, K)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    st = hk.hk_gemm_mxfp8(a.data_ptr(), b.data_ptr(), sa_buf.data_ptr() + oa, sb_buf.data_ptr() + ob, c.data_ptr(),
+                          M, N, K, K, K, lds[0], lds[1], ldc, ws.data_ptr(), nbytes, 0)
+    assert st == hk.HK_OK, hk.hk_gemm_last_error_string()
+    torch.cuda.synchronize()
+    assert hk.hk_gemm_last_device_status(0) == hk.HK_OK
+    got = c.view(torch.int16).cpu().numpy().view(np.uint16)[:, :N]
+    assert_bitexact(got, oracle.gemm_mxfp8(A, B, SA, SB), f"mxfp8 strided scales {lds} {offset}")
 
 
 def test_mx_argument_errors(hk):
