@@ -320,6 +320,9 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         prefetch_tensor_map(&tmap_a);
         prefetch_tensor_map(&tmap_b);
         prefetch_tensor_map(&tmap_c);
+        // the split-K reduction, launched after this kernel as a programmatic
+        // dependent, may be scheduled now; it waits for this grid to complete
+        griddep_launch_dependents();
     }
     if (warp == 1) {
         if constexpr (kCG == 2) {
@@ -588,35 +591,35 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                 }
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c) store_packed(w[c], row0, col_base + c * kEpiCols);
-                continue;
-            }
+            } else {
 #pragma unroll 1
-            for (int c = 0; c < chunks; ++c) {
-                uint32_t v[32];
-                if (p.k_blocks > 0) {
-                    tmem_load_32cols(t_row + c * kEpiCols, v);
-                    tmem_wait_ld();
-                } else {
+                for (int c = 0; c < chunks; ++c) {
+                    uint32_t v[32];
+                    if (p.k_blocks > 0) {
+                        tmem_load_32cols(t_row + c * kEpiCols, v);
+                        tmem_wait_ld();
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0u;
-                }
-                if (c == chunks - 1) {
-                    // every TMEM read of this accumulator is done: release it to the MMA
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (kCG == 2) mbar_arrive_cluster(map_to_cta(acc_empty_bar(buf), 0));
-                        else mbar_arrive(acc_empty_bar(buf));
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;
                     }
-                }
-                if (p.splits == 1) {
-                    store_chunk(v, row0, col_base + c * kEpiCols);
-                } else if (row < p.M) {
-                    float4* dst = reinterpret_cast<float4*>(part_row + c * kEpiCols);
+                    if (c == chunks - 1) {
+                        // every TMEM read of this accumulator is done: release it to the MMA
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if constexpr (kCG == 2) mbar_arrive_cluster(map_to_cta(acc_empty_bar(buf), 0));
+                            else mbar_arrive(acc_empty_bar(buf));
+                        }
+                    }
+                    if (p.splits == 1) {
+                        store_chunk(v, row0, col_base + c * kEpiCols);
+                    } else if (row < p.M) {
+                        float4* dst = reinterpret_cast<float4*>(part_row + c * kEpiCols);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                             __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                    }
                 }
             }
         }
@@ -638,11 +641,13 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
 // Split K, second pass: C = bf16_rne(act(P[0] + P[1] + ... + P[splits-1] +
 // bias)), summed in this fixed order (so the result does not depend on
 // which split finished first). Each thread handles 8 consecutive columns of
-// one row.
+// one row. Launched as a programmatic dependent of the GEMM, so that its launch
+// overlaps the GEMM; it waits for the GEMM grid to complete before reading.
 __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float* __restrict__ partials, int32_t splits, int32_t M, int32_t N, int64_t n_pad,
                      uint16_t* __restrict__ C, int64_t ldc, const uint16_t* __restrict__ bias, int32_t act,
                      float alpha) {
+    griddep_wait();
     const int64_t groups_per_row = (N + 7) / 8;
     const int64_t total = static_cast<int64_t>(M) * groups_per_row;
     const int64_t split_stride = static_cast<int64_t>(M) * n_pad;

@@ -267,6 +267,13 @@ __device__ __forceinline__ void mma_bf16_one(uint32_t d_tmem, uint64_t a_desc, u
         : "memory");
 }
 
+// Programmatic dependent launch: allow the grid launched after this one (with
+// the programmatic-serialization attribute) to be scheduled before this grid
+// ends; and, in that dependent grid, wait until every grid it depends on has
+// completed and its memory operations are visible.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void mma_commit_one(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
