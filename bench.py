@@ -41,16 +41,19 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources whose digest is given; see profiles/.
 MEASURED_TRAFFIC = {
-    "fp8_gemm_8192": {"source_digest": "65485f133f7bc8ea", "bytes_per_launch": 341788416 + 116316928,
-                      "profile": "profiles/gemm_fp8_kernel_pair256_fp8_gemm_8192.md"},
-    "gemm_8192": {"source_digest": "ec8f7a99b9ec3031", "bytes_per_launch": 1082111000 + 127698432,
+    "gemm_8192": {"source_digest": "18ef9a610517fc10", "bytes_per_launch": 1108934912 + 128995072,
                   "profile": "profiles/gemm_bf16_kernel_pair256_gemm_8192.md"},
-    "skinny_128x28672x8192": {"source_digest": "ec8f7a99b9ec3031", "bytes_per_launch": 471968000 + 3932160,
+    "skinny_128x28672x8192": {"source_digest": "18ef9a610517fc10", "bytes_per_launch": 471969024 + 3466752,
                               "profile": "profiles/gemm_bf16_kernel_single128x192_skinny_128x28672x8192.md"},
+    "fp8_gemm_8192": {"source_digest": "18ef9a610517fc10", "bytes_per_launch": 343133184 + 117728768,
+                      "profile": "profiles/gemm_fp8_kernel_pair256_fp8_gemm_8192.md"},
+    # the block-scaled GEMM kernel alone (the scale arrangement kernel moves ~8 MB more)
+    "mxfp8_gemm_8192": {"source_digest": "18ef9a610517fc10", "bytes_per_launch": 354504960 + 116727552,
+                        "profile": "profiles/gemm_mxfp8_kernel_pair256_mxfp8_gemm_8192.md"},
     # attention: captured at B2 (one launch); the B16 figure scales it by 8 (traffic grows with B)
-    "attn_gqa_b2_s4096_d128": {"source_digest": "d7a38284885b41be", "bytes_per_launch": 185660416 + 124675328,
+    "attn_gqa_b2_s4096_d128": {"source_digest": "1257e6d8823e4d83", "bytes_per_launch": 187219968 + 123094784,
                                "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
-    "attn_gqa_b16_s4096_d128": {"source_digest": "d7a38284885b41be", "bytes_per_launch": 8 * (185660416 + 124675328),
+    "attn_gqa_b16_s4096_d128": {"source_digest": "1257e6d8823e4d83", "bytes_per_launch": 8 * (187219968 + 123094784),
                                 "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
 }
 
