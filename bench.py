@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -41,19 +42,19 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources whose digest is given; see profiles/.
 MEASURED_TRAFFIC = {
-    "gemm_8192": {"source_digest": "18ef9a610517fc10", "bytes_per_launch": 1108934912 + 128995072,
+    "gemm_8192": {"source_digest": "f11918802710d8df", "bytes_per_launch": 1108934912 + 128995072,
                   "profile": "profiles/gemm_bf16_kernel_pair256_gemm_8192.md"},
-    "skinny_128x28672x8192": {"source_digest": "18ef9a610517fc10", "bytes_per_launch": 471969024 + 3466752,
+    "skinny_128x28672x8192": {"source_digest": "f11918802710d8df", "bytes_per_launch": 471969024 + 3466752,
                               "profile": "profiles/gemm_bf16_kernel_single128x192_skinny_128x28672x8192.md"},
-    "fp8_gemm_8192": {"source_digest": "18ef9a610517fc10", "bytes_per_launch": 343133184 + 117728768,
+    "fp8_gemm_8192": {"source_digest": "f11918802710d8df", "bytes_per_launch": 343133184 + 117728768,
                       "profile": "profiles/gemm_fp8_kernel_pair256_fp8_gemm_8192.md"},
     # the block-scaled GEMM kernel alone (the scale arrangement kernel moves ~8 MB more)
-    "mxfp8_gemm_8192": {"source_digest": "18ef9a610517fc10", "bytes_per_launch": 354504960 + 116727552,
+    "mxfp8_gemm_8192": {"source_digest": "f11918802710d8df", "bytes_per_launch": 354504960 + 116727552,
                         "profile": "profiles/gemm_mxfp8_kernel_pair256_mxfp8_gemm_8192.md"},
     # attention: captured at B2 (one launch); the B16 figure scales it by 8 (traffic grows with B)
-    "attn_gqa_b2_s4096_d128": {"source_digest": "1257e6d8823e4d83", "bytes_per_launch": 187219968 + 123094784,
+    "attn_gqa_b2_s4096_d128": {"source_digest": "78bf4b24f62b6284", "bytes_per_launch": 187219968 + 123094784,
                                "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
-    "attn_gqa_b16_s4096_d128": {"source_digest": "1257e6d8823e4d83", "bytes_per_launch": 8 * (187219968 + 123094784),
+    "attn_gqa_b16_s4096_d128": {"source_digest": "78bf4b24f62b6284", "bytes_per_launch": 8 * (187219968 + 123094784),
                                 "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
 }
 
@@ -64,14 +65,23 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and with whitespace runs collapsed: two
+    sources that differ only in comments or layout compile to the same code."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_digest(kind: str = "gemm") -> str:
-    """Digest of the sources one kernel is built from (a stored ncu traffic
-    figure is valid only while they are unchanged)."""
+    """Digest of the code of the sources one kernel is built from, comments
+    and layout excluded (a stored ncu traffic figure is valid only while that
+    code is unchanged)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_bf16_gemm_02_gb300", "csrc")
     for f in KERNEL_SOURCES[kind]:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

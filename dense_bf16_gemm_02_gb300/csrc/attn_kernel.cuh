@@ -159,7 +159,7 @@ __device__ __forceinline__ bool attn_wait(const AttnParams& p, uint32_t bar, uin
     }
 }
 
-// Lane 0 waits; the verdict is broadcast and every lane then observes the
+// Lane 0 waits; the result is broadcast and every lane then observes the
 // completed phase itself.
 __device__ __forceinline__ bool attn_wait_warp(const AttnParams& p, uint32_t bar, uint32_t parity, uint32_t code) {
     uint32_t ok = 0;

@@ -199,7 +199,7 @@ __device__ __forceinline__ bool wait_bounded_cluster(const GemmParams& p, uint32
     return wait_bounded_slow(p, bar, parity, code, true);
 }
 
-// Warp-uniform variant: lane 0 waits, the verdict is broadcast, and every
+// Warp-uniform variant: lane 0 waits, the result is broadcast, and every
 // lane then observes the completed phase itself (acquire per thread).
 __device__ __forceinline__ bool wait_bounded_warp(const GemmParams& p, uint32_t bar, uint32_t parity,
                                                   uint32_t code) {

@@ -163,8 +163,8 @@ hk_status hk_gemm_plan_get_info(const hk_gemm_plan* plan, hk_gemm_plan_info* inf
 hk_status hk_gemm_plan_run(const hk_gemm_plan* plan, const void* A, const void* B, void* C,
                            void* workspace, size_t workspace_bytes, void* stream);
 
-/* GEMM with a fused epilogue (a "next" step the survey lists after the plain
- * GEMM; the HipKittens pages fuse nothing into their GEMM):
+/* GEMM with a fused epilogue (the HipKittens pages fuse nothing into their
+ * GEMM; this is the cheapest extension once the epilogue stage exists):
  *     C[i,j] = bf16_rne( act( Σ_k A[i,k]·B[j,k] + bias[j] ) )
  * computed in fp32 (accumulator + bias, then the activation) before the one
  * rounding. `bias` is a device vector of N bf16 values, 16-byte aligned, or
