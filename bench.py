@@ -42,15 +42,18 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources whose digest is given; see profiles/.
 MEASURED_TRAFFIC = {
-    "gemm_8192": {"source_digest": "f11918802710d8df", "bytes_per_launch": 1108934912 + 128995072,
+    "gemm_8192": {"source_digest": "abb2922440ef9855", "bytes_per_launch": 1086247680 + 128632576,
                   "profile": "profiles/gemm_bf16_kernel_pair256_gemm_8192.md"},
-    "skinny_128x28672x8192": {"source_digest": "f11918802710d8df", "bytes_per_launch": 471969024 + 3466752,
+    "skinny_128x28672x8192": {"source_digest": "abb2922440ef9855", "bytes_per_launch": 471981568 + 4365824,
                               "profile": "profiles/gemm_bf16_kernel_single128x192_skinny_128x28672x8192.md"},
-    "fp8_gemm_8192": {"source_digest": "f11918802710d8df", "bytes_per_launch": 343133184 + 117728768,
+    "fp8_gemm_8192": {"source_digest": "abb2922440ef9855", "bytes_per_launch": 349363200 + 117921792,
                       "profile": "profiles/gemm_fp8_kernel_pair256_fp8_gemm_8192.md"},
     # the block-scaled GEMM kernel alone (the scale arrangement kernel moves ~8 MB more)
-    "mxfp8_gemm_8192": {"source_digest": "f11918802710d8df", "bytes_per_launch": 354504960 + 116727552,
+    "mxfp8_gemm_8192": {"source_digest": "abb2922440ef9855", "bytes_per_launch": 360049408 + 116597504,
                         "profile": "profiles/gemm_mxfp8_kernel_pair256_mxfp8_gemm_8192.md"},
+    # the GEMM kernel alone (the split-K reduction reads the fp32 partials and writes C)
+    "decode_64x8192x28672": {"source_digest": "abb2922440ef9855", "bytes_per_launch": 473516800 + 3975424,
+                             "profile": "profiles/gemm_bf16_kernel_single_decode_shapes.md"},
     # attention: captured at B2 (one launch); the B16 figure scales it by 8 (traffic grows with B)
     "attn_gqa_b2_s4096_d128": {"source_digest": "78bf4b24f62b6284", "bytes_per_launch": 187219968 + 123094784,
                                "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
@@ -332,9 +335,14 @@ def run_hk(args, w):
     stream = torch.cuda.Stream(device=dev)
     sh = int(stream.cuda_stream)
     sa, sb = synth.FP8_SCALES
-    plan = hk.Plan(w.M, w.N, w.K, device=local, group_m=args.group_m, split_k=1,
+    # decode-regime workloads run through a plan that may split K (with a workspace);
+    # the others through the one-shot call, which never splits
+    decode = w.name.startswith("decode_")
+    plan = hk.Plan(w.M, w.N, w.K, device=local, group_m=args.group_m, split_k=0 if decode else 1,
                    input_type=hk.HK_INPUT_E4M3 if fp8 else hk.HK_INPUT_BF16, alpha=sa * sb if fp8 else 0.0)
     info = plan.info()
+    ws_bytes = plan.workspace_size
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev) if decode else None
     flops = gemm_flops(w.M, w.N, w.K)
 
     act = {"none": 0, "bias": 0, "bias_relu": 1, "bias_gelu": 2, "bias_silu": 3}[args.epilogue]
@@ -356,7 +364,10 @@ def run_hk(args, w):
             if st != hk.HK_OK:
                 raise hk.HKError(st, "hk_gemm_bf16_epilogue")
             return
-        if args.group_m:
+        if decode:
+            st = plan.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), ws.data_ptr(), ws_bytes, sh)
+            where = "hk_gemm_plan_run"
+        elif args.group_m:
             # an explicit schedule goes through a plan (hk_gemm_plan_run)
             st = plan.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), 0, 0, sh)
             where = "hk_gemm_plan_run"
@@ -435,6 +446,8 @@ def run_hk(args, w):
             if fp8:
                 st = hk.hk_gemm_fp8_e4m3(A_d[k].data_ptr(), B_d[k].data_ptr(), C_d[k].data_ptr(), w.M, w.N, w.K,
                                          w.K, w.K, w.N, sa, sb, sh)
+            elif decode:
+                st = plan.run_raw(A_d[k].data_ptr(), B_d[k].data_ptr(), C_d[k].data_ptr(), ws.data_ptr(), ws_bytes, sh)
             else:
                 st = hk.hk_gemm_bf16(A_d[k].data_ptr(), B_d[k].data_ptr(), C_d[k].data_ptr(), w.M, w.N, w.K, w.K,
                                      w.K, w.N, sh)

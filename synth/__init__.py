@@ -49,6 +49,9 @@ WORKLOADS = {
     "gemm_16384": Workload("gemm_16384", 4, 16384, 16384, 16384, 1.0, True),
     "proj_16384x28672x8192": Workload("proj_16384x28672x8192", 5, 16384, 28672, 8192, 0.02, True),
     "skinny_128x28672x8192": Workload("skinny_128x28672x8192", 6, 128, 28672, 8192, 0.02, False),
+    # decode-regime projections (one token; a batch of 64) over a 448 MiB weight matrix, 3.5x the L2
+    "decode_1x28672x8192": Workload("decode_1x28672x8192", 11, 1, 28672, 8192, 0.02, False),
+    "decode_64x8192x28672": Workload("decode_64x8192x28672", 12, 64, 8192, 28672, 0.02, True),
 }
 
 # FP8 (E4M3) workloads: operands N(0,1) rounded to E4M3, per-tensor scales

@@ -187,13 +187,17 @@ def _operands(name, integer=False):
     return synth.operands(synth.WORKLOADS[name], integer=integer)
 
 
-def _check_workload(hk, name, integer=False):
+def _check_workload(hk, name, integer=False, via_plan=False):
     import torch
     w = synth.WORKLOADS[name]
     A, B = _operands(name, integer)
     At, _ = to_device(A)
     Bt, _ = to_device(B)
-    C = hk.gemm(At, Bt)
+    if via_plan:   # a plan may split K (workspace allocated by Plan.run), as bench.py runs decode shapes
+        plan = hk.Plan(w.M, w.N, w.K)
+        C = plan.run(At, Bt, torch.empty((w.M, w.N), dtype=torch.bfloat16, device=At.device))
+    else:
+        C = hk.gemm(At, Bt)
     torch.cuda.synchronize()
     assert hk.hk_gemm_last_device_status(torch.cuda.current_device()) == hk.HK_OK
     got = to_host(C)
@@ -233,6 +237,14 @@ def test_workload_projection(hk):
 
 def test_workload_skinny(hk):
     _check_workload(hk, "skinny_128x28672x8192")
+
+
+def test_workload_decode_one_token(hk):
+    _check_workload(hk, "decode_1x28672x8192", via_plan=True)
+
+
+def test_workload_decode_batch_64(hk):
+    _check_workload(hk, "decode_64x8192x28672", via_plan=True)
 
 
 # ------------------------------------------------------ kernel variants --
