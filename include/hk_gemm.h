@@ -206,7 +206,8 @@ hk_status hk_gemm_fp8_e4m3(const void* A, const void* B, void* C,
  * row-major with row strides ldsfa, ldsfb ≥ K/32 (bytes, any alignment); C is
  * bf16 as in hk_gemm_bf16. K must be a multiple of 32 (else
  * HK_ERR_INVALID_ARG). The products accumulate in fp32 on the tensor cores
- * (tcgen05.mma kind::mxf8f6f4 with block scales, 128×192 tiles on one CTA).
+ * (tcgen05.mma kind::mxf8f6f4 with block scales: 256×256 tiles on CTA pairs
+ * when M > 128, else 128×192 tiles on one CTA).
  * `workspace` (device memory, 256-byte aligned, caller-owned, at least
  * hk_gemm_mxfp8_workspace_size(M, N, K) bytes, else HK_ERR_WORKSPACE)
  * receives the scales rearranged per tile and K stage by a small kernel
