@@ -347,6 +347,9 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
+            // launched as a programmatic dependent (block-scaled GEMM after the scale
+            // arrangement): nothing the earlier grid writes is read before this
+            if constexpr (kMx) griddep_wait();
             int stage = 0;
             uint32_t phase = 0;
             bool dropped = false;
@@ -747,6 +750,7 @@ __global__ void mx_scale_blocks_kernel(const uint8_t* __restrict__ sa, int64_t l
                                        int64_t ldsb, int M, int N, int kb_total, int tiles_m, int tiles_n,
                                        int k_blocks, int tile_n, int b_groups, int words, uint8_t* __restrict__ out_a,
                                        uint8_t* __restrict__ out_b) {
+    griddep_launch_dependents();   // the GEMM (a programmatic dependent) may be scheduled now
     const int64_t atoms_a = static_cast<int64_t>(tiles_m) * k_blocks;
     const int64_t atoms = atoms_a + static_cast<int64_t>(tiles_n) * k_blocks;
     const int line = static_cast<int>(threadIdx.x);

@@ -501,17 +501,28 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
     if (g.splits > 1) g.partials = static_cast<float*>(workspace);
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(v->cg);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2];
+    int nattr = 0;
+    if (v->cg > 1) {
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = static_cast<unsigned>(v->cg);
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
+    }
+    if (mx_scales != nullptr) {
+        // a programmatic dependent of the scale arrangement: the prologue overlaps
+        // it, the producer waits (griddepcontrol.wait) before its first load
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
+    }
     cfg.gridDim = dim3(p->grid_ctas, 1, 1);
     cfg.blockDim = dim3(hk::kThreads, 1, 1);
     cfg.dynamicSmemBytes = v->smem_bytes;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = v->cg > 1 ? 1 : 0;
+    cfg.numAttrs = nattr;
     cudaError_t e = cudaLaunchKernelEx(&cfg, v->fn, ta, tb, tc, tbh, g);
     if (e != cudaSuccess) return cuda_fail(HK_ERR_LAUNCH, "launching the GEMM kernel", e);
     if (g.splits > 1) {
