@@ -81,8 +81,8 @@ struct AttnGeometry {
     static constexpr int kOffP = kQBytes;
     static constexpr int kOffKV = kOffP + kTiles * kPBytes;
     static constexpr int kOffBars = kOffKV + kSlots * kTileBytes;
-    // q_full, kv_full[kSlots], kv_empty[kSlots], s_full[2], s_free[2], p_full[2], o_done[2]
-    static constexpr int kNumBars = 1 + 2 * kSlots + 8;
+    // q_full, kv_full[kSlots], kv_empty[kSlots], s_full[2], s_free[2], p_full[2], o_done[2], q_empty
+    static constexpr int kNumBars = 1 + 2 * kSlots + 9;
     static constexpr int kOffTmemHolder = kOffBars + kNumBars * 8;
     static constexpr int kSmemBytes = kOffTmemHolder + 16 + 1024;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
@@ -105,7 +105,8 @@ __device__ __forceinline__ int pos_v(int j, int n) { return j + 1 < n ? 2 * j + 
 struct AttnParams {
     int32_t B, Hq, Hkv, S;
     int32_t causal;
-    int32_t q_pairs;          // ceil(S / 256): CTAs per (batch, query head)
+    int32_t q_pairs;          // ceil(S / 256): work items per (batch, query head)
+    int32_t n_items;          // B * Hq * q_pairs
     int32_t kv_blocks;        // ceil(S / 128)
     float scale_log2;         // log2(e) / sqrt(D)
     uint16_t* O;              // [B, Hq, S, D] bf16
@@ -179,6 +180,29 @@ __device__ __forceinline__ int tile_blocks(const AttnParams& p, int row0) {
     return last < p.kv_blocks ? last : p.kv_blocks;
 }
 
+// One work item: two query tiles (256 rows) of one (batch, query head).
+// Items are numbered head-fastest, so the query heads of one KV group run
+// side by side; causal: the longest rows first.
+struct AttnItem {
+    int bh, kvh, q0, n_t0, n_t1, n_all;
+};
+
+__device__ __forceinline__ AttnItem attn_item(const AttnParams& p, int w) {
+    AttnItem it;
+    const int bh_count = p.B * p.Hq;
+    const int slot_q = w / bh_count;
+    it.bh = w - slot_q * bh_count;
+    const int qp = p.causal ? p.q_pairs - 1 - slot_q : slot_q;
+    const int b = it.bh / p.Hq;
+    const int h = it.bh - b * p.Hq;
+    it.kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
+    it.q0 = qp * (kTiles * kTileQ);
+    it.n_t0 = tile_blocks(p, it.q0);
+    it.n_t1 = tile_blocks(p, it.q0 + kTileQ);
+    it.n_all = it.n_t0 > it.n_t1 ? it.n_t0 : it.n_t1;
+    return it;
+}
+
 template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -192,20 +216,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = lane_id();
 
-    // CTA -> (query-row pair, batch·head); heads fastest, so the query heads
-    // of one KV group run side by side. Causal: the longest rows first.
-    const int bh_count = p.B * p.Hq;
-    const int slot_q = static_cast<int>(blockIdx.x) / bh_count;
-    const int bh = static_cast<int>(blockIdx.x) - slot_q * bh_count;
-    const int qp = p.causal ? p.q_pairs - 1 - slot_q : slot_q;
-    const int b = bh / p.Hq;
-    const int h = bh - b * p.Hq;
-    const int kvh = b * p.Hkv + h / (p.Hq / p.Hkv);
-    const int q0 = qp * (kTiles * kTileQ);
-    const int n_t0 = tile_blocks(p, q0), n_t1 = tile_blocks(p, q0 + kTileQ);
-    auto n_t = [&](int t) { return t ? n_t1 : n_t0; };
-    const int n_all = n_t0 > n_t1 ? n_t0 : n_t1;
-
+    // Persistent: CTA c takes work items c, c + G, c + 2G, ... (G = gridDim.x).
+    // Barrier phases run on across items: the K/V ring by a running position,
+    // S/P/O of each tile by a running block count.
     const uint32_t q_full = base + G::kOffBars;
     auto kv_full = [&](int s) { return base + G::kOffBars + 8u * (1 + s); };
     auto kv_empty = [&](int s) { return base + G::kOffBars + 8u * (1 + G::kSlots + s); };
@@ -213,15 +226,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     auto s_free = [&](int t) { return base + G::kOffBars + 8u * (3 + 2 * G::kSlots + t); };
     auto p_full = [&](int t) { return base + G::kOffBars + 8u * (5 + 2 * G::kSlots + t); };
     auto o_done = [&](int t) { return base + G::kOffBars + 8u * (7 + 2 * G::kSlots + t); };
+    const uint32_t q_empty = base + G::kOffBars + 8u * (9 + 2 * G::kSlots);
     auto p_smem = [&](int t) { return base + G::kOffP + static_cast<uint32_t>(t) * G::kPBytes; };
     auto slot_addr = [&](int s) { return base + G::kOffKV + static_cast<uint32_t>(s) * G::kTileBytes; };
     const uint32_t tmem_holder = base + G::kOffTmemHolder;
+    const int first_item = static_cast<int>(blockIdx.x);
+    const int item_step = static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, kTiles);   // each tile's MMA issuer, once its last S of the item is done
         for (int s = 0; s < G::kSlots; ++s) {
             mbar_init(kv_full(s), 1);
-            mbar_init(kv_empty(s), n_t1 > 0 ? 2 : 1);   // one commit per active tile
+            mbar_init(kv_empty(s), kTiles);   // each tile's issuer arrives once per K/V position
         }
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(s_full(t), 1);
@@ -248,103 +265,134 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 
     if (warp == kWarpTma) {
         // ------------------------------------------------ TMA producer --
-        if (lane == 0 && n_all > 0) {
-            const int tiles = n_t1 > 0 ? 2 : 1;
-            mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(tiles * G::kTileBytes));
-            for (int t = 0; t < tiles; ++t)
-                for (int c = 0; c < G::kChunks; ++c)
-                    tma_load_3d(base + G::kOffQ + t * G::kTileBytes + c * G::kChunkBytes, &tmap_q, c * 64,
-                                q0 + t * kTileQ, bh, q_full);
-            for (int u = 0; u < 2 * n_all && !abort_seen; ++u) {
-                const int s = u % G::kSlots;
-                const uint32_t parity = ((u / G::kSlots) & 1) ^ 1;
-                if (!attn_wait(p, kv_empty(s), parity, kErrTmaEmpty, Wait::kSuspend)) {
+        if (lane == 0) {
+            int g = 0;   // running K/V ring position
+            int li = 0;      // items done by this CTA
+            for (int w = first_item; w < p.n_items && !abort_seen; w += item_step, ++li) {
+                const AttnItem it = attn_item(p, w);
+                // Q of this item once both issuers have finished the previous item's S
+                if (li > 0 && !attn_wait(p, q_empty, (li - 1) & 1, kErrTmaEmpty, Wait::kSuspend)) {
                     abort_seen = true;
                     break;
                 }
-                if ((p.flags & kFlagDropArrive) && u == 0) continue;   // test hook: never fill slot 0
-                // position u of the consumption order: K_0, (K_{j+1}, V_j)..., V_{n-1}
-                bool is_k;
-                int blk;
-                if (u == 0) {
-                    is_k = true;
-                    blk = 0;
-                } else if (u - 1 < 2 * (n_all - 1)) {
-                    is_k = ((u - 1) & 1) == 0;
-                    blk = is_k ? (u - 1) / 2 + 1 : (u - 1) / 2;
-                } else {
-                    is_k = false;
-                    blk = n_all - 1;
+                const int tiles = it.n_t1 > 0 ? 2 : 1;
+                mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(tiles * G::kTileBytes));
+                for (int t = 0; t < tiles; ++t)
+                    for (int c = 0; c < G::kChunks; ++c)
+                        tma_load_3d(base + G::kOffQ + t * G::kTileBytes + c * G::kChunkBytes, &tmap_q, c * 64,
+                                    it.q0 + t * kTileQ, it.bh, q_full);
+                for (int u = 0; u < 2 * it.n_all && !abort_seen; ++u, ++g) {
+                    const int s = g % G::kSlots;
+                    const uint32_t parity = static_cast<uint32_t>((g / G::kSlots) & 1) ^ 1u;
+                    if (!attn_wait(p, kv_empty(s), parity, kErrTmaEmpty, Wait::kSuspend)) {
+                        abort_seen = true;
+                        break;
+                    }
+                    if ((p.flags & kFlagDropArrive) && g == 0) continue;   // test hook: never fill the first slot
+                    // position u of the item's consumption order: K_0, (K_{j+1}, V_j)..., V_{n-1}
+                    bool is_k;
+                    int blk;
+                    if (u == 0) {
+                        is_k = true;
+                        blk = 0;
+                    } else if (u - 1 < 2 * (it.n_all - 1)) {
+                        is_k = ((u - 1) & 1) == 0;
+                        blk = is_k ? (u - 1) / 2 + 1 : (u - 1) / 2;
+                    } else {
+                        is_k = false;
+                        blk = it.n_all - 1;
+                    }
+                    mbar_arrive_expect_tx(kv_full(s), G::kTileBytes);
+                    for (int c = 0; c < G::kChunks; ++c)
+                        tma_load_3d(slot_addr(s) + c * G::kChunkBytes, is_k ? &tmap_k : &tmap_v, c * 64,
+                                    blk * kBlockKV, it.kvh, kv_full(s));
                 }
-                mbar_arrive_expect_tx(kv_full(s), G::kTileBytes);
-                for (int c = 0; c < G::kChunks; ++c)
-                    tma_load_3d(slot_addr(s) + c * G::kChunkBytes, is_k ? &tmap_k : &tmap_v, c * 64, blk * kBlockKV,
-                                kvh, kv_full(s));
             }
         }
     } else if (warp == kWarpMma || warp == kWarpMma + 1) {
         // ------------------------------------------- MMA issue, one warp per tile --
         // A tcgen05.mma holds its issuing thread for about the time it
         // computes; with one issuer per tile, each issuer's barrier waits and
-        // commits overlap the other tile's MMAs. A K/V slot is released when
-        // the issuers of every active tile have committed on it.
+        // commits overlap the other tile's MMAs. Both issuers arrive once on
+        // every K/V position and on q_empty for every item (a plain arrive,
+        // after the data landed, for what their tile does not use), so the
+        // barrier counts stay fixed across items.
         const int t = static_cast<int>(warp) - kWarpMma;
-        const int n = n_t(t);
-        if (lane == 0 && n > 0) {
+        if (lane == 0) {
             auto wait = [&](uint32_t bar, uint32_t parity, uint32_t code) {
                 if (abort_seen) return false;
                 if (!attn_wait(p, bar, parity, code)) abort_seen = true;
                 return !abort_seen;
             };
-            auto kv_slot = [&](int u) { return u % G::kSlots; };
-            auto kv_parity = [&](int u) { return static_cast<uint32_t>((u / G::kSlots) & 1); };
+            auto kv_slot = [&](int g) { return g % G::kSlots; };
+            auto kv_parity = [&](int g) { return static_cast<uint32_t>((g / G::kSlots) & 1); };
             const uint32_t qa = base + G::kOffQ + t * G::kTileBytes;
             const uint32_t s_tmem = tmem_base + G::kColS + t * kBlockKV;
             const uint32_t o_tmem = tmem_base + G::kColO + t * kD;
             const uint32_t pa = p_smem(t);
             const uint32_t p_tmem = tmem_base + G::kColP + t * (kBlockKV / 2);
-            auto issue_s = [&](int u) {   // S_t = Q_t · K_uᵀ
-                const uint32_t ka = slot_addr(kv_slot(u));
-#pragma unroll
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-                    mma_bf16_one(s_tmem, smem_desc_kmajor_sw128(qa + off), smem_desc_kmajor_sw128(ka + off),
-                                 G::kIdescS, kk > 0 ? 1u : 0u);
-                }
-                mma_commit_one(s_full(t));
-                mma_commit_one(kv_empty(kv_slot(u)));
-            };
-            if (wait(q_full, 0, kErrMmaKv) && wait(kv_full(kv_slot(0)), kv_parity(0), kErrMmaKv)) {
-                tc_fence_after_sync();
-                issue_s(0);
-            }
-            for (int j = 0; j < n && !abort_seen; ++j) {
-                // S for block j+1, once this tile's softmax has read its S of block j
-                if (j + 1 < n) {
-                    const int uk = pos_k(j + 1);
-                    if (!wait(kv_full(kv_slot(uk)), kv_parity(uk), kErrMmaKv)) break;
-                    if (!wait(s_free(t), j & 1, kErrMmaP)) break;
+            int g0 = 0;   // ring position of the item's first K/V block
+            int J = 0;    // this tile's blocks in earlier items
+            int li = 0;
+            for (int w = first_item; w < p.n_items && !abort_seen; w += item_step, ++li) {
+                const AttnItem it = attn_item(p, w);
+                const int n = t ? it.n_t1 : it.n_t0;
+                const int n_all = it.n_all;
+                if (!wait(q_full, li & 1, kErrMmaKv)) break;
+                // S_t = Q_t · K_jᵀ of block j (ring position g0 + u), once the softmax has
+                // read this tile's previous S; the last S of the item releases Q
+                auto issue_s = [&](int j, int u) {
+                    if (J + j > 0 && !wait(s_free(t), static_cast<uint32_t>((J + j - 1) & 1), kErrMmaP)) return false;
+                    if (!wait(kv_full(kv_slot(g0 + u)), kv_parity(g0 + u), kErrMmaKv)) return false;
                     tc_fence_after_sync();
-                    issue_s(uk);
-                }
-                // O_t += P_t · V_j once P_t is in shared memory
-                const int uv = pos_v(j, n_all);
-                if (!wait(kv_full(kv_slot(uv)), kv_parity(uv), kErrMmaKv)) break;
-                if (!wait(p_full(t), j & 1, kErrMmaP)) break;
-                tc_fence_after_sync();
-                const uint32_t va = slot_addr(kv_slot(uv));
+                    const uint32_t ka = slot_addr(kv_slot(g0 + u));
 #pragma unroll
-                for (int kk = 0; kk < kBlockKV / 16; ++kk) {
-                    const uint64_t vdesc = smem_desc_mnmajor(va + kk * 2048, 128, G::kChunkBytes);
-                    const uint32_t acc = (j == 0 && kk == 0) ? 0u : 1u;
-                    if constexpr (G::kPInTmem)
-                        mma_bf16_ts_one(o_tmem, p_tmem + kk * 8, vdesc, G::kIdescPV, acc);
-                    else
-                        mma_bf16_one(o_tmem, smem_desc_kmajor_sw128(pa + (kk >> 2) * G::kChunkBytes + (kk & 3) * 32),
-                                     vdesc, G::kIdescPV, acc);
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
+                        mma_bf16_one(s_tmem, smem_desc_kmajor_sw128(qa + off), smem_desc_kmajor_sw128(ka + off),
+                                     G::kIdescS, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit_one(s_full(t));
+                    mma_commit_one(kv_empty(kv_slot(g0 + u)));
+                    if (j == n - 1) mma_commit_one(q_empty);
+                    return true;
+                };
+                if (n == 0) {
+                    mbar_arrive(q_empty);   // this tile has no rows in the item
+                } else if (issue_s(0, 0)) {
+                    for (int j = 0; j < n && !abort_seen; ++j) {
+                        if (j + 1 < n && !issue_s(j + 1, pos_k(j + 1))) break;
+                        // O_t += P_t · V_j once P_t is ready
+                        const int uv = pos_v(j, n_all);
+                        if (!wait(kv_full(kv_slot(g0 + uv)), kv_parity(g0 + uv), kErrMmaKv)) break;
+                        if (!wait(p_full(t), static_cast<uint32_t>((J + j) & 1), kErrMmaP)) break;
+                        tc_fence_after_sync();
+                        const uint32_t va = slot_addr(kv_slot(g0 + uv));
+#pragma unroll
+                        for (int kk = 0; kk < kBlockKV / 16; ++kk) {
+                            const uint64_t vdesc = smem_desc_mnmajor(va + kk * 2048, 128, G::kChunkBytes);
+                            const uint32_t acc = (j == 0 && kk == 0) ? 0u : 1u;
+                            if constexpr (G::kPInTmem)
+                                mma_bf16_ts_one(o_tmem, p_tmem + kk * 8, vdesc, G::kIdescPV, acc);
+                            else
+                                mma_bf16_one(o_tmem,
+                                             smem_desc_kmajor_sw128(pa + (kk >> 2) * G::kChunkBytes + (kk & 3) * 32),
+                                             vdesc, G::kIdescPV, acc);
+                        }
+                        mma_commit_one(o_done(t));
+                        mma_commit_one(kv_empty(kv_slot(g0 + uv)));
+                    }
                 }
-                mma_commit_one(o_done(t));
-                mma_commit_one(kv_empty(kv_slot(uv)));
+                // K/V positions of blocks this tile does not use: arrive once each has landed
+                auto release = [&](int u) {
+                    if (!wait(kv_full(kv_slot(g0 + u)), kv_parity(g0 + u), kErrMmaKv)) return false;
+                    mbar_arrive(kv_empty(kv_slot(g0 + u)));
+                    return true;
+                };
+                for (int j = n; j < n_all && !abort_seen; ++j)
+                    if (!release(pos_k(j)) || !release(pos_v(j, n_all))) break;
+                g0 += 2 * n_all;
+                J += n;
             }
         }
     } else {
@@ -352,148 +400,164 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         const int t = static_cast<int>(warp) >> 2;
         const uint32_t quarter = warp & 3u;
         const int r = static_cast<int>(quarter * 32 + lane);
-        const int q = q0 + t * kTileQ + r;              // this thread's query row
         const uint32_t lane_off = (quarter * 32u) << 16;
         const uint32_t s_addr = tmem_base + lane_off + G::kColS + t * kBlockKV;
         const uint32_t o_addr = tmem_base + lane_off + G::kColO + t * kD;
-        const int n = n_t(t);
-        const int key_end = p.causal ? (q + 1 < p.S ? q + 1 : p.S) : p.S;   // keys [0, key_end) are visible
         const float c = p.scale_log2;
-        float m = 0.0f;   // running max of the scaled scores (log2 units) used for P
-        float l = 0.0f;   // running sum of P
-        for (int j = 0; j < n; ++j) {
-            if (!attn_wait_warp(p, s_full(t), j & 1, kErrSoftmaxS)) {
-                abort_seen = true;
-                break;
-            }
-            tc_fence_after_sync();
-            uint32_t v[128];
-            tmem_load_32cols_at<0>(s_addr + 0, v);
-            tmem_load_32cols_at<32>(s_addr + 32, v);
-            tmem_load_32cols_at<64>(s_addr + 64, v);
-            tmem_load_32cols_at<96>(s_addr + 96, v);
-            tmem_wait_ld();
-            // S is in registers: the MMA thread may compute the next block's S here
-            tc_fence_before_sync();
-            mbar_arrive(s_free(t));
-            const int lim = key_end - j * kBlockKV;     // visible columns of this block
-            if (lim < kBlockKV) {
-#pragma unroll
-                for (int e = 0; e < 128; ++e)
-                    if (e >= lim) v[e] = __float_as_uint(-INFINITY);
-            }
-            // row max: eight independent chains of three-input maxima, then a tree
-            float acc[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int e0 = 16 * k;
-                float a = fmax3(__uint_as_float(v[e0]), __uint_as_float(v[e0 + 1]), __uint_as_float(v[e0 + 2]));
-#pragma unroll
-                for (int e = 3; e < 15; e += 2)
-                    a = fmax3(a, __uint_as_float(v[e0 + e]), __uint_as_float(v[e0 + e + 1]));
-                acc[k] = fmaxf(a, __uint_as_float(v[e0 + 15]));
-            }
-            const float mx = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
-                                   fmaxf(acc[6], acc[7]));
-            const float m_blk = mx * c;
-            float alpha = 1.0f;
-            if (j == 0) {
-                m = m_blk;
-            } else if (m_blk > m + kRescaleThreshold) {
-                alpha = ex2_approx(m - m_blk);
-                m = m_blk;
-                l *= alpha;
-            }
-            // P = 2^(s·c - m) in bf16; the scale-and-shift and the row sum run on packed pairs
-            const uint64_t c2 = f32x2(c, c);
-            const uint64_t nm2 = f32x2(-m, -m);
-            uint64_t sum2[4] = {0, 0, 0, 0};
-            uint32_t pk[64];
-#pragma unroll
-            for (int e = 0; e < 64; ++e) {
-                const uint64_t x = ffma2(f32x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), c2, nm2);
-                float x0, x1;
-                f32x2_split(x, x0, x1);
-                const float p0 = ex2_approx(x0);
-                const float p1 = ex2_approx(x1);
-                sum2[e & 3] = fadd2(sum2[e & 3], f32x2(p0, p1));
-                pk[e] = pack_bf16x2_rn(__float_as_uint(p0), __float_as_uint(p1));
-            }
+        int J = 0;   // this tile's blocks in earlier items
+        for (int w = first_item; w < p.n_items && !abort_seen; w += item_step) {
+            int n, key_end;
             {
-                const uint64_t s01 = fadd2(fadd2(sum2[0], sum2[1]), fadd2(sum2[2], sum2[3]));
-                float lo, hi;
-                f32x2_split(s01, lo, hi);
-                l += lo + hi;
+                const AttnItem it = attn_item(p, w);
+                n = t ? it.n_t1 : it.n_t0;
+                const int q = it.q0 + t * kTileQ + r;       // this thread's query row
+                key_end = p.causal ? (q + 1 < p.S ? q + 1 : p.S) : p.S;   // keys [0, key_end) are visible
             }
-            // P·V of the previous block must be done before its P is overwritten and O rescaled
-            if (j > 0 && !attn_wait_warp(p, o_done(t), (j - 1) & 1, kErrEpilogueO)) {
-                abort_seen = true;
-                break;
-            }
-            tc_fence_after_sync();
-            // rescale the running output (warp-wide when any row of the warp needs it)
-            if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll
-                for (int cc = 0; cc < kD / 32; ++cc) {
-                    uint32_t o[32];
-                    tmem_load_32cols(o_addr + 32 * cc, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_store_32cols(o_addr + 32 * cc, o);
+            float m = 0.0f;   // running max of the scaled scores (log2 units) used for P
+            float l = 0.0f;   // running sum of P
+            for (int j = 0; j < n; ++j) {
+                const int jg = J + j;
+                if (!attn_wait_warp(p, s_full(t), static_cast<uint32_t>(jg & 1), kErrSoftmaxS)) {
+                    abort_seen = true;
+                    break;
                 }
-                tmem_wait_st();
-            }
-            if constexpr (G::kPInTmem) {
-                // this row of P into the tile's own TMEM columns
-                const uint32_t p_addr = tmem_base + lane_off + G::kColP + t * (kBlockKV / 2);
-                tmem_store_32cols(p_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-                tmem_store_32cols(p_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-                tmem_wait_st();
-            } else {
-                // this row of P into the 128-byte-swizzled K-major tile the MMA reads:
-                // keys [64 h, 64 h + 64) in chunk h, 16-byte unit x of row r at unit x ^ (r % 8)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const uint32_t row = p_smem(t) + hh * G::kChunkBytes + static_cast<uint32_t>(r) * 128u;
-#pragma unroll
-                    for (int x = 0; x < 8; ++x)
-                        st_shared_v4(row + ((static_cast<uint32_t>(x) ^ (static_cast<uint32_t>(r) & 7u)) << 4),
-                                     pk[32 * hh + 4 * x], pk[32 * hh + 4 * x + 1], pk[32 * hh + 4 * x + 2],
-                                     pk[32 * hh + 4 * x + 3]);
-                }
-                fence_proxy_async_smem();
-            }
-            tc_fence_before_sync();
-            mbar_arrive(p_full(t));
-        }
-        // ------------------------------------------------------ epilogue --
-        if (!abort_seen && n > 0) {
-            if (!attn_wait_warp(p, o_done(t), (n - 1) & 1, kErrEpilogueO)) {
-                abort_seen = true;
-            } else {
                 tc_fence_after_sync();
-                const float inv_l = 1.0f / l;
-                uint16_t* out = p.O + (static_cast<int64_t>(bh) * p.S + q) * kD;
+                uint32_t v[128];
+                tmem_load_32cols_at<0>(s_addr + 0, v);
+                tmem_load_32cols_at<32>(s_addr + 32, v);
+                tmem_load_32cols_at<64>(s_addr + 64, v);
+                tmem_load_32cols_at<96>(s_addr + 96, v);
+                tmem_wait_ld();
+                // S is in registers: the MMA thread may compute the next block's S here
+                tc_fence_before_sync();
+                mbar_arrive(s_free(t));
+                const int lim = key_end - j * kBlockKV;     // visible columns of this block
+                if (lim < kBlockKV) {
 #pragma unroll
-                for (int cc = 0; cc < kD / 32; ++cc) {
-                    uint32_t o[32];
-                    tmem_load_32cols(o_addr + 32 * cc, o);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pk[e] = pack_bf16x2_rn(__float_as_uint(__uint_as_float(o[2 * e]) * inv_l),
-                                               __float_as_uint(__uint_as_float(o[2 * e + 1]) * inv_l));
-                    if (q < p.S) {
-#pragma unroll
-                        for (int w = 0; w < 4; ++w)
-                            st_global_v4(out + 32 * cc + 8 * w, pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
-                    }
+                    for (int e = 0; e < 128; ++e)
+                        if (e >= lim) v[e] = __float_as_uint(-INFINITY);
                 }
-                if (p.lse != nullptr && q < p.S)
-                    p.lse[static_cast<int64_t>(bh) * p.S + q] = (m + log2f(l)) * 0.69314718055994531f;
+                // row max: eight independent chains of three-input maxima, then a tree
+                float acc[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int e0 = 16 * k;
+                    float a = fmax3(__uint_as_float(v[e0]), __uint_as_float(v[e0 + 1]), __uint_as_float(v[e0 + 2]));
+#pragma unroll
+                    for (int e = 3; e < 15; e += 2)
+                        a = fmax3(a, __uint_as_float(v[e0 + e]), __uint_as_float(v[e0 + e + 1]));
+                    acc[k] = fmaxf(a, __uint_as_float(v[e0 + 15]));
+                }
+                const float mx = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
+                                       fmaxf(acc[6], acc[7]));
+                const float m_blk = mx * c;
+                float alpha = 1.0f;
+                if (j == 0) {
+                    m = m_blk;
+                } else if (m_blk > m + kRescaleThreshold) {
+                    alpha = ex2_approx(m - m_blk);
+                    m = m_blk;
+                    l *= alpha;
+                }
+                // P = 2^(s·c - m) in bf16; the scale-and-shift and the row sum run on packed pairs
+                const uint64_t c2 = f32x2(c, c);
+                const uint64_t nm2 = f32x2(-m, -m);
+                uint64_t sum2[4] = {0, 0, 0, 0};
+                uint32_t pk[64];
+#pragma unroll
+                for (int e = 0; e < 64; ++e) {
+                    const uint64_t x =
+                        ffma2(f32x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), c2, nm2);
+                    float x0, x1;
+                    f32x2_split(x, x0, x1);
+                    const float p0 = ex2_approx(x0);
+                    const float p1 = ex2_approx(x1);
+                    sum2[e & 3] = fadd2(sum2[e & 3], f32x2(p0, p1));
+                    pk[e] = pack_bf16x2_rn(__float_as_uint(p0), __float_as_uint(p1));
+                }
+                {
+                    const uint64_t s01 = fadd2(fadd2(sum2[0], sum2[1]), fadd2(sum2[2], sum2[3]));
+                    float lo, hi;
+                    f32x2_split(s01, lo, hi);
+                    l += lo + hi;
+                }
+                // P·V of the previous block must be done before its P is overwritten and O rescaled
+                if (j > 0 && !attn_wait_warp(p, o_done(t), static_cast<uint32_t>((jg - 1) & 1), kErrEpilogueO)) {
+                    abort_seen = true;
+                    break;
+                }
+                tc_fence_after_sync();
+                // rescale the running output (warp-wide when any row of the warp needs it)
+                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+                    for (int cc = 0; cc < kD / 32; ++cc) {
+                        uint32_t o[32];
+                        tmem_load_32cols(o_addr + 32 * cc, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_store_32cols(o_addr + 32 * cc, o);
+                    }
+                    tmem_wait_st();
+                }
+                if constexpr (G::kPInTmem) {
+                    // this row of P into the tile's own TMEM columns
+                    const uint32_t p_addr = tmem_base + lane_off + G::kColP + t * (kBlockKV / 2);
+                    tmem_store_32cols(p_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+                    tmem_store_32cols(p_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+                    tmem_wait_st();
+                } else {
+                    // this row of P into the 128-byte-swizzled K-major tile the MMA reads:
+                    // keys [64 h, 64 h + 64) in chunk h, 16-byte unit x of row r at unit x ^ (r % 8)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t row = p_smem(t) + hh * G::kChunkBytes + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+                        for (int x = 0; x < 8; ++x)
+                            st_shared_v4(row + ((static_cast<uint32_t>(x) ^ (static_cast<uint32_t>(r) & 7u)) << 4),
+                                         pk[32 * hh + 4 * x], pk[32 * hh + 4 * x + 1], pk[32 * hh + 4 * x + 2],
+                                         pk[32 * hh + 4 * x + 3]);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before_sync();
+                mbar_arrive(p_full(t));
             }
+            // -------------------------------------------------- epilogue --
+            // (reading O here, before this warp publishes the next item's first P,
+            // orders these reads before the P·V that overwrites O)
+            if (!abort_seen && n > 0) {
+                if (!attn_wait_warp(p, o_done(t), static_cast<uint32_t>((J + n - 1) & 1), kErrEpilogueO)) {
+                    abort_seen = true;
+                } else {
+                    tc_fence_after_sync();
+                    const AttnItem it = attn_item(p, w);
+                    const int q = it.q0 + t * kTileQ + r;
+                    const float inv_l = 1.0f / l;
+                    uint16_t* out = p.O + (static_cast<int64_t>(it.bh) * p.S + q) * kD;
+#pragma unroll
+                    for (int cc = 0; cc < kD / 32; ++cc) {
+                        uint32_t o[32];
+                        tmem_load_32cols(o_addr + 32 * cc, o);
+                        tmem_wait_ld();
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            pk[e] = pack_bf16x2_rn(__float_as_uint(__uint_as_float(o[2 * e]) * inv_l),
+                                                   __float_as_uint(__uint_as_float(o[2 * e + 1]) * inv_l));
+                        if (q < p.S) {
+#pragma unroll
+                            for (int w4 = 0; w4 < 4; ++w4)
+                                st_global_v4(out + 32 * cc + 8 * w4, pk[4 * w4], pk[4 * w4 + 1], pk[4 * w4 + 2],
+                                             pk[4 * w4 + 3]);
+                        }
+                    }
+                    if (p.lse != nullptr && q < p.S)
+                        p.lse[static_cast<int64_t>(it.bh) * p.S + q] = (m + log2f(l)) * 0.69314718055994531f;
+                    tc_fence_before_sync();
+                }
+            }
+            J += n;
         }
     }
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -112,6 +113,7 @@ extern "C" hk_status hk_attention_fwd_ex(const void* Q, const void* K, const voi
     p.S = static_cast<int32_t>(S);
     p.causal = causal ? 1 : 0;
     p.q_pairs = static_cast<int32_t>((S + 255) / 256);
+    p.n_items = static_cast<int32_t>(B * Hq * p.q_pairs);
     p.kv_blocks = static_cast<int32_t>((S + 127) / 128);
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     p.O = static_cast<uint16_t*>(O);
@@ -121,7 +123,8 @@ extern "C" hk_status hk_attention_fwd_ex(const void* Q, const void* K, const voi
     p.flags = flags;
     p.timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
 
-    const unsigned grid = static_cast<unsigned>(B * Hq * p.q_pairs);
+    // persistent: one CTA per SM (at most one per work item), each walking its items
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>(B * Hq * p.q_pairs, sm_count));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (D == 64) {
         hk::attn::attn_fwd_kernel<64><<<grid, hk::attn::kThreads, hk::attn::AttnGeometry<64>::kSmemBytes, st>>>(
