@@ -42,22 +42,22 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources whose digest is given; see profiles/.
 MEASURED_TRAFFIC = {
-    "gemm_8192": {"source_digest": "abb2922440ef9855", "bytes_per_launch": 1086247680 + 128632576,
+    "gemm_8192": {"source_digest": "6f948220b571b79e", "bytes_per_launch": 1079986688 + 127984896,
                   "profile": "profiles/gemm_bf16_kernel_pair256_gemm_8192.md"},
-    "skinny_128x28672x8192": {"source_digest": "abb2922440ef9855", "bytes_per_launch": 471981568 + 4365824,
+    "skinny_128x28672x8192": {"source_digest": "6f948220b571b79e", "bytes_per_launch": 471969536 + 3940352,
                               "profile": "profiles/gemm_bf16_kernel_single128x192_skinny_128x28672x8192.md"},
-    "fp8_gemm_8192": {"source_digest": "abb2922440ef9855", "bytes_per_launch": 349363200 + 117921792,
+    "fp8_gemm_8192": {"source_digest": "6f948220b571b79e", "bytes_per_launch": 342054912 + 117001984,
                       "profile": "profiles/gemm_fp8_kernel_pair256_fp8_gemm_8192.md"},
     # the block-scaled GEMM kernel alone (the scale arrangement kernel moves ~8 MB more)
-    "mxfp8_gemm_8192": {"source_digest": "abb2922440ef9855", "bytes_per_launch": 360049408 + 116597504,
+    "mxfp8_gemm_8192": {"source_digest": "6f948220b571b79e", "bytes_per_launch": 353340928 + 116872192,
                         "profile": "profiles/gemm_mxfp8_kernel_pair256_mxfp8_gemm_8192.md"},
     # the GEMM kernel alone (the split-K reduction reads the fp32 partials and writes C)
-    "decode_64x8192x28672": {"source_digest": "abb2922440ef9855", "bytes_per_launch": 473516800 + 3975424,
+    "decode_64x8192x28672": {"source_digest": "6f948220b571b79e", "bytes_per_launch": 473519872 + 3529728,
                              "profile": "profiles/gemm_bf16_kernel_single_decode_shapes.md"},
     # attention: captured at B2 (one launch); the B16 figure scales it by 8 (traffic grows with B)
-    "attn_gqa_b2_s4096_d128": {"source_digest": "78bf4b24f62b6284", "bytes_per_launch": 187219968 + 123094784,
+    "attn_gqa_b2_s4096_d128": {"source_digest": "da69eff21b5d0f51", "bytes_per_launch": 199823616 + 110772480,
                                "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
-    "attn_gqa_b16_s4096_d128": {"source_digest": "78bf4b24f62b6284", "bytes_per_launch": 8 * (187219968 + 123094784),
+    "attn_gqa_b16_s4096_d128": {"source_digest": "da69eff21b5d0f51", "bytes_per_launch": 8 * (199823616 + 110772480),
                                 "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
 }
 

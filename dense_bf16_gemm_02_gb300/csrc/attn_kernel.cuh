@@ -9,9 +9,12 @@
 // The pages' kernel is an 8-wave ping-pong on AMD matrix cores. This one is
 // a Blackwell design:
 //
-//  * one CTA owns two 128-row query tiles of one (batch, query head); both
+//  * a work item is two 128-row query tiles of one (batch, query head); both
 //    tiles share every K/V block that a TMA producer warp streams through a
 //    shared-memory ring (128 keys per block, 128-byte swizzle);
+//  * the grid is persistent (one CTA per SM) and each CTA walks its work
+//    items back to back, so the next item's Q and first K/V blocks load while
+//    the current item ends, and launch and set-up are paid once per CTA;
 //  * one thread issues tcgen05.mma: S_t = Q_t·K_jᵀ (M=128, N=128, K=D) into
 //    Tensor Memory, and O_t += P_t·V_j (M=128, N=D, K=128) with P_t and V_j
 //    (MN-major, so V is never transposed) read from shared memory;
@@ -31,8 +34,9 @@
 //  * the epilogue multiplies by 1/l, rounds to bf16 (RNE) and stores each
 //    row directly; the log-sum-exp goes to an optional fp32 array.
 //
-// Each KV head's K and V are read by Hq/Hkv query heads; CTAs are numbered
-// head-fastest so the heads of a group run together and share K/V in L2.
+// Each KV head's K and V are read by Hq/Hkv query heads; work items are
+// numbered head-fastest so the heads of a group run together and share K/V
+// in L2.
 // Every mbarrier wait is bounded like the GEMM's: a wait that runs out
 // records an error in the device status word, the CTA drains and returns.
 #pragma once
