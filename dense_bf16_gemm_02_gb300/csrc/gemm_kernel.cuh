@@ -60,11 +60,18 @@ constexpr int pow2_at_least(int x) {
 }
 
 // Compile-time geometry of one kernel instance. kMx: block-scaled FP8
-// (MXFP8, one UE8M0 scale per 32 K elements).
-template <int kCG, int kTileN_, bool kFp8 = false, bool kMx = false>
+// (MXFP8, one UE8M0 scale per 32 K elements). kSmallA (single CTA, M <= 16):
+// each stage keeps room for 16 rows of A instead of 128, so more stages fit
+// and more of B is in flight; the MMA still reads a 128-row A tile, whose rows
+// past 16 fall on other (in-bounds) shared memory and only feed rows of C
+// that are never stored.
+template <int kCG, int kTileN_, bool kFp8 = false, bool kMx = false, bool kSmallA = false>
 struct Geometry {
     static_assert(kCG == 1 || kCG == 2, "one CTA or a CTA pair");
     static_assert(!kMx || kFp8, "block scales come with FP8 operands");
+    static_assert(!kSmallA || (kCG == 1 && !kMx), "small-A stages: single-CTA kernels only");
+    static constexpr int kARowsMax = kSmallA ? 16 : kCtaM;          // rows of A a stage holds
+    static constexpr int kAStageBytes = kARowsMax * kRowBytes;
     static_assert(kTileN_ % (16 * kCG) == 0 && kTileN_ >= 32 && kTileN_ <= 256, "MMA N");
     static constexpr int kTileM = kCtaM * kCG;              // rows of C per tile
     static constexpr int kTileN = kTileN_;                  // columns of C per tile (MMA N)
@@ -78,13 +85,16 @@ struct Geometry {
     static constexpr int kSfbAtoms = (kTileN + 127) / 128;
     static constexpr int kSfBytes = kMx ? 512 * (1 + kSfbAtoms) : 0;
     static constexpr int kSfCols = kMx ? 4 * (1 + kSfbAtoms) : 0;   // TMEM columns per stage
-    static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
+    static constexpr int kStageBytes = kAStageBytes + kBBytes + kSfBytes;
     static constexpr int kFixed = kEpiWarps * 2 * kEpiBufBytes + 256 + 1024;   // epilogue, barriers, alignment
     static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
-    static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+    static constexpr int kMaxStages = kSmallA ? 12 : 8;
+    static constexpr int kStages = kStagesFit > kMaxStages ? kMaxStages : kStagesFit;
     static_assert(kStages >= 3, "pipeline too shallow");
     static constexpr int kOffA = 0;
-    static constexpr int kOffB = kOffA + kStages * kABytes;
+    static constexpr int kOffB = kOffA + kStages * kAStageBytes;
+    // the MMA reads kABytes from the last stage's A: it must stay inside the buffer
+    static_assert(kOffA + (kStages - 1) * kAStageBytes + kABytes <= kOffB + kStages * kBBytes, "A read");
     static constexpr int kOffSf = kOffB + kStages * kBBytes;
     static constexpr int kOffEpi = kOffSf + kStages * kSfBytes;
     static constexpr int kOffBars = kOffEpi + kEpiWarps * 2 * kEpiBufBytes;
@@ -283,12 +293,12 @@ __device__ __forceinline__ void drain_after_abort() {
     for (int i = 0; i < 200; ++i) __nanosleep(1000);
 }
 
-template <int kCG, int kTileN, bool kFp8, bool kMx = false>
+template <int kCG, int kTileN, bool kFp8, bool kMx = false, bool kSmallA = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                  const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_b_half,
                  const GemmParams p) {
-    using G = Geometry<kCG, kTileN, kFp8, kMx>;
+    using G = Geometry<kCG, kTileN, kFp8, kMx, kSmallA>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -379,7 +389,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                             mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
                         }
                     }
-                    const uint32_t a_dst = base + G::kOffA + stage * kABytes;
+                    const uint32_t a_dst = base + G::kOffA + stage * G::kAStageBytes;
                     const uint32_t b_dst = base + G::kOffB + stage * G::kBBytes;
                     if constexpr (kCG == 2) {
                         // both CTAs' copies complete on the leader's barrier
@@ -444,7 +454,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint64_t a_desc = smem_desc_kmajor_sw128(base + G::kOffA + stage * kABytes);
+                    const uint64_t a_desc = smem_desc_kmajor_sw128(base + G::kOffA + stage * G::kAStageBytes);
                     const uint64_t b_desc = smem_desc_kmajor_sw128(base + G::kOffB + stage * G::kBBytes);
                     if constexpr (kMx) {
                         // this stage's scales, copied into its TMEM slot by the scale copier
