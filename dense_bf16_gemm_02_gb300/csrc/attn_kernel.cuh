@@ -221,8 +221,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     const uint32_t lane = lane_id();
 
     // Persistent: CTA c takes work items c, c + G, c + 2G, ... (G = gridDim.x).
-    // Barrier phases run on across items: the K/V ring by a running position,
-    // S/P/O of each tile by a running block count.
+    // Barrier phases run on across items: the K/V ring's as a slot index and a
+    // phase bit, S/P/O's of each tile as the parity of its blocks so far (state
+    // that stays bounded however many items a CTA takes).
     const uint32_t q_full = base + G::kOffBars;
     auto kv_full = [&](int s) { return base + G::kOffBars + 8u * (1 + s); };
     auto kv_empty = [&](int s) { return base + G::kOffBars + 8u * (1 + G::kSlots + s); };
@@ -270,7 +271,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     if (warp == kWarpTma) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
-            int g = 0;   // running K/V ring position
+            int slot = 0;          // K/V ring slot of the next position
+            uint32_t ring_ph = 0;  // its phase: flips each time the ring wraps
             int li = 0;      // items done by this CTA
             for (int w = first_item; w < p.n_items && !abort_seen; w += item_step, ++li) {
                 const AttnItem it = attn_item(p, w);
@@ -285,14 +287,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     for (int c = 0; c < G::kChunks; ++c)
                         tma_load_3d(base + G::kOffQ + t * G::kTileBytes + c * G::kChunkBytes, &tmap_q, c * 64,
                                     it.q0 + t * kTileQ, it.bh, q_full);
-                for (int u = 0; u < 2 * it.n_all && !abort_seen; ++u, ++g) {
-                    const int s = g % G::kSlots;
-                    const uint32_t parity = static_cast<uint32_t>((g / G::kSlots) & 1) ^ 1u;
+                for (int u = 0; u < 2 * it.n_all && !abort_seen; ++u) {
+                    const int s = slot;
+                    const uint32_t parity = ring_ph ^ 1u;
+                    if (++slot == G::kSlots) {
+                        slot = 0;
+                        ring_ph ^= 1u;
+                    }
                     if (!attn_wait(p, kv_empty(s), parity, kErrTmaEmpty, Wait::kSuspend)) {
                         abort_seen = true;
                         break;
                     }
-                    if ((p.flags & kFlagDropArrive) && g == 0) continue;   // test hook: never fill the first slot
+                    if ((p.flags & kFlagDropArrive) && li == 0 && u == 0) continue;   // test hook: never fill the first slot
                     // position u of the item's consumption order: K_0, (K_{j+1}, V_j)..., V_{n-1}
                     bool is_k;
                     int blk;
@@ -328,28 +334,31 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 if (!attn_wait(p, bar, parity, code)) abort_seen = true;
                 return !abort_seen;
             };
-            auto kv_slot = [&](int g) { return g % G::kSlots; };
-            auto kv_parity = [&](int g) { return static_cast<uint32_t>((g / G::kSlots) & 1); };
+            int s0 = 0;          // ring slot of the item's first K/V position
+            uint32_t ph0 = 0;    // and its phase
+            auto kv_slot = [&](int u) { return (s0 + u) % G::kSlots; };
+            auto kv_parity = [&](int u) { return ph0 ^ static_cast<uint32_t>(((s0 + u) / G::kSlots) & 1); };
             const uint32_t qa = base + G::kOffQ + t * G::kTileBytes;
             const uint32_t s_tmem = tmem_base + G::kColS + t * kBlockKV;
             const uint32_t o_tmem = tmem_base + G::kColO + t * kD;
             const uint32_t pa = p_smem(t);
             const uint32_t p_tmem = tmem_base + G::kColP + t * (kBlockKV / 2);
-            int g0 = 0;   // ring position of the item's first K/V block
-            int J = 0;    // this tile's blocks in earlier items
+            uint32_t jp = 0;       // parity of this tile's blocks in earlier items
+            bool any_block = false;  // has this tile had a block before (then S waits for s_free)
             int li = 0;
             for (int w = first_item; w < p.n_items && !abort_seen; w += item_step, ++li) {
                 const AttnItem it = attn_item(p, w);
                 const int n = t ? it.n_t1 : it.n_t0;
                 const int n_all = it.n_all;
                 if (!wait(q_full, li & 1, kErrMmaKv)) break;
-                // S_t = Q_t · K_jᵀ of block j (ring position g0 + u), once the softmax has
+                // S_t = Q_t · K_jᵀ of block j (item position u), once the softmax has
                 // read this tile's previous S; the last S of the item releases Q
                 auto issue_s = [&](int j, int u) {
-                    if (J + j > 0 && !wait(s_free(t), static_cast<uint32_t>((J + j - 1) & 1), kErrMmaP)) return false;
-                    if (!wait(kv_full(kv_slot(g0 + u)), kv_parity(g0 + u), kErrMmaKv)) return false;
+                    if ((j > 0 || any_block) && !wait(s_free(t), jp ^ static_cast<uint32_t>((j - 1) & 1), kErrMmaP))
+                        return false;
+                    if (!wait(kv_full(kv_slot(u)), kv_parity(u), kErrMmaKv)) return false;
                     tc_fence_after_sync();
-                    const uint32_t ka = slot_addr(kv_slot(g0 + u));
+                    const uint32_t ka = slot_addr(kv_slot(u));
 #pragma unroll
                     for (int kk = 0; kk < kD / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
@@ -357,7 +366,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                      G::kIdescS, kk > 0 ? 1u : 0u);
                     }
                     mma_commit_one(s_full(t));
-                    mma_commit_one(kv_empty(kv_slot(g0 + u)));
+                    mma_commit_one(kv_empty(kv_slot(u)));
                     if (j == n - 1) mma_commit_one(q_empty);
                     return true;
                 };
@@ -368,10 +377,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         if (j + 1 < n && !issue_s(j + 1, pos_k(j + 1))) break;
                         // O_t += P_t · V_j once P_t is ready
                         const int uv = pos_v(j, n_all);
-                        if (!wait(kv_full(kv_slot(g0 + uv)), kv_parity(g0 + uv), kErrMmaKv)) break;
-                        if (!wait(p_full(t), static_cast<uint32_t>((J + j) & 1), kErrMmaP)) break;
+                        if (!wait(kv_full(kv_slot(uv)), kv_parity(uv), kErrMmaKv)) break;
+                        if (!wait(p_full(t), jp ^ static_cast<uint32_t>(j & 1), kErrMmaP)) break;
                         tc_fence_after_sync();
-                        const uint32_t va = slot_addr(kv_slot(g0 + uv));
+                        const uint32_t va = slot_addr(kv_slot(uv));
 #pragma unroll
                         for (int kk = 0; kk < kBlockKV / 16; ++kk) {
                             const uint64_t vdesc = smem_desc_mnmajor(va + kk * 2048, 128, G::kChunkBytes);
@@ -384,19 +393,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                                              vdesc, G::kIdescPV, acc);
                         }
                         mma_commit_one(o_done(t));
-                        mma_commit_one(kv_empty(kv_slot(g0 + uv)));
+                        mma_commit_one(kv_empty(kv_slot(uv)));
                     }
                 }
                 // K/V positions of blocks this tile does not use: arrive once each has landed
                 auto release = [&](int u) {
-                    if (!wait(kv_full(kv_slot(g0 + u)), kv_parity(g0 + u), kErrMmaKv)) return false;
-                    mbar_arrive(kv_empty(kv_slot(g0 + u)));
+                    if (!wait(kv_full(kv_slot(u)), kv_parity(u), kErrMmaKv)) return false;
+                    mbar_arrive(kv_empty(kv_slot(u)));
                     return true;
                 };
                 for (int j = n; j < n_all && !abort_seen; ++j)
                     if (!release(pos_k(j)) || !release(pos_v(j, n_all))) break;
-                g0 += 2 * n_all;
-                J += n;
+                ph0 ^= static_cast<uint32_t>(((s0 + 2 * n_all) / G::kSlots) & 1);
+                s0 = (s0 + 2 * n_all) % G::kSlots;
+                jp ^= static_cast<uint32_t>(n & 1);
+                any_block = any_block || n > 0;
             }
         }
     } else {
@@ -408,7 +419,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         const uint32_t s_addr = tmem_base + lane_off + G::kColS + t * kBlockKV;
         const uint32_t o_addr = tmem_base + lane_off + G::kColO + t * kD;
         const float c = p.scale_log2;
-        int J = 0;   // this tile's blocks in earlier items
+        uint32_t jp = 0;   // parity of this tile's blocks in earlier items
         for (int w = first_item; w < p.n_items && !abort_seen; w += item_step) {
             int n, key_end;
             {
@@ -420,8 +431,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             float m = 0.0f;   // running max of the scaled scores (log2 units) used for P
             float l = 0.0f;   // running sum of P
             for (int j = 0; j < n; ++j) {
-                const int jg = J + j;
-                if (!attn_wait_warp(p, s_full(t), static_cast<uint32_t>(jg & 1), kErrSoftmaxS)) {
+                const uint32_t par = jp ^ static_cast<uint32_t>(j & 1);   // phase of this block's barriers
+                if (!attn_wait_warp(p, s_full(t), par, kErrSoftmaxS)) {
                     abort_seen = true;
                     break;
                 }
@@ -486,7 +497,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     l += lo + hi;
                 }
                 // P·V of the previous block must be done before its P is overwritten and O rescaled
-                if (j > 0 && !attn_wait_warp(p, o_done(t), static_cast<uint32_t>((jg - 1) & 1), kErrEpilogueO)) {
+                if (j > 0 && !attn_wait_warp(p, o_done(t), par ^ 1u, kErrEpilogueO)) {
                     abort_seen = true;
                     break;
                 }
@@ -531,7 +542,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             // (reading O here, before this warp publishes the next item's first P,
             // orders these reads before the P·V that overwrites O)
             if (!abort_seen && n > 0) {
-                if (!attn_wait_warp(p, o_done(t), static_cast<uint32_t>((J + n - 1) & 1), kErrEpilogueO)) {
+                if (!attn_wait_warp(p, o_done(t), jp ^ static_cast<uint32_t>((n - 1) & 1), kErrEpilogueO)) {
                     abort_seen = true;
                 } else {
                     tc_fence_after_sync();
@@ -561,7 +572,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     tc_fence_before_sync();
                 }
             }
-            J += n;
+            jp ^= static_cast<uint32_t>(n & 1);
         }
     }
 
