@@ -147,6 +147,29 @@ def test_attention_matches_oracle(hk, oracle, shape, causal):
     check_lse(lse, want_lse, f"{shape} causal={causal}")
 
 
+# Many more work items (256 query rows of one head) than CTAs (one per SM), so
+# each CTA walks several items back to back: ragged S makes the last item of
+# every head end with an empty second tile (S = 300: rows 256..299 only) or a
+# short one (S = 520), and causal items differ in length; every element is
+# checked against the oracle.
+MULTI_ITEM_SHAPES = [
+    (8, 32, 8, 300, 128),    # 512 items, every second one with an empty second tile
+    (4, 32, 4, 520, 64),     # 384 items of three lengths
+    (16, 16, 4, 1, 128),     # 256 items of a single row
+]
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("shape", MULTI_ITEM_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_attention_many_items_per_cta(hk, oracle, shape, causal):
+    B, Hq, Hkv, S, D = shape
+    Q, K, V = _inputs(B, Hq, Hkv, S, D, 700 + S + D)
+    got, lse = run_attention(hk, Q, K, V, causal)
+    want, want_lse = oracle.attention_fwd(Q, K, V, causal=causal, with_lse=True)
+    check_heads(got, want, Q, K, V, causal, what=f"{shape} causal={causal}")
+    check_lse(lse, want_lse, f"{shape} causal={causal}")
+
+
 def test_attention_growing_scores_rescale(hk, oracle):
     """Keys whose norm grows along the sequence make every row's maximum
     jump by more than 2^8 between blocks, exercising the output rescale."""
