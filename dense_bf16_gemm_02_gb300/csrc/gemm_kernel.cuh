@@ -60,17 +60,18 @@ constexpr int pow2_at_least(int x) {
 }
 
 // Compile-time geometry of one kernel instance. kMx: block-scaled FP8
-// (MXFP8, one UE8M0 scale per 32 K elements). kSmallA (single CTA, M <= 16):
-// each stage keeps room for 16 rows of A instead of 128, so more stages fit
-// and more of B is in flight; the MMA still reads a 128-row A tile, whose rows
-// past 16 fall on other (in-bounds) shared memory and only feed rows of C
-// that are never stored.
-template <int kCG, int kTileN_, bool kFp8 = false, bool kMx = false, bool kSmallA = false>
+// (MXFP8, one UE8M0 scale per 32 K elements). kARows < 128 (single CTA,
+// M <= kARows): each stage keeps room for kARows rows of A instead of 128, so
+// more stages fit and more of B is in flight; the MMA still reads a 128-row A
+// tile, whose rows past kARows fall on other (in-bounds) shared memory and
+// only feed rows of C that are never stored.
+template <int kCG, int kTileN_, bool kFp8 = false, bool kMx = false, int kARows = kCtaM>
 struct Geometry {
     static_assert(kCG == 1 || kCG == 2, "one CTA or a CTA pair");
     static_assert(!kMx || kFp8, "block scales come with FP8 operands");
-    static_assert(!kSmallA || (kCG == 1 && !kMx), "small-A stages: single-CTA kernels only");
-    static constexpr int kARowsMax = kSmallA ? 16 : kCtaM;          // rows of A a stage holds
+    static_assert(kARows == kCtaM || (kCG == 1 && !kMx && kARows % 8 == 0 && kARows >= 8),
+                  "short A stages: single-CTA kernels only, whole 8-row swizzle atoms");
+    static constexpr int kARowsMax = kARows;                          // rows of A a stage holds
     static constexpr int kAStageBytes = kARowsMax * kRowBytes;
     static_assert(kTileN_ % (16 * kCG) == 0 && kTileN_ >= 32 && kTileN_ <= 256, "MMA N");
     static constexpr int kTileM = kCtaM * kCG;              // rows of C per tile
@@ -88,7 +89,7 @@ struct Geometry {
     static constexpr int kStageBytes = kAStageBytes + kBBytes + kSfBytes;
     static constexpr int kFixed = kEpiWarps * 2 * kEpiBufBytes + 256 + 1024;   // epilogue, barriers, alignment
     static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
-    static constexpr int kMaxStages = kSmallA ? 12 : 8;
+    static constexpr int kMaxStages = kARows < kCtaM ? 12 : 8;
     static constexpr int kStages = kStagesFit > kMaxStages ? kMaxStages : kStagesFit;
     static_assert(kStages >= 3, "pipeline too shallow");
     static constexpr int kOffA = 0;
@@ -293,12 +294,12 @@ __device__ __forceinline__ void drain_after_abort() {
     for (int i = 0; i < 200; ++i) __nanosleep(1000);
 }
 
-template <int kCG, int kTileN, bool kFp8, bool kMx = false, bool kSmallA = false>
+template <int kCG, int kTileN, bool kFp8, bool kMx = false, int kARows = kCtaM>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                  const __grid_constant__ CUtensorMap tmap_c, const __grid_constant__ CUtensorMap tmap_b_half,
                  const GemmParams p) {
-    using G = Geometry<kCG, kTileN, kFp8, kMx, kSmallA>;
+    using G = Geometry<kCG, kTileN, kFp8, kMx, kARows>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;

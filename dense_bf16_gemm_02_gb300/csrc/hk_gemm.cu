@@ -54,27 +54,32 @@ struct Variant {
     int stages, smem_bytes;
     bool fp8;          // E4M3 operands (else bf16)
     bool mx;           // block-scaled E4M3 (MXFP8); never chosen automatically
-    int a_rows_max;    // rows of A a stage holds (16 for the small-A decode kernels, else 128)
+    int a_rows_max;    // rows of A a stage holds (16 or 64 for the decode kernels, else 128)
     int k_elems;       // K elements per pipeline stage
     int sf_bytes;      // MXFP8: bytes of scale blocks per stage and CTA
     KernelFn fn;
     const char* name;
 };
 
-template <int kCG, int kTileN, bool kFp8, bool kMx = false, bool kSmallA = false>
+template <int kCG, int kTileN, bool kFp8, bool kMx = false, int kARows = hk::kCtaM>
 constexpr Variant make_variant(int id, const char* name) {
-    using G = hk::Geometry<kCG, kTileN, kFp8, kMx, kSmallA>;
+    using G = hk::Geometry<kCG, kTileN, kFp8, kMx, kARows>;
     return Variant{id, kCG, G::kTileM, G::kTileN, G::kStages, G::kSmemBytes, kFp8, kMx, G::kARowsMax, G::kKElems,
-                   G::kSfBytes, &hk::gemm_bf16_kernel<kCG, kTileN, kFp8, kMx, kSmallA>, name};
+                   G::kSfBytes, &hk::gemm_bf16_kernel<kCG, kTileN, kFp8, kMx, kARows>, name};
 }
 
 const Variant kVariants[] = {
-    // decode (M <= 16): single-CTA tiles with 16-row A stages, so more stages of B are in
-    // flight; listed before the 128-row forms so that they win the time model's ties
-    make_variant<1, 256, false, false, true>(HK_KERNEL_SINGLE_128x256, "single 128x256, 16-row A"),
-    make_variant<1, 192, false, false, true>(HK_KERNEL_SINGLE_128x192, "single 128x192, 16-row A"),
-    make_variant<1, 128, false, false, true>(HK_KERNEL_SINGLE_128x128, "single 128x128, 16-row A"),
-    make_variant<1, 64, false, false, true>(HK_KERNEL_SINGLE_128x64, "single 128x64, 16-row A"),
+    // decode (M <= 16, M <= 64): single-CTA tiles with 16- or 64-row A stages, so more
+    // stages of B are in flight; listed before the 128-row forms (shortest first) so that
+    // they win the time model's ties
+    make_variant<1, 256, false, false, 16>(HK_KERNEL_SINGLE_128x256, "single 128x256, 16-row A"),
+    make_variant<1, 192, false, false, 16>(HK_KERNEL_SINGLE_128x192, "single 128x192, 16-row A"),
+    make_variant<1, 128, false, false, 16>(HK_KERNEL_SINGLE_128x128, "single 128x128, 16-row A"),
+    make_variant<1, 64, false, false, 16>(HK_KERNEL_SINGLE_128x64, "single 128x64, 16-row A"),
+    make_variant<1, 256, false, false, 64>(HK_KERNEL_SINGLE_128x256, "single 128x256, 64-row A"),
+    make_variant<1, 192, false, false, 64>(HK_KERNEL_SINGLE_128x192, "single 128x192, 64-row A"),
+    make_variant<1, 128, false, false, 64>(HK_KERNEL_SINGLE_128x128, "single 128x128, 64-row A"),
+    make_variant<1, 64, false, false, 64>(HK_KERNEL_SINGLE_128x64, "single 128x64, 64-row A"),
     make_variant<2, 256, false>(HK_KERNEL_PAIR_256x256, "pair 256x256"),
     make_variant<1, 256, false>(HK_KERNEL_SINGLE_128x256, "single 128x256"),
     make_variant<1, 192, false>(HK_KERNEL_SINGLE_128x192, "single 128x192"),
@@ -360,7 +365,7 @@ void choose_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo* di, int max_
     for (int i = 0; i < kNumVariants; ++i) {
         const Variant& v = kVariants[i];
         if (v.fp8 != fp8 || v.mx) continue;
-        if (a_rows_for(v, M) > v.a_rows_max) continue;   // the 16-row A stages serve M <= 16 only
+        if (a_rows_for(v, M) > v.a_rows_max) continue;   // short A stages serve only M up to their rows
         if (forced_kernel != HK_KERNEL_AUTO ? v.id != forced_kernel : ((M > hk::kCtaM) != (v.cg == 2))) continue;
         const int64_t k_blocks = ceil_div(K, v.k_elems);
         int64_t slots = di->max_units[i];
