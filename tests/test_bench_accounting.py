@@ -38,3 +38,26 @@ def test_workload_config_names_the_shape():
     c = bench.workload_config(synth.WORKLOADS["gemm_8192"])
     assert c["workload"] == "gemm_8192" and (c["M"], c["N"], c["K"]) == (8192, 8192, 8192)
     assert "larger than L2" in c["l2"]
+
+
+def test_tensor_peak_burst_or_sustained_by_timed_length():
+    peaks = {"bf16_tflops": 1937.8, "bf16_tflops_sustained": 1734.0, "hbm_gbs": 6773.9}
+    short, src_short = bench.tensor_peak(peaks, "measured", 0.06)
+    long_, src_long = bench.tensor_peak(peaks, "measured", 0.66)
+    assert short == 1937.8 and "burst" in src_short
+    assert long_ == 1734.0 and "sustained" in src_long
+    fp8, src_fp8 = bench.tensor_peak(peaks, "measured", 0.06, fp8=True)
+    assert fp8 == 2 * 1937.8 and "fp8/bf16" in src_fp8
+    only_burst = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}   # no sustained figure: burst
+    assert bench.tensor_peak(only_burst, "fallback", 5.0)[0] == 1900.0
+
+
+def test_decode_workloads_are_hbm_bound_and_larger_than_l2():
+    import synth
+    peaks = dict(bench.FALLBACK_PEAKS)
+    knee = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)   # flop per byte
+    for name in ("decode_1x28672x8192", "decode_64x8192x28672"):
+        w = synth.WORKLOADS[name]
+        ai = bench.gemm_flops(w.M, w.N, w.K) / bench.gemm_bytes(w.M, w.N, w.K)
+        assert ai < knee, name
+        assert "larger than L2" in bench.workload_config(w)["l2"], name
