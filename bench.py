@@ -42,22 +42,22 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources whose digest is given; see profiles/.
 MEASURED_TRAFFIC = {
-    "gemm_8192": {"source_digest": "fb2ca3460de56241", "bytes_per_launch": 1070466304 + 125692416,
+    "gemm_8192": {"source_digest": "3c2dfb949bab1ad5", "bytes_per_launch": 1150159616 + 128739072,
                   "profile": "profiles/gemm_bf16_kernel_pair256_gemm_8192.md"},
-    "skinny_128x28672x8192": {"source_digest": "fb2ca3460de56241", "bytes_per_launch": 471981824 + 4028160,
+    "skinny_128x28672x8192": {"source_digest": "3c2dfb949bab1ad5", "bytes_per_launch": 471958528 + 3589120,
                               "profile": "profiles/gemm_bf16_kernel_single128x192_skinny_128x28672x8192.md"},
-    "fp8_gemm_8192": {"source_digest": "fb2ca3460de56241", "bytes_per_launch": 347210752 + 116006912,
+    "fp8_gemm_8192": {"source_digest": "3c2dfb949bab1ad5", "bytes_per_launch": 345619712 + 117902848,
                       "profile": "profiles/gemm_fp8_kernel_pair256_fp8_gemm_8192.md"},
     # the block-scaled GEMM kernel alone (the scale arrangement kernel moves ~8 MB more)
-    "mxfp8_gemm_8192": {"source_digest": "fb2ca3460de56241", "bytes_per_launch": 360048896 + 116911872,
+    "mxfp8_gemm_8192": {"source_digest": "3c2dfb949bab1ad5", "bytes_per_launch": 354771712 + 116889344,
                         "profile": "profiles/gemm_mxfp8_kernel_pair256_mxfp8_gemm_8192.md"},
     # the GEMM kernel alone (the split-K reduction reads the fp32 partials and writes C)
-    "decode_64x8192x28672": {"source_digest": "fb2ca3460de56241", "bytes_per_launch": 473515008 + 3504896,
+    "decode_64x8192x28672": {"source_digest": "3c2dfb949bab1ad5", "bytes_per_launch": 473515264 + 3873280,
                              "profile": "profiles/gemm_bf16_kernel_single_decode_shapes.md"},
     # attention: captured at B2 (one launch); the B16 figure scales it by 8 (traffic grows with B)
-    "attn_gqa_b2_s4096_d128": {"source_digest": "d6514cb48c3fcb48", "bytes_per_launch": 201136640 + 111190784,
+    "attn_gqa_b2_s4096_d128": {"source_digest": "e2bf2e29b78c0df1", "bytes_per_launch": 199983616 + 110758144,
                                "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
-    "attn_gqa_b16_s4096_d128": {"source_digest": "d6514cb48c3fcb48", "bytes_per_launch": 8 * (201136640 + 111190784),
+    "attn_gqa_b16_s4096_d128": {"source_digest": "e2bf2e29b78c0df1", "bytes_per_launch": 8 * (199983616 + 110758144),
                                 "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
 }
 

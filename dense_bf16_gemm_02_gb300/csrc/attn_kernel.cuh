@@ -134,7 +134,7 @@ __device__ __forceinline__ bool attn_aborted(const AttnParams& p) {
 // local memory on every wait); the clock is read every 4096 probes (or after
 // each suspension), and only a wait that has lasted 20 µs calls out to check
 // the launch's abort flag (a global load) and the time limit.
-enum class Wait { kPoll, kPollCluster, kSuspend };
+enum class Wait { kPoll, kSuspend };
 
 // Returns true when the wait must give up (this launch was aborted, or the
 // time limit ran out; then it records `code` and aborts the launch).
@@ -153,7 +153,6 @@ __device__ __forceinline__ bool attn_wait(const AttnParams& p, uint32_t bar, uin
     for (uint32_t it = 1;; ++it) {
         bool done;
         if (mode == Wait::kSuspend) done = mbar_try_wait_suspend(bar, parity, 20000);
-        else if (mode == Wait::kPollCluster) done = mbar_test_wait_cluster(bar, parity);
         else done = mbar_test_wait(bar, parity);
         if (done) return true;
         if (mode == Wait::kSuspend || (it & 4095u) == 0) {

@@ -185,7 +185,7 @@ __device__ __noinline__ bool wait_bounded_slow(const GemmParams& p, uint32_t bar
                                                uint32_t code, bool cluster_scope) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if (cluster_scope ? mbar_try_wait_cluster_relaxed(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (aborted(p)) return false;
             if (global_timer_ns() - t0 > p.timeout_ns) {
@@ -204,10 +204,11 @@ __device__ __forceinline__ bool wait_bounded(const GemmParams& p, uint32_t bar, 
     return wait_bounded_slow(p, bar, parity, code, false);
 }
 
-// For barriers that the peer CTA's threads arrive on (cluster-scope acquire).
+// For barriers that the peer CTA's threads arrive on (relaxed at cluster scope,
+// as the arrives; they order tcgen05 operations only).
 __device__ __forceinline__ bool wait_bounded_cluster(const GemmParams& p, uint32_t bar, uint32_t parity,
                                                      uint32_t code) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (mbar_try_wait_cluster_relaxed(bar, parity)) return true;
     return wait_bounded_slow(p, bar, parity, code, true);
 }
 
@@ -638,7 +639,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) {
-                    if constexpr (kCG == 2) mbar_arrive_cluster(map_to_cta(acc_empty_bar(buf), 0));
+                    if constexpr (kCG == 2) mbar_arrive_cluster_relaxed(map_to_cta(acc_empty_bar(buf), 0));
                     else mbar_arrive(acc_empty_bar(buf));
                 }
 #pragma unroll
@@ -659,7 +660,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         tc_fence_before_sync();
                         __syncwarp();
                         if (lane == 0) {
-                            if constexpr (kCG == 2) mbar_arrive_cluster(map_to_cta(acc_empty_bar(buf), 0));
+                            if constexpr (kCG == 2) mbar_arrive_cluster_relaxed(map_to_cta(acc_empty_bar(buf), 0));
                             else mbar_arrive(acc_empty_bar(buf));
                         }
                     }

@@ -57,9 +57,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-// Arrive on a barrier given by its shared::cluster address (any CTA of the cluster).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+// Arrive on a barrier given by its shared::cluster address (any CTA of the
+// cluster), relaxed at cluster scope. For barriers that only order tcgen05
+// operations across threads: the arriving thread's
+// tcgen05.fence::before_thread_sync and the waiter's
+// tcgen05.fence::after_thread_sync order the Tensor Memory accesses, so no
+// generic memory is released. (With release semantics at cluster scope the
+// waiter was measured to see the phase complete about 1 µs later.)
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                  : "memory");
 }
 
@@ -93,18 +99,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // One probe that may suspend the thread for up to `hint_ns` nanoseconds while
 // the phase is incomplete; the thread resumes as soon as the phase completes.
 __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
@@ -119,13 +113,14 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
-// The same with acquire at cluster scope, for barriers that threads of the
-// peer CTA arrive on.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+// A probe of a barrier that threads of the peer CTA arrive on with
+// mbar_arrive_cluster_relaxed: relaxed at cluster scope, like the arrives
+// (the caller's tcgen05.fence::after_thread_sync orders what follows).
+__device__ __forceinline__ bool mbar_try_wait_cluster_relaxed(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.relaxed.cluster.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
