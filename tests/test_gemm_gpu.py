@@ -160,24 +160,56 @@ def test_stream_argument(hk):
     assert_bitexact(to_host(C), oracle.gemm(A, B), "side stream")
 
 
-def test_bounded_wait_reports_timeout_and_recovers(hk):
+# (label, M, N, K, plan options, expected kernel id, expected stages or 0, expected K splits)
+TIMEOUT_CASES = [
+    ("pair bf16", 512, 512, 512, {}, 1, 0, 1),
+    ("single 128x256, 16-row A stages", 1, 512, 512, {"kernel": 2}, 2, 6, 1),
+    ("single 128x256, 64-row A stages", 40, 512, 512, {"kernel": 2}, 2, 5, 1),
+    ("single 128x64", 100, 512, 512, {"kernel": 5}, 5, 0, 1),
+    ("single 128x256, split K", 64, 1024, 2048, {"kernel": 2, "split_k": 4}, 2, 0, 4),
+    ("pair bf16, split K", 512, 512, 2048, {"kernel": 1, "split_k": 2}, 1, 0, 2),
+    ("fp8 pair", 512, 512, 512, {"input_type": 1}, 1, 0, 1),
+    ("fp8 single 128x192", 128, 600, 512, {"input_type": 1, "kernel": 3}, 3, 0, 1),
+]
+
+
+@pytest.mark.parametrize("case", TIMEOUT_CASES, ids=[c[0] for c in TIMEOUT_CASES])
+def test_bounded_wait_reports_timeout_and_recovers(hk, case):
     """Fault injected on the host side of the protocol: the producer withholds
-    one arrival, the MMA issuer's bounded wait runs out, the kernel drains and
-    returns, the status word reports HK_ERR_TIMEOUT, and the context stays
-    usable."""
+    one arrival, a bounded wait runs out, every role of the kernel drains and
+    returns (pair and single-CTA kernels, short-A stages, split K with its
+    dependent reduction, E4M3), the status word reports HK_ERR_TIMEOUT, and
+    the context stays usable: the same plan without the fault is then exact."""
     import torch
-    A = synth.int_bf16(512, 512, 3)
-    B = synth.int_bf16(512, 512, 4)
-    At, _ = to_device(A)
-    Bt, _ = to_device(B)
-    C = torch.empty((512, 512), dtype=torch.bfloat16, device="cuda")
-    plan = hk.Plan(512, 512, 512, timeout_ns=20_000_000, flags=hk.HK_FLAG_FAULT_DROP_ARRIVE)
+    label, M, N, K, opts, kernel, stages, splits = case
+    fp8 = opts.get("input_type", 0) == hk.HK_INPUT_E4M3
+    if fp8:
+        A, B = synth.int_e4m3(M, K, 3 + M), synth.int_e4m3(N, K, 4 + N)
+        At, Bt = torch.from_numpy(A).to("cuda"), torch.from_numpy(B).to("cuda")
+        want = oracle.gemm_fp8(A, B, 1.0, 1.0)
+    else:
+        A, B = synth.int_bf16(M, K, 3 + M), synth.int_bf16(N, K, 4 + N)
+        At, _ = to_device(A)
+        Bt, _ = to_device(B)
+        want = oracle.gemm(A, B)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    plan = hk.Plan(M, N, K, timeout_ns=20_000_000, flags=hk.HK_FLAG_FAULT_DROP_ARRIVE, **opts)
+    info = plan.info()
+    assert info["kernel"] == kernel and info["split_k"] == splits, (label, info)
+    if stages:
+        assert info["stages"] == stages, (label, info)
     plan.run(At, Bt, C)
     torch.cuda.synchronize()
-    assert plan.device_status() == hk.HK_ERR_TIMEOUT
-    assert plan.device_status() == hk.HK_OK       # read-and-clear
+    assert plan.device_status() == hk.HK_ERR_TIMEOUT, label
+    assert plan.device_status() == hk.HK_OK, label       # read-and-clear
     plan.close()
-    assert_bitexact(to_host(hk.gemm(At, Bt)), oracle.gemm(A, B), "after timeout")
+    good = hk.Plan(M, N, K, **opts)
+    C.zero_()
+    good.run(At, Bt, C)
+    torch.cuda.synchronize()
+    assert good.device_status() == hk.HK_OK, label
+    good.close()
+    assert_bitexact(to_host(C), want, f"{label}: after timeout")
 
 
 # ------------------------------------------------------- full workloads --
