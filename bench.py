@@ -42,17 +42,17 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
 # sources whose digest is given; see profiles/.
 MEASURED_TRAFFIC = {
-    "gemm_8192": {"source_digest": "3c2dfb949bab1ad5", "bytes_per_launch": 1150159616 + 128739072,
+    "gemm_8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 1062652928 + 127742976,
                   "profile": "profiles/gemm_bf16_kernel_pair256_gemm_8192.md"},
-    "skinny_128x28672x8192": {"source_digest": "3c2dfb949bab1ad5", "bytes_per_launch": 471958528 + 3589120,
+    "skinny_128x28672x8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 471969536 + 3475200,
                               "profile": "profiles/gemm_bf16_kernel_single128x192_skinny_128x28672x8192.md"},
-    "fp8_gemm_8192": {"source_digest": "3c2dfb949bab1ad5", "bytes_per_launch": 345619712 + 117902848,
+    "fp8_gemm_8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 345377792 + 117171712,
                       "profile": "profiles/gemm_fp8_kernel_pair256_fp8_gemm_8192.md"},
     # the block-scaled GEMM kernel alone (the scale arrangement kernel moves ~8 MB more)
-    "mxfp8_gemm_8192": {"source_digest": "3c2dfb949bab1ad5", "bytes_per_launch": 354771712 + 116889344,
+    "mxfp8_gemm_8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 356308480 + 116700416,
                         "profile": "profiles/gemm_mxfp8_kernel_pair256_mxfp8_gemm_8192.md"},
     # the GEMM kernel alone (the split-K reduction reads the fp32 partials and writes C)
-    "decode_64x8192x28672": {"source_digest": "3c2dfb949bab1ad5", "bytes_per_launch": 473515264 + 3873280,
+    "decode_64x8192x28672": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 473515776 + 3584768,
                              "profile": "profiles/gemm_bf16_kernel_single_decode_shapes.md"},
     # attention: captured at B2 (one launch); the B16 figure scales it by 8 (traffic grows with B)
     "attn_gqa_b2_s4096_d128": {"source_digest": "e2bf2e29b78c0df1", "bytes_per_launch": 199983616 + 110758144,

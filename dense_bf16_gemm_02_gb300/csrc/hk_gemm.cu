@@ -869,9 +869,11 @@ size_t hk_gemm_mxfp8_workspace_size(int64_t M, int64_t N, int64_t K) {
     return mx_layout(M, N, K).total;
 }
 
-hk_status hk_gemm_mxfp8(const void* A, const void* B, const void* SFA, const void* SFB, void* C, int64_t M,
-                        int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldc,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+hk_status hk_gemm_mxfp8_ex(const void* A, const void* B, const void* SFA, const void* SFB, void* C, int64_t M,
+                           int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldc,
+                           void* workspace, size_t workspace_bytes, uint32_t flags, uint64_t timeout_ns,
+                           void* stream) {
+    if (flags & ~HK_FLAG_FAULT_DROP_ARRIVE) return fail(HK_ERR_INVALID_ARG, "unknown MXFP8 flags 0x%x", flags);
     hk_status s = check_shape(M, N, K, lda, ldb, ldc);
     if (s != HK_OK) return s;
     if (K % 32) return fail(HK_ERR_INVALID_ARG, "K=%lld is not a multiple of the scale block 32", (long long)K);
@@ -934,7 +936,8 @@ hk_status hk_gemm_mxfp8(const void* A, const void* B, const void* SFA, const voi
     g.n_pad = int64_t(g.tiles_n) * v->tile_n;
     g.n_tma = static_cast<int32_t>(N & ~int64_t(7));
     g.ldc = ldc;
-    g.timeout_ns = kDefaultTimeoutNs;
+    g.flags = flags;
+    g.timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
     g.tail_start = -1;
     g.total_units = g.num_tiles;
     if (units > g.total_units) units = g.total_units;
@@ -955,6 +958,13 @@ hk_status hk_gemm_mxfp8(const void* A, const void* B, const void* SFA, const voi
         if (e != cudaSuccess) return cuda_fail(HK_ERR_LAUNCH, "launching the MXFP8 scale arrangement", e);
     }
     return launch(&plan, &sw, A, B, C, nullptr, st, nullptr, K > 0 ? workspace : nullptr, lay.total);
+}
+
+hk_status hk_gemm_mxfp8(const void* A, const void* B, const void* SFA, const void* SFB, void* C, int64_t M,
+                        int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldc,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    return hk_gemm_mxfp8_ex(A, B, SFA, SFB, C, M, N, K, lda, ldb, ldsfa, ldsfb, ldc, workspace, workspace_bytes, 0u,
+                            0u, stream);
 }
 
 // ------------------------------------------------- no-allocation variant --

@@ -49,7 +49,7 @@ EXPORTED = (
     "hk_gemm_plan_run", "hk_gemm_plan_device_status", "hk_gemm_last_device_status",
     "hk_gemm_plan_destroy", "hk_status_string", "hk_gemm_last_error_string", "hk_gemm_bf16_noalloc",
     "hk_gemm_bf16_epilogue", "hk_gemm_plan_run_epilogue", "hk_gemm_fp8_e4m3",
-    "hk_attention_fwd", "hk_attention_fwd_ex", "hk_gemm_mxfp8", "hk_gemm_mxfp8_workspace_size",
+    "hk_attention_fwd", "hk_attention_fwd_ex", "hk_gemm_mxfp8", "hk_gemm_mxfp8_ex", "hk_gemm_mxfp8_workspace_size",
 )
 
 
@@ -128,6 +128,9 @@ def load() -> ctypes.CDLL:
         lib.hk_gemm_bf16_noalloc.restype = I32
         lib.hk_gemm_mxfp8.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I64, I64, I64, P, ctypes.c_size_t, P]
         lib.hk_gemm_mxfp8.restype = I32
+        lib.hk_gemm_mxfp8_ex.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I64, I64, I64, P, ctypes.c_size_t,
+                                         ctypes.c_uint32, ctypes.c_uint64, P]
+        lib.hk_gemm_mxfp8_ex.restype = I32
         lib.hk_gemm_mxfp8_workspace_size.argtypes = [I64, I64, I64]
         lib.hk_gemm_mxfp8_workspace_size.restype = ctypes.c_size_t
         lib.hk_attention_fwd.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I32, P]
@@ -169,6 +172,13 @@ def hk_gemm_mxfp8(A: int, B: int, SFA: int, SFB: int, C: int, M: int, N: int, K:
     """C (bf16) = block-scaled A·Bᵀ: E4M3 A (M×K), B (N×K), UE8M0 scales per 32 K elements."""
     return load().hk_gemm_mxfp8(A, B, SFA, SFB, C, M, N, K, lda, ldb, ldsfa, ldsfb, ldc, workspace or None,
                                 workspace_bytes, stream)
+
+
+def hk_gemm_mxfp8_ex(A: int, B: int, SFA: int, SFB: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                     ldsfa: int, ldsfb: int, ldc: int, workspace: int, workspace_bytes: int, flags: int = 0,
+                     timeout_ns: int = 0, stream: int = 0) -> int:
+    return load().hk_gemm_mxfp8_ex(A, B, SFA, SFB, C, M, N, K, lda, ldb, ldsfa, ldsfb, ldc, workspace or None,
+                                   workspace_bytes, flags, timeout_ns, stream)
 
 
 def hk_gemm_mxfp8_workspace_size(M: int, N: int, K: int) -> int:

@@ -218,6 +218,17 @@ hk_status hk_gemm_mxfp8(const void* A, const void* B, const void* SFA, const voi
                         int64_t lda, int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldc,
                         void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same with test and tuning controls: `flags` takes
+ * HK_FLAG_FAULT_DROP_ARRIVE (the producer withholds one arrival on the
+ * first stage, so a bounded wait runs out and the status word reports
+ * HK_ERR_TIMEOUT; other bits are rejected with HK_ERR_INVALID_ARG),
+ * `timeout_ns` bounds each wait (0: 1 s). */
+hk_status hk_gemm_mxfp8_ex(const void* A, const void* B, const void* SFA, const void* SFB, void* C,
+                           int64_t M, int64_t N, int64_t K,
+                           int64_t lda, int64_t ldb, int64_t ldsfa, int64_t ldsfb, int64_t ldc,
+                           void* workspace, size_t workspace_bytes, uint32_t flags, uint64_t timeout_ns,
+                           void* stream);
+
 /* Bytes of workspace hk_gemm_mxfp8 needs for this shape (0 when M, N or K is 0). */
 size_t hk_gemm_mxfp8_workspace_size(int64_t M, int64_t N, int64_t K);
 
@@ -227,7 +238,7 @@ size_t hk_gemm_mxfp8_workspace_size(int64_t M, int64_t N, int64_t K);
 hk_status hk_gemm_plan_device_status(hk_gemm_plan* plan);
 
 /* The same for the calls of the one-shot entry points (hk_gemm_bf16,
- * hk_gemm_bf16_epilogue, hk_gemm_fp8_e4m3, hk_gemm_mxfp8, hk_attention_fwd)
+ * hk_gemm_bf16_epilogue, hk_gemm_fp8_e4m3, hk_gemm_mxfp8(_ex), hk_attention_fwd(_ex))
  * on `device`. */
 hk_status hk_gemm_last_device_status(int device);
 

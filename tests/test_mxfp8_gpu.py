@@ -173,3 +173,38 @@ def test_mx_argument_errors(hk):
     assert need > 0
     assert hk.hk_gemm_mxfp8(p, p, p, p, p, 64, 64, 64, 64, 64, 2, 2, 64, p, need - 1, 0) == hk.HK_ERR_WORKSPACE
     assert hk.hk_gemm_mxfp8(p, p, p, p, p, 64, 64, 64, 64, 64, 1, 2, 64, p, need, 0) == hk.HK_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("M", [300, 100], ids=["pair_256x256", "single_128x192"])
+def test_mx_bounded_wait_reports_timeout_and_recovers(hk, oracle, M):
+    """Fault set on the host: the producer withholds one arrival, so the scale
+    copier's wait on that stage (and the MMA thread's behind it) runs out
+    after 20 ms; every role drains and returns, the status word reports
+    HK_ERR_TIMEOUT once, and the next call on the same context is exact.
+    Unknown flag bits are rejected."""
+    import torch
+    N, K = 260, 256
+    kb = K // 32
+    A, B = synth.int_e4m3(M, K, 2700 + M), synth.int_e4m3(N, K, 2800)
+    SA, SB = synth.mx_scales(M, kb, 2900, 126, 128), synth.mx_scales(N, kb, 3000, 126, 128)
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to("cuda")
+    a, b, sa, sb = dev(A), dev(B), dev(SA), dev(SB)
+    ldc = N + (-N) % 8
+    c = torch.zeros((M, ldc), dtype=torch.bfloat16, device="cuda")
+    nbytes = hk.hk_gemm_mxfp8_workspace_size(M, N, K)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
+    def call(flags, timeout_ns):
+        return hk.hk_gemm_mxfp8_ex(a.data_ptr(), b.data_ptr(), sa.data_ptr(), sb.data_ptr(), c.data_ptr(), M, N, K,
+                                   K, K, kb, kb, ldc, ws.data_ptr(), nbytes, flags, timeout_ns, 0)
+
+    assert call(hk.HK_FLAG_FAULT_DROP_ARRIVE, 20_000_000) == hk.HK_OK, hk.hk_gemm_last_error_string()
+    torch.cuda.synchronize()
+    assert hk.hk_gemm_last_device_status(0) == hk.HK_ERR_TIMEOUT
+    assert hk.hk_gemm_last_device_status(0) == hk.HK_OK   # read-and-clear
+    assert call(0, 0) == hk.HK_OK, hk.hk_gemm_last_error_string()
+    torch.cuda.synchronize()
+    assert hk.hk_gemm_last_device_status(0) == hk.HK_OK
+    got = c.view(torch.int16).cpu().numpy().view(np.uint16)[:, :N]
+    assert_bitexact(got, oracle.gemm_mxfp8(A, B, SA, SB), f"mxfp8 {M}x{N}x{K} after timeout")
+    assert call(0x4, 0) == hk.HK_ERR_INVALID_ARG
