@@ -643,3 +643,100 @@ def test_concurrent_streams_with_different_plans(hk):
     for i, C in enumerate(outs):
         assert_bitexact(to_host(C), refs[i % 2], f"stream {i % 2} rep {i // 2}")
     assert hk.hk_gemm_last_device_status(torch.cuda.current_device()) == hk.HK_OK
+
+
+# ------------------------------------------------ special values (IEEE) --
+
+def _exact_bf16(x: np.ndarray) -> np.ndarray:
+    """float64 values that bf16 holds exactly (incl. ±Inf, NaN, subnormals) -> bf16 bits."""
+    x = np.asarray(x, dtype=np.float64)
+    f = np.ascontiguousarray(x.astype(np.float32))
+    finite = np.isfinite(x)
+    assert np.array_equal(f[finite].astype(np.float64), x[finite]), "value not exact in fp32"
+    u = f.view(np.uint32)
+    assert not np.any(u[finite] & np.uint32(0xFFFF)), "value not exact in bf16"
+    return (u >> np.uint32(16)).astype(np.uint16)
+
+
+def _isnan_bf16(bits: np.ndarray) -> np.ndarray:
+    return ((bits & 0x7F80) == 0x7F80) & ((bits & 0x007F) != 0)
+
+
+def _gemm_bits(hk, A, B):
+    At, _ = to_device(A)
+    Bt, _ = to_device(B)
+    C = hk.gemm(At, Bt)
+    import torch
+    torch.cuda.synchronize()
+    assert hk.hk_gemm_last_device_status(torch.cuda.current_device()) == hk.HK_OK
+    return to_host(C)
+
+
+def _assert_same_ieee(got, want, what):
+    gn, wn = _isnan_bf16(got), _isnan_bf16(want)
+    assert np.array_equal(gn, wn), f"{what}: NaN at {np.argwhere(gn != wn)[:5].tolist()}"
+    assert np.array_equal(got[~gn], want[~wn]), f"{what}: differs at {np.argwhere((got != want) & ~gn)[:5].tolist()}"
+
+
+@pytest.mark.parametrize("M", [64, 300], ids=["single_cta", "cta_pair"])
+def test_subnormal_inputs_are_not_flushed(hk, M):
+    """A holds bf16 subnormals m·2^-133 (|m| ≤ 127), B holds k·2^100: every
+    product m·k·2^-33 is normal and every sum is exact in fp32, so C matches
+    the IEEE oracle bit for bit only if no subnormal input is flushed."""
+    N, K = 200, 256
+    g = np.random.Generator(np.random.PCG64(7100 + M))
+    a = g.integers(-127, 128, size=(M, K)).astype(np.float64) * 2.0 ** -133
+    b = g.integers(-4, 5, size=(N, K)).astype(np.float64) * 2.0 ** 100
+    A, B = _exact_bf16(a), _exact_bf16(b)
+    assert np.all((A & 0x7F80) == 0)                  # every input of A is subnormal or zero
+    want = oracle.gemm(A, B)
+    assert np.count_nonzero(want) > 0.9 * want.size
+    assert_bitexact(_gemm_bits(hk, A, B), want, f"subnormal A, M={M}")
+
+
+@pytest.mark.parametrize("M", [64, 300], ids=["single_cta", "cta_pair"])
+def test_inf_and_nan_propagate_like_ieee(hk, M):
+    """±Inf and NaN operands: Inf·k gives ±Inf, Inf·0 and Inf − Inf give NaN,
+    NaN poisons its row (and a NaN in B its column); the other entries stay
+    exact (integer data)."""
+    N, K = 200, 256
+    g = np.random.Generator(np.random.PCG64(7200 + M))
+    a = g.integers(-4, 5, size=(M, K)).astype(np.float64)
+    b = g.integers(-4, 5, size=(N, K)).astype(np.float64)
+    a[1, 5] = np.inf
+    a[2, 7] = -np.inf
+    a[3, 9] = np.nan
+    a[4, 11], a[4, 12] = np.inf, -np.inf
+    b[6, 20] = np.inf
+    b[7, 21] = np.nan
+    A, B = _exact_bf16(a), _exact_bf16(b)
+    want = oracle.gemm(A, B)
+    nan = _isnan_bf16(want)
+    assert nan.any() and np.any(want == 0x7F80) and np.any(want == 0xFF80) and (~nan).sum() > 0.9 * want.size
+    _assert_same_ieee(_gemm_bits(hk, A, B), want, f"Inf/NaN, M={M}")
+
+
+@pytest.mark.parametrize("M", [64, 300], ids=["single_cta", "cta_pair"])
+def test_overflow_at_the_bf16_rounding(hk, M):
+    """Sums that are finite in fp32 but round past the largest bf16
+    ((2 − 2^-7)·2^127) become ±Inf, including the exact tie
+    (2 − 2^-8)·2^127 (ties to even: the largest bf16 has an odd mantissa);
+    the largest bf16 itself and 2^127 stay finite; 2^128 overflows."""
+    N, K = 64, 8
+    big = (2.0 - 2.0 ** -7) * 2.0 ** 126
+    a = np.zeros((M, K))
+    a[0, :2] = [2.0 ** 127, big]        # sum with B row 0: (2 - 2^-8)·2^127, a tie -> +Inf
+    a[1, :2] = [big, big]               # (2 - 2^-7)·2^127: the largest bf16
+    a[2, :2] = [2.0 ** 127, 2.0 ** 127]  # 2^128: overflows
+    a[3, :2] = [-2.0 ** 127, -big]      # the negative tie -> -Inf
+    a[4:, :] = np.random.Generator(np.random.PCG64(7300 + M)).integers(-4, 5, size=(M - 4, K))
+    b = np.random.Generator(np.random.PCG64(7400 + M)).integers(-4, 5, size=(N, K)).astype(np.float64)
+    b[0, :2] = [1.0, 1.0]
+    b[1, :2] = [1.0, 0.0]               # row 0 of A: 2^127, finite
+    b[2, :2] = [0.5, 0.5]               # halves: all of rows 0-3 finite
+    b[:3, 2:] = 0.0
+    A, B = _exact_bf16(a), _exact_bf16(b)
+    want = oracle.gemm(A, B)
+    assert want[0, 0] == 0x7F80 and want[1, 0] == 0x7F7F and want[2, 0] == 0x7F80 and want[3, 0] == 0xFF80
+    assert want[0, 1] == 0x7F00 and want[2, 2] == 0x7F00
+    _assert_same_ieee(_gemm_bits(hk, A, B), want, f"overflow, M={M}")
