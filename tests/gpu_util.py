@@ -59,3 +59,15 @@ def assert_bitexact(got_bits: np.ndarray, ref_bits: np.ndarray, what: str = ""):
         raise AssertionError(f"{what}: {int((~same).sum())} of {same.size} entries differ; first {idx.tolist()}: "
                              f"got {[hex(int(x)) for x in got_bits[~same][:5]]} "
                              f"want {[hex(int(x)) for x in ref_bits[~same][:5]]}")
+
+
+def isnan_bf16(bits: np.ndarray) -> np.ndarray:
+    """NaN bit patterns of bf16 (any payload)."""
+    return ((bits & 0x7F80) == 0x7F80) & ((bits & 0x007F) != 0)
+
+
+def assert_same_ieee(got: np.ndarray, want: np.ndarray, what: str = ""):
+    """NaN in the same places (payloads may differ), every other entry bit-exact."""
+    gn, wn = isnan_bf16(got), isnan_bf16(want)
+    assert np.array_equal(gn, wn), f"{what}: NaN at {np.argwhere(gn != wn)[:5].tolist()}"
+    assert np.array_equal(got[~gn], want[~wn]), f"{what}: differs at {np.argwhere((got != want) & ~gn)[:5].tolist()}"

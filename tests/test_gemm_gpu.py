@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import SENTINEL, assert_bitexact, assert_close, to_device, to_host
+from gpu_util import SENTINEL, assert_bitexact, assert_close, assert_same_ieee, isnan_bf16, to_device, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -658,10 +658,6 @@ def _exact_bf16(x: np.ndarray) -> np.ndarray:
     return (u >> np.uint32(16)).astype(np.uint16)
 
 
-def _isnan_bf16(bits: np.ndarray) -> np.ndarray:
-    return ((bits & 0x7F80) == 0x7F80) & ((bits & 0x007F) != 0)
-
-
 def _gemm_bits(hk, A, B):
     At, _ = to_device(A)
     Bt, _ = to_device(B)
@@ -670,12 +666,6 @@ def _gemm_bits(hk, A, B):
     torch.cuda.synchronize()
     assert hk.hk_gemm_last_device_status(torch.cuda.current_device()) == hk.HK_OK
     return to_host(C)
-
-
-def _assert_same_ieee(got, want, what):
-    gn, wn = _isnan_bf16(got), _isnan_bf16(want)
-    assert np.array_equal(gn, wn), f"{what}: NaN at {np.argwhere(gn != wn)[:5].tolist()}"
-    assert np.array_equal(got[~gn], want[~wn]), f"{what}: differs at {np.argwhere((got != want) & ~gn)[:5].tolist()}"
 
 
 @pytest.mark.parametrize("M", [64, 300], ids=["single_cta", "cta_pair"])
@@ -711,9 +701,9 @@ def test_inf_and_nan_propagate_like_ieee(hk, M):
     b[7, 21] = np.nan
     A, B = _exact_bf16(a), _exact_bf16(b)
     want = oracle.gemm(A, B)
-    nan = _isnan_bf16(want)
+    nan = isnan_bf16(want)
     assert nan.any() and np.any(want == 0x7F80) and np.any(want == 0xFF80) and (~nan).sum() > 0.9 * want.size
-    _assert_same_ieee(_gemm_bits(hk, A, B), want, f"Inf/NaN, M={M}")
+    assert_same_ieee(_gemm_bits(hk, A, B), want, f"Inf/NaN, M={M}")
 
 
 @pytest.mark.parametrize("M", [64, 300], ids=["single_cta", "cta_pair"])
@@ -739,4 +729,26 @@ def test_overflow_at_the_bf16_rounding(hk, M):
     want = oracle.gemm(A, B)
     assert want[0, 0] == 0x7F80 and want[1, 0] == 0x7F7F and want[2, 0] == 0x7F80 and want[3, 0] == 0xFF80
     assert want[0, 1] == 0x7F00 and want[2, 2] == 0x7F00
-    _assert_same_ieee(_gemm_bits(hk, A, B), want, f"overflow, M={M}")
+    assert_same_ieee(_gemm_bits(hk, A, B), want, f"overflow, M={M}")
+
+
+@pytest.mark.parametrize("M", [64, 300], ids=["single_cta", "cta_pair"])
+def test_fp8_subnormal_and_nan_codes(hk, M):
+    """E4M3 subnormal operands (±m/8·2^-6) against small integers: every sum
+    is exact in fp32, so C matches the oracle bit for bit only if no
+    subnormal is flushed. The NaN codes S.1111.111 in A and in B poison
+    their row and column; the other entries stay exact."""
+    N, K = 200, 256
+    g = np.random.Generator(np.random.PCG64(7500 + M))
+    A = (g.integers(0, 8, size=(M, K)) | (g.integers(0, 2, size=(M, K)) << 7)).astype(np.uint8)
+    B = synth.int_e4m3(N, K, 7600 + M)
+    want = oracle.gemm_fp8(A, B, 1.0, 1.0)
+    assert np.count_nonzero(want) > 0.9 * want.size
+    assert_bitexact(run_fp8(hk, A, B, 1.0, 1.0), want, f"fp8 subnormal A, M={M}")
+    A2 = synth.int_e4m3(M, K, 7700 + M)
+    A2[1, 3], A2[2, 5] = 0x7F, 0xFF
+    B2 = B.copy()
+    B2[4, 7] = 0x7F
+    want = oracle.gemm_fp8(A2, B2, 1.0, 1.0)
+    assert isnan_bf16(want).any()
+    assert_same_ieee(run_fp8(hk, A2, B2, 1.0, 1.0), want, f"fp8 NaN codes, M={M}")

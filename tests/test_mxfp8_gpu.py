@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_util import assert_bitexact
+from gpu_util import assert_bitexact, assert_same_ieee, isnan_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -208,3 +208,30 @@ def test_mx_bounded_wait_reports_timeout_and_recovers(hk, oracle, M):
     got = c.view(torch.int16).cpu().numpy().view(np.uint16)[:, :N]
     assert_bitexact(got, oracle.gemm_mxfp8(A, B, SA, SB), f"mxfp8 {M}x{N}x{K} after timeout")
     assert call(0x4, 0) == hk.HK_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("M", [100, 300], ids=["single_128x192", "pair_256x256"])
+def test_mx_subnormal_and_nan_codes(hk, oracle, M):
+    """E4M3 subnormal operands against small integers with scales 2^-1..2^1:
+    exact in fp32, so bit-exact only if nothing is flushed. E4M3 NaN codes
+    in A and B, and the UE8M0 NaN scale (255) on one block of a row of A and
+    of a row of B, give NaN where IEEE arithmetic on the decoded values does
+    (a NaN scale poisons its whole row or column); the rest stays exact."""
+    N, K = 200, 128
+    kb = K // 32
+    g = np.random.Generator(np.random.PCG64(7800 + M))
+    A = (g.integers(0, 8, size=(M, K)) | (g.integers(0, 2, size=(M, K)) << 7)).astype(np.uint8)
+    B = synth.int_e4m3(N, K, 7900 + M)
+    SA, SB = synth.mx_scales(M, kb, 8000 + M, 126, 128), synth.mx_scales(N, kb, 8100, 126, 128)
+    want = oracle.gemm_mxfp8(A, B, SA, SB)
+    assert np.count_nonzero(want) > 0.9 * want.size
+    assert_bitexact(run_mx(hk, A, B, SA, SB), want, f"mxfp8 subnormal A, M={M}")
+    A2, B2 = synth.int_e4m3(M, K, 8200 + M), B.copy()
+    A2[1, 3] = 0x7F
+    B2[4, 40] = 0xFF
+    SA2, SB2 = SA.copy(), SB.copy()
+    SA2[5, 2] = 255
+    SB2[6, 1] = 255
+    want = oracle.gemm_mxfp8(A2, B2, SA2, SB2)
+    assert isnan_bf16(want[5]).all() and isnan_bf16(want[:, 6]).all()
+    assert_same_ieee(run_mx(hk, A2, B2, SA2, SB2), want, f"mxfp8 NaN codes and scale, M={M}")
