@@ -170,8 +170,36 @@ def pin_rounding(o):
     return None
 
 
+def pin_non_finite(o):
+    """IEEE 754 on non-finite values: ±Inf round to themselves and NaN to a
+    NaN; in a dot product Inf·k is ±Inf, Inf·0 and Inf + (−Inf) are NaN,
+    and a NaN operand makes its whole row NaN. Expected entries worked out
+    by hand from those rules."""
+    def is_nan(b):
+        return (b & 0x7F80) == 0x7F80 and (b & 0x7F) != 0
+    if o.round_bf16(float("inf")) != 0x7F80 or o.round_bf16(float("-inf")) != 0xFF80:
+        return "round_bf16(±inf)"
+    if not is_nan(o.round_bf16(float("nan"))):
+        return "round_bf16(nan) is not a NaN"
+    INF, NINF, NAN, ONE, TWO, ZERO, M1 = 0x7F80, 0xFF80, 0x7FC0, 0x3F80, 0x4000, 0x0000, 0xBF80
+    A = np.array([[INF, ONE], [INF, NINF], [NAN, ZERO], [ONE, TWO]], dtype=np.uint16)
+    B = np.array([[TWO, ONE], [ZERO, ONE], [M1, ZERO], [ONE, ONE]], dtype=np.uint16)
+    N_ = None   # a NaN entry
+    want = [[INF, N_, NINF, INF],           # Inf·2+1, Inf·0+1, Inf·(−1)+0, Inf+1
+            [N_, N_, N_, N_],               # Inf−Inf, NaN+(−Inf), −Inf+NaN, Inf−Inf
+            [N_, N_, N_, N_],               # NaN·anything
+            [0x4080, 0x4000, M1, 0x4040]]   # 4, 2, −1, 3
+    C = o.gemm(A, B)
+    for i in range(4):
+        for j in range(4):
+            w, g = want[i][j], int(C[i, j])
+            if (w is None and not is_nan(g)) or (w is not None and g != w):
+                return f"non-finite case C[{i},{j}] = {g:#06x}"
+    return None
+
+
 PINS = [pin_bruteforce, pin_ties, pin_identity_permutation, pin_closed_form, pin_invariants,
-        pin_integer, pin_rounding]
+        pin_integer, pin_rounding, pin_non_finite]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -226,6 +254,9 @@ MUTANTS = {
                    "s += fabs(bf16_bits_to_double(a[k])) * bf16_bits_to_double(b[k]);"),
     "via_binary32": ("double a = fabs(x);", "double a = (double)(float)fabs(x);"),
     "subnormal_quantum": ("int qexp = (E < -126 ? -126 : E) - 7;", "int qexp = E - 7;"),
+    "nan_as_inf": ("if (isnan(x)) return (uint16_t)(sign | 0x7FC0u);", "if (isnan(x)) return (uint16_t)(sign | 0x7F80u);"),
+    "nan_terms_skipped": ("s += bf16_bits_to_double(a[k]) * bf16_bits_to_double(b[k]);",
+                          "{ double t = bf16_bits_to_double(a[k]) * bf16_bits_to_double(b[k]); if (t == t) s += t; }"),
 }
 
 
