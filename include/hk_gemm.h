@@ -70,8 +70,9 @@ typedef enum hk_status {
 /* Plan flags (hk_gemm_config.flags). */
 #define HK_FLAG_NONE 0u
 /* Test only: the producer withholds its arrival on the first shared-memory
- * stage, so the MMA issuer's bounded wait runs out and the call reports
- * HK_ERR_TIMEOUT through the device status word. No GPU fault is caused. */
+ * stage, so a bounded wait on that stage runs out (the MMA issuer's; for
+ * MXFP8 the scale copier's) and the call reports HK_ERR_TIMEOUT through the
+ * device status word. No GPU fault is caused. */
 #define HK_FLAG_FAULT_DROP_ARRIVE 0x1u
 /* Keep the tiles of the last partial round whole (by default, when they fill
  * at most half of the CTA pairs, each runs as two 256x128 halves). */
