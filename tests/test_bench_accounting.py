@@ -61,3 +61,17 @@ def test_decode_workloads_are_hbm_bound_and_larger_than_l2():
         ai = bench.gemm_flops(w.M, w.N, w.K) / bench.gemm_bytes(w.M, w.N, w.K)
         assert ai < knee, name
         assert "larger than L2" in bench.workload_config(w)["l2"], name
+
+
+def test_source_digest_sees_code_not_comments():
+    """Stored ncu traffic stays valid across comment and layout edits of the
+    kernel sources, and only those: any change of code (a string literal
+    included) changes the text the digest is taken over."""
+    src = 'int f(int x) {  // add one\n    /* the sum */ return x + 1;\n}\nconst char* s = "a";\n'
+    same = 'int f(int x) {\n  return x + 1;   // different comment\n}\n/* block */ const char* s = "a";\n'
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(src.replace("x + 1", "x + 2"))
+    assert bench._code_only(src) != bench._code_only(src.replace('"a"', '"b"'))
+    for kind in ("gemm", "attention"):
+        d = bench.kernel_source_digest(kind)
+        assert len(d) == 16 and d == bench.kernel_source_digest(kind)
