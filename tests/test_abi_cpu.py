@@ -116,3 +116,35 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(hk_gemm, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         hk_gemm.load()
+
+
+def test_mxfp8_host_validation_without_gpu(lib):
+    """Argument checks of the block-scaled entry points run on the host,
+    before any device call; the workspace size is a host computation."""
+    from dense_bf16_gemm_02_gb300 import hk_gemm as h
+    P = 1 << 20
+    lib.hk_gemm_mxfp8_ex.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 8 + [
+        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_void_p]
+    lib.hk_gemm_mxfp8_ex.restype = ctypes.c_int32
+    lib.hk_gemm_mxfp8_workspace_size.argtypes = [ctypes.c_int64] * 3
+    lib.hk_gemm_mxfp8_workspace_size.restype = ctypes.c_size_t
+
+    def mx(M=64, N=64, K=64, lda=64, ldb=64, ldsa=2, ldsb=2, ldc=64, a=P, sa=P, ws=P, wsb=1 << 20, flags=0):
+        return lib.hk_gemm_mxfp8_ex(a, P, sa, P, P, M, N, K, lda, ldb, ldsa, ldsb, ldc, ws, wsb, flags, 0, None)
+
+    assert mx(flags=0x4) == h.HK_ERR_INVALID_ARG and b"flags" in lib.hk_gemm_last_error_string()
+    assert mx(K=48, lda=48, ldb=48) == h.HK_ERR_INVALID_ARG               # K not a multiple of 32
+    assert mx(K=32, lda=40, ldb=40) == h.HK_ERR_MISALIGNED                 # FP8 ld not a multiple of 16
+    assert mx(ldsa=1) == h.HK_ERR_INVALID_ARG                              # scale ld below K/32
+    assert mx(M=0) == h.HK_OK and mx(N=0) == h.HK_OK                       # nothing to do
+    assert mx(a=0) == h.HK_ERR_INVALID_ARG                                 # null operand
+    assert mx(sa=0) == h.HK_ERR_INVALID_ARG                                # null scales
+    need = lib.hk_gemm_mxfp8_workspace_size(64, 64, 64)
+    assert need > 0 and need % 256 == 0
+    assert mx(wsb=need - 1) == h.HK_ERR_WORKSPACE
+    assert mx(ws=P + 128, wsb=need) == h.HK_ERR_WORKSPACE                  # not 256-byte aligned
+    assert lib.hk_gemm_mxfp8_workspace_size(0, 64, 64) == 0
+    # more K blocks or more tiles never need less workspace
+    sizes = [lib.hk_gemm_mxfp8_workspace_size(m, n, k) for m, n, k in
+             [(64, 64, 128), (64, 64, 256), (64, 512, 256), (300, 512, 256), (8192, 8192, 8192)]]
+    assert sizes == sorted(sizes) and sizes[0] < sizes[-1]
