@@ -11,7 +11,7 @@ second operand used transposed as in the "ABt" GEMM of §7/§9.2:
 
     C[i, j] = RNE_bf16( Σ_k  A[i, k] · B[j, k] )      (sum in binary64)
 
-It also holds the fused-epilogue GEMM (bias + activation), the FP8 (E4M3)
+It also holds the fused-epilogue GEMM (bias + activation + residual), the FP8 (E4M3)
 GEMM with per-tensor scales, and the attention forward of the same page's
 "MHA fwd" / "GQA fwd" rows (softmax(Q·Kᵀ/√D)·V, bf16 in and out).
 
@@ -81,6 +81,12 @@ def _load():
             lib.oracle_gemm_bf16_epilogue_entries.argtypes = [_P, _P, _P, _P, _I64, _I64, _I64, ctypes.c_int,
                                                               _P, _P, _I64, ctypes.c_int]
             lib.oracle_gemm_bf16_epilogue_entries.restype = ctypes.c_int
+            lib.oracle_gemm_bf16_fused.argtypes = [_P, _P, _P, _P, _I64, _P, _I64, _I64, _I64, _I64, _I64, _I64,
+                                                   ctypes.c_int, ctypes.c_int]
+            lib.oracle_gemm_bf16_fused.restype = ctypes.c_int
+            lib.oracle_gemm_bf16_fused_entries.argtypes = [_P, _P, _P, _P, _I64, _P, _I64, _I64, _I64, ctypes.c_int,
+                                                           _P, _P, _I64, ctypes.c_int]
+            lib.oracle_gemm_bf16_fused_entries.restype = ctypes.c_int
             lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_to_double.restype = ctypes.c_double
             lib.oracle_gemm_fp8e4m3.argtypes = [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, ctypes.c_double,
@@ -203,33 +209,60 @@ def _bias_ptr(bias, N):
     return bias, bias.ctypes.data
 
 
-def gemm_epilogue(A: np.ndarray, B: np.ndarray, bias=None, act: int = ACT_NONE, threads: int = 0) -> np.ndarray:
-    """C = RNE_bf16(act(A·Bᵀ + bias)), bias a length-N bf16 vector or None."""
+def _residual(residual, M, N):
+    """(array kept alive, pointer, leading dimension in elements) of an M×N bf16 residual, or (None, None, 0)."""
+    if residual is None:
+        return None, None, 0
+    if residual.dtype != np.uint16 or residual.ndim != 2 or residual.shape != (M, N):
+        raise TypeError(f"residual must be an {M}x{N} uint16 array of bf16 bit patterns")
+    if N > 1 and residual.strides[1] != 2 or residual.strides[0] % 2:
+        raise ValueError("residual must have a unit stride along N")
+    return residual, _ptr(residual), max(residual.strides[0] // 2, N)
+
+
+def gemm_epilogue(A: np.ndarray, B: np.ndarray, bias=None, act: int = ACT_NONE, threads: int = 0,
+                  residual=None) -> np.ndarray:
+    """C = RNE_bf16(act(A·Bᵀ + bias) + R), bias a length-N bf16 vector or None,
+    R (``residual``) an M×N bf16 matrix or None."""
     A = _as_bits(A, "A")
     B = _as_bits(B, "B")
     M, K = A.shape
     N = B.shape[0]
     keep, bptr = _bias_ptr(bias, N)
+    keep_r, rptr, ldr = _residual(residual, M, N)
     C = np.zeros((M, N), dtype=np.uint16)
     if M and N:
-        _load().oracle_gemm_bf16_epilogue(_ptr(A), _ptr(B), bptr, _ptr(C), M, N, K, max(A.strides[0] // 2, K),
-                                          max(B.strides[0] // 2, K), N, int(act), int(threads))
+        if rptr is None:
+            _load().oracle_gemm_bf16_epilogue(_ptr(A), _ptr(B), bptr, _ptr(C), M, N, K, max(A.strides[0] // 2, K),
+                                              max(B.strides[0] // 2, K), N, int(act), int(threads))
+        else:
+            _load().oracle_gemm_bf16_fused(_ptr(A), _ptr(B), bptr, rptr, ldr, _ptr(C), M, N, K,
+                                           max(A.strides[0] // 2, K), max(B.strides[0] // 2, K), N, int(act),
+                                           int(threads))
     return C
 
 
 def gemm_epilogue_entries(A: np.ndarray, B: np.ndarray, rows, cols, bias=None, act: int = ACT_NONE,
-                          threads: int = 0) -> np.ndarray:
-    """Entries of RNE_bf16(act(A·Bᵀ + bias)) at (rows[t], cols[t])."""
+                          threads: int = 0, residual=None) -> np.ndarray:
+    """Entries of RNE_bf16(act(A·Bᵀ + bias) + R) at (rows[t], cols[t])."""
     A = _as_bits(A, "A")
     B = _as_bits(B, "B")
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     cols = np.ascontiguousarray(np.asarray(cols, dtype=np.int64))
     keep, bptr = _bias_ptr(bias, B.shape[0])
+    keep_r, rptr, ldr = _residual(residual, A.shape[0], B.shape[0])
     out = np.zeros(rows.size, dtype=np.uint16)
     if rows.size:
-        _load().oracle_gemm_bf16_epilogue_entries(_ptr(A), _ptr(B), bptr, _ptr(out), A.shape[1],
-                                                  A.strides[0] // 2, B.strides[0] // 2, int(act), _ptr(rows),
-                                                  _ptr(cols), rows.size, int(threads))
+        if rows.min() < 0 or rows.max() >= A.shape[0] or cols.min() < 0 or cols.max() >= B.shape[0]:
+            raise IndexError("entry index out of range")
+        if rptr is None:
+            _load().oracle_gemm_bf16_epilogue_entries(_ptr(A), _ptr(B), bptr, _ptr(out), A.shape[1],
+                                                      A.strides[0] // 2, B.strides[0] // 2, int(act), _ptr(rows),
+                                                      _ptr(cols), rows.size, int(threads))
+        else:
+            _load().oracle_gemm_bf16_fused_entries(_ptr(A), _ptr(B), bptr, rptr, ldr, _ptr(out), A.shape[1],
+                                                   A.strides[0] // 2, B.strides[0] // 2, int(act), _ptr(rows),
+                                                   _ptr(cols), rows.size, int(threads))
     return out
 
 

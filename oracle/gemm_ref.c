@@ -99,7 +99,15 @@ double oracle_dot_f64(const uint16_t* A, const uint16_t* B, int64_t K,
  *   1 ReLU:  max(x, 0)
  *   2 GELU:  x * Phi(x) = 0.5 * x * (1 + erf(x / sqrt(2)))   (the exact, erf form)
  *   3 SiLU:  x * sigmoid(x) = x / (1 + exp(-x))
- * all evaluated in binary64 before the single rounding to bf16. */
+ * all evaluated in binary64 before the single rounding to bf16.
+ *
+ * Residual add (the fused epilogue's third step; the HipKittens "L2" detail
+ * page, §8 "Deployment context", Fusion scope, names the residual add among
+ * the memory-bound operations the pages keep in a kernel of their own):
+ *   C[i][j] = round_bf16_rne( act( sum_k A[i][k] * B[j][k] + bias[j] ) + R[i][j] )
+ * R an M x N bf16 matrix with leading dimension ldr, added after the
+ * activation (the residual stream of a transformer block takes the block's
+ * output unchanged), still in binary64 and still before the one rounding. */
 double oracle_activation(double x, int act) {
     switch (act) {
         case 1: return x > 0.0 ? x : 0.0;
@@ -122,15 +130,19 @@ typedef struct {
     const int64_t* cols;   /* entry mode only */
     int64_t begin, end;    /* range of work items for this thread */
     int mode;              /* 0: full rows, 1: single entries */
+    const uint16_t* res;   /* epilogue: residual R (bf16, M x N, leading dimension ldr) or NULL */
+    int64_t ldr;
 } work_t;
 
-/* One output entry: the dot product, then (if requested) bias and activation. */
+/* One output entry: the dot product, then (if requested) bias and
+ * activation, then (if requested) the residual. */
 static uint16_t entry(const work_t* w, int64_t i, int64_t j) {
     double x = oracle_dot_f64(w->A, w->B, w->K, w->lda, w->ldb, i, j);
     if (w->bias || w->act) {
         if (w->bias) x += bf16_bits_to_double(w->bias[j]);
         x = oracle_activation(x, w->act);
     }
+    if (w->res) x += bf16_bits_to_double(w->res[i * w->ldr + j]);
     return oracle_round_bf16(x);
 }
 
@@ -186,7 +198,7 @@ static int run_parallel(work_t base, int64_t items, int threads) {
 int oracle_gemm_bf16(const uint16_t* A, const uint16_t* B, uint16_t* C,
                      int64_t M, int64_t N, int64_t K,
                      int64_t lda, int64_t ldb, int64_t ldc, int threads) {
-    work_t w = {A, B, C, NULL, 0, N, K, lda, ldb, ldc, NULL, NULL, 0, 0, 0};
+    work_t w = {A, B, C, NULL, 0, N, K, lda, ldb, ldc, NULL, NULL, 0, 0, 0, NULL, 0};
     return run_parallel(w, M, threads);
 }
 
@@ -195,7 +207,7 @@ int oracle_gemm_bf16(const uint16_t* A, const uint16_t* B, uint16_t* C,
 int oracle_gemm_bf16_rows(const uint16_t* A, const uint16_t* B, uint16_t* out,
                           int64_t N, int64_t K, int64_t lda, int64_t ldb,
                           const int64_t* rows, int64_t nrows, int threads) {
-    work_t w = {A, B, out, NULL, 0, N, K, lda, ldb, N, rows, NULL, 0, 0, 0};
+    work_t w = {A, B, out, NULL, 0, N, K, lda, ldb, N, rows, NULL, 0, 0, 0, NULL, 0};
     return run_parallel(w, nrows, threads);
 }
 
@@ -204,7 +216,7 @@ int oracle_gemm_bf16_entries(const uint16_t* A, const uint16_t* B, uint16_t* out
                              int64_t K, int64_t lda, int64_t ldb,
                              const int64_t* rows, const int64_t* cols, int64_t count,
                              int threads) {
-    work_t w = {A, B, out, NULL, 0, 0, K, lda, ldb, 0, rows, cols, 0, 0, 1};
+    work_t w = {A, B, out, NULL, 0, 0, K, lda, ldb, 0, rows, cols, 0, 0, 1, NULL, 0};
     return run_parallel(w, count, threads);
 }
 
@@ -212,7 +224,7 @@ int oracle_gemm_bf16_entries(const uint16_t* A, const uint16_t* B, uint16_t* out
 int oracle_gemm_bf16_epilogue(const uint16_t* A, const uint16_t* B, const uint16_t* bias, uint16_t* C,
                               int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                               int act, int threads) {
-    work_t w = {A, B, C, bias, act, N, K, lda, ldb, ldc, NULL, NULL, 0, 0, 0};
+    work_t w = {A, B, C, bias, act, N, K, lda, ldb, ldc, NULL, NULL, 0, 0, 0, NULL, 0};
     return run_parallel(w, M, threads);
 }
 
@@ -220,7 +232,24 @@ int oracle_gemm_bf16_epilogue(const uint16_t* A, const uint16_t* B, const uint16
 int oracle_gemm_bf16_epilogue_entries(const uint16_t* A, const uint16_t* B, const uint16_t* bias,
                                       uint16_t* out, int64_t K, int64_t lda, int64_t ldb, int act,
                                       const int64_t* rows, const int64_t* cols, int64_t count, int threads) {
-    work_t w = {A, B, out, bias, act, 0, K, lda, ldb, 0, rows, cols, 0, 0, 1};
+    work_t w = {A, B, out, bias, act, 0, K, lda, ldb, 0, rows, cols, 0, 0, 1, NULL, 0};
+    return run_parallel(w, count, threads);
+}
+
+/* Full GEMM with bias, activation and residual:
+ * C = round(act(A * B^T + bias) + R); bias and R may each be NULL. */
+int oracle_gemm_bf16_fused(const uint16_t* A, const uint16_t* B, const uint16_t* bias, const uint16_t* R,
+                           int64_t ldr, uint16_t* C, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                           int64_t ldc, int act, int threads) {
+    work_t w = {A, B, C, bias, act, N, K, lda, ldb, ldc, NULL, NULL, 0, 0, 0, R, ldr};
+    return run_parallel(w, M, threads);
+}
+
+/* Selected entries of the same. */
+int oracle_gemm_bf16_fused_entries(const uint16_t* A, const uint16_t* B, const uint16_t* bias, const uint16_t* R,
+                                   int64_t ldr, uint16_t* out, int64_t K, int64_t lda, int64_t ldb, int act,
+                                   const int64_t* rows, const int64_t* cols, int64_t count, int threads) {
+    work_t w = {A, B, out, bias, act, 0, K, lda, ldb, 0, rows, cols, 0, 0, 1, R, ldr};
     return run_parallel(w, count, threads);
 }
 

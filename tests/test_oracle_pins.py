@@ -392,6 +392,141 @@ def test_epilogue_mutants_fail_pins(tmp_path, name):
         f"mutant {name} passed the epilogue pins"
 
 
+# ------------------------------------------------- fused residual add --
+
+def pin_residual(o):
+    """The residual R is added after the activation, per (row, column), before
+    the one rounding. Exact rational sums on a tiny non-square shape with a
+    padded leading dimension for R (a transposed or mis-strided R reads other
+    values); ReLU on sums that are negative where R is positive (so adding R
+    before the activation gives another value); A = 0 gives RNE(act(bias) + R)
+    for every activation; integer data against int64 arithmetic."""
+    if not hasattr(o, "gemm_fused"):
+        return "no residual entry"
+    M, N, K = 5, 7, 9
+    A = synth.normal_bf16(M, K, 191)
+    B = synth.normal_bf16(N, K, 192)
+    bias = synth.normal_bf16(1, N, 193, 2.0)[0]
+    Rstore = synth.normal_bf16(M, N + 9, 194, 3.0)      # leading dimension 16 > N
+    R = Rstore[:, :N]
+    Af = [[bits_to_fraction(int(x)) for x in r] for r in A]
+    Bf = [[bits_to_fraction(int(x)) for x in r] for r in B]
+    dots = [[sum(Af[i][k] * Bf[j][k] for k in range(K)) for j in range(N)] for i in range(M)]
+    for act in (0, 1):
+        want = np.zeros((M, N), dtype=np.uint16)
+        for i in range(M):
+            for j in range(N):
+                x = dots[i][j] + bits_to_fraction(int(bias[j]))
+                if act == 1:
+                    x = max(x, Fraction(0))
+                want[i, j] = round_fraction(x + bits_to_fraction(int(R[i, j])))
+        if not np.array_equal(o.gemm_fused(A, B, bias, R, act), want):
+            return f"act {act}: act(dot + bias) + R is not exact"
+    # no bias, no activation: only the residual
+    want = np.array([[round_fraction(dots[i][j] + bits_to_fraction(int(R[i, j]))) for j in range(N)]
+                     for i in range(M)], dtype=np.uint16)
+    if not np.array_equal(o.gemm_fused(A, B, None, R, 0), want):
+        return "dot + R is not exact"
+    Z = np.zeros_like(A)
+    for act in (1, 2, 3):
+        got = o.gemm_fused(Z, B, bias, R, act)
+        ref = np.array([[round_fraction(Fraction(o.activation(float(bits_to_fraction(int(bias[j]))), act))
+                                        + bits_to_fraction(int(R[i, j]))) for j in range(N)] for i in range(M)],
+                       dtype=np.uint16)
+        if not np.array_equal(got, ref):
+            return f"A = 0 with act {act}"
+    Ai, Bi = synth.int_bf16(6, 40, 195), synth.int_bf16(8, 40, 196)
+    bi, Ri = synth.int_bf16(1, 8, 197)[0], synth.int_bf16(6, 8, 198, -40, 40)
+    ref = synth.bf16_bits_to_f32(Ai).astype(np.int64) @ synth.bf16_bits_to_f32(Bi).astype(np.int64).T
+    ref = np.maximum(ref + synth.bf16_bits_to_f32(bi).astype(np.int64), 0) + synth.bf16_bits_to_f32(Ri).astype(np.int64)
+    want = np.array([[round_fraction(Fraction(int(v))) for v in r] for r in ref], dtype=np.uint16)
+    if not np.array_equal(o.gemm_fused(Ai, Bi, bi, Ri, 1), want):
+        return "ReLU + residual on integers"
+    return None
+
+
+def test_residual_pin(oracle_lib):
+    assert pin_residual(_FusedView(oracle_lib)) is None
+
+
+def test_residual_entries_agree_with_full():
+    import oracle
+    M, N, K = 37, 29, 50
+    A, B = synth.normal_bf16(M, K, 181), synth.normal_bf16(N, K, 182)
+    bias, R = synth.normal_bf16(1, N, 183)[0], synth.normal_bf16(M, N, 184)
+    full = oracle.gemm_epilogue(A, B, bias, 2, residual=R)
+    rows, cols = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    got = oracle.gemm_epilogue_entries(A, B, rows.ravel(), cols.ravel(), bias, 2, residual=R)
+    assert np.array_equal(got.reshape(M, N), full)
+    # without a residual the fused function is the epilogue GEMM
+    assert np.array_equal(oracle.gemm_epilogue(A, B, bias, 2), oracle.gemm_epilogue(A, B, bias, 2, residual=None))
+
+
+class _FusedView:
+    """The package oracle seen through the interface the residual pin uses."""
+
+    def __init__(self, lib):
+        import oracle
+        self._o = oracle
+
+    def activation(self, x, act):
+        return self._o.activation(x, act)
+
+    def gemm_fused(self, A, B, bias, R, act):
+        return self._o.gemm_epilogue(A, B, bias, act, residual=R)
+
+
+RESIDUAL_MUTANTS = {
+    "residual_transposed": ("x += bf16_bits_to_double(w->res[i * w->ldr + j]);",
+                            "x += bf16_bits_to_double(w->res[j * w->ldr + i]);"),
+    "residual_ld_ignored": ("x += bf16_bits_to_double(w->res[i * w->ldr + j]);",
+                            "x += bf16_bits_to_double(w->res[i * w->N + j]);"),
+    "residual_subtracted": ("x += bf16_bits_to_double(w->res[i * w->ldr + j]);",
+                            "x -= bf16_bits_to_double(w->res[i * w->ldr + j]);"),
+    "residual_before_activation": (
+        "        x = oracle_activation(x, w->act);\n    }\n    if (w->res) x += bf16_bits_to_double(w->res[i * w->ldr + j]);",
+        "        if (w->res) x += bf16_bits_to_double(w->res[i * w->ldr + j]);\n        x = oracle_activation(x, w->act);\n    }"),
+    "residual_dropped_when_no_epilogue": ("    if (w->res) x += bf16_bits_to_double(w->res[i * w->ldr + j]);",
+                                          "    if (w->res && (w->bias || w->act)) x += bf16_bits_to_double(w->res[i * w->ldr + j]);"),
+    "residual_rounded_separately": (
+        "    if (w->res) x += bf16_bits_to_double(w->res[i * w->ldr + j]);",
+        "    if (w->res) x = bf16_bits_to_double(oracle_round_bf16(x)) + bf16_bits_to_double(w->res[i * w->ldr + j]);"),
+}
+
+
+class _ResLib(_EpiLib):
+    def __init__(self, path):
+        super().__init__(path)
+        P, I = ctypes.c_void_p, ctypes.c_int64
+        self.lib.oracle_gemm_bf16_fused.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I, ctypes.c_int, ctypes.c_int]
+
+    def gemm_fused(self, A, B, bias, R, act):
+        A = np.ascontiguousarray(A, dtype=np.uint16)
+        B = np.ascontiguousarray(B, dtype=np.uint16)
+        M, K = A.shape
+        N = B.shape[0]
+        ldr = R.strides[0] // 2
+        C = np.zeros((M, N), dtype=np.uint16)
+        bptr = None if bias is None else np.ascontiguousarray(bias, dtype=np.uint16)
+        self.lib.oracle_gemm_bf16_fused(A.ctypes.data, B.ctypes.data, None if bptr is None else bptr.ctypes.data,
+                                        R.ctypes.data, ldr, C.ctypes.data, M, N, K, K, K, N, act, 1)
+        return C
+
+
+@pytest.mark.parametrize("name", sorted(RESIDUAL_MUTANTS))
+def test_residual_mutants_fail_pins(tmp_path, name):
+    src = open(os.path.join(ROOT, "oracle", "gemm_ref.c")).read()
+    old, new = RESIDUAL_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    path_c = tmp_path / f"{name}.c"
+    path_so = tmp_path / f"{name}.so"
+    path_c.write_text(src.replace(old, new))
+    subprocess.run(["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+                    "-D_GNU_SOURCE", str(path_c), "-o", str(path_so), "-lm"], check=True)
+    mutant = _ResLib(str(path_so))
+    assert pin_residual(mutant) is not None, f"mutant {name} passed the residual pin"
+
+
 # ------------------------------------------------------------ FP8 (E4M3) --
 
 def pin_e4m3_decode(o):
