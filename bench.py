@@ -40,25 +40,19 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 
 # DRAM traffic of one launch of the GEMM kernel from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only for the kernel
-# sources whose digest is given; see profiles/.
+# sources whose digest is given (the code of those sources, comments and
+# layout excluded).
 MEASURED_TRAFFIC = {
-    "gemm_8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 1062652928 + 127742976,
-                  "profile": "profiles/gemm_bf16_kernel_pair256_gemm_8192.md"},
-    "skinny_128x28672x8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 471969536 + 3475200,
-                              "profile": "profiles/gemm_bf16_kernel_single128x192_skinny_128x28672x8192.md"},
-    "fp8_gemm_8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 345377792 + 117171712,
-                      "profile": "profiles/gemm_fp8_kernel_pair256_fp8_gemm_8192.md"},
+    "gemm_8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 1062652928 + 127742976},
+    "skinny_128x28672x8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 471969536 + 3475200},
+    "fp8_gemm_8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 345377792 + 117171712},
     # the block-scaled GEMM kernel alone (the scale arrangement kernel moves ~8 MB more)
-    "mxfp8_gemm_8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 356308480 + 116700416,
-                        "profile": "profiles/gemm_mxfp8_kernel_pair256_mxfp8_gemm_8192.md"},
+    "mxfp8_gemm_8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 356308480 + 116700416},
     # the GEMM kernel alone (the split-K reduction reads the fp32 partials and writes C)
-    "decode_64x8192x28672": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 473515776 + 3584768,
-                             "profile": "profiles/gemm_bf16_kernel_single_decode_shapes.md"},
+    "decode_64x8192x28672": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 473515776 + 3584768},
     # attention: captured at B2 (one launch); the B16 figure scales it by 8 (traffic grows with B)
-    "attn_gqa_b2_s4096_d128": {"source_digest": "e2bf2e29b78c0df1", "bytes_per_launch": 199983616 + 110758144,
-                               "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
-    "attn_gqa_b16_s4096_d128": {"source_digest": "e2bf2e29b78c0df1", "bytes_per_launch": 8 * (199983616 + 110758144),
-                                "profile": "profiles/attn_fwd_kernel_d128_attn_gqa_b16_s4096_d128.md"},
+    "attn_gqa_b2_s4096_d128": {"source_digest": "e2bf2e29b78c0df1", "bytes_per_launch": 199983616 + 110758144},
+    "attn_gqa_b16_s4096_d128": {"source_digest": "e2bf2e29b78c0df1", "bytes_per_launch": 8 * (199983616 + 110758144)},
 }
 
 
@@ -238,7 +232,8 @@ def operands_of(w):
     return synth.operands_fp8(w) if is_fp8(w) else synth.operands(w)
 
 
-def oracle_rows_timed(A, B, rows) -> tuple[float, int]:
+def oracle_rows_timed(A, B, rows, with_values: bool = False):
+    """Time the oracle on full rows of C; returns (seconds, threads used[, the rows' bf16 bits])."""
     import oracle
     t0 = time.perf_counter()
     if A.dtype == np.uint8:      # FP8 operands: full rows as entries
@@ -246,24 +241,67 @@ def oracle_rows_timed(A, B, rows) -> tuple[float, int]:
         rr = np.repeat(np.asarray(rows, dtype=np.int64), N)
         cc = np.tile(np.arange(N, dtype=np.int64), len(rows))
         sa, sb = synth.FP8_SCALES
-        oracle.gemm_fp8_entries(A, B, rr, cc, sa, sb)
+        vals = oracle.gemm_fp8_entries(A, B, rr, cc, sa, sb).reshape(len(rows), N)
         used = os.cpu_count() or 1
     else:
-        _, used = oracle.gemm_rows(A, B, rows)
-    return time.perf_counter() - t0, used
+        vals, used = oracle.gemm_rows(A, B, rows)
+    dt = time.perf_counter() - t0
+    return (dt, used, vals) if with_values else (dt, used)
 
 
-def cpu_baseline(w, A, B, budget_s: float = 15.0) -> dict:
-    """The oracle, as it stands, on full rows of this workload's C."""
+def oracle_entries_timed(A, B, rows, cols):
+    """Time the oracle on single entries of C; returns (seconds, the entries' bf16 bits)."""
+    import oracle
+    t0 = time.perf_counter()
+    if A.dtype == np.uint8:
+        sa, sb = synth.FP8_SCALES
+        vals = oracle.gemm_fp8_entries(A, B, rows, cols, sa, sb)
+    else:
+        vals, _ = oracle.gemm_entries(A, B, rows, cols)
+    return time.perf_counter() - t0, vals
+
+
+def parity_tolerance(ref_bits: np.ndarray, K: int, sigma_ab: float) -> np.ndarray:
+    """Per-entry bound |C_gpu − C_ref| ≤ 2⁻⁷·|C_ref| + 2⁻¹²·√K·σ_A·σ_B
+    (σ_A·σ_B = ``sigma_ab``, the generator's nominal standard deviations, times
+    the FP8 scales where they apply): one bf16 ulp of the value for a
+    rounding-boundary flip, plus fp32 cancellation near 0."""
+    ref = synth.bf16_bits_to_f32(ref_bits).astype(np.float64)
+    return 2.0 ** -7 * np.abs(ref) + 2.0 ** -12 * np.sqrt(max(K, 1)) * sigma_ab
+
+
+def cpu_baseline(w, A, B, C_gpu=None, budget_s: float = 15.0):
+    """The oracle, as it stands, on full rows of this workload's C plus 1024
+    seeded single entries (tile edges included). The rows and entries it
+    computes are then compared with the GPU's C of the timed run (``C_gpu``,
+    host bf16 bits), entry by entry within the parity tolerance: a miss fails
+    the bench. Returns (the baseline, the check or None)."""
     probe = np.arange(min(64, w.M), dtype=np.int64)   # enough rows to occupy every host core
     t, _ = oracle_rows_timed(A, B, probe)
     per_row = max(t / len(probe), 1e-6)
     nrows = int(max(1, min(w.M, budget_s / per_row)))
     rows = np.arange(nrows, dtype=np.int64)
-    t, used = oracle_rows_timed(A, B, rows)
-    tflops = gemm_flops(nrows, w.N, w.K) / t / 1e12
-    return {"value": tflops, "unit": UNIT, "cores": used, "kind": "oracle",
-            "sample": f"rows 0..{nrows - 1} of C ({nrows}x{w.N}x{w.K}, fp64 C oracle, {t:.1f} s)"}
+    t, used, row_vals = oracle_rows_timed(A, B, rows, with_values=True)
+    er, ec = synth.sample_positions(w.M, w.N, 3000 + w.wid, count=1024)
+    te, ent_vals = oracle_entries_timed(A, B, er, ec)
+    tflops = (gemm_flops(nrows, w.N, w.K) + gemm_flops(len(er), 1, w.K)) / (t + te) / 1e12
+    base = {"value": tflops, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": f"rows 0..{nrows - 1} of C ({nrows}x{w.N}x{w.K}) and {len(er)} seeded entries "
+                      f"(tile edges included), fp64 C oracle, {t + te:.1f} s"}
+    if C_gpu is None:
+        return base, None
+    got = np.concatenate([C_gpu[:nrows].ravel(), C_gpu[er, ec]])
+    ref = np.concatenate([row_vals.ravel(), ent_vals])
+    sigma_ab = float(np.prod(synth.FP8_SCALES)) if is_fp8(w) else w.scale * w.scale
+    err = np.abs(synth.bf16_bits_to_f32(got).astype(np.float64) - synth.bf16_bits_to_f32(ref).astype(np.float64))
+    tol = parity_tolerance(ref, w.K, sigma_ab)
+    bad = ~(err <= tol)
+    check = {"entries": int(got.size), "full_rows": nrows, "sampled_entries": int(len(er)), "misses": int(bad.sum()),
+             "max_err_over_tol": float(np.max(err / tol)),
+             "tolerance": "2^-7·|C_ref| + 2^-12·sqrt(K)·σ_A·σ_B per entry, against the fp64 oracle"}
+    if bad.any():
+        raise RuntimeError(f"parity check of the timed run's C against the oracle failed: {check}")
+    return base, check
 
 
 def run_reference(args, w):
@@ -560,7 +598,9 @@ def run_hk(args, w):
         "context_cublas": cublas,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, A_bits, B_bits)
+        C_host = C.view(torch.int16).cpu().numpy().view(np.uint16)   # the device C of the timed steps
+        line["cpu_baseline"], line["parity_check"] = cpu_baseline(
+            w, A_bits, B_bits, C_host if args.epilogue == "none" else None)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -12,6 +12,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <new>
 #include <string>
@@ -39,6 +40,13 @@ hk_status cuda_fail(hk_status s, const char* what, cudaError_t e) {
     return fail(s, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+#ifndef HK_PAIR_ATOMS
+#define HK_PAIR_ATOMS 2   // K atoms per stage of the bf16 pair kernel (128 K elements, 3 stages)
+#endif
+#ifndef HK_FP8_PAIR_ATOMS
+#define HK_FP8_PAIR_ATOMS 1
+#endif
+
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;   // 1 s per bounded wait
 constexpr int kDefaultGroupM = 8;
@@ -56,16 +64,17 @@ struct Variant {
     bool mx;           // block-scaled E4M3 (MXFP8); never chosen automatically
     int a_rows_max;    // rows of A a stage holds (16 or 64 for the decode kernels, else 128)
     int k_elems;       // K elements per pipeline stage
+    int atoms;         // 128-byte K atoms per stage (TMA boxes per operand and stage)
     int sf_bytes;      // MXFP8: bytes of scale blocks per stage and CTA
     KernelFn fn;
     const char* name;
 };
 
-template <int kCG, int kTileN, bool kFp8, bool kMx = false, int kARows = hk::kCtaM>
+template <int kCG, int kTileN, bool kFp8, bool kMx = false, int kARows = hk::kCtaM, int kAtoms = 1>
 constexpr Variant make_variant(int id, const char* name) {
-    using G = hk::Geometry<kCG, kTileN, kFp8, kMx, kARows>;
+    using G = hk::Geometry<kCG, kTileN, kFp8, kMx, kARows, kAtoms>;
     return Variant{id, kCG, G::kTileM, G::kTileN, G::kStages, G::kSmemBytes, kFp8, kMx, G::kARowsMax, G::kKElems,
-                   G::kSfBytes, &hk::gemm_bf16_kernel<kCG, kTileN, kFp8, kMx, kARows>, name};
+                   kAtoms, G::kSfBytes, &hk::gemm_bf16_kernel<kCG, kTileN, kFp8, kMx, kARows, kAtoms>, name};
 }
 
 const Variant kVariants[] = {
@@ -80,12 +89,12 @@ const Variant kVariants[] = {
     make_variant<1, 192, false, false, 64>(HK_KERNEL_SINGLE_128x192, "single 128x192, 64-row A"),
     make_variant<1, 128, false, false, 64>(HK_KERNEL_SINGLE_128x128, "single 128x128, 64-row A"),
     make_variant<1, 64, false, false, 64>(HK_KERNEL_SINGLE_128x64, "single 128x64, 64-row A"),
-    make_variant<2, 256, false>(HK_KERNEL_PAIR_256x256, "pair 256x256"),
+    make_variant<2, 256, false, false, hk::kCtaM, HK_PAIR_ATOMS>(HK_KERNEL_PAIR_256x256, "pair 256x256"),
     make_variant<1, 256, false>(HK_KERNEL_SINGLE_128x256, "single 128x256"),
     make_variant<1, 192, false>(HK_KERNEL_SINGLE_128x192, "single 128x192"),
     make_variant<1, 128, false>(HK_KERNEL_SINGLE_128x128, "single 128x128"),
     make_variant<1, 64, false>(HK_KERNEL_SINGLE_128x64, "single 128x64"),
-    make_variant<2, 256, true>(HK_KERNEL_PAIR_256x256, "fp8 pair 256x256"),
+    make_variant<2, 256, true, false, hk::kCtaM, HK_FP8_PAIR_ATOMS>(HK_KERNEL_PAIR_256x256, "fp8 pair 256x256"),
     make_variant<1, 256, true>(HK_KERNEL_SINGLE_128x256, "fp8 single 128x256"),
     make_variant<1, 192, true>(HK_KERNEL_SINGLE_128x192, "fp8 single 128x192"),
     make_variant<1, 128, true>(HK_KERNEL_SINGLE_128x128, "fp8 single 128x128"),
@@ -275,6 +284,27 @@ hk_status check_pointers(const void* A, const void* B, const void* C, int64_t K)
     return HK_OK;
 }
 
+// The residual of a fused epilogue: NULL, or an M×N bf16 matrix, 16-byte
+// aligned with ldr a multiple of 8 and at least N, that is C itself (same
+// pointer and leading dimension: an in-place update) or does not overlap C.
+hk_status check_residual(const void* R, int64_t ldr, const void* C, int64_t M, int64_t N, int64_t ldc) {
+    if (!R) return HK_OK;
+    if (ldr < (N > 0 ? N : 1) || ldr > (int64_t(1) << 31) - 1)
+        return fail(HK_ERR_INVALID_ARG, "residual leading dimension %lld outside [N, 2^31)", (long long)ldr);
+    if (!aligned16(R) || (ldr % 8))
+        return fail(HK_ERR_MISALIGNED, "the residual must be 16-byte aligned with ldr a multiple of 8 (ldr=%lld)",
+                    (long long)ldr);
+    if (R == C) {
+        if (ldr != ldc) return fail(HK_ERR_INVALID_ARG, "a residual that is C must have ldr == ldc");
+        return HK_OK;
+    }
+    const uintptr_t r0 = reinterpret_cast<uintptr_t>(R), c0 = reinterpret_cast<uintptr_t>(C);
+    const uintptr_t r1 = r0 + 2u * static_cast<uintptr_t>((M - 1) * ldr + N);
+    const uintptr_t c1 = c0 + 2u * static_cast<uintptr_t>((M - 1) * ldc + N);
+    if (r0 < c1 && c0 < r1) return fail(HK_ERR_INVALID_ARG, "the residual overlaps C without being C");
+    return HK_OK;
+}
+
 struct DeviceGuard {
     int prev = -1;
     explicit DeviceGuard(int device) {
@@ -291,6 +321,18 @@ struct DeviceGuard {
 
 // ------------------------------------------------------------------ plans --
 
+// Tensor maps of one set of operand pointers (encoding them costs host time
+// on every call otherwise; a plan keeps the last set it ran with).
+struct TensorMaps {
+    bool valid = false;
+    const void* a = nullptr;
+    const void* b = nullptr;
+    const void* c = nullptr;
+    const void* scales = nullptr;   // MXFP8: the arranged scale blocks
+    size_t scale_bytes = 0;
+    CUtensorMap ta, tb, tc, tbh;
+};
+
 struct hk_gemm_plan {
     int64_t M, N, K, lda, ldb, ldc;
     int device;
@@ -302,6 +344,9 @@ struct hk_gemm_plan {
     hk_gemm_config cfg;
     StatusWord status;
     bool owns_status;
+    // the tensor maps of the last run's pointers (runs may come from several threads)
+    mutable std::mutex tmap_mutex;
+    mutable TensorMaps tmaps;
 };
 
 namespace {
@@ -344,7 +389,7 @@ double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int64_t sl
     const double waves = double(ceil_div(units, slots));
     const double kb = double(ceil_div(ceil_div(K, v.k_elems), splits));
     const double elem = v.fp8 ? 1.0 : 2.0;
-    const double stage_bytes = double(a_rows_for(v, M) + v.tile_n / v.cg) * hk::kRowBytes;
+    const double stage_bytes = double(a_rows_for(v, M) + v.tile_n / v.cg) * hk::kRowBytes * v.atoms;
     const double cta_bytes = stage_bytes * kb;
     const double sm_rate = std::min(kSmBytesPerUs, stage_bytes * v.stages / kLoadLatencyUs);
     const double t_stream = waves * (cta_bytes / sm_rate + kFillUs);
@@ -352,7 +397,7 @@ double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int64_t sl
     const double partials = splits > 1 ? 4.0 * splits * M * n_pad : 0.0;
     const double operands = elem * (double(N) * K + double(M) * K);
     const double t_hbm = (operands + (splits > 1 ? partials : 2.0 * M * N)) / kHbmBytesPerUs;
-    const double t_mma = waves * kb * kKStepUsPair * (double(v.tile_n) / 256.0);
+    const double t_mma = waves * kb * kKStepUsPair * v.atoms * (double(v.tile_n) / 256.0);
     const double t_reduce = splits > 1 ? (partials + 2.0 * M * N) / kHbmBytesPerUs + kLaunchUs : 0.0;
     return std::max(t_stream, std::max(t_hbm, t_mma)) + t_reduce;
 }
@@ -413,8 +458,8 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
         return fail(HK_ERR_INVALID_ARG, "unknown kernel id %d", (int)p->cfg.kernel);
     const int64_t k_blocks_all = ceil_div(K, fp8 ? 128 : hk::kTileK);
     if (p->cfg.split_k > 1 && (p->cfg.split_k > k_blocks_all || p->cfg.split_k > 4096))
-        return fail(HK_ERR_INVALID_ARG, "split_k %d exceeds the %lld K blocks of 64", (int)p->cfg.split_k,
-                    (long long)k_blocks_all);
+        return fail(HK_ERR_INVALID_ARG, "split_k %d exceeds the %lld K blocks of %d", (int)p->cfg.split_k,
+                    (long long)k_blocks_all, fp8 ? 128 : hk::kTileK);
     const Variant* v = nullptr;
     int splits = 1;
     choose_plan(M, N, K, di, p->cfg.max_clusters, allow_split, p->cfg.kernel, p->cfg.split_k, fp8, &v, &splits);
@@ -430,6 +475,9 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     g.tiles_m = static_cast<int32_t>(ceil_div(M, v->tile_m));
     g.tiles_n = static_cast<int32_t>(ceil_div(N, v->tile_n));
     g.k_blocks = static_cast<int32_t>(ceil_div(K, v->k_elems));
+    if (splits > 1 && splits > g.k_blocks)   // every split must own at least one K stage
+        return fail(HK_ERR_INVALID_ARG, "split_k %d exceeds the %d K stages of %d elements of kernel %s", splits,
+                    (int)g.k_blocks, v->k_elems, v->name);
     g.alpha = alpha;
     const int64_t tiles = int64_t(g.tiles_m) * g.tiles_n;
     if (tiles > (int64_t(1) << 30)) return fail(HK_ERR_INVALID_ARG, "too many output tiles");
@@ -437,7 +485,7 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     g.splits = splits;
     if (int64_t(splits) * tiles > (int64_t(1) << 30)) return fail(HK_ERR_INVALID_ARG, "too many work units");
     g.a_rows = a_rows_for(*v, M);
-    g.expect_bytes = static_cast<uint32_t>(v->cg * (g.a_rows + v->tile_n / v->cg) * hk::kRowBytes);
+    g.expect_bytes = static_cast<uint32_t>(v->cg * (g.a_rows + v->tile_n / v->cg) * hk::kRowBytes * v->atoms);
     g.n_pad = int64_t(g.tiles_n) * v->tile_n;
     p->ws_bytes = splits > 1 ? static_cast<size_t>(splits) * static_cast<size_t>(M) * g.n_pad * 4 : 0;
     g.group_m = group_m;
@@ -462,7 +510,7 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
             g.total_units = static_cast<int32_t>(g.num_tiles + last);
         }
     }
-    g.expect_bytes_half = static_cast<uint32_t>(v->cg * (g.a_rows + v->tile_n / v->cg / 2) * hk::kRowBytes);
+    g.expect_bytes_half = static_cast<uint32_t>(v->cg * (g.a_rows + v->tile_n / v->cg / 2) * hk::kRowBytes * v->atoms);
     if (units > g.total_units) units = g.total_units;
     p->grid_ctas = v->cg * units;
     if (const char* log = std::getenv("HK_LOG"); log && log[0] == '1')
@@ -472,13 +520,15 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     return HK_OK;
 }
 
-hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const void* B, void* C, void* workspace,
-                 cudaStream_t stream, const void* bias = nullptr, const void* mx_scales = nullptr,
-                 size_t mx_scale_bytes = 0) {
-    if (p->M == 0 || p->N == 0) return HK_OK;
+// Encode the four tensor maps of a run (A, B, C and the half-width B or the
+// MXFP8 scale blocks) for these pointers.
+hk_status encode_maps(const hk_gemm_plan* p, const void* A, const void* B, void* C, const void* mx_scales,
+                      size_t mx_scale_bytes, TensorMaps* m) {
     hk_status s = get_encoder();
     if (s != HK_OK) return s;
-    CUtensorMap ta, tb, tc;
+    CUtensorMap& ta = m->ta;
+    CUtensorMap& tb = m->tb;
+    CUtensorMap& tc = m->tc;
     // A with K == 0 is never read; give the map a valid 1-column shape over C's memory
     const Variant* v = p->variant;
     const bool bytes = v->fp8;               // FP8 operands: 1-byte elements
@@ -489,10 +539,10 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
     const int64_t ldb = p->K > 0 ? p->ldb : (bytes ? 2 * p->ldc : p->ldc);
     const uint32_t b_rows = static_cast<uint32_t>(v->tile_n / v->cg);
     const uint32_t a_box_rows = static_cast<uint32_t>(p->params.a_rows);
-    const uint32_t box_k = static_cast<uint32_t>(v->k_elems);
+    const uint32_t box_k = static_cast<uint32_t>(v->k_elems / v->atoms);   // one 128-byte K atom per box
     if ((s = encode_2d(&ta, a_ptr, p->K > 0 ? p->M : 1, kk, lda, box_k, a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B, "A", bytes)) != HK_OK) return s;
     if ((s = encode_2d(&tb, b_ptr, p->K > 0 ? p->N : 1, kk, ldb, box_k, b_rows, CU_TENSOR_MAP_SWIZZLE_128B, "B", bytes)) != HK_OK) return s;
-    CUtensorMap tbh;   // B in boxes of half the rows, for half-width units (MXFP8: the scale blocks)
+    CUtensorMap& tbh = m->tbh;   // B in boxes of half the rows, for half-width units (MXFP8: the scale blocks)
     if (v->mx && mx_scales != nullptr) {
         // prearranged scale blocks as rows of 256 bytes, one 512-byte block = 2 rows
         if ((s = encode_2d(&tbh, mx_scales, static_cast<int64_t>(mx_scale_bytes / 256), 256, 256, 256, 2,
@@ -505,10 +555,43 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
     // least 8 columns so that it stays valid when N < 8 (then it is unused)
     const int64_t n_tma = p->N & ~int64_t(7);
     if ((s = encode_2d(&tc, C, p->M, n_tma > 0 ? n_tma : 8, p->ldc, hk::kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B, "C")) != HK_OK) return s;
+    m->a = A;
+    m->b = B;
+    m->c = C;
+    m->scales = mx_scales;
+    m->scale_bytes = mx_scale_bytes;
+    m->valid = true;
+    return HK_OK;
+}
+
+hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const void* B, void* C, void* workspace,
+                 cudaStream_t stream, const void* bias = nullptr, const void* mx_scales = nullptr,
+                 size_t mx_scale_bytes = 0, const void* residual = nullptr, int64_t ldr = 0) {
+    if (p->M == 0 || p->N == 0) return HK_OK;
+    const Variant* v = p->variant;
+    TensorMaps maps;
+    {
+        std::lock_guard<std::mutex> lock(p->tmap_mutex);
+        const TensorMaps& t = p->tmaps;
+        if (t.valid && t.a == A && t.b == B && t.c == C && t.scales == mx_scales && t.scale_bytes == mx_scale_bytes)
+            maps = t;
+    }
+    if (!maps.valid) {
+        hk_status s = encode_maps(p, A, B, C, mx_scales, mx_scale_bytes, &maps);
+        if (s != HK_OK) return s;
+        std::lock_guard<std::mutex> lock(p->tmap_mutex);
+        p->tmaps = maps;
+    }
+    const CUtensorMap& ta = maps.ta;
+    const CUtensorMap& tb = maps.tb;
+    const CUtensorMap& tc = maps.tc;
+    const CUtensorMap& tbh = maps.tbh;
 
     hk::GemmParams g = p->params;
     g.c_ptr = static_cast<uint16_t*>(C);
     g.bias = static_cast<const uint16_t*>(bias);
+    g.residual = static_cast<const uint16_t*>(residual);
+    g.ldr = ldr;
     g.status = sw->dev;
     g.launch_id = next_launch_id();
     if (g.splits > 1) g.partials = static_cast<float*>(workspace);
@@ -553,9 +636,97 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
         rc.attrs = ra;
         rc.numAttrs = 1;
         e = cudaLaunchKernelEx(&rc, hk::splitk_reduce_kernel, static_cast<const float*>(g.partials), g.splits, g.M,
-                               g.N, g.n_pad, g.c_ptr, g.ldc, g.bias, g.act, g.alpha);
+                               g.N, g.n_pad, g.c_ptr, g.ldc, g.bias, g.act, g.alpha, g.residual, g.ldr);
         if (e != cudaSuccess) return cuda_fail(HK_ERR_LAUNCH, "launching the split-K reduction", e);
     }
+    return HK_OK;
+}
+
+// Per-device status word of the one-shot entry points, created by the first call on the device.
+hk_status context_status(int device, StatusWord** out) {
+    std::lock_guard<std::mutex> lock(g_ctx_mutex);
+    if (!g_ctx[device]) {
+        StatusWord* w = new (std::nothrow) StatusWord();
+        if (!w) return fail(HK_ERR_INVALID_ARG, "out of host memory");
+        hk_status s = alloc_status(w);
+        if (s != HK_OK) {
+            delete w;
+            return s;
+        }
+        g_ctx[device] = w;
+    }
+    *out = g_ctx[device];
+    return HK_OK;
+}
+
+// ------------------------------------------------- one-shot plan cache --
+//
+// The one-shot entry points keep the plans they fill (argument checks done,
+// kernel, split and schedule chosen by the time model) in a small
+// least-recently-used cache keyed by everything that choice depends on; a
+// repeated call is then a lookup, and the plan's tensor-map cache makes a
+// call with the same pointers encode nothing. Entries are shared pointers:
+// a call still running on an evicted plan keeps it alive.
+struct OneShotKey {
+    int device;
+    int fp8;
+    uint32_t act;
+    uint32_t alpha_bits;
+    int64_t M, N, K, lda, ldb, ldc;
+    bool operator==(const OneShotKey& o) const {
+        return device == o.device && fp8 == o.fp8 && act == o.act && alpha_bits == o.alpha_bits && M == o.M &&
+               N == o.N && K == o.K && lda == o.lda && ldb == o.ldb && ldc == o.ldc;
+    }
+};
+
+constexpr int kOneShotCacheSize = 32;
+
+struct OneShotEntry {
+    OneShotKey key;
+    std::shared_ptr<hk_gemm_plan> plan;
+    uint64_t last_use = 0;
+};
+
+std::mutex g_oneshot_mutex;
+OneShotEntry g_oneshot[kOneShotCacheSize];
+uint64_t g_oneshot_clock = 0;
+
+hk_status one_shot_plan(int device, const DeviceInfo* di, int64_t M, int64_t N, int64_t K, int64_t lda,
+                        int64_t ldb, int64_t ldc, bool fp8, uint32_t act, float alpha,
+                        std::shared_ptr<hk_gemm_plan>* out) {
+    OneShotKey key{device, fp8 ? 1 : 0, act, 0u, M, N, K, lda, ldb, ldc};
+    std::memcpy(&key.alpha_bits, &alpha, sizeof alpha);
+    {
+        std::lock_guard<std::mutex> lock(g_oneshot_mutex);
+        for (OneShotEntry& e : g_oneshot)
+            if (e.plan && e.key == key) {
+                e.last_use = ++g_oneshot_clock;
+                *out = e.plan;
+                return HK_OK;
+            }
+    }
+    std::shared_ptr<hk_gemm_plan> p(new (std::nothrow) hk_gemm_plan());
+    if (!p) return fail(HK_ERR_INVALID_ARG, "out of host memory");
+    hk_gemm_config cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.activation = act;
+    cfg.input_type = fp8 ? HK_INPUT_E4M3 : HK_INPUT_BF16;   // cfg.alpha stays 0: `alpha` below is used
+    hk_status s = fill_plan(p.get(), M, N, K, lda, ldb, ldc, device, &cfg, di, false, fp8, alpha);
+    if (s != HK_OK) return s;
+    p->owns_status = false;
+    std::lock_guard<std::mutex> lock(g_oneshot_mutex);
+    OneShotEntry* victim = &g_oneshot[0];
+    for (OneShotEntry& e : g_oneshot) {
+        if (!e.plan) {
+            victim = &e;
+            break;
+        }
+        if (e.last_use < victim->last_use) victim = &e;
+    }
+    victim->key = key;
+    victim->plan = p;
+    victim->last_use = ++g_oneshot_clock;
+    *out = p;
     return HK_OK;
 }
 
@@ -570,18 +741,10 @@ hk_status set_error(hk_status s, const char* msg) {
 
 hk_status status_word(int device, uint32_t** out) {
     if (device < 0 || device >= kMaxDevices) return fail(HK_ERR_INVALID_ARG, "device %d out of range", device);
-    std::lock_guard<std::mutex> lock(g_ctx_mutex);
-    if (!g_ctx[device]) {
-        StatusWord* w = new (std::nothrow) StatusWord();
-        if (!w) return fail(HK_ERR_INVALID_ARG, "out of host memory");
-        hk_status s = alloc_status(w);
-        if (s != HK_OK) {
-            delete w;
-            return s;
-        }
-        g_ctx[device] = w;
-    }
-    *out = g_ctx[device]->dev;
+    StatusWord* w = nullptr;
+    hk_status s = context_status(device, &w);
+    if (s != HK_OK) return s;
+    *out = w->dev;
     return HK_OK;
 }
 
@@ -712,23 +875,10 @@ hk_status hk_gemm_bf16(const void* A, const void* B, void* C, int64_t M, int64_t
     const DeviceInfo* di = nullptr;
     if ((s = device_info(device, &di)) != HK_OK) return s;
     StatusWord* sw = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_ctx_mutex);
-        if (!g_ctx[device]) {
-            StatusWord* w = new (std::nothrow) StatusWord();
-            if (!w) return fail(HK_ERR_INVALID_ARG, "out of host memory");
-            if ((s = alloc_status(w)) != HK_OK) {
-                delete w;
-                return s;
-            }
-            g_ctx[device] = w;
-        }
-        sw = g_ctx[device];
-    }
-    hk_gemm_plan plan;
-    if ((s = fill_plan(&plan, M, N, K, lda, ldb, ldc, device, nullptr, di, false)) != HK_OK) return s;
-    plan.owns_status = false;
-    return launch(&plan, sw, A, B, C, nullptr, static_cast<cudaStream_t>(stream));
+    if ((s = context_status(device, &sw)) != HK_OK) return s;
+    std::shared_ptr<hk_gemm_plan> plan;
+    if ((s = one_shot_plan(device, di, M, N, K, lda, ldb, ldc, false, 0u, 1.0f, &plan)) != HK_OK) return s;
+    return launch(plan.get(), sw, A, B, C, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 hk_status hk_gemm_last_device_status(int device) {
@@ -744,12 +894,18 @@ hk_status hk_gemm_last_device_status(int device) {
 
 hk_status hk_gemm_plan_run_epilogue(const hk_gemm_plan* p, const void* A, const void* B, void* C, const void* bias,
                                     void* workspace, size_t workspace_bytes, void* stream) {
+    return hk_gemm_plan_run_fused(p, A, B, C, bias, nullptr, 0, workspace, workspace_bytes, stream);
+}
+
+hk_status hk_gemm_plan_run_fused(const hk_gemm_plan* p, const void* A, const void* B, void* C, const void* bias,
+                                 const void* R, int64_t ldr, void* workspace, size_t workspace_bytes, void* stream) {
     if (!p) return fail(HK_ERR_INVALID_ARG, "NULL plan");
     if (p->M == 0 || p->N == 0) return HK_OK;
     hk_status s = check_pointers(A, B, C, p->K);
     if (s != HK_OK) return s;
     if (bias && (reinterpret_cast<uintptr_t>(bias) & 15u))
         return fail(HK_ERR_MISALIGNED, "the bias vector must be 16-byte aligned");
+    if ((s = check_residual(R, ldr, C, p->M, p->N, p->ldc)) != HK_OK) return s;
     if (p->ws_bytes > 0) {
         if (!workspace || workspace_bytes < p->ws_bytes)
             return fail(HK_ERR_WORKSPACE, "the plan needs %zu bytes of workspace, %zu given", p->ws_bytes,
@@ -759,11 +915,17 @@ hk_status hk_gemm_plan_run_epilogue(const hk_gemm_plan* p, const void* A, const 
     }
     DeviceGuard guard(p->device);
     return launch(p, const_cast<StatusWord*>(&p->status), A, B, C, workspace, static_cast<cudaStream_t>(stream),
-                  bias);
+                  bias, nullptr, 0, R, ldr);
 }
 
 hk_status hk_gemm_bf16_epilogue(const void* A, const void* B, void* C, const void* bias, int64_t M, int64_t N,
                                 int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int32_t activation, void* stream) {
+    return hk_gemm_bf16_fused(A, B, C, bias, nullptr, M, N, K, lda, ldb, ldc, 0, activation, stream);
+}
+
+hk_status hk_gemm_bf16_fused(const void* A, const void* B, void* C, const void* bias, const void* R, int64_t M,
+                             int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t ldr,
+                             int32_t activation, void* stream) {
     hk_status s = check_shape(M, N, K, lda, ldb, ldc);
     if (s != HK_OK) return s;
     if (activation < 0 || activation > HK_ACT_SILU) return fail(HK_ERR_INVALID_ARG, "unknown activation %d", (int)activation);
@@ -771,32 +933,19 @@ hk_status hk_gemm_bf16_epilogue(const void* A, const void* B, void* C, const voi
     if ((s = check_pointers(A, B, C, K)) != HK_OK) return s;
     if (bias && (reinterpret_cast<uintptr_t>(bias) & 15u))
         return fail(HK_ERR_MISALIGNED, "the bias vector must be 16-byte aligned");
+    if ((s = check_residual(R, ldr, C, M, N, ldc)) != HK_OK) return s;
     int device = 0;
     cudaError_t e = cudaGetDevice(&device);
     if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "cudaGetDevice", e);
     const DeviceInfo* di = nullptr;
     if ((s = device_info(device, &di)) != HK_OK) return s;
     StatusWord* sw = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_ctx_mutex);
-        if (!g_ctx[device]) {
-            StatusWord* w = new (std::nothrow) StatusWord();
-            if (!w) return fail(HK_ERR_INVALID_ARG, "out of host memory");
-            if ((s = alloc_status(w)) != HK_OK) {
-                delete w;
-                return s;
-            }
-            g_ctx[device] = w;
-        }
-        sw = g_ctx[device];
-    }
-    hk_gemm_config cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.activation = static_cast<uint32_t>(activation);
-    hk_gemm_plan plan;
-    if ((s = fill_plan(&plan, M, N, K, lda, ldb, ldc, device, &cfg, di, false)) != HK_OK) return s;
-    plan.owns_status = false;
-    return launch(&plan, sw, A, B, C, nullptr, static_cast<cudaStream_t>(stream), bias);
+    if ((s = context_status(device, &sw)) != HK_OK) return s;
+    std::shared_ptr<hk_gemm_plan> plan;
+    if ((s = one_shot_plan(device, di, M, N, K, lda, ldb, ldc, false, static_cast<uint32_t>(activation), 1.0f,
+                           &plan)) != HK_OK)
+        return s;
+    return launch(plan.get(), sw, A, B, C, nullptr, static_cast<cudaStream_t>(stream), bias, nullptr, 0, R, ldr);
 }
 
 hk_status hk_gemm_fp8_e4m3(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
@@ -818,24 +967,11 @@ hk_status hk_gemm_fp8_e4m3(const void* A, const void* B, void* C, int64_t M, int
     const DeviceInfo* di = nullptr;
     if ((s = device_info(device, &di)) != HK_OK) return s;
     StatusWord* sw = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_ctx_mutex);
-        if (!g_ctx[device]) {
-            StatusWord* w = new (std::nothrow) StatusWord();
-            if (!w) return fail(HK_ERR_INVALID_ARG, "out of host memory");
-            if ((s = alloc_status(w)) != HK_OK) {
-                delete w;
-                return s;
-            }
-            g_ctx[device] = w;
-        }
-        sw = g_ctx[device];
-    }
-    hk_gemm_plan plan;
+    if ((s = context_status(device, &sw)) != HK_OK) return s;
     const float alpha = static_cast<float>(static_cast<double>(scale_a) * static_cast<double>(scale_b));
-    if ((s = fill_plan(&plan, M, N, K, lda, ldb, ldc, device, nullptr, di, false, true, alpha)) != HK_OK) return s;
-    plan.owns_status = false;
-    return launch(&plan, sw, A, B, C, nullptr, static_cast<cudaStream_t>(stream));
+    std::shared_ptr<hk_gemm_plan> plan;
+    if ((s = one_shot_plan(device, di, M, N, K, lda, ldb, ldc, true, 0u, alpha, &plan)) != HK_OK) return s;
+    return launch(plan.get(), sw, A, B, C, nullptr, static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------- MXFP8 --

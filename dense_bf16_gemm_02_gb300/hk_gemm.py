@@ -48,7 +48,8 @@ EXPORTED = (
     "hk_gemm_bf16", "hk_gemm_plan_create", "hk_gemm_plan_workspace_size", "hk_gemm_plan_get_info",
     "hk_gemm_plan_run", "hk_gemm_plan_device_status", "hk_gemm_last_device_status",
     "hk_gemm_plan_destroy", "hk_status_string", "hk_gemm_last_error_string", "hk_gemm_bf16_noalloc",
-    "hk_gemm_bf16_epilogue", "hk_gemm_plan_run_epilogue", "hk_gemm_fp8_e4m3",
+    "hk_gemm_bf16_epilogue", "hk_gemm_plan_run_epilogue", "hk_gemm_bf16_fused", "hk_gemm_plan_run_fused",
+    "hk_gemm_fp8_e4m3",
     "hk_attention_fwd", "hk_attention_fwd_ex", "hk_gemm_mxfp8", "hk_gemm_mxfp8_ex", "hk_gemm_mxfp8_workspace_size",
 )
 
@@ -122,6 +123,10 @@ def load() -> ctypes.CDLL:
         lib.hk_gemm_bf16_epilogue.restype = I32
         lib.hk_gemm_plan_run_epilogue.argtypes = [P, P, P, P, P, P, ctypes.c_size_t, P]
         lib.hk_gemm_plan_run_epilogue.restype = I32
+        lib.hk_gemm_bf16_fused.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, I64, I64, ctypes.c_int32, P]
+        lib.hk_gemm_bf16_fused.restype = I32
+        lib.hk_gemm_plan_run_fused.argtypes = [P, P, P, P, P, P, I64, P, ctypes.c_size_t, P]
+        lib.hk_gemm_plan_run_fused.restype = I32
         lib.hk_gemm_fp8_e4m3.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, ctypes.c_float, ctypes.c_float, P]
         lib.hk_gemm_fp8_e4m3.restype = I32
         lib.hk_gemm_bf16_noalloc.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, ctypes.c_int32, P]
@@ -153,6 +158,13 @@ def hk_gemm_bf16_epilogue(A: int, B: int, C: int, bias: int, M: int, N: int, K: 
                           ldc: int, activation: int = 0, stream: int = 0) -> int:
     """C = bf16(act(A·Bᵀ + bias)) (bias: device pointer or 0)."""
     return load().hk_gemm_bf16_epilogue(A, B, C, bias or None, M, N, K, lda, ldb, ldc, activation, stream)
+
+
+def hk_gemm_bf16_fused(A: int, B: int, C: int, bias: int, R: int, M: int, N: int, K: int, lda: int, ldb: int,
+                       ldc: int, ldr: int, activation: int = 0, stream: int = 0) -> int:
+    """C = bf16(act(A·Bᵀ + bias) + R) (bias, R: device pointers or 0; R may be C with ldr == ldc)."""
+    return load().hk_gemm_bf16_fused(A, B, C, bias or None, R or None, M, N, K, lda, ldb, ldc, ldr, activation,
+                                     stream)
 
 
 def hk_gemm_fp8_e4m3(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
@@ -332,6 +344,11 @@ class Plan:
                          stream: int = 0) -> int:
         return self._lib.hk_gemm_plan_run_epilogue(self._h, A, B, C, bias or None, workspace, workspace_bytes,
                                                    stream)
+
+    def run_fused_raw(self, A: int, B: int, C: int, bias: int = 0, R: int = 0, ldr: int = 0, workspace: int = 0,
+                      workspace_bytes: int = 0, stream: int = 0) -> int:
+        return self._lib.hk_gemm_plan_run_fused(self._h, A, B, C, bias or None, R or None, ldr, workspace,
+                                                workspace_bytes, stream)
 
     def device_status(self) -> int:
         return int(self._lib.hk_gemm_plan_device_status(self._h))

@@ -78,7 +78,7 @@ typedef enum hk_status {
  * at most half of the CTA pairs, each runs as two 256x128 halves). */
 #define HK_FLAG_NO_TAIL_SPLIT 0x2u
 
-/* Fused epilogue activations: C = bf16(act(A·Bᵀ + bias)). */
+/* Fused epilogue activations: C = bf16(act(A·Bᵀ + bias) [+ R]). */
 #define HK_ACT_NONE 0
 #define HK_ACT_RELU 1               /* max(x, 0) */
 #define HK_ACT_GELU 2               /* x·Φ(x) = 0.5·x·(1 + erf(x/√2)) */
@@ -181,6 +181,31 @@ hk_status hk_gemm_bf16_epilogue(const void* A, const void* B, void* C, const voi
 hk_status hk_gemm_plan_run_epilogue(const hk_gemm_plan* plan, const void* A, const void* B, void* C,
                                     const void* bias, void* workspace, size_t workspace_bytes,
                                     void* stream);
+
+/* GEMM with a fused epilogue that also adds a residual:
+ *     C[i,j] = bf16_rne( act( Σ_k A[i,k]·B[j,k] + bias[j] ) + R[i,j] )
+ * in fp32 before the one rounding. The HipKittens "L2" detail page (§8
+ * "Deployment context", Fusion scope) keeps the residual add in a separate
+ * memory-bound kernel; here it rides in the GEMM's epilogue, which reads R
+ * once while the tensor cores work on the next tile. `R` is a device matrix
+ * of M×N bf16 values, row-major with leading dimension `ldr` (elements, a
+ * multiple of 8 and ≥ N), 16-byte aligned (else HK_ERR_MISALIGNED), or NULL
+ * (no residual). R may be C itself (same pointer, ldr == ldc): an in-place
+ * update C ← act(A·Bᵀ + bias) + C; any other overlap of R and C is rejected
+ * with HK_ERR_INVALID_ARG. `bias` and `activation` as hk_gemm_bf16_epilogue;
+ * everything else as hk_gemm_bf16. */
+hk_status hk_gemm_bf16_fused(const void* A, const void* B, void* C, const void* bias, const void* R,
+                             int64_t M, int64_t N, int64_t K,
+                             int64_t lda, int64_t ldb, int64_t ldc, int64_t ldr,
+                             int32_t activation, void* stream);
+
+/* Plan form of hk_gemm_bf16_fused: the activation is the plan's
+ * hk_gemm_config.activation; bias, R and ldr are given per run (a K split
+ * adds bias, activation and R in its reduction kernel). Also for E4M3 plans:
+ * alpha, then bias, activation and R. Otherwise as hk_gemm_plan_run. */
+hk_status hk_gemm_plan_run_fused(const hk_gemm_plan* plan, const void* A, const void* B, void* C,
+                                 const void* bias, const void* R, int64_t ldr,
+                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /* FP8 GEMM (the pages' second GEMM: 8-bit floating-point inputs, FP32
  * accumulation, bf16 output), with one scale per operand tensor:

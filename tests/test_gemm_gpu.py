@@ -530,6 +530,156 @@ def test_epilogue_argument_errors(hk):
                                     64, 64, 64, 7, 0) == hk.HK_ERR_INVALID_ARG
 
 
+# ------------------------------------------------- fused residual add --
+
+def run_fused(hk, A_bits, B_bits, bias_bits, R_bits, act, split_k=None, kernel=0, in_place=False, ldr_pad=0):
+    """C = bf16(act(A·Bᵀ + bias) + R) through hk_gemm_bf16_fused (or a plan with a
+    forced kernel and K split); R in its own padded storage, or C itself."""
+    import torch
+    M, K = A_bits.shape
+    N = B_bits.shape[0]
+    kp = (-K) % 8
+    A, Astore = to_device(A_bits, cols_pad=kp)
+    B, Bstore = to_device(B_bits, cols_pad=kp)
+    ldc = N + ((-N) % 8)
+    if in_place:
+        C, Cstore = to_device(R_bits, rows_pad=1, cols_pad=ldc - N, fill=SENTINEL)
+        Rptr, ldr = C.data_ptr(), Cstore.stride(0)
+    else:
+        C, Cstore = to_device(np.full((M, N), SENTINEL, dtype=np.uint16), rows_pad=1, cols_pad=ldc - N,
+                              fill=SENTINEL)
+        ldr_cols = N + ((-N) % 8) + ldr_pad
+        Rt, Rstore = to_device(R_bits, cols_pad=ldr_cols - N, fill=SENTINEL)
+        Rptr, ldr = Rt.data_ptr(), Rstore.stride(0)
+    bias_t = None
+    if bias_bits is not None:
+        bias_t = torch.from_numpy(np.ascontiguousarray(bias_bits).view(np.int16)).to("cuda")
+    bptr = bias_t.data_ptr() if bias_t is not None else 0
+    stream = int(torch.cuda.current_stream().cuda_stream)
+    if split_k is None:
+        st = hk.hk_gemm_bf16_fused(A.data_ptr(), B.data_ptr(), C.data_ptr(), bptr, Rptr, M, N, K, Astore.stride(0),
+                                   Bstore.stride(0), Cstore.stride(0), ldr, act, stream)
+    else:
+        plan = hk.Plan(M, N, K, lda=Astore.stride(0), ldb=Bstore.stride(0), ldc=Cstore.stride(0),
+                       split_k=split_k, kernel=kernel, activation=act)
+        assert plan.info()["split_k"] == split_k
+        ws = torch.zeros(max(plan.workspace_size, 1) + 256, dtype=torch.uint8, device="cuda")
+        st = plan.run_fused_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), bptr, Rptr, ldr,
+                                (ws.data_ptr() + 255) & ~255, plan.workspace_size, stream)
+    assert st == hk.HK_OK, hk.hk_gemm_last_error_string()
+    torch.cuda.synchronize()
+    assert hk.hk_gemm_last_device_status(torch.cuda.current_device()) == hk.HK_OK
+    full = to_host(Cstore)
+    guard = full.copy()
+    guard[:M, :N] = SENTINEL
+    assert np.all(guard == SENTINEL), "a write landed outside C"
+    return full[:M, :N]
+
+
+@pytest.mark.parametrize("act,with_bias", [(0, False), (0, True), (2, True), (3, False)])
+@pytest.mark.parametrize("M,N,K", [(300, 517, 200), (64, 1000, 640), (1024, 768, 1536), (7, 333, 96)])
+def test_residual_normal(hk, act, with_bias, M, N, K):
+    A = synth.normal_bf16(M, K, 1700 + M)
+    B = synth.normal_bf16(N, K, 2700 + N)
+    bias = synth.normal_bf16(1, N, 3700 + N, 2.0)[0] if with_bias else None
+    R = synth.normal_bf16(M, N, 4700 + M + N, 4.0)
+    got = run_fused(hk, A, B, bias, R, act)
+    ref = oracle.gemm_epilogue(A, B, bias, act, residual=R)
+    assert_close(got, ref, K, 1, 1, f"residual act {act} bias {with_bias} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(257, 300, 128), (128, 2050, 96), (520, 1030, 264)])
+def test_residual_relu_integer_bitexact(hk, M, N, K):
+    """Integer data: every fp32 step is exact, so act(dot + bias) + R matches bit for bit."""
+    A = synth.int_bf16(M, K, 1800 + M)
+    B = synth.int_bf16(N, K, 2800 + N)
+    bias = synth.int_bf16(1, N, 3800 + N)[0]
+    R = synth.int_bf16(M, N, 4800 + N, -60, 60)
+    got = run_fused(hk, A, B, bias, R, 1)
+    assert_bitexact(got, oracle.gemm_epilogue(A, B, bias, 1, residual=R), "relu + bias + residual integer")
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 517, 200), (130, 264, 72)])
+def test_residual_in_place(hk, M, N, K):
+    """R = C (same pointer and leading dimension): C ← act(A·Bᵀ + bias) + C."""
+    A = synth.int_bf16(M, K, 1900 + M)
+    B = synth.int_bf16(N, K, 2900 + N)
+    bias = synth.int_bf16(1, N, 3900 + N)[0]
+    R = synth.int_bf16(M, N, 4900 + N, -30, 30)
+    got = run_fused(hk, A, B, bias, R, 0, in_place=True)
+    assert_bitexact(got, oracle.gemm_epilogue(A, B, bias, 0, residual=R), "in-place residual")
+
+
+def test_residual_padded_leading_dimension(hk):
+    M, N, K = 200, 120, 64
+    A, B = synth.int_bf16(M, K, 61), synth.int_bf16(N, K, 62)
+    R = synth.int_bf16(M, N, 63, -9, 9)
+    got = run_fused(hk, A, B, None, R, 0, ldr_pad=40)
+    assert_bitexact(got, oracle.gemm_epilogue(A, B, None, 0, residual=R), "ldr > N")
+
+
+@pytest.mark.parametrize("kernel,splits", [(4, 4), (1, 3), (2, 2)])
+def test_residual_in_split_k_reduction(hk, kernel, splits):
+    """A K split adds bias, activation and R in its reduction kernel."""
+    M, N, K = (300 if kernel == 1 else 64), 1200, 2048
+    A = synth.int_bf16(M, K, 81)
+    B = synth.int_bf16(N, K, 82)
+    bias = synth.int_bf16(1, N, 83)[0]
+    R = synth.int_bf16(M, N, 84, -50, 50)
+    got = run_fused(hk, A, B, bias, R, 1, split_k=splits, kernel=kernel)
+    assert_bitexact(got, oracle.gemm_epilogue(A, B, bias, 1, residual=R), f"split-K residual {kernel}/{splits}")
+    An, Bn = synth.normal_bf16(M, K, 85), synth.normal_bf16(N, K, 86)
+    Rn = synth.normal_bf16(M, N, 87, 3.0)
+    got = run_fused(hk, An, Bn, None, Rn, 2, split_k=splits, kernel=kernel)
+    assert_close(got, oracle.gemm_epilogue(An, Bn, None, 2, residual=Rn), K, 1, 1, "split-K residual normal")
+
+
+def test_residual_fp8_plan(hk):
+    """An E4M3 plan: alpha, then the residual."""
+    import torch
+    M, N, K = 260, 300, 256
+    A8, B8 = synth.int_e4m3(M, K, 91), synth.int_e4m3(N, K, 92)
+    R = synth.int_bf16(M, N, 93, -20, 20)
+    ldc = N + ((-N) % 8)
+    a = torch.from_numpy(A8).to("cuda")
+    b = torch.from_numpy(B8).to("cuda")
+    C, Cstore = to_device(np.zeros((M, N), dtype=np.uint16), cols_pad=ldc - N)
+    Rt, Rstore = to_device(R, cols_pad=ldc - N)
+    plan = hk.Plan(M, N, K, lda=K, ldb=K, ldc=ldc, input_type=hk.HK_INPUT_E4M3, alpha=2.0)
+    st = plan.run_fused_raw(a.data_ptr(), b.data_ptr(), C.data_ptr(), 0, Rt.data_ptr(), Rstore.stride(0), 0, 0,
+                            int(torch.cuda.current_stream().cuda_stream))
+    assert st == hk.HK_OK, hk.hk_gemm_last_error_string()
+    torch.cuda.synchronize()
+    got = to_host(Cstore)[:M, :N]
+    table = np.array([oracle.e4m3_value(c) for c in range(256)])
+    prod = 2.0 * (table[A8] @ table[B8].T)                     # exact: small integers
+    want = synth.f32_to_bf16_bits((prod + synth.bf16_bits_to_f32(R)).astype(np.float32))
+    assert_bitexact(got, want, "fp8 + residual")
+
+
+def test_residual_argument_errors(hk):
+    import torch
+    A = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    R = torch.zeros((64, 80), dtype=torch.bfloat16, device="cuda")
+    f = hk.hk_gemm_bf16_fused
+    assert f(A.data_ptr(), A.data_ptr(), C.data_ptr(), 0, R.data_ptr() + 2, 64, 64, 64, 64, 64, 64, 80, 0, 0) \
+        == hk.HK_ERR_MISALIGNED
+    assert f(A.data_ptr(), A.data_ptr(), C.data_ptr(), 0, R.data_ptr(), 64, 64, 64, 64, 64, 64, 68, 0, 0) \
+        == hk.HK_ERR_MISALIGNED
+    assert f(A.data_ptr(), A.data_ptr(), C.data_ptr(), 0, R.data_ptr(), 64, 64, 64, 64, 64, 64, 56, 0, 0) \
+        == hk.HK_ERR_INVALID_ARG
+    # R == C needs ldr == ldc; a partial overlap with C is rejected
+    Cw = torch.zeros((64, 80), dtype=torch.bfloat16, device="cuda")
+    assert f(A.data_ptr(), A.data_ptr(), Cw.data_ptr(), 0, Cw.data_ptr(), 64, 64, 64, 64, 64, 80, 72, 0, 0) \
+        == hk.HK_ERR_INVALID_ARG
+    assert f(A.data_ptr(), A.data_ptr(), Cw.data_ptr(), 0, Cw.data_ptr() + 16, 64, 64, 64, 64, 64, 80, 80, 0, 0) \
+        == hk.HK_ERR_INVALID_ARG
+    assert f(A.data_ptr(), A.data_ptr(), C.data_ptr(), 0, R.data_ptr(), 64, 64, 64, 64, 64, 64, 80, 9, 0) \
+        == hk.HK_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+
+
 # ------------------------------------------------------------ FP8 (E4M3) --
 
 def run_fp8(hk, A_codes, B_codes, sa=1.0, sb=1.0):
