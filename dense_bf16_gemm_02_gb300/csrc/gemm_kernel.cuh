@@ -113,7 +113,7 @@ struct Geometry {
     static constexpr int kOffBars = kOffEpi + kEpiWarps * 2 * kEpiBufBytes;
     // full[S], empty[S], acc_full[2], acc_empty[2], sf_full[S] (MXFP8), drain[2] (abort path)
     static constexpr int kNumBars = (kMx ? 3 : 2) * kStages + 6;
-    static constexpr int kOffTmemHolder = kOffBars + kNumBars * 8;
+    static constexpr int kOffTmemHolder = kOffBars + kNumBars * 8;   // [0]: TMEM address, [1..2]: epilogue flags
     static constexpr int kSmemBytes = kOffTmemHolder + 16 + 1024;   // + slack for aligning the base
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
     static constexpr int kAccCols = kTileN;                 // TMEM columns per accumulator
@@ -225,6 +225,25 @@ __device__ __forceinline__ bool wait_bounded_cluster(const GemmParams& p, uint32
                                                      uint32_t code) {
     if (mbar_try_wait_cluster_relaxed(bar, parity)) return true;
     return wait_bounded_slow(p, bar, parity, code, true);
+}
+
+// Bounded wait for a phase expected to take long (a whole main loop): each
+// probe lets the hardware suspend the thread for up to 20 µs (it resumes
+// when the phase completes), so the waiting thread does not take issue slots
+// from the warps that do work. Same failure behaviour as wait_bounded_slow.
+__device__ __noinline__ bool wait_bounded_suspend(const GemmParams& p, uint32_t bar, uint32_t parity,
+                                                  uint32_t code) {
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait_suspend(bar, parity, 20000)) return true;
+        if (aborted(p)) return false;
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+            atomicOr(p.status, code);
+            atomicExch(p.status + 1, p.launch_id);
+            __threadfence();
+            return false;
+        }
+    }
 }
 
 // Warp-uniform variant: lane 0 waits, the result is broadcast, and every
@@ -427,9 +446,10 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
-            // launched as a programmatic dependent (block-scaled GEMM after the scale
-            // arrangement): nothing the earlier grid writes is read before this
-            if constexpr (kMx) griddep_wait();
+            // launched as a programmatic dependent (of the previous kernel on the stream,
+            // which may have written A or B; of the scale arrangement for the block-scaled
+            // GEMM): nothing from global memory is read before that grid has completed
+            griddep_wait();
             int stage = 0;
             uint32_t phase = 0;
             bool dropped = false;
@@ -662,6 +682,9 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         }
     } else {
         // --------------------------------------------------- epilogue --
+        // no global read or write (C, bias, residual, split partials) before the
+        // grid this one depends on has completed
+        griddep_wait();
         const uint32_t q = warp & 3u;                  // TMEM lane quarter this warp may read
         const uint32_t epi = base + G::kOffEpi + (warp - 2) * 2 * kEpiBufBytes;
         const uint32_t swz = (lane >> 1) & 3u;         // 64-byte swizzle of this lane's row
@@ -718,7 +741,25 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             const int col_base = tn * G::kTileN + (half < 0 ? 0 : half * (G::kTileN / 2));
             const int buf = G::kAccBufs == 2 ? (local & 1) : 0;
             const uint32_t acc_phase = G::kAccBufs == 2 ? ((local >> 1) & 1) : (local & 1);
-            if (!wait_bounded_warp(p, acc_full_bar(buf), acc_phase, kErrEpiAccFull)) {
+            if constexpr (G::kAccBufs == 2) {
+                // One thread waits for the accumulator, suspended rather than polling (the
+                // issuing threads of the producer and the MMA share the SM's issue slots;
+                // measured 2-3 % fewer kernel cycles); the four epilogue warps then meet at
+                // a named barrier, where the other three wait without issuing. The result
+                // goes through a flag per tile parity: the writer of tile t+2's flag has
+                // passed tile t+1's barrier, so every warp has read tile t's.
+                volatile uint32_t* const acc_ok =
+                    reinterpret_cast<volatile uint32_t*>(smem + G::kOffTmemHolder + 4) + (local & 1);
+                if (warp == 2 && lane == 0)
+                    *acc_ok = wait_bounded_suspend(p, acc_full_bar(buf), acc_phase, kErrEpiAccFull) ? 1u : 0u;
+                __syncwarp();
+                named_barrier_sync(1, 32 * kEpiWarps);
+                if (*acc_ok == 0u) {
+                    abort_seen = true;
+                    break;
+                }
+            } else if (!wait_bounded_warp(p, acc_full_bar(buf), acc_phase, kErrEpiAccFull)) {
+                // one accumulator: the handoff is on the MMA's critical path, so every warp polls
                 abort_seen = true;
                 break;
             }

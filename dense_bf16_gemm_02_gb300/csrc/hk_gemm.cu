@@ -43,6 +43,9 @@ hk_status cuda_fail(hk_status s, const char* what, cudaError_t e) {
 #ifndef HK_PAIR_ATOMS
 #define HK_PAIR_ATOMS 2   // K atoms per stage of the bf16 pair kernel (128 K elements, 3 stages)
 #endif
+#ifndef HK_PDL
+#define HK_PDL 1   // launch every GEMM as a programmatic dependent of the previous kernel on its stream
+#endif
 #ifndef HK_FP8_PAIR_ATOMS
 #define HK_FP8_PAIR_ATOMS 1
 #endif
@@ -606,9 +609,11 @@ hk_status launch(const hk_gemm_plan* p, StatusWord* sw, const void* A, const voi
         attr[nattr].val.clusterDim.z = 1;
         ++nattr;
     }
-    if (mx_scales != nullptr) {
-        // a programmatic dependent of the scale arrangement: the prologue overlaps
-        // it, the producer waits (griddepcontrol.wait) before its first load
+    if (HK_PDL || mx_scales != nullptr) {
+        // a programmatic dependent of the previous kernel on the stream (for the
+        // block-scaled GEMM: of the scale arrangement): its prologue (barriers, TMEM,
+        // tensor-map prefetch) overlaps that kernel's last CTAs; the producer and the
+        // epilogue wait (griddepcontrol.wait) for that grid before any global access
         attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[nattr].val.programmaticStreamSerializationAllowed = 1;
         ++nattr;
@@ -728,6 +733,19 @@ hk_status one_shot_plan(int device, const DeviceInfo* di, int64_t M, int64_t N, 
     victim->last_use = ++g_oneshot_clock;
     *out = p;
     return HK_OK;
+}
+
+// Device address of hk_gemm_bf16_noalloc's fixed array per device (looked
+// up by its first call on the device); its first bytes are that entry
+// point's status word.
+std::mutex g_noalloc_mutex;
+unsigned char* g_noalloc_ptr[kMaxDevices] = {};
+
+// Status word of hk_gemm_bf16_noalloc's calls on `device`, or null when that
+// entry point has not run there.
+uint32_t* noalloc_status_word(int device) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    return reinterpret_cast<uint32_t*>(g_noalloc_ptr[device]);
 }
 
 }  // namespace
@@ -888,8 +906,15 @@ hk_status hk_gemm_last_device_status(int device) {
         std::lock_guard<std::mutex> lock(g_ctx_mutex);
         sw = g_ctx[device];
     }
-    if (!sw) return HK_OK;
-    return read_status(sw, device);
+    hk_status s = sw ? read_status(sw, device) : HK_OK;
+    // the calls of hk_gemm_bf16_noalloc keep their status word in the library's fixed array
+    StatusWord fixed;
+    fixed.dev = noalloc_status_word(device);
+    if (fixed.dev) {
+        const hk_status s2 = read_status(&fixed, device);   // read and cleared with no allocation
+        if (s == HK_OK) s = s2;
+    }
+    return s;
 }
 
 hk_status hk_gemm_plan_run_epilogue(const hk_gemm_plan* p, const void* A, const void* B, void* C, const void* bias,
@@ -1126,14 +1151,18 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocStatusB
 
 namespace {
 
-std::mutex g_noalloc_mutex;
-unsigned char* g_noalloc_ptr[kMaxDevices] = {};
-
 // Device address of the fixed array on `device` (the current device). Looked
 // up once per device; the host-side symbol itself is not a device address.
-hk_status noalloc_scratch(int device, unsigned char** out) {
+// The look-up is set-up work that a stream capture does not allow, so a first
+// call on a device made while `stream` captures is refused with a clear error.
+hk_status noalloc_scratch(int device, cudaStream_t stream, unsigned char** out) {
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
     if (!g_noalloc_ptr[device]) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs != cudaStreamCaptureStatusNone)
+            return fail(HK_ERR_INVALID_ARG,
+                        "the first hk_gemm_bf16_noalloc call on device %d looks up its fixed scratch array and must "
+                        "come before any stream capture", device);
         void* ptr = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess) return cuda_fail(HK_ERR_CUDA, "looking up the fixed scratch array", e);
@@ -1158,7 +1187,7 @@ hk_status hk_gemm_bf16_noalloc(const void* A, const void* B, void* C, int64_t M,
     const DeviceInfo* di = nullptr;
     if ((s = device_info(device, &di)) != HK_OK) return s;
     unsigned char* scratch = nullptr;
-    if ((s = noalloc_scratch(device, &scratch)) != HK_OK) return s;
+    if ((s = noalloc_scratch(device, static_cast<cudaStream_t>(stream), &scratch)) != HK_OK) return s;
 
     hk_gemm_config cfg;
     std::memset(&cfg, 0, sizeof cfg);

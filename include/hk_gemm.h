@@ -135,7 +135,11 @@ typedef struct hk_gemm_plan hk_gemm_plan;
  * Equivalent to a plan with the default config run with no workspace (the
  * default plan never needs one). The first call on a device creates a small
  * per-device context (a 16-byte device status word) and is therefore not
- * capturable in a CUDA graph; later calls allocate nothing. */
+ * capturable in a CUDA graph; later calls allocate nothing. The plans of
+ * recent shapes are kept (a small per-process cache, also used by
+ * hk_gemm_bf16_epilogue, hk_gemm_bf16_fused and hk_gemm_fp8_e4m3), and each
+ * keeps the tensor maps of its last A, B and C, so a repeated call does no
+ * planning and, with the same pointers, no tensor-map encoding. */
 hk_status hk_gemm_bf16(const void* A, const void* B, void* C,
                        int64_t M, int64_t N, int64_t K,
                        int64_t lda, int64_t ldb, int64_t ldc, void* stream);
@@ -264,8 +268,8 @@ size_t hk_gemm_mxfp8_workspace_size(int64_t M, int64_t N, int64_t K);
 hk_status hk_gemm_plan_device_status(hk_gemm_plan* plan);
 
 /* The same for the calls of the one-shot entry points (hk_gemm_bf16,
- * hk_gemm_bf16_epilogue, hk_gemm_fp8_e4m3, hk_gemm_mxfp8(_ex), hk_attention_fwd(_ex))
- * on `device`. */
+ * hk_gemm_bf16_epilogue, hk_gemm_bf16_fused, hk_gemm_fp8_e4m3, hk_gemm_mxfp8(_ex),
+ * hk_attention_fwd(_ex), hk_gemm_bf16_noalloc) on `device`. */
 hk_status hk_gemm_last_device_status(int device);
 
 void hk_gemm_plan_destroy(hk_gemm_plan* plan);
@@ -287,12 +291,13 @@ void hk_gemm_plan_destroy(hk_gemm_plan* plan);
  * set up through an allocating library routine.
  *
  * The first call on a device looks up the array's device address (once, with
- * that device current); make that first call before any stream capture.
+ * that device current); make that first call before any stream capture (a
+ * first call whose stream is capturing is refused with HK_ERR_INVALID_ARG).
  * All calls on a device share the array and it keeps the last call's
  * contents (nothing in it needs to start at zero). Calls that overlap on the
  * GPU race on it: order them on one stream or serialise them. A bounded wait
- * that runs out in this variant ends the kernel early without a status that
- * can be queried. */
+ * that runs out in this variant is reported by hk_gemm_last_device_status(),
+ * which reads and clears the status word in the array without allocating. */
 hk_status hk_gemm_bf16_noalloc(const void* A, const void* B, void* C,
                                int64_t M, int64_t N, int64_t K,
                                int64_t lda, int64_t ldb, int64_t ldc,

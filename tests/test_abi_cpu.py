@@ -148,3 +148,27 @@ def test_mxfp8_host_validation_without_gpu(lib):
     sizes = [lib.hk_gemm_mxfp8_workspace_size(m, n, k) for m, n, k in
              [(64, 64, 128), (64, 64, 256), (64, 512, 256), (300, 512, 256), (8192, 8192, 8192)]]
     assert sizes == sorted(sizes) and sizes[0] < sizes[-1]
+
+
+def test_no_multicast_bulk_copies():
+    """No TMA or bulk copy in the library's sources carries a multicast
+    qualifier: every load reads this GPU's memory into the issuing CTA only
+    (a pair's loads of one stage complete on the leader CTA's barrier, without
+    multicast). The one multicast form that stays is tcgen05.commit's
+    `.multicast::cluster`, an mbarrier arrival on the two CTAs of one pair, not
+    a copy. The rule is checked on the code of every source under csrc/ and
+    include/ (comments excluded)."""
+    bad = []
+    for d in ("dense_bf16_gemm_02_gb300/csrc", "include"):
+        for f in sorted(os.listdir(os.path.join(ROOT, d))):
+            if not f.endswith((".cu", ".cuh", ".h")):
+                continue
+            text = open(os.path.join(ROOT, d, f), encoding="utf-8").read()
+            code = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            code = re.sub(r"//[^\n]*", " ", code)
+            for m in re.finditer(r'"[^"\n]*multicast[^"\n]*"', code):
+                lit = m.group(0)
+                if "cp.async.bulk" in lit or "cp.reduce.async.bulk" in lit or not lit.lstrip('"').startswith(
+                        "tcgen05.commit"):
+                    bad.append(f"{d}/{f}: {lit}")
+    assert not bad, bad

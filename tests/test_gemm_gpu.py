@@ -530,6 +530,55 @@ def test_epilogue_argument_errors(hk):
                                     64, 64, 64, 7, 0) == hk.HK_ERR_INVALID_ARG
 
 
+# ------------------------------------------------------- plan caches --
+
+def test_one_shot_cache_with_changing_pointers_and_many_shapes(hk):
+    """The one-shot call caches plans (32 shapes, least recently used) and each
+    plan the tensor maps of its last pointers: calls that alternate buffers of
+    one shape, and more shapes than the cache holds (evictions), stay exact."""
+    import torch
+    M, N, K = 300, 520, 136
+    bufs = []
+    for i in range(3):
+        A, B = synth.int_bf16(M, K, 5100 + i), synth.int_bf16(N, K, 5200 + i)
+        bufs.append((A, B, to_device(A)[0], to_device(B)[0]))
+    Cs = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    stream = int(torch.cuda.current_stream().cuda_stream)
+    for it in range(6):
+        A, B, At, Bt = bufs[it % 3]
+        C = Cs[it % 2]
+        assert hk.hk_gemm_bf16(At.data_ptr(), Bt.data_ptr(), C.data_ptr(), M, N, K, K, K, N, stream) == hk.HK_OK
+        torch.cuda.synchronize()
+        assert_bitexact(to_host(C), oracle.gemm(A, B), f"alternating buffers, call {it}")
+    for i in range(40):                      # 40 distinct shapes: the cache evicts
+        m, n, k = 16 + 8 * i, 40 + 8 * (i % 7), 24 + 8 * (i % 5)
+        A, B = synth.int_bf16(m, k, 5300 + i), synth.int_bf16(n, k, 5400 + i)
+        At, _ = to_device(A)
+        Bt, _ = to_device(B)
+        C = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+        assert hk.hk_gemm_bf16(At.data_ptr(), Bt.data_ptr(), C.data_ptr(), m, n, k, k, k, n, stream) == hk.HK_OK
+        torch.cuda.synchronize()
+        assert_bitexact(to_host(C), oracle.gemm(A, B), f"shape {m}x{n}x{k}")
+    assert hk.hk_gemm_last_device_status(torch.cuda.current_device()) == hk.HK_OK
+
+
+def test_plan_run_with_changing_pointers(hk):
+    import torch
+    M, N, K = 260, 300, 200
+    plan = hk.Plan(M, N, K, lda=K + 8, ldb=K + 8, ldc=N + 4)
+    for it in range(4):
+        A, B = synth.int_bf16(M, K, 5500 + it), synth.int_bf16(N, K, 5600 + it)
+        At, _ = to_device(A, cols_pad=8)
+        Bt, _ = to_device(B, cols_pad=8)
+        C, Cstore = to_device(np.zeros((M, N), dtype=np.uint16), cols_pad=4)
+        st = plan.run_raw(At.data_ptr(), Bt.data_ptr(), C.data_ptr(), 0, 0, int(torch.cuda.current_stream().cuda_stream))
+        assert st == hk.HK_OK, hk.hk_gemm_last_error_string()
+        torch.cuda.synchronize()
+        assert_bitexact(to_host(Cstore)[:M, :N], oracle.gemm(A, B), f"plan run {it}")
+    assert plan.device_status() == hk.HK_OK
+    plan.close()
+
+
 # ------------------------------------------------- fused residual add --
 
 def run_fused(hk, A_bits, B_bits, bias_bits, R_bits, act, split_k=None, kernel=0, in_place=False, ldr_pad=0):
