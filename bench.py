@@ -624,14 +624,39 @@ def mx_config(w) -> dict:
             "tile": "256x256 per CTA pair (M > 128; 128x192 per CTA otherwise)"}
 
 
-def oracle_mx_rows_timed(A, B, SA, SB, rows) -> tuple[float, int]:
+def oracle_mx_rows_timed(A, B, SA, SB, rows, with_values: bool = False):
     import oracle
     N = B.shape[0]
     rr = np.repeat(np.asarray(rows, dtype=np.int64), N)
     cc = np.tile(np.arange(N, dtype=np.int64), len(rows))
     t0 = time.perf_counter()
-    oracle.gemm_mxfp8_entries(A, B, SA, SB, rr, cc)
-    return time.perf_counter() - t0, os.cpu_count() or 1
+    vals = oracle.gemm_mxfp8_entries(A, B, SA, SB, rr, cc).reshape(len(rows), N)
+    dt = time.perf_counter() - t0
+    return (dt, os.cpu_count() or 1, vals) if with_values else (dt, os.cpu_count() or 1)
+
+
+def mx_parity_check(A, B, SA, SB, rows_ref, C_gpu) -> dict:
+    """Rows 0..r-1 of the timed run's C against the oracle's, per entry within
+    2^-7·|C_ref| + 2^-16·Σ_b 2^(SA+SB-254)·Σ_{k in b} |A·B| (one bf16 rounding
+    plus fp32 accumulation with margin); a miss fails the bench."""
+    r = rows_ref.shape[0]
+    import torch
+    dec = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    dec = np.where(np.isnan(dec), 0.0, dec)
+    a = np.abs(dec[A[:r]]) * np.repeat(np.exp2(SA[:r].astype(np.float64) - 127), 32, axis=1)
+    b = np.abs(dec[B]) * np.repeat(np.exp2(SB.astype(np.float64) - 127), 32, axis=1)
+    mag = a @ b.T
+    ref = synth.bf16_bits_to_f32(rows_ref).astype(np.float64)
+    got = synth.bf16_bits_to_f32(C_gpu[:r]).astype(np.float64)
+    tol = 2.0 ** -7 * np.abs(ref) + 2.0 ** -16 * mag
+    err = np.abs(got - ref)
+    bad = ~(err <= tol)
+    check = {"entries": int(ref.size), "full_rows": r, "misses": int(bad.sum()),
+             "max_err_over_tol": float(np.max(err / np.maximum(tol, 1e-300))),
+             "tolerance": "2^-7·|C_ref| + 2^-16·Σ_b scale_a·scale_b·Σ|A·B| per entry, against the fp64 oracle"}
+    if bad.any():
+        raise RuntimeError(f"parity check of the timed run's C against the oracle failed: {check}")
+    return check
 
 
 def run_reference_mx(args, w):
@@ -814,9 +839,11 @@ def run_mx(args, w):
     if not args.no_cpu_baseline:
         t, used = oracle_mx_rows_timed(Ab, Bb, SAb, SBb, np.arange(2))
         rows = int(max(1, min(w.M, 15.0 / max(t / 2, 1e-6))))
-        t, used = oracle_mx_rows_timed(Ab, Bb, SAb, SBb, np.arange(rows))
+        t, used, ref_rows = oracle_mx_rows_timed(Ab, Bb, SAb, SBb, np.arange(rows), with_values=True)
         line["cpu_baseline"] = {"value": gemm_flops(rows, w.N, w.K) / t / 1e12, "unit": UNIT, "cores": used,
                                 "kind": "oracle", "sample": f"rows 0..{rows - 1} of C (fp64 C oracle, {t:.1f} s)"}
+        line["parity_check"] = mx_parity_check(Ab, Bb, SAb, SBb, ref_rows,
+                                               C.view(torch.int16).cpu().numpy().view(np.uint16))
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -850,13 +877,15 @@ def attn_config(w) -> dict:
             "softmax_scale": "1/sqrt(D)", "accumulate": "fp32", "output": "bf16"}
 
 
-def oracle_attn_rows_timed(Q, K, V, w, rows) -> tuple[float, int]:
-    """The oracle on `rows` (query rows of head (0, 0)); returns (seconds, threads)."""
+def oracle_attn_rows_timed(Q, K, V, w, rows, with_values: bool = False):
+    """The oracle on `rows` (query rows of head (0, 0)); returns (seconds, threads[, O rows as bf16 bits])."""
     import oracle
     q1, k1, v1 = (np.ascontiguousarray(x[:1, :1]) for x in (Q, K, V))
     t0 = time.perf_counter()
-    oracle.attention_fwd(q1, k1, v1, causal=w.causal, rows=(0, rows))
-    return time.perf_counter() - t0, min(os.cpu_count() or 1, rows)
+    O = oracle.attention_fwd(q1, k1, v1, causal=w.causal, rows=(0, rows))
+    dt = time.perf_counter() - t0
+    used = min(os.cpu_count() or 1, rows)
+    return (dt, used, O[0, 0, :rows]) if with_values else (dt, used)
 
 
 def attn_row_flops(w, rows: int) -> float:
@@ -864,14 +893,35 @@ def attn_row_flops(w, rows: int) -> float:
     return 4.0 * w.D * pairs
 
 
-def attn_cpu_sample(w, Q, K, V, budget_s: float) -> tuple[float, int, int, float]:
+def attn_cpu_sample(w, Q, K, V, budget_s: float):
+    """(oracle TFLOP/s, threads, query rows, seconds, those rows of O) on head (0, 0)."""
     rows = min(w.S, 64)
     t, _ = oracle_attn_rows_timed(Q, K, V, w, rows)
     rate = attn_row_flops(w, rows) / max(t, 1e-6)
     while rows < w.S and attn_row_flops(w, min(w.S, rows * 2)) / rate < budget_s:
         rows = min(w.S, rows * 2)
-    t, used = oracle_attn_rows_timed(Q, K, V, w, rows)
-    return attn_row_flops(w, rows) / t / 1e12, used, rows, t
+    t, used, O_ref = oracle_attn_rows_timed(Q, K, V, w, rows, with_values=True)
+    return attn_row_flops(w, rows) / t / 1e12, used, rows, t, O_ref
+
+
+def attn_parity_check(w, V, O_ref, O_gpu) -> dict:
+    """Query rows 0..r-1 of head (0, 0) of the timed run's O against the
+    oracle's, per entry within (2^-7 + S·2^-24)·max|V| + 2^-8·|O_ref| (bf16
+    rounding of P, fp32 scores and accumulation, the output rounding; the
+    weighted |V| of a row is at most max|V|); a miss fails the bench."""
+    r = O_ref.shape[0]
+    vmax = float(np.max(np.abs(synth.bf16_bits_to_f32(V[0, 0]).astype(np.float64))))
+    ref = synth.bf16_bits_to_f32(O_ref).astype(np.float64)
+    got = synth.bf16_bits_to_f32(O_gpu[0, 0, :r]).astype(np.float64)
+    tol = (2.0 ** -7 + w.S * 2.0 ** -24) * vmax + 2.0 ** -8 * np.abs(ref)
+    err = np.abs(got - ref)
+    bad = ~(err <= tol)
+    check = {"entries": int(ref.size), "query_rows": r, "misses": int(bad.sum()),
+             "max_err_over_tol": float(np.max(err / tol)),
+             "tolerance": "(2^-7 + S·2^-24)·max|V| + 2^-8·|O_ref| per entry, against the fp64 oracle"}
+    if bad.any():
+        raise RuntimeError(f"parity check of the timed run's O against the oracle failed: {check}")
+    return check
 
 
 def run_reference_attn(args, w):
@@ -880,7 +930,7 @@ def run_reference_attn(args, w):
         return 0
     Q, K, V = synth.attn_operands(w)
     per_step = 120.0 / (args.steps + args.warmup)
-    _, _, rows, _ = attn_cpu_sample(w, Q, K, V, per_step)
+    _, _, rows, _, _ = attn_cpu_sample(w, Q, K, V, per_step)
     for _ in range(args.warmup):
         oracle_attn_rows_timed(Q, K, V, w, rows)
     total, used = 0.0, 0
@@ -1063,9 +1113,10 @@ def run_attn(args, w):
         "context_sdpa": sdpa,
     }
     if not args.no_cpu_baseline:
-        v, used, rows, t = attn_cpu_sample(w, Qb, Kb, Vb, 15.0)
+        v, used, rows, t, O_ref = attn_cpu_sample(w, Qb, Kb, Vb, 15.0)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": used, "kind": "oracle",
                                 "sample": f"query rows 0..{rows - 1} of head (0,0) (fp64 C oracle, {t:.1f} s)"}
+        line["parity_check"] = attn_parity_check(w, Vb, O_ref, O.view(torch.int16).cpu().numpy().view(np.uint16))
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
