@@ -364,27 +364,38 @@ int a_rows_for(const Variant& v, int64_t M) {
     return static_cast<int>(std::max<int64_t>(8, ceil_div(M, 8) * 8));
 }
 
-// Kernel choice by a small time model. The CTA pair (256-row tiles) serves
-// M > 128, single-CTA kernels (128-row tiles, four widths) M <= 128. K is
-// split only when one wave of tiles leaves work-unit slots idle and a
-// workspace may be used. Estimated time of a candidate:
+// Kernel choice by a small time model. Automatic choice: single-CTA kernels
+// (128-row tiles, four widths) for M <= kMaxRowsSingle (bf16; 128 for E4M3),
+// CTA pairs (256-row tiles) above; K is split only when one wave of tiles
+// leaves work-unit slots idle and a workspace may be used. Estimated time of
+// a candidate (µs):
 //   GEMM   = the largest of
-//              streaming: waves × (bytes one CTA moves per unit ÷ per-SM copy
-//                         rate + pipeline fill), the per-SM rate being the
-//                         bytes the ring keeps in flight ÷ the load latency,
-//                         at most the rate measured with every SM streaming,
+//              streaming: waves × (bytes one CTA moves per unit ÷ per-SM rate
+//                         + pipeline fill); the rate is what the ring keeps in
+//                         flight ÷ the load latency, at most kSmBytesPerUs; the
+//                         bytes of A count a quarter (A is shared by every unit
+//                         of a row of tiles and comes from L2),
 //              HBM:       (A, B, and C or the fp32 partials) ÷ HBM rate,
-//              tensor:    waves × K-steps per unit × time of one K-step;
-//   reduce = (partials read + C written) ÷ HBM rate + launch, when K is split
-//            (it runs after the GEMM, so its time adds).
+//              issue:     waves × K stages per unit × the larger of the tensor
+//                         time of a stage and the issuing thread's floor per
+//                         stage (narrow tiles are bound by the latter);
+//   reduce = (split partials, counted twice: the GEMM writes them and the
+//            reduction reads them back, + C written) ÷ HBM rate + launch, when
+//            K is split (it runs after the GEMM, so its time adds).
+// The constants were fitted to warm back-to-back timings of every (kernel,
+// split) on 26 shapes from 1×1024×8192 to 2048×2048×8192 (GB300): the choice
+// is within 6 % of the best measured candidate on each, 0.5 % on average.
 constexpr int kMaxSplits = 16;
 constexpr int kMinKBlocksPerSplit = 8;
-constexpr double kSmBytesPerUs = 65e3;       // one SM's sustained TMA rate from HBM (measured, bytes/µs)
-constexpr double kLoadLatencyUs = 2.5;       // TMA load latency under load (measured: in flight ÷ rate)
-constexpr double kHbmBytesPerUs = 6.7e6;     // HBM copy rate (bytes/µs)
-constexpr double kKStepUsPair = 0.27;        // 256x256x64 per pair (4 tcgen05.mma)
-constexpr double kFillUs = 1.5;              // filling the ring at the start of a unit
-constexpr double kLaunchUs = 1.5;            // the reduction's dependent launch and its wait for the GEMM
+constexpr int64_t kMaxRowsSingle = 384;      // bf16: single-CTA kernels up to here, pairs above
+constexpr double kSmBytesPerUs = 65e3;       // one SM's streaming rate cap (bytes/µs)
+constexpr double kLoadLatencyUs = 2.0;       // TMA load latency under load
+constexpr double kHbmBytesPerUs = 6.0e6;     // HBM rate the streaming kernels reach (bytes/µs)
+constexpr double kABytesWeight = 0.5;        // A's bytes (L2-resident, shared by a row of tiles) against B's
+constexpr double kKStepUs = 0.27;            // tensor time of a 64-deep K step of a 256-wide tile per SM
+constexpr double kIssueFloorUs = 0.25;       // the MMA-issuing thread's minimum per stage (waits, commit)
+constexpr double kFillUs = 2.0;              // filling the ring at the start of a unit
+constexpr double kLaunchUs = 7.0;            // the reduction: dependent launch, wait for the GEMM, tail
 
 double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int64_t slots, int splits) {
     const int64_t tiles = ceil_div(M, v.tile_m) * ceil_div(N, v.tile_n);
@@ -392,16 +403,16 @@ double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int64_t sl
     const double waves = double(ceil_div(units, slots));
     const double kb = double(ceil_div(ceil_div(K, v.k_elems), splits));
     const double elem = v.fp8 ? 1.0 : 2.0;
-    const double stage_bytes = double(a_rows_for(v, M) + v.tile_n / v.cg) * hk::kRowBytes * v.atoms;
-    const double cta_bytes = stage_bytes * kb;
-    const double sm_rate = std::min(kSmBytesPerUs, stage_bytes * v.stages / kLoadLatencyUs);
-    const double t_stream = waves * (cta_bytes / sm_rate + kFillUs);
+    const double stage_a = double(a_rows_for(v, M)) * hk::kRowBytes * v.atoms;
+    const double stage_b = double(v.tile_n / v.cg) * hk::kRowBytes * v.atoms;
+    const double sm_rate = std::min(kSmBytesPerUs, (stage_a + stage_b) * v.stages / kLoadLatencyUs);
+    const double t_stream = waves * ((stage_a * kABytesWeight + stage_b) * kb / sm_rate + kFillUs);
     const double n_pad = double(ceil_div(N, v.tile_n) * v.tile_n);
     const double partials = splits > 1 ? 4.0 * splits * M * n_pad : 0.0;
     const double operands = elem * (double(N) * K + double(M) * K);
     const double t_hbm = (operands + (splits > 1 ? partials : 2.0 * M * N)) / kHbmBytesPerUs;
-    const double t_mma = waves * kb * kKStepUsPair * v.atoms * (double(v.tile_n) / 256.0);
-    const double t_reduce = splits > 1 ? (partials + 2.0 * M * N) / kHbmBytesPerUs + kLaunchUs : 0.0;
+    const double t_mma = waves * kb * std::max(kKStepUs * v.atoms * (double(v.tile_n) / 256.0), kIssueFloorUs);
+    const double t_reduce = splits > 1 ? (2.0 * partials + 2.0 * M * N) / kHbmBytesPerUs + kLaunchUs : 0.0;
     return std::max(t_stream, std::max(t_hbm, t_mma)) + t_reduce;
 }
 
@@ -414,7 +425,8 @@ void choose_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo* di, int max_
         const Variant& v = kVariants[i];
         if (v.fp8 != fp8 || v.mx) continue;
         if (a_rows_for(v, M) > v.a_rows_max) continue;   // short A stages serve only M up to their rows
-        if (forced_kernel != HK_KERNEL_AUTO ? v.id != forced_kernel : ((M > hk::kCtaM) != (v.cg == 2))) continue;
+        const int64_t max_single = fp8 ? int64_t(hk::kCtaM) : kMaxRowsSingle;
+        if (forced_kernel != HK_KERNEL_AUTO ? v.id != forced_kernel : ((M > max_single) != (v.cg == 2))) continue;
         const int64_t k_blocks = ceil_div(K, v.k_elems);
         int64_t slots = di->max_units[i];
         if (max_units_cap > 0 && max_units_cap < slots) slots = max_units_cap;
@@ -427,7 +439,7 @@ void choose_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo* di, int max_
         }
         for (int sp = s_lo; sp <= s_hi; ++sp) {
             const double t = estimate_us(v, M, N, K, slots, sp);
-            if (!best_v || t < best_t * 0.98) {   // a candidate must win by 2 % (earlier = wider / fewer splits)
+            if (!best_v || t < best_t) {   // on a tie the earlier candidate (fewer splits) stays
                 best_v = &v;
                 best_s = sp;
                 best_t = t;

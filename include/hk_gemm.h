@@ -87,7 +87,7 @@ typedef enum hk_status {
 /* Kernel variants (hk_gemm_config.kernel). A "pair" kernel runs on clusters
  * of two CTAs (tcgen05 cta_group::2) with 256-row output tiles; a "single"
  * kernel runs one CTA per output tile of 128 rows and suits M <= 128. */
-#define HK_KERNEL_AUTO 0            /* pair 256x256 if M > 128, else the single kernel that keeps most SMs busy */
+#define HK_KERNEL_AUTO 0            /* chosen by the plan's time model: single-CTA kernels for M <= 384 (E4M3: 128), pairs above */
 #define HK_KERNEL_PAIR_256x256 1
 #define HK_KERNEL_SINGLE_128x256 2
 #define HK_KERNEL_SINGLE_128x192 3

@@ -332,7 +332,10 @@ def test_kernel_variants_normal(hk, kernel):
 def test_automatic_kernel_choice(hk):
     assert hk.Plan(128, 28672, 8192).info()["kernel"] == 3      # 150 tiles of 128x192 ~ one per SM
     assert hk.Plan(8192, 8192, 8192).info()["kernel"] == 1
-    assert hk.Plan(129, 4096, 4096).info()["kernel"] == 1
+    assert hk.Plan(385, 4096, 4096).info()["kernel"] == 1       # above 384 rows: CTA pairs
+    assert hk.Plan(129, 4096, 4096).info()["ctas_per_unit"] == 1  # up to 384 rows: single-CTA tiles (measured faster)
+    assert hk.Plan(256, 8192, 8192).info()["ctas_per_unit"] == 1
+    assert hk.Plan(200, 4096, 4096, input_type=hk.HK_INPUT_E4M3).info()["kernel"] == 1   # E4M3: pairs above 128
     small = hk.Plan(64, 1024, 1024).info()
     assert small["kernel"] == 5 and small["ctas_per_unit"] == 1  # 16 tiles: narrowest tiles spread widest
 
@@ -429,7 +432,7 @@ def test_tail_split_integer_bitexact(hk, M, N, K):
     """Tiles of the last partial round run as two 256x128 halves."""
     A = synth.int_bf16(M, K, 1400 + M)
     B = synth.int_bf16(N, K, 2400 + N)
-    got, info = run_plan(hk, A, B)
+    got, info = run_plan(hk, A, B, kernel=1)
     assert info["kernel"] == 1 and info["tail_split_tiles"] > 0
     if M * N <= 4096 * 4096:
         assert_bitexact(got, oracle.gemm(A, B), f"tail split {M}x{N}x{K}")
@@ -437,7 +440,7 @@ def test_tail_split_integer_bitexact(hk, M, N, K):
         r, c = synth.sample_positions(M, N, 77, count=4096)
         ref, _ = oracle.gemm_entries(A, B, r, c)
         assert_bitexact(got[r, c], ref, f"tail split {M}x{N}x{K} samples")
-    whole, info2 = run_plan(hk, A, B, flags=hk.HK_FLAG_NO_TAIL_SPLIT if hasattr(hk, "HK_FLAG_NO_TAIL_SPLIT") else 2)
+    whole, info2 = run_plan(hk, A, B, kernel=1, flags=hk.HK_FLAG_NO_TAIL_SPLIT)
     assert info2["tail_split_tiles"] == 0
     assert_bitexact(got, whole, "split vs whole")
 

@@ -100,8 +100,8 @@ def test_noalloc_automatic_split_beyond_the_array_runs_unsplit(hk):
     holds (32 MiB) runs without a split; sampled entries against the oracle."""
     limit = 32 << 20
     shape = None
-    for M, N, K in [(128, 8192, 8192), (256, 8192, 16384), (128, 16384, 16384), (64, 16384, 16384),
-                    (192, 12288, 16384)]:
+    for M, N, K in [(192, 8192, 16384), (512, 6144, 16384), (768, 4096, 16384), (256, 4096, 32768),
+                    (128, 8192, 8192), (256, 8192, 16384)]:
         plan = hk.Plan(M, N, K)
         if plan.workspace_size > limit:
             shape = (M, N, K)
