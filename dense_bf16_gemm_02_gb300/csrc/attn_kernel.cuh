@@ -18,7 +18,10 @@
 //  * one thread issues tcgen05.mma: S_t = Q_t·K_jᵀ (M=128, N=128, K=D) into
 //    Tensor Memory, and O_t += P_t·V_j (M=128, N=D, K=128) with P_t and V_j
 //    (MN-major, so V is never transposed) read from shared memory;
-//  * two softmax warpgroups, one per query tile, each thread owning one row:
+//  * two softmax warpgroups, one per query tile, each thread owning one row
+//    (optionally at D = 64 two warpgroups per tile, each thread owning half a
+//    row: the halves swap partial row maxima and, at the end, row sums through
+//    shared memory with a bounded tagged exchange):
 //    tcgen05.ld of the row of S, then at once a "S read" signal, so that the
 //    MMA thread computes S_t for the next block while this one is still in
 //    masking, row max, exp2 on the special function unit and row sum; the
@@ -46,15 +49,16 @@
 
 #include "ptx.cuh"
 
+#ifndef HK_ATTN_D64_ROW_SPLIT
+#define HK_ATTN_D64_ROW_SPLIT 1
+#endif
+
 namespace hk {
 namespace attn {
 
 constexpr int kTileQ = 128;         // query rows per tile (MMA M)
 constexpr int kTiles = 2;           // query tiles per CTA
 constexpr int kBlockKV = 128;       // keys per K/V block
-constexpr int kThreads = 352;       // warps 0-3 softmax tile 0, 4-7 softmax tile 1, 8 TMA, 9-10 MMA
-constexpr int kWarpTma = 8;
-constexpr int kWarpMma = 9;
 constexpr int kSmemLimit = 232448;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O when the max grows by > 2^8
 
@@ -64,12 +68,27 @@ constexpr uint32_t kErrMmaP = 1u << 10;
 constexpr uint32_t kErrMmaO = 1u << 11;
 constexpr uint32_t kErrSoftmaxS = 1u << 12;
 constexpr uint32_t kErrEpilogueO = 1u << 13;
+constexpr uint32_t kErrSoftmaxPair = 1u << 14;
 
 constexpr uint32_t kFlagDropArrive = 0x1u;
 
 template <int kD>
 struct AttnGeometry {
     static_assert(kD == 64 || kD == 128, "head dimension 64 or 128");
+    // Softmax threads per query row. At D = 64 a block's MMAs take half the
+    // time of D = 128's while its softmax work per score is the same; a row can
+    // be split over two threads (64 scores each; warps w and w + 8 read the
+    // same TMEM lanes) that exchange partial maxima through shared memory
+    // (HK_ATTN_D64_ROW_SPLIT = 2). Measured at B16 H64/8 S4096 D64: 848 TFLOP/s
+    // split against 943 whole (608 threads leave ~100 registers per thread,
+    // and each row then waits for its partner), so rows stay whole.
+    static constexpr int kRowSplit = kD == 64 ? HK_ATTN_D64_ROW_SPLIT : 1;
+    static constexpr int kCols = kBlockKV / kRowSplit;         // scores of a block per softmax thread
+    static constexpr int kSoftmaxWarps = 4 * kTiles * kRowSplit;
+    static constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+    static constexpr int kWarpTma = kSoftmaxWarps;             // then one MMA-issuing warp per tile
+    static constexpr int kWarpMma = kSoftmaxWarps + 1;
+    static constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kTiles);
     static constexpr int kChunks = kD / 64;                   // 128-byte column chunks per row
     static constexpr int kChunkBytes = 128 * 128;             // 128 rows × 128 B (one TMA box)
     static constexpr int kTileBytes = kChunks * kChunkBytes;  // one Q tile, one K block or one V block
@@ -88,7 +107,11 @@ struct AttnGeometry {
     // q_full, kv_full[kSlots], kv_empty[kSlots], s_full[2], s_free[2], p_full[2], o_done[2], q_empty
     static constexpr int kNumBars = 1 + 2 * kSlots + 9;
     static constexpr int kOffTmemHolder = kOffBars + kNumBars * 8;
-    static constexpr int kSmemBytes = kOffTmemHolder + 16 + 1024;
+    // split rows: the halves' exchange slots, [parity][tile][row][half] of
+    // (value, tag) pairs (a partial maximum or row sum and its exchange number)
+    static constexpr int kOffXchg = (kOffTmemHolder + 16 + 15) & ~15;
+    static constexpr int kXchgBytes = kRowSplit > 1 ? 2 * kTiles * kTileQ * kRowSplit * 8 : 0;
+    static constexpr int kSmemBytes = kOffXchg + kXchgBytes + 1024;
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
     // TMEM columns: O_0, O_1 (kD each), then S_0, S_1 (128 each), then (D = 64)
     // P_0, P_1 (64 each: two bf16 per column)
@@ -207,10 +230,12 @@ __device__ __forceinline__ AttnItem attn_item(const AttnParams& p, int w) {
 }
 
 template <int kD>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(AttnGeometry<kD>::kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
     using G = AttnGeometry<kD>;
+    constexpr int kWarpTma = G::kWarpTma;
+    constexpr int kWarpMma = G::kWarpMma;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -246,8 +271,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         }
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(s_full(t), 1);
-            mbar_init(s_free(t), 4 * 32);
-            mbar_init(p_full(t), 4 * 32);
+            mbar_init(s_free(t), 4 * 32 * G::kRowSplit);   // every softmax thread of the tile
+            mbar_init(p_full(t), 4 * 32 * G::kRowSplit);
             mbar_init(o_done(t), 1);
         }
         fence_mbar_init_cluster();
@@ -260,6 +285,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     if (warp == kWarpMma) {
         tmem_alloc_one(tmem_holder, G::kTmemCols);
         tmem_relinquish_one();
+    }
+    if constexpr (G::kXchgBytes > 0) {   // exchange tags start at 0 (the first exchange is number 1)
+        for (int i = static_cast<int>(threadIdx.x); i < G::kXchgBytes / 4; i += static_cast<int>(blockDim.x))
+            reinterpret_cast<volatile uint32_t*>(smem + G::kOffXchg)[i] = 0u;
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -411,13 +440,45 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         }
     } else {
         // ------------------------------------------ softmax warpgroups --
-        const int t = static_cast<int>(warp) >> 2;
+        // Warp w: tile (w / 4) % 2, TMEM lane quarter w % 4 (the quarter a warp
+        // may access), and with split rows half w / 8 of each row's scores.
+        constexpr int kSplit = G::kRowSplit;
+        constexpr int kCols = G::kCols;
+        const int t = static_cast<int>(warp >> 2) & 1;
         const uint32_t quarter = warp & 3u;
+        const int half = kSplit > 1 ? static_cast<int>(warp >> 3) : 0;
         const int r = static_cast<int>(quarter * 32 + lane);
         const uint32_t lane_off = (quarter * 32u) << 16;
-        const uint32_t s_addr = tmem_base + lane_off + G::kColS + t * kBlockKV;
+        const uint32_t s_addr = tmem_base + lane_off + G::kColS + t * kBlockKV + half * kCols;
         const uint32_t o_addr = tmem_base + lane_off + G::kColO + t * kD;
         const float c = p.scale_log2;
+        // Split rows: the two threads of a row swap a value (partial maximum, row
+        // sum) through shared memory. Each writes its value, then the exchange's
+        // number as a tag, and polls (bounded) for its partner's tag: no hardware
+        // barrier, so a half that gives up on a wait cannot leave the other
+        // stuck. Slots alternate by exchange parity: a half writes a slot again
+        // only after reading its partner's next tag, written after the partner
+        // read this slot.
+        uint32_t xn = 0;   // exchanges so far (the same sequence in both halves)
+        auto exchange = [&](float mine, float& theirs) -> bool {
+            volatile uint32_t* const x = reinterpret_cast<volatile uint32_t*>(smem + G::kOffXchg) +
+                                         2 * ((((xn & 1) * kTiles + t) * kTileQ + r) * kSplit);
+            const uint32_t tag = ++xn;
+            x[2 * half] = __float_as_uint(mine);
+            __threadfence_block();
+            x[2 * half + 1] = tag;
+            uint64_t t0 = 0;
+            for (uint32_t it = 1; x[2 * (half ^ 1) + 1] != tag; ++it) {
+                if ((it & 1023u) == 0) {
+                    const uint64_t now = global_timer_ns();
+                    if (t0 == 0) t0 = now;
+                    else if (now - t0 >= 20000 && attn_wait_expired(p, now - t0, kErrSoftmaxPair)) return false;
+                }
+            }
+            __threadfence_block();
+            theirs = __uint_as_float(x[2 * (half ^ 1)]);
+            return true;
+        };
         uint32_t jp = 0;   // parity of this tile's blocks in earlier items
         for (int w = first_item; w < p.n_items && !abort_seen; w += item_step) {
             int n, key_end;
@@ -428,7 +489,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 key_end = p.causal ? (q + 1 < p.S ? q + 1 : p.S) : p.S;   // keys [0, key_end) are visible
             }
             float m = 0.0f;   // running max of the scaled scores (log2 units) used for P
-            float l = 0.0f;   // running sum of P
+            float l = 0.0f;   // running sum of P (of this thread's columns)
             for (int j = 0; j < n; ++j) {
                 const uint32_t par = jp ^ static_cast<uint32_t>(j & 1);   // phase of this block's barriers
                 if (!attn_wait_warp(p, s_full(t), par, kErrSoftmaxS)) {
@@ -436,25 +497,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     break;
                 }
                 tc_fence_after_sync();
-                uint32_t v[128];
+                uint32_t v[kCols];
                 tmem_load_32cols_at<0>(s_addr + 0, v);
                 tmem_load_32cols_at<32>(s_addr + 32, v);
-                tmem_load_32cols_at<64>(s_addr + 64, v);
-                tmem_load_32cols_at<96>(s_addr + 96, v);
+                if constexpr (kCols == 128) {
+                    tmem_load_32cols_at<64 % kCols>(s_addr + 64, v);
+                    tmem_load_32cols_at<96 % kCols>(s_addr + 96, v);
+                }
                 tmem_wait_ld();
                 // S is in registers: the MMA thread may compute the next block's S here
                 tc_fence_before_sync();
                 mbar_arrive(s_free(t));
-                const int lim = key_end - j * kBlockKV;     // visible columns of this block
-                if (lim < kBlockKV) {
+                const int lim = key_end - j * kBlockKV - half * kCols;     // visible columns of this thread's share
+                if (lim < kCols) {
 #pragma unroll
-                    for (int e = 0; e < 128; ++e)
+                    for (int e = 0; e < kCols; ++e)
                         if (e >= lim) v[e] = __float_as_uint(-INFINITY);
                 }
-                // row max: eight independent chains of three-input maxima, then a tree
-                float acc[8];
+                // row max: independent chains of three-input maxima, then a tree
+                constexpr int kChains = kCols / 16;
+                float acc[kChains];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
+                for (int k = 0; k < kChains; ++k) {
                     const int e0 = 16 * k;
                     float a = fmax3(__uint_as_float(v[e0]), __uint_as_float(v[e0 + 1]), __uint_as_float(v[e0 + 2]));
 #pragma unroll
@@ -462,8 +526,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         a = fmax3(a, __uint_as_float(v[e0 + e]), __uint_as_float(v[e0 + e + 1]));
                     acc[k] = fmaxf(a, __uint_as_float(v[e0 + 15]));
                 }
-                const float mx = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
-                                       fmaxf(acc[6], acc[7]));
+                float mx;
+                if constexpr (kChains == 8)
+                    mx = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]), fmaxf(acc[6], acc[7]));
+                else
+                    mx = fmaxf(fmax3(acc[0], acc[1], acc[2]), acc[3]);
+                if constexpr (kSplit > 1) {   // the row's maximum over both halves
+                    float other;
+                    if (!exchange(mx, other)) {
+                        abort_seen = true;
+                        break;
+                    }
+                    mx = fmaxf(mx, other);
+                }
                 const float m_blk = mx * c;
                 float alpha = 1.0f;
                 if (j == 0) {
@@ -477,9 +552,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 const uint64_t c2 = f32x2(c, c);
                 const uint64_t nm2 = f32x2(-m, -m);
                 uint64_t sum2[4] = {0, 0, 0, 0};
-                uint32_t pk[64];
+                uint32_t pk[kCols / 2];
 #pragma unroll
-                for (int e = 0; e < 64; ++e) {
+                for (int e = 0; e < kCols / 2; ++e) {
                     const uint64_t x =
                         ffma2(f32x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])), c2, nm2);
                     float x0, x1;
@@ -501,28 +576,32 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     break;
                 }
                 tc_fence_after_sync();
-                // rescale the running output (warp-wide when any row of the warp needs it)
+                // rescale the running output (warp-wide when any row of the warp needs it);
+                // with split rows each half rescales its half of O's columns
                 if (__any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
-                    for (int cc = 0; cc < kD / 32; ++cc) {
+                    for (int cc = 0; cc < kD / 32 / kSplit; ++cc) {
+                        const uint32_t oc = o_addr + 32 * (cc + half * (kD / 32 / kSplit));
                         uint32_t o[32];
-                        tmem_load_32cols(o_addr + 32 * cc, o);
+                        tmem_load_32cols(oc, o);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_store_32cols(o_addr + 32 * cc, o);
+                        tmem_store_32cols(oc, o);
                     }
                     tmem_wait_st();
                 }
                 if constexpr (G::kPInTmem) {
-                    // this row of P into the tile's own TMEM columns
-                    const uint32_t p_addr = tmem_base + lane_off + G::kColP + t * (kBlockKV / 2);
-                    tmem_store_32cols(p_addr, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-                    tmem_store_32cols(p_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+                    // this thread's keys of P into the tile's own TMEM columns (two bf16 per column)
+                    const uint32_t p_addr = tmem_base + lane_off + G::kColP + t * (kBlockKV / 2) + half * (kCols / 2);
+#pragma unroll
+                    for (int cc = 0; cc < kCols / 64; ++cc)
+                        tmem_store_32cols(p_addr + 32 * cc, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32 * cc]));
                     tmem_wait_st();
                 } else {
                     // this row of P into the 128-byte-swizzled K-major tile the MMA reads:
                     // keys [64 h, 64 h + 64) in chunk h, 16-byte unit x of row r at unit x ^ (r % 8)
+                    static_assert(kSplit == 1 || G::kPInTmem, "P in shared memory with whole rows per thread");
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const uint32_t row = p_smem(t) + hh * G::kChunkBytes + static_cast<uint32_t>(r) * 128u;
@@ -545,14 +624,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                     abort_seen = true;
                 } else {
                     tc_fence_after_sync();
+                    float l_other = 0.0f;
+                    if constexpr (kSplit > 1) abort_seen = !exchange(l, l_other);   // the row sum over both halves
+                    l += l_other;
                     const AttnItem it = attn_item(p, w);
-                    const int q = it.q0 + t * kTileQ + r;
+                    const int q = abort_seen ? p.S : it.q0 + t * kTileQ + r;   // no stores after a failed exchange
                     const float inv_l = 1.0f / l;
                     uint16_t* out = p.O + (static_cast<int64_t>(it.bh) * p.S + q) * kD;
 #pragma unroll
-                    for (int cc = 0; cc < kD / 32; ++cc) {
+                    for (int cc = 0; cc < kD / 32 / kSplit; ++cc) {
+                        const int col = 32 * (cc + half * (kD / 32 / kSplit));
                         uint32_t o[32];
-                        tmem_load_32cols(o_addr + 32 * cc, o);
+                        tmem_load_32cols(o_addr + col, o);
                         tmem_wait_ld();
                         uint32_t pk[16];
 #pragma unroll
@@ -562,11 +645,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                         if (q < p.S) {
 #pragma unroll
                             for (int w4 = 0; w4 < 4; ++w4)
-                                st_global_v4(out + 32 * cc + 8 * w4, pk[4 * w4], pk[4 * w4 + 1], pk[4 * w4 + 2],
+                                st_global_v4(out + col + 8 * w4, pk[4 * w4], pk[4 * w4 + 1], pk[4 * w4 + 2],
                                              pk[4 * w4 + 3]);
                         }
                     }
-                    if (p.lse != nullptr && q < p.S)
+                    if (p.lse != nullptr && q < p.S && half == 0)
                         p.lse[static_cast<int64_t>(it.bh) * p.S + q] = (m + log2f(l)) * 0.69314718055994531f;
                     tc_fence_before_sync();
                 }

@@ -76,8 +76,7 @@ struct Geometry {
     static_assert(!kMx || kFp8, "block scales come with FP8 operands");
     static_assert(kARows == kCtaM || (kCG == 1 && !kMx && kARows % 8 == 0 && kARows >= 8),
                   "short A stages: single-CTA kernels only, whole 8-row swizzle atoms");
-    static_assert(kAtoms == 1 || (kAtoms == 2 && kARows == kCtaM && !kMx),
-                  "two K atoms per stage: 128-row A stages, no block scales");
+    static_assert(kAtoms == 1 || (kAtoms == 2 && kARows == kCtaM), "two K atoms per stage: 128-row A stages");
     static constexpr int kKAtoms = kAtoms;
     static constexpr int kARowsMax = kARows;                          // rows of A a stage holds
     static constexpr int kAAtomBytes = kARowsMax * kRowBytes;         // one K atom of A
@@ -91,12 +90,16 @@ struct Geometry {
     static constexpr int kBBytes = kBAtomBytes * kAtoms;
     static constexpr int kAtomElems = kFp8 ? 128 : 64;     // K elements per atom (one TMA box)
     static constexpr int kKElems = kAtomElems * kAtoms;    // K elements per stage
-    // MXFP8: per stage one 512-byte scale block for the CTA's 128 A rows and
-    // one per 128 B rows of the whole tile (scale blocks of 32 rows × 16
-    // bytes, see tmem_cp_128x16b; in a pair each CTA holds all B scales)
+    // MXFP8: per K atom of a stage (128 elements = 4 scale blocks of 32) one
+    // 512-byte scale block for the CTA's 128 A rows and one per 128 B rows of
+    // the whole tile (scale blocks of 32 rows × 16 bytes, see tmem_cp_128x16b;
+    // in a pair each CTA holds all B scales); in shared memory and in the
+    // stage's TMEM slot the blocks go atom by atom: A, B 0, B 1, …
     static constexpr int kSfbAtoms = (kTileN + 127) / 128;
-    static constexpr int kSfBytes = kMx ? 512 * (1 + kSfbAtoms) : 0;
-    static constexpr int kSfCols = kMx ? 4 * (1 + kSfbAtoms) : 0;   // TMEM columns per stage
+    static constexpr int kSfBlocksPerAtom = 1 + kSfbAtoms;
+    static constexpr int kSfBytes = kMx ? 512 * kSfBlocksPerAtom * kAtoms : 0;
+    static constexpr int kSfColsPerAtom = kMx ? 4 * kSfBlocksPerAtom : 0;
+    static constexpr int kSfCols = kSfColsPerAtom * kAtoms;                  // TMEM columns per stage
     static constexpr int kStageBytes = kAStageBytes + kBBytes + kSfBytes;
     static constexpr int kFixed = kEpiWarps * 2 * kEpiBufBytes + 256 + 1024;   // epilogue, barriers, alignment
     static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
@@ -152,6 +155,7 @@ struct GemmParams {
     uint32_t expect_bytes;        // bytes that land per stage in the cluster (both CTAs of a pair)
     int64_t n_pad;                // split K: row stride of the partial matrices (tiles_n * tile width)
     float* partials;              // split K: fp32 partial matrices P[split][M][n_pad]
+    int32_t sf_k_blocks;          // MXFP8: K blocks of 128 of the arranged scales (k_blocks × atoms per stage)
     float alpha;                  // scale of the accumulator (FP8: scale_a * scale_b; bf16: 1)
     const uint16_t* bias;         // fused epilogue: per-column bf16 bias (N values) or null
     int32_t act;                  // fused epilogue: 0 none, 1 ReLU, 2 GELU (erf), 3 SiLU
@@ -498,20 +502,24 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         }
                     }
                     if constexpr (kMx) {   // this stage's scale blocks (tensor map in the half-B slot)
-                        const uint32_t sf_dst = base + G::kOffSf + stage * G::kSfBytes;
                         const int64_t a_group = static_cast<int64_t>(tm) * kCG + rank;   // 128-row group
-                        const int a_row_sf = static_cast<int>((a_group * p.k_blocks + kb) * 2);
-                        const int b_row_sf = static_cast<int>(
-                            p.sf_b_row + (static_cast<int64_t>(tn) * p.k_blocks + kb) * (2 * G::kSfbAtoms));
-                        if constexpr (kCG == 2) {
-                            const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
-                            tma_load_2d_pair(sf_dst, &tmap_b_half, 0, a_row_sf, leader_full);
-                            for (int q = 0; q < G::kSfbAtoms; ++q)
-                                tma_load_2d_pair(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 2 * q, leader_full);
-                        } else {
-                            tma_load_2d(sf_dst, &tmap_b_half, 0, a_row_sf, full_bar(stage));
-                            for (int q = 0; q < G::kSfbAtoms; ++q)
-                                tma_load_2d(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 2 * q, full_bar(stage));
+#pragma unroll
+                        for (int at = 0; at < kAtoms; ++at) {
+                            const int64_t kb128 = static_cast<int64_t>(kb) * kAtoms + at;   // K block of 128
+                            const uint32_t sf_dst = base + G::kOffSf + stage * G::kSfBytes + at * 512 * G::kSfBlocksPerAtom;
+                            const int a_row_sf = static_cast<int>((a_group * p.sf_k_blocks + kb128) * 2);
+                            const int b_row_sf = static_cast<int>(
+                                p.sf_b_row + (static_cast<int64_t>(tn) * p.sf_k_blocks + kb128) * (2 * G::kSfbAtoms));
+                            if constexpr (kCG == 2) {
+                                const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
+                                tma_load_2d_pair(sf_dst, &tmap_b_half, 0, a_row_sf, leader_full);
+                                for (int q = 0; q < G::kSfbAtoms; ++q)
+                                    tma_load_2d_pair(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 2 * q, leader_full);
+                            } else {
+                                tma_load_2d(sf_dst, &tmap_b_half, 0, a_row_sf, full_bar(stage));
+                                for (int q = 0; q < G::kSfbAtoms; ++q)
+                                    tma_load_2d(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 2 * q, full_bar(stage));
+                            }
                         }
                     }
                     ++fills;
@@ -567,19 +575,24 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                     const uint64_t a_desc = smem_desc_kmajor_sw128(base + G::kOffA + stage * G::kAStageBytes);
                     const uint64_t b_desc = smem_desc_kmajor_sw128(base + G::kOffB + stage * G::kBBytes);
                     if constexpr (kMx) {
-                        // this stage's scales, copied into its TMEM slot by the scale copier
-                        const uint32_t sf_tmem = tmem_base + G::kColSf + stage * G::kSfCols;
 #pragma unroll
-                        for (int k = 0; k < kRowBytes / kMmaKBytes; ++k) {
-                            const uint32_t acc = (kb != kb_begin || k != 0) ? 1u : 0u;
-                            // scale block k of the 4 in this stage: byte k of each scale word
-                            const uint32_t id = idesc | (static_cast<uint32_t>(k) << 4) |
-                                                (static_cast<uint32_t>(k) << 29);
-                            if (lane == 0) {
-                                if constexpr (kCG == 2)
-                                    mma_mxf8_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, id, sf_tmem, sf_tmem + 4, acc);
-                                else
-                                    mma_mxf8_one(d_tmem, a_desc + 2u * k, b_desc + 2u * k, id, sf_tmem, sf_tmem + 4, acc);
+                        for (int at = 0; at < kAtoms; ++at) {
+                            // this atom's scales, copied into the stage's TMEM slot by the scale copier
+                            const uint32_t sf_tmem = tmem_base + G::kColSf + stage * G::kSfCols + at * G::kSfColsPerAtom;
+                            const uint64_t ad = a_desc + static_cast<uint64_t>((at * G::kAAtomBytes) >> 4);
+                            const uint64_t bd = b_desc + static_cast<uint64_t>((at * G::kBAtomBytes) >> 4);
+#pragma unroll
+                            for (int k = 0; k < kRowBytes / kMmaKBytes; ++k) {
+                                const uint32_t acc = (kb != kb_begin || at != 0 || k != 0) ? 1u : 0u;
+                                // scale block k of the 4 in this atom: byte k of each scale word
+                                const uint32_t id = idesc | (static_cast<uint32_t>(k) << 4) |
+                                                    (static_cast<uint32_t>(k) << 29);
+                                if (lane == 0) {
+                                    if constexpr (kCG == 2)
+                                        mma_mxf8_pair(d_tmem, ad + 2u * k, bd + 2u * k, id, sf_tmem, sf_tmem + 4, acc);
+                                    else
+                                        mma_mxf8_one(d_tmem, ad + 2u * k, bd + 2u * k, id, sf_tmem, sf_tmem + 4, acc);
+                                }
                             }
                         }
                     } else {
@@ -658,7 +671,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         const uint32_t sf_src = base + G::kOffSf + stage * G::kSfBytes;
                         const uint32_t sf_tmem = tmem_base + G::kColSf + stage * G::kSfCols;
 #pragma unroll
-                        for (int q = 0; q < 1 + G::kSfbAtoms; ++q) {
+                        for (int q = 0; q < G::kSfBlocksPerAtom * kAtoms; ++q) {   // atom by atom: A, B 0, B 1, …
                             if constexpr (kCG == 2)
                                 tmem_cp_128x16b_pair(sf_tmem + 4 * q, smem_desc_plain(sf_src + 512 * q, 16, 128));
                             else
@@ -963,7 +976,9 @@ __global__ void mx_scale_blocks_kernel(const uint8_t* __restrict__ sa, int64_t l
             if ((is_a || local < tile_n) && row < rows) {
                 const uint8_t* p = src + static_cast<int64_t>(row) * ld;
                 if (words) {
-                    v = __ldg(reinterpret_cast<const uint32_t*>(p + blk0));
+                    // kb_total is a multiple of 4 here: a word is either in the row or past it
+                    // (a K block added to make the count of 128-element blocks even)
+                    if (blk0 < kb_total) v = __ldg(reinterpret_cast<const uint32_t*>(p + blk0));
                 } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j)

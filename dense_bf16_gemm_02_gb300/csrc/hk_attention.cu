@@ -127,10 +127,10 @@ extern "C" hk_status hk_attention_fwd_ex(const void* Q, const void* K, const voi
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>(B * Hq * p.q_pairs, sm_count));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (D == 64) {
-        hk::attn::attn_fwd_kernel<64><<<grid, hk::attn::kThreads, hk::attn::AttnGeometry<64>::kSmemBytes, st>>>(
+        hk::attn::attn_fwd_kernel<64><<<grid, hk::attn::AttnGeometry<64>::kThreads, hk::attn::AttnGeometry<64>::kSmemBytes, st>>>(
             tq, tk, tv, p);
     } else {
-        hk::attn::attn_fwd_kernel<128><<<grid, hk::attn::kThreads, hk::attn::AttnGeometry<128>::kSmemBytes, st>>>(
+        hk::attn::attn_fwd_kernel<128><<<grid, hk::attn::AttnGeometry<128>::kThreads, hk::attn::AttnGeometry<128>::kSmemBytes, st>>>(
             tq, tk, tv, p);
     }
     e = cudaGetLastError();

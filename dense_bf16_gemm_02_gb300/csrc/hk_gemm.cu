@@ -46,6 +46,11 @@ hk_status cuda_fail(hk_status s, const char* what, cudaError_t e) {
 #ifndef HK_PDL
 #define HK_PDL 1   // launch every GEMM as a programmatic dependent of the previous kernel on its stream
 #endif
+#ifndef HK_MX_PAIR_ATOMS
+// K atoms per stage of the block-scaled pair kernel: two (256 K elements, 3 stages)
+// measured no faster than one (626K vs 621K kernel cycles at 8192^3)
+#define HK_MX_PAIR_ATOMS 1
+#endif
 #ifndef HK_FP8_PAIR_ATOMS
 #define HK_FP8_PAIR_ATOMS 1
 #endif
@@ -103,14 +108,14 @@ const Variant kVariants[] = {
     make_variant<1, 128, true>(HK_KERNEL_SINGLE_128x128, "fp8 single 128x128"),
     make_variant<1, 64, true>(HK_KERNEL_SINGLE_128x64, "fp8 single 128x64"),
     make_variant<1, 192, true, true>(HK_KERNEL_SINGLE_128x192, "mxfp8 single 128x192"),
-    make_variant<2, 256, true, true>(HK_KERNEL_PAIR_256x256, "mxfp8 pair 256x256"),
+    make_variant<2, 256, true, true, hk::kCtaM, HK_MX_PAIR_ATOMS>(HK_KERNEL_PAIR_256x256, "mxfp8 pair 256x256"),
 };
 // N of the MXFP8 tiles: one CTA 128x192 (two TMEM accumulators), a pair
 // 256x256 (one accumulator, see Geometry::kAccBufs)
 constexpr int kMxTileNSingle = 192;
 constexpr int kMxTileNPair = 256;
 using GeomMxSingle = hk::Geometry<1, kMxTileNSingle, true, true>;
-using GeomMxPair = hk::Geometry<2, kMxTileNPair, true, true>;
+using GeomMxPair = hk::Geometry<2, kMxTileNPair, true, true, hk::kCtaM, HK_MX_PAIR_ATOMS>;
 static_assert(GeomMxSingle::kSfbAtoms == GeomMxPair::kSfbAtoms, "one scale layout");
 static_assert(GeomMxPair::kAccBufs == 1 && GeomMxSingle::kAccBufs == 2, "MXFP8 accumulator buffering");
 constexpr int kMxSfbAtoms = GeomMxPair::kSfbAtoms;
@@ -1028,7 +1033,10 @@ MxLayout mx_layout(int64_t M, int64_t N, int64_t K) {
     l.tiles_m = M <= hk::kCtaM ? 1 : 2 * ceil_div(M, 2 * hk::kCtaM);
     l.tile_n = M <= hk::kCtaM ? kMxTileNSingle : kMxTileNPair;
     l.tiles_n = ceil_div(N, l.tile_n);
+    // K blocks of 128: the pair kernel loads HK_MX_PAIR_ATOMS of them per stage, so
+    // their count is rounded up to that multiple (the extra blocks hold scale 0)
     l.k_blocks = ceil_div(K, 128);
+    if (M > hk::kCtaM) l.k_blocks = ceil_div(l.k_blocks, HK_MX_PAIR_ATOMS) * HK_MX_PAIR_ATOMS;
     l.a_bytes = static_cast<size_t>(l.tiles_m * l.k_blocks * 512);
     l.b_offset = (l.a_bytes + 255) & ~size_t(255);
     l.total = l.b_offset + static_cast<size_t>(l.tiles_n * l.k_blocks * 512 * kMxSfbAtoms);
@@ -1105,7 +1113,8 @@ hk_status hk_gemm_mxfp8_ex(const void* A, const void* B, const void* SFA, const 
     g.splits = 1;
     g.group_m = kDefaultGroupM;
     g.a_rows = a_rows_for(*v, M);
-    g.expect_bytes = static_cast<uint32_t>(v->cg * ((g.a_rows + v->tile_n / v->cg) * hk::kRowBytes + v->sf_bytes));
+    g.expect_bytes = static_cast<uint32_t>(v->cg * ((g.a_rows + v->tile_n / v->cg) * hk::kRowBytes * v->atoms + v->sf_bytes));
+    g.sf_k_blocks = static_cast<int32_t>(lay.k_blocks);
     g.n_pad = int64_t(g.tiles_n) * v->tile_n;
     g.n_tma = static_cast<int32_t>(N & ~int64_t(7));
     g.ldc = ldc;
