@@ -43,16 +43,16 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # sources whose digest is given (the code of those sources, comments and
 # layout excluded).
 MEASURED_TRAFFIC = {
-    "gemm_8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 1062652928 + 127742976},
-    "skinny_128x28672x8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 471969536 + 3475200},
-    "fp8_gemm_8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 345377792 + 117171712},
+    "gemm_8192": {"source_digest": "73555b022c453987", "bytes_per_launch": 1084814592 + 125188608},
+    "skinny_128x28672x8192": {"source_digest": "73555b022c453987", "bytes_per_launch": 471969536 + 3217152},
+    "fp8_gemm_8192": {"source_digest": "73555b022c453987", "bytes_per_launch": 340099328 + 115825152},
     # the block-scaled GEMM kernel alone (the scale arrangement kernel moves ~8 MB more)
-    "mxfp8_gemm_8192": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 356308480 + 116700416},
+    "mxfp8_gemm_8192": {"source_digest": "73555b022c453987", "bytes_per_launch": 354526208 + 116764160},
     # the GEMM kernel alone (the split-K reduction reads the fp32 partials and writes C)
-    "decode_64x8192x28672": {"source_digest": "36be903dca9f10c9", "bytes_per_launch": 473515776 + 3584768},
+    "decode_64x8192x28672": {"source_digest": "73555b022c453987", "bytes_per_launch": 473578752 + 3216896},
     # attention: captured at B2 (one launch); the B16 figure scales it by 8 (traffic grows with B)
-    "attn_gqa_b2_s4096_d128": {"source_digest": "e2bf2e29b78c0df1", "bytes_per_launch": 199983616 + 110758144},
-    "attn_gqa_b16_s4096_d128": {"source_digest": "e2bf2e29b78c0df1", "bytes_per_launch": 8 * (199983616 + 110758144)},
+    "attn_gqa_b2_s4096_d128": {"source_digest": "325cd38bad1c92ef", "bytes_per_launch": 200060160 + 110417152},
+    "attn_gqa_b16_s4096_d128": {"source_digest": "325cd38bad1c92ef", "bytes_per_launch": 8 * (200060160 + 110417152)},
 }
 
 
