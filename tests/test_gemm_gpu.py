@@ -582,6 +582,45 @@ def test_plan_run_with_changing_pointers(hk):
     plan.close()
 
 
+# ------------------------------------- programmatic dependent launches --
+
+def test_dependent_chain_on_one_stream(hk):
+    """Every GEMM is launched as a programmatic dependent of the kernel before it:
+    its prologue may overlap that kernel, but its loads of A/B and its stores of C
+    must wait for it. A chain on one stream with no host synchronisation: each
+    GEMM reads the previous one's C (read after write), and the last one writes
+    over the first one's A (write after read); pair and single-CTA kernels, and a
+    K split whose reduction is itself a dependent launch. Integer data: exact."""
+    import torch
+    stream = int(torch.cuda.current_stream().cuda_stream)
+    M, K = 512, 256
+    A0 = synth.int_bf16(M, K, 5701, -1, 1)   # every partial sum of the chain stays an integer below 2^24
+    Bs = [synth.int_bf16(K, K, 5710 + i, -1, 1) for i in range(3)]
+    A0d, _ = to_device(A0)
+    Bd = [to_device(b)[0] for b in Bs]
+    C1 = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    C2 = torch.empty((64, K), dtype=torch.bfloat16, device="cuda")
+    # C1 = A0·B0ᵀ (pair kernel); C2 = C1[:64]·B1ᵀ (single-CTA, K split through a plan);
+    # A0[:64] = C2·B2ᵀ (overwrites rows of A0, which the first GEMM read)
+    assert hk.hk_gemm_bf16(A0d.data_ptr(), Bd[0].data_ptr(), C1.data_ptr(), M, K, K, K, K, K, stream) == hk.HK_OK
+    plan = hk.Plan(64, K, K, split_k=2, kernel=4)
+    ws = torch.empty(plan.workspace_size + 256, dtype=torch.uint8, device="cuda")
+    assert plan.run_raw(C1.data_ptr(), Bd[1].data_ptr(), C2.data_ptr(), (ws.data_ptr() + 255) & ~255,
+                        plan.workspace_size, stream) == hk.HK_OK
+    assert hk.hk_gemm_bf16(C2.data_ptr(), Bd[2].data_ptr(), A0d.data_ptr(), 64, K, K, K, K, K, stream) == hk.HK_OK
+    torch.cuda.synchronize()
+    assert hk.hk_gemm_last_device_status(torch.cuda.current_device()) == hk.HK_OK
+    c1 = oracle.gemm(A0, Bs[0])
+    c2 = oracle.gemm(np.ascontiguousarray(c1[:64]), Bs[1])
+    a_new = oracle.gemm(c2, Bs[2])
+    assert_bitexact(to_host(C1), c1, "first GEMM")
+    assert_bitexact(to_host(C2), c2, "second GEMM (reads the first's C)")
+    got_a = to_host(A0d)
+    assert_bitexact(got_a[:64], a_new, "third GEMM (writes the first's A)")
+    assert_bitexact(got_a[64:], A0[64:], "rows of A the chain does not write")
+    plan.close()
+
+
 # ------------------------------------------------- fused residual add --
 
 def run_fused(hk, A_bits, B_bits, bias_bits, R_bits, act, split_k=None, kernel=0, in_place=False, ldr_pad=0):
