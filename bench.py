@@ -6,6 +6,8 @@ HipKittens "L2" detail page, §2 Q3 and §5 Tab. 2) through the C-ABI
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hk|reference]
                     [--workload NAME] [--no-cpu-baseline]
+    python bench.py --calibrate plans [--shapes MxNxK ...]   # plan sweep
+    python bench.py --calibrate l2                           # L2 latency probe
 
 With N > 1 (launched by torchrun) every rank runs an independent replica of
 the workload on its own GPU (the GEMM has no exchange step); the reported
@@ -1123,6 +1125,85 @@ def run_attn(args, w):
         dist.destroy_process_group()
     return 0
 
+# ---------------------------------------------------------------- calibration
+
+CALIBRATE_SHAPES = [(1, 8192, 8192), (16, 8192, 8192), (64, 8192, 8192), (128, 8192, 8192), (192, 8192, 8192),
+                  (256, 8192, 8192), (384, 8192, 8192), (512, 8192, 8192), (128, 28672, 8192), (1, 1024, 8192),
+                  (1, 4096, 8192), (1, 8192, 28672), (1, 28672, 8192), (64, 8192, 28672), (256, 28672, 8192),
+                  (128, 4096, 4096), (256, 4096, 16384), (2048, 2048, 8192), (1024, 8192, 8192), (64, 2048, 8192)]
+
+
+def _calib_calib_warm_us(fn, reps: int = 25) -> float:
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
+def sweep_plans(shapes) -> None:
+    """Every plan a shape can be forced to (kernel ids 1-5, K splits 1, 2, 3, 4,
+    6, 8, 12), warm back-to-back calls between CUDA events, next to
+    torch.matmul (cuBLAS) on the same inputs; per shape the automatic plan's
+    time and every candidate sorted by time. The plan's time model
+    (``estimate_us`` in the package's ``csrc/hk_gemm.cu``) is fitted to these."""
+    import torch
+    from dense_bf16_gemm_02_gb300 import hk_gemm as hk
+    dev = torch.device("cuda", 0)
+    for (M, N, K) in shapes:
+        A = torch.randn(M, K, device=dev).to(torch.bfloat16)
+        B = torch.randn(N, K, device=dev).to(torch.bfloat16)
+        C = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
+        ref = A.float() @ B.float().T
+        st = int(torch.cuda.current_stream().cuda_stream)
+
+        def timed(plan):
+            ws = torch.empty(max(plan.workspace_size, 256), dtype=torch.uint8, device=dev)
+            run = lambda: plan.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), ws.data_ptr(), plan.workspace_size, st)
+            if run() != hk.HK_OK:
+                raise hk.HKError(run(), "hk_gemm_plan_run")
+            torch.cuda.synchronize()
+            err = (C.float() - ref).abs().max().item() / max(ref.abs().max().item(), 1e-30)
+            if err > 0.02:
+                raise AssertionError(f"{M}x{N}x{K} plan {plan.info()}: relative error {err}")
+            return _calib_warm_us(run)
+
+        auto = hk.Plan(M, N, K)
+        ai = auto.info()
+        t_auto = timed(auto)
+        auto.close()
+        t_lib = _calib_warm_us(lambda: torch.matmul(A, B.t()))
+        res = []
+        for kernel in (1, 2, 3, 4, 5):
+            for split in (1, 2, 3, 4, 6, 8, 12):
+                try:
+                    plan = hk.Plan(M, N, K, kernel=kernel, split_k=split)
+                except hk.HKError:
+                    continue
+                inf = plan.info()
+                res.append((timed(plan), kernel, split, inf["tile_n"], inf["grid_ctas"], inf["stages"]))
+                plan.close()
+        res.sort()
+        print(f"{M}x{N}x{K}: cuBLAS {t_lib:.1f} us; auto kernel {ai['kernel']} split {ai['split_k']} -> {t_auto:.1f} us; "
+              "best: " + "; ".join(f"k{k} n{tn} s{s} g{g} st{stg}: {t:.1f}" for t, k, s, tn, g, stg in res), flush=True)
+
+
+def l2_latency() -> None:
+    """Builds and runs the package's ``csrc/diag_l2_latency.cu``: L2-hit latency
+    by SM and by address region (the die question of the grid schedule)."""
+    from dense_bf16_gemm_02_gb300.build import ARCH_FLAGS, BUILD_DIR, nvcc_path
+    src = os.path.join(ROOT, "dense_bf16_gemm_02_gb300", "csrc", "diag_l2_latency.cu")
+    exe = os.path.join(BUILD_DIR, "diag_l2_latency")
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    subprocess.run([nvcc_path(), *ARCH_FLAGS, "-O3", "-std=c++17", "-o", exe, src], check=True)
+    subprocess.run([exe], check=True)
+
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
@@ -1138,7 +1219,17 @@ def main(argv=None):
                     help="fused epilogue of each step (hk_gemm_bf16_epilogue)")
     ap.add_argument("--group-m", type=int, default=0,
                     help="raster group height in tile rows (0: the library default via hk_gemm_bf16)")
+    ap.add_argument("--calibrate", choices=["plans", "l2"],
+                    help="instead of a bench line: 'plans' times every forced plan of --shapes next to "
+                         "cuBLAS (the data the plan time model is fitted to); 'l2' runs the L2 latency probe")
+    ap.add_argument("--shapes", nargs="*", default=[], help="MxNxK shapes for --calibrate plans")
     args = ap.parse_args(argv)
+    if args.calibrate == "plans":
+        sweep_plans([tuple(map(int, s.split("x"))) for s in args.shapes] or CALIBRATE_SHAPES)
+        return 0
+    if args.calibrate == "l2":
+        l2_latency()
+        return 0
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     if args.workload in synth.MX_WORKLOADS:
         w = synth.MX_WORKLOADS[args.workload]
