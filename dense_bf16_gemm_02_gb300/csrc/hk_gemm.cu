@@ -41,7 +41,7 @@ hk_status cuda_fail(hk_status s, const char* what, cudaError_t e) {
 }
 
 #ifndef HK_PAIR_ATOMS
-#define HK_PAIR_ATOMS 2   // K atoms per stage of the bf16 pair kernel (128 K elements, 3 stages)
+#define HK_PAIR_ATOMS 1   // K atoms per stage of the bf16 pair kernel (1: 64 K elements, 6 stages; 2: 128, 3 stages)
 #endif
 #ifndef HK_PDL
 #define HK_PDL 1   // launch every GEMM as a programmatic dependent of the previous kernel on its stream
