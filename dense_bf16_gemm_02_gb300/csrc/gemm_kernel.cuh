@@ -59,6 +59,13 @@ constexpr int pow2_at_least(int x) {
     return r;
 }
 
+// Operand stages of `stage_bytes` that fit in `avail` bytes beside a ring of
+// (stages + ahead) scale slots of `sf_bytes` (no ring when sf_bytes is 0).
+constexpr int stages_fit(int avail, int stage_bytes, int sf_bytes, int ahead, int max_stages) {
+    const int s = (avail - ahead * sf_bytes) / (stage_bytes + sf_bytes);
+    return s > max_stages ? max_stages : s;
+}
+
 // Compile-time geometry of one kernel instance. kMx: block-scaled FP8
 // (MXFP8, one UE8M0 scale per 32 K elements). kARows < 128 (single CTA,
 // M <= kARows): each stage keeps room for kARows rows of A instead of 128, so
@@ -93,18 +100,27 @@ struct Geometry {
     // MXFP8: per K atom of a stage (128 elements = 4 scale blocks of 32) one
     // 512-byte scale block for the CTA's 128 A rows and one per 128 B rows of
     // the whole tile (scale blocks of 32 rows × 16 bytes, see tmem_cp_128x16b;
-    // in a pair each CTA holds all B scales); in shared memory and in the
-    // stage's TMEM slot the blocks go atom by atom: A, B 0, B 1, …
+    // in a pair each CTA holds all B scales); in shared memory and in a TMEM
+    // slot the blocks go atom by atom: A, B 0, B 1, …
     static constexpr int kSfbAtoms = (kTileN + 127) / 128;
     static constexpr int kSfBlocksPerAtom = 1 + kSfbAtoms;
-    static constexpr int kSfBytes = kMx ? 512 * kSfBlocksPerAtom * kAtoms : 0;
+    static constexpr int kSfBytes = kMx ? 512 * kSfBlocksPerAtom * kAtoms : 0;   // per K block and CTA
     static constexpr int kSfColsPerAtom = kMx ? 4 * kSfBlocksPerAtom : 0;
-    static constexpr int kSfCols = kSfColsPerAtom * kAtoms;                  // TMEM columns per stage
-    static constexpr int kStageBytes = kAStageBytes + kBBytes + kSfBytes;
+    static constexpr int kSfCols = kSfColsPerAtom * kAtoms;                  // TMEM columns per K block
+    static constexpr int kStageBytes = kAStageBytes + kBBytes;              // operands of one K block
     static constexpr int kFixed = kEpiWarps * 2 * kEpiBufBytes + 256 + 1024;   // epilogue, barriers, alignment
-    static constexpr int kStagesFit = (kSmemLimit - kFixed) / kStageBytes;
     static constexpr int kMaxStages = kARows < kCtaM ? 12 : 8;
-    static constexpr int kStages = kStagesFit > kMaxStages ? kMaxStages : kStagesFit;
+    // MXFP8: the scales of a K block travel in their own ring of
+    // kStages + kSfAhead slots (shared memory and TMEM), loaded kSfAhead K
+    // blocks ahead of the operands, so that copying them into TMEM is off the
+    // MMA's path. The lead is the largest (up to 4) that costs no operand stage.
+    static constexpr int kStages = stages_fit(kSmemLimit - kFixed, kStageBytes, kSfBytes, kMx ? 1 : 0, kMaxStages);
+    static constexpr int kSfAhead = !kMx ? 0
+                                    : stages_fit(kSmemLimit - kFixed, kStageBytes, kSfBytes, 4, kMaxStages) == kStages ? 4
+                                    : stages_fit(kSmemLimit - kFixed, kStageBytes, kSfBytes, 3, kMaxStages) == kStages ? 3
+                                    : stages_fit(kSmemLimit - kFixed, kStageBytes, kSfBytes, 2, kMaxStages) == kStages ? 2
+                                                                                                                : 1;
+    static constexpr int kSfSlots = kMx ? kStages + kSfAhead : 0;
     static_assert(kStages >= 3, "pipeline too shallow");
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kAStageBytes;
@@ -112,10 +128,13 @@ struct Geometry {
     static_assert(kOffA + (kStages - 1) * kAStageBytes + (kAtoms - 1) * kAAtomBytes + kABytes <=
                       kOffB + kStages * kBBytes, "A read");
     static constexpr int kOffSf = kOffB + kStages * kBBytes;
-    static constexpr int kOffEpi = kOffSf + kStages * kSfBytes;
+    static constexpr int kOffEpi = kOffSf + kSfSlots * kSfBytes;
     static constexpr int kOffBars = kOffEpi + kEpiWarps * 2 * kEpiBufBytes;
-    // full[S], empty[S], acc_full[2], acc_empty[2], sf_full[S] (MXFP8), drain[2] (abort path)
-    static constexpr int kNumBars = (kMx ? 3 : 2) * kStages + 6;
+    // full[S], empty[S], acc_full[2], acc_empty[2], sf_full[SF] and sf_land[SF] (MXFP8), drain[2] (abort path)
+    static constexpr int kBarSfFull = 2 * kStages + 4;
+    static constexpr int kBarSfLand = kBarSfFull + kSfSlots;
+    static constexpr int kBarDrain = kBarSfLand + kSfSlots;
+    static constexpr int kNumBars = kBarDrain + 2;
     static constexpr int kOffTmemHolder = kOffBars + kNumBars * 8;   // [0]: TMEM address, [1..2]: epilogue flags
     static constexpr int kSmemBytes = kOffTmemHolder + 16 + 1024;   // + slack for aligning the base
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
@@ -125,9 +144,9 @@ struct Geometry {
     // 256-wide block-scaled tile keeps one, which its epilogue reads whole
     // into registers before it stores anything, so the MMAs wait only for
     // the TMEM reads.
-    static constexpr int kAccBufs = 2 * kAccCols + kStages * kSfCols <= 512 ? 2 : 1;
-    static constexpr int kColSf = kAccBufs * kAccCols;      // MXFP8: scale ring, kSfCols per stage
-    static constexpr int kTmemCols = pow2_at_least(kAccBufs * kAccCols + kStages * kSfCols);
+    static constexpr int kAccBufs = 2 * kAccCols + kSfSlots * kSfCols <= 512 ? 2 : 1;
+    static constexpr int kColSf = kAccBufs * kAccCols;      // MXFP8: scale ring, kSfCols per slot
+    static constexpr int kTmemCols = pow2_at_least(kAccBufs * kAccCols + kSfSlots * kSfCols);
     static_assert(kTmemCols <= 512, "TMEM");
     static constexpr uint32_t kIdesc = kMx    ? idesc_mxf8_f32(kTileM, kTileN)
                                        : kFp8 ? idesc_e4m3_f32(kTileM, kTileN)
@@ -248,18 +267,6 @@ __device__ __noinline__ bool wait_bounded_suspend(const GemmParams& p, uint32_t 
             return false;
         }
     }
-}
-
-// Warp-uniform variant: lane 0 waits, the result is broadcast, and every
-// lane then observes the completed phase itself (acquire per thread).
-__device__ __forceinline__ bool wait_bounded_warp(const GemmParams& p, uint32_t bar, uint32_t parity,
-                                                  uint32_t code) {
-    uint32_t ok = 0;
-    if (lane_id() == 0) ok = wait_bounded(p, bar, parity, code) ? 1u : 0u;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) (void)mbar_try_wait(bar, parity);
-    __syncwarp();
-    return ok != 0;
 }
 
 // Fused epilogue on one fp32 accumulator value: + bias, then the activation.
@@ -403,9 +410,11 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     auto empty_bar = [&](int s) { return base + G::kOffBars + 8u * (G::kStages + s); };
     auto acc_full_bar = [&](int b) { return base + G::kOffBars + 8u * (2 * G::kStages + b); };
     auto acc_empty_bar = [&](int b) { return base + G::kOffBars + 8u * (2 * G::kStages + 2 + b); };
-    auto sf_full_bar = [&](int s) { return base + G::kOffBars + 8u * (2 * G::kStages + 4 + s); };
+    // MXFP8 scale slot j: its scales are in TMEM (sf_full) / have landed in shared memory (sf_land)
+    auto sf_full_bar = [&](int j) { return base + G::kOffBars + 8u * (G::kBarSfFull + j); };
+    auto sf_land_bar = [&](int j) { return base + G::kOffBars + 8u * (G::kBarSfLand + j); };
     // abort path: all tcgen05 operations of the MMA issuer ([0]) and of the scale copier ([1]) complete
-    auto drain_bar = [&](int i) { return base + G::kOffBars + 8u * ((kMx ? 3 : 2) * G::kStages + 4 + i); };
+    auto drain_bar = [&](int i) { return base + G::kOffBars + 8u * (G::kBarDrain + i); };
     const uint32_t tmem_holder = base + G::kOffTmemHolder;
 
     if (threadIdx.x == 0) {
@@ -418,7 +427,10 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             mbar_init(acc_empty_bar(b), kCG * kEpiWarps);
         }
         if constexpr (kMx)
-            for (int s = 0; s < G::kStages; ++s) mbar_init(sf_full_bar(s), 1);
+            for (int j = 0; j < G::kSfSlots; ++j) {
+                mbar_init(sf_full_bar(j), 1);
+                mbar_init(sf_land_bar(j), 1);
+            }
         mbar_init(drain_bar(0), 1);
         mbar_init(drain_bar(1), 1);
         fence_mbar_init_cluster();
@@ -460,6 +472,56 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             int64_t fills = 0;            // stages armed and loaded by this producer so far
             int64_t dropped_fill = -1;    // the fill whose arrival the test fault withheld
             const int total = p.total_units;
+            // MXFP8 scales: a second cursor over the same (unit, K block) sequence,
+            // kSfAhead K blocks ahead of the operand loads, filling the scale ring.
+            // Scale slot j is reused for K block g + kSfSlots only once the MMAs of
+            // K block g completed; the operand stage wait for K block
+            // g + kSfSlots - kSfAhead = g + kStages establishes exactly that.
+            int sf_u = unit, sf_kb = 0, sf_kb_end = 0, sf_tm = 0, sf_tn = 0, sf_slot = 0;
+            int64_t sf_fills = 0;         // scale slots armed and loaded so far
+            auto sf_seek = [&]() {        // the cursor's unit is sf_u: its tile and K range
+                if (sf_u >= total) return;
+                int t, split, half;
+                unit_info(p, sf_u, t, split, half);
+                tile_coords(p, t, sf_tm, sf_tn);
+                split_range(p, split, sf_kb, sf_kb_end);
+            };
+            auto sf_load_next = [&]() {   // the next K block's scale blocks into the next slot
+                while (sf_u < total && sf_kb >= sf_kb_end) {
+                    sf_u += num_units;
+                    sf_seek();
+                }
+                if (sf_u >= total) return;
+                const uint32_t land = sf_land_bar(sf_slot);
+                if (rank == 0) mbar_arrive_expect_tx(land, static_cast<uint32_t>(kCG * G::kSfBytes));
+                const uint32_t land_leader = kCG == 2 ? map_to_cta(land, 0) : land;
+                const int64_t a_group = static_cast<int64_t>(sf_tm) * kCG + rank;   // 128-row group
+#pragma unroll
+                for (int at = 0; at < kAtoms; ++at) {
+                    const int64_t kb128 = static_cast<int64_t>(sf_kb) * kAtoms + at;   // K block of 128
+                    const uint32_t sf_dst = base + G::kOffSf + sf_slot * G::kSfBytes + at * 512 * G::kSfBlocksPerAtom;
+                    const int a_row_sf = static_cast<int>((a_group * p.sf_k_blocks + kb128) * 2);
+                    const int b_row_sf = static_cast<int>(
+                        p.sf_b_row + (static_cast<int64_t>(sf_tn) * p.sf_k_blocks + kb128) * (2 * G::kSfbAtoms));
+                    // (the scale blocks' tensor map rides in the half-B slot)
+                    if constexpr (kCG == 2) {
+                        tma_load_2d_pair(sf_dst, &tmap_b_half, 0, a_row_sf, land_leader);
+                        for (int q = 0; q < G::kSfbAtoms; ++q)
+                            tma_load_2d_pair(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 2 * q, land_leader);
+                    } else {
+                        tma_load_2d(sf_dst, &tmap_b_half, 0, a_row_sf, land);
+                        for (int q = 0; q < G::kSfbAtoms; ++q)
+                            tma_load_2d(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 2 * q, land);
+                    }
+                }
+                ++sf_kb;
+                ++sf_fills;
+                if (++sf_slot == G::kSfSlots) sf_slot = 0;
+            };
+            if constexpr (kMx) {
+                sf_seek();
+                for (int i = 0; i < G::kSfAhead; ++i) sf_load_next();   // slots never used before
+            }
             for (int u = unit; u < total && !abort_seen; u += num_units) {
                 int t, split, half;
                 unit_info(p, u, t, split, half);
@@ -501,42 +563,26 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                             tma_load_2d(b_dst + at * G::kBAtomBytes, b_map, kx, b_row, full_bar(stage));
                         }
                     }
-                    if constexpr (kMx) {   // this stage's scale blocks (tensor map in the half-B slot)
-                        const int64_t a_group = static_cast<int64_t>(tm) * kCG + rank;   // 128-row group
-#pragma unroll
-                        for (int at = 0; at < kAtoms; ++at) {
-                            const int64_t kb128 = static_cast<int64_t>(kb) * kAtoms + at;   // K block of 128
-                            const uint32_t sf_dst = base + G::kOffSf + stage * G::kSfBytes + at * 512 * G::kSfBlocksPerAtom;
-                            const int a_row_sf = static_cast<int>((a_group * p.sf_k_blocks + kb128) * 2);
-                            const int b_row_sf = static_cast<int>(
-                                p.sf_b_row + (static_cast<int64_t>(tn) * p.sf_k_blocks + kb128) * (2 * G::kSfbAtoms));
-                            if constexpr (kCG == 2) {
-                                const uint32_t leader_full = map_to_cta(full_bar(stage), 0);
-                                tma_load_2d_pair(sf_dst, &tmap_b_half, 0, a_row_sf, leader_full);
-                                for (int q = 0; q < G::kSfbAtoms; ++q)
-                                    tma_load_2d_pair(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 2 * q, leader_full);
-                            } else {
-                                tma_load_2d(sf_dst, &tmap_b_half, 0, a_row_sf, full_bar(stage));
-                                for (int q = 0; q < G::kSfbAtoms; ++q)
-                                    tma_load_2d(sf_dst + 512 * (1 + q), &tmap_b_half, 0, b_row_sf + 2 * q, full_bar(stage));
-                            }
-                        }
-                    }
                     ++fills;
+                    if constexpr (kMx) sf_load_next();   // the scales kSfAhead K blocks ahead
                     if (++stage == G::kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            // Abort: the leader's full barriers count the bytes of both CTAs' loads;
-            // wait (bounded) for the fills it armed that may still be in flight.
+            // Abort: the leader's full and scale barriers count the bytes of both CTAs'
+            // loads; wait (bounded) for the fills it armed that may still be in flight.
             if (rank == 0 && (abort_seen || aborted(p))) {
                 for (int64_t f = fills - 1; f >= 0 && f >= fills - G::kStages; --f) {
                     if (f == dropped_fill) continue;
                     (void)wait_drain(full_bar(static_cast<int>(f % G::kStages)),
                                      static_cast<uint32_t>((f / G::kStages) & 1), kDrainLimitNs);
                 }
+                if constexpr (kMx)
+                    for (int64_t f = sf_fills - 1; f >= 0 && f >= sf_fills - G::kSfSlots; --f)
+                        (void)wait_drain(sf_land_bar(static_cast<int>(f % G::kSfSlots)),
+                                         static_cast<uint32_t>((f / G::kSfSlots) & 1), kDrainLimitNs);
             }
         }
     } else if (warp == 1) {
@@ -547,6 +593,8 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         if (rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
+            int sf_slot = 0;              // MXFP8: scale slot of the current K block
+            uint32_t sf_phase = 0;
             int local = 0;
             const int total = p.total_units;
             for (int u = unit; u < total && !abort_seen; u += num_units, ++local) {
@@ -567,7 +615,8 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * G::kAccCols;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!wait_bounded(p, kMx ? sf_full_bar(stage) : full_bar(stage), phase, kErrMmaFull)) {
+                    if (!wait_bounded(p, full_bar(stage), phase, kErrMmaFull) ||
+                        (kMx && !wait_bounded(p, sf_full_bar(sf_slot), sf_phase, kErrMmaFull))) {
                         abort_seen = true;
                         break;
                     }
@@ -578,7 +627,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
 #pragma unroll
                         for (int at = 0; at < kAtoms; ++at) {
                             // this atom's scales, copied into the stage's TMEM slot by the scale copier
-                            const uint32_t sf_tmem = tmem_base + G::kColSf + stage * G::kSfCols + at * G::kSfColsPerAtom;
+                            const uint32_t sf_tmem = tmem_base + G::kColSf + sf_slot * G::kSfCols + at * G::kSfColsPerAtom;
                             const uint64_t ad = a_desc + static_cast<uint64_t>((at * G::kAAtomBytes) >> 4);
                             const uint64_t bd = b_desc + static_cast<uint64_t>((at * G::kBAtomBytes) >> 4);
 #pragma unroll
@@ -627,6 +676,10 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         stage = 0;
                         phase ^= 1u;
                     }
+                    if (kMx && ++sf_slot == G::kSfSlots) {
+                        sf_slot = 0;
+                        sf_phase ^= 1u;
+                    }
                 }
                 if (abort_seen) break;
                 // accumulator complete: hand it to the epilogue(s)
@@ -646,30 +699,32 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         }
     } else if (warp == 2 + kEpiWarps) {
         // ---------------------------------------- MXFP8 scale copier --
-        // Once a stage has landed, copy its scale blocks into the stage's TMEM
-        // slot and signal sf_full[stage], on which the MMA thread waits instead
-        // of full[stage]. Issued here rather than by the MMA thread, the copies
-        // never stand between two MMAs in that thread's stream (measured: 397
-        // -> 354 us at 8192^3). A slot is free again when its stage lands next:
-        // the producer reloads a stage only after the MMAs that read it (and
-        // its scale slot) completed.
+        // Once a K block's scale blocks have landed in their slot (sf_land), copy
+        // them into the slot's TMEM columns and signal sf_full, on which the MMA
+        // thread waits besides the operands' full barrier. Issued here rather
+        // than by the MMA thread, the copies never stand between two MMAs in
+        // that thread's stream (measured: 397 -> 354 us at 8192^3); loaded
+        // kSfAhead K blocks ahead of the operands, they are done before the MMA
+        // needs them (measured at 8192^3: 576K -> 509K kernel cycles against
+        // copying a stage's scales once its operands had landed, when the MMA
+        // waited for the copy after the operands).
         if constexpr (kMx) {
             if (rank == 0 && lane == 0) {
-                int stage = 0;
-                uint32_t phase = 0;
+                int sf_slot = 0;
+                uint32_t sf_phase = 0;
                 for (int u = unit; u < p.total_units && !abort_seen; u += num_units) {
                     int t, split, half;
                     unit_info(p, u, t, split, half);
                     int kb_begin, kb_end;
                     split_range(p, split, kb_begin, kb_end);
                     for (int kb = kb_begin; kb < kb_end; ++kb) {
-                        if (!wait_bounded(p, full_bar(stage), phase, kErrMmaFull)) {
+                        if (!wait_bounded(p, sf_land_bar(sf_slot), sf_phase, kErrMmaFull)) {
                             abort_seen = true;
                             break;
                         }
                         tc_fence_after_sync();
-                        const uint32_t sf_src = base + G::kOffSf + stage * G::kSfBytes;
-                        const uint32_t sf_tmem = tmem_base + G::kColSf + stage * G::kSfCols;
+                        const uint32_t sf_src = base + G::kOffSf + sf_slot * G::kSfBytes;
+                        const uint32_t sf_tmem = tmem_base + G::kColSf + sf_slot * G::kSfCols;
 #pragma unroll
                         for (int q = 0; q < G::kSfBlocksPerAtom * kAtoms; ++q) {   // atom by atom: A, B 0, B 1, …
                             if constexpr (kCG == 2)
@@ -677,11 +732,11 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                             else
                                 tmem_cp_128x16b(sf_tmem + 4 * q, smem_desc_plain(sf_src + 512 * q, 16, 128));
                         }
-                        if constexpr (kCG == 2) mma_commit_pair_mask(sf_full_bar(stage), 0x1);
-                        else mma_commit_one(sf_full_bar(stage));
-                        if (++stage == G::kStages) {
-                            stage = 0;
-                            phase ^= 1u;
+                        if constexpr (kCG == 2) mma_commit_pair_mask(sf_full_bar(sf_slot), 0x1);
+                        else mma_commit_one(sf_full_bar(sf_slot));
+                        if (++sf_slot == G::kSfSlots) {
+                            sf_slot = 0;
+                            sf_phase ^= 1u;
                         }
                     }
                 }
@@ -754,13 +809,15 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             const int col_base = tn * G::kTileN + (half < 0 ? 0 : half * (G::kTileN / 2));
             const int buf = G::kAccBufs == 2 ? (local & 1) : 0;
             const uint32_t acc_phase = G::kAccBufs == 2 ? ((local >> 1) & 1) : (local & 1);
-            if constexpr (G::kAccBufs == 2) {
+            {
                 // One thread waits for the accumulator, suspended rather than polling (the
                 // issuing threads of the producer and the MMA share the SM's issue slots;
-                // measured 2-3 % fewer kernel cycles); the four epilogue warps then meet at
-                // a named barrier, where the other three wait without issuing. The result
-                // goes through a flag per tile parity: the writer of tile t+2's flag has
-                // passed tile t+1's barrier, so every warp has read tile t's.
+                // measured 2-3 % fewer kernel cycles with two accumulators, 7 % with the
+                // block-scaled pair's one, where four polling warps took the MMA thread's
+                // issue slots for the whole main loop); the four epilogue warps then meet
+                // at a named barrier, where the other three wait without issuing. The
+                // result goes through a flag per tile parity: the writer of tile t+2's flag
+                // has passed tile t+1's barrier, so every warp has read tile t's.
                 volatile uint32_t* const acc_ok =
                     reinterpret_cast<volatile uint32_t*>(smem + G::kOffTmemHolder + 4) + (local & 1);
                 if (warp == 2 && lane == 0)
@@ -771,10 +828,6 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                     abort_seen = true;
                     break;
                 }
-            } else if (!wait_bounded_warp(p, acc_full_bar(buf), acc_phase, kErrEpiAccFull)) {
-                // one accumulator: the handoff is on the MMA's critical path, so every warp polls
-                abort_seen = true;
-                break;
             }
             tc_fence_after_sync();
             const int tile_row = static_cast<int>(rank) * kCtaM + static_cast<int>(q) * 32;   // in the tile

@@ -73,7 +73,7 @@ struct Variant {
     int a_rows_max;    // rows of A a stage holds (16 or 64 for the decode kernels, else 128)
     int k_elems;       // K elements per pipeline stage
     int atoms;         // 128-byte K atoms per stage (TMA boxes per operand and stage)
-    int sf_bytes;      // MXFP8: bytes of scale blocks per stage and CTA
+    int sf_bytes;      // MXFP8: bytes of scale blocks per K block and CTA
     KernelFn fn;
     const char* name;
 };
@@ -1113,7 +1113,8 @@ hk_status hk_gemm_mxfp8_ex(const void* A, const void* B, const void* SFA, const 
     g.splits = 1;
     g.group_m = kDefaultGroupM;
     g.a_rows = a_rows_for(*v, M);
-    g.expect_bytes = static_cast<uint32_t>(v->cg * ((g.a_rows + v->tile_n / v->cg) * hk::kRowBytes * v->atoms + v->sf_bytes));
+    // operand bytes of a stage (the scale blocks complete on their own barriers)
+    g.expect_bytes = static_cast<uint32_t>(v->cg * (g.a_rows + v->tile_n / v->cg) * hk::kRowBytes * v->atoms);
     g.sf_k_blocks = static_cast<int32_t>(lay.k_blocks);
     g.n_pad = int64_t(g.tiles_n) * v->tile_n;
     g.n_tma = static_cast<int32_t>(N & ~int64_t(7));
