@@ -1133,7 +1133,7 @@ CALIBRATE_SHAPES = [(1, 8192, 8192), (16, 8192, 8192), (64, 8192, 8192), (128, 8
                   (128, 4096, 4096), (256, 4096, 16384), (2048, 2048, 8192), (1024, 8192, 8192), (64, 2048, 8192)]
 
 
-def _calib_calib_warm_us(fn, reps: int = 25) -> float:
+def _calib_warm_us(fn, reps: int = 25) -> float:
     import torch
     for _ in range(3):
         fn()

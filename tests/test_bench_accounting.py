@@ -75,3 +75,20 @@ def test_source_digest_sees_code_not_comments():
     for kind in ("gemm", "attention"):
         d = bench.kernel_source_digest(kind)
         assert len(d) == 16 and d == bench.kernel_source_digest(kind)
+
+
+def test_calibration_mode_names_resolve():
+    """Every global name the calibration functions use exists in the module
+    (they only run on a GPU, so a broken name would otherwise go unseen)."""
+    import ast
+    import builtins
+    tree = ast.parse(open(bench.__file__).read())
+    for fn in (n for n in tree.body if isinstance(n, ast.FunctionDef) and n.name in ("sweep_plans", "l2_latency",
+                                                                                      "_calib_warm_us")):
+        local = {a.arg for a in ast.walk(fn) if isinstance(a, ast.arg)}
+        local |= {t.id for t in ast.walk(fn) if isinstance(t, ast.Name) and isinstance(t.ctx, ast.Store)}
+        local |= {n.name for n in ast.walk(fn) if isinstance(n, (ast.FunctionDef, ast.Lambda)) and hasattr(n, "name")}
+        local |= {a.asname or a.name.split(".")[0] for n in ast.walk(fn) if isinstance(n, (ast.Import, ast.ImportFrom))
+                  for a in n.names}
+        for name in {t.id for t in ast.walk(fn) if isinstance(t, ast.Name) and isinstance(t.ctx, ast.Load)}:
+            assert name in local or hasattr(bench, name) or hasattr(builtins, name), (fn.name, name)
