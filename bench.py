@@ -1148,7 +1148,7 @@ def _calib_warm_us(fn, reps: int = 25) -> float:
 
 
 def sweep_plans(shapes) -> None:
-    """Every plan a shape can be forced to (kernel ids 1-5, K splits 1, 2, 3, 4,
+    """Every plan a shape can be forced to (kernel ids 1-6, K splits 1, 2, 3, 4,
     6, 8, 12), warm back-to-back calls between CUDA events, next to
     torch.matmul (cuBLAS) on the same inputs; per shape the automatic plan's
     time and every candidate sorted by time. The plan's time model
@@ -1180,7 +1180,7 @@ def sweep_plans(shapes) -> None:
         auto.close()
         t_lib = _calib_warm_us(lambda: torch.matmul(A, B.t()))
         res = []
-        for kernel in (1, 2, 3, 4, 5):
+        for kernel in (1, 2, 3, 4, 5, 6):
             for split in (1, 2, 3, 4, 6, 8, 12):
                 try:
                     plan = hk.Plan(M, N, K, kernel=kernel, split_k=split)

@@ -98,6 +98,7 @@ const Variant kVariants[] = {
     make_variant<1, 128, false, false, 64>(HK_KERNEL_SINGLE_128x128, "single 128x128, 64-row A"),
     make_variant<1, 64, false, false, 64>(HK_KERNEL_SINGLE_128x64, "single 128x64, 64-row A"),
     make_variant<2, 256, false, false, hk::kCtaM, HK_PAIR_ATOMS>(HK_KERNEL_PAIR_256x256, "pair 256x256"),
+    make_variant<2, 128, false, false>(HK_KERNEL_PAIR_256x128, "pair 256x128"),
     make_variant<1, 256, false>(HK_KERNEL_SINGLE_128x256, "single 128x256"),
     make_variant<1, 192, false>(HK_KERNEL_SINGLE_128x192, "single 128x192"),
     make_variant<1, 128, false>(HK_KERNEL_SINGLE_128x128, "single 128x128"),
@@ -369,17 +370,20 @@ int a_rows_for(const Variant& v, int64_t M) {
     return static_cast<int>(std::max<int64_t>(8, ceil_div(M, 8) * 8));
 }
 
-// Kernel choice by a small time model. Automatic choice: single-CTA kernels
-// (128-row tiles, four widths) for M <= kMaxRowsSingle (bf16; 128 for E4M3),
-// CTA pairs (256-row tiles) above; K is split only when one wave of tiles
-// leaves work-unit slots idle and a workspace may be used. Estimated time of
-// a candidate (µs):
-//   GEMM   = the largest of
+// Kernel choice by a small time model. Automatic choice among single-CTA
+// kernels (128-row tiles, four widths) for M <= kMaxRowsSingle (bf16; 128 for
+// E4M3) and CTA pairs (256-row tiles: 256 or, bf16, 128 wide) for M > 128;
+// between the two limits both compete. K is split only when one wave of
+// tiles leaves work-unit slots idle and a workspace may be used. Estimated
+// time of a candidate (µs):
+//   GEMM   = the p-norm (kBoundNorm) of three bounds, so that two bounds near
+//            each other cost more than either (their overlap is imperfect):
 //              streaming: waves × (bytes one CTA moves per unit ÷ per-SM rate
 //                         + pipeline fill); the rate is what the ring keeps in
-//                         flight ÷ the load latency, at most kSmBytesPerUs; the
-//                         bytes of A count a quarter (A is shared by every unit
-//                         of a row of tiles and comes from L2),
+//                         flight ÷ the load latency, at most a cap (one for
+//                         single-CTA kernels, one per SM of a pair); A's bytes
+//                         count kABytesWeight (A is shared by every unit of a
+//                         row of tiles and comes from L2),
 //              HBM:       (A, B, and C or the fp32 partials) ÷ HBM rate,
 //              issue:     waves × K stages per unit × the larger of the tensor
 //                         time of a stage and the issuing thread's floor per
@@ -388,19 +392,22 @@ int a_rows_for(const Variant& v, int64_t M) {
 //            reduction reads them back, + C written) ÷ HBM rate + launch, when
 //            K is split (it runs after the GEMM, so its time adds).
 // The constants were fitted to warm back-to-back timings of every (kernel,
-// split) on 26 shapes from 1×1024×8192 to 2048×2048×8192 (GB300): the choice
-// is within 6 % of the best measured candidate on each, 0.5 % on average.
+// split) on 32 shapes from 1×1024×8192 to 2048×2048×8192 (GB300), with the
+// tensor time of a K step fixed at its measured value: the choice is within
+// 4.5 % of the best measured candidate on each shape, 0.6 % on average.
 constexpr int kMaxSplits = 16;
 constexpr int kMinKBlocksPerSplit = 8;
-constexpr int64_t kMaxRowsSingle = 384;      // bf16: single-CTA kernels up to here, pairs above
-constexpr double kSmBytesPerUs = 65e3;       // one SM's streaming rate cap (bytes/µs)
-constexpr double kLoadLatencyUs = 2.0;       // TMA load latency under load
-constexpr double kHbmBytesPerUs = 6.0e6;     // HBM rate the streaming kernels reach (bytes/µs)
-constexpr double kABytesWeight = 0.5;        // A's bytes (L2-resident, shared by a row of tiles) against B's
+constexpr int64_t kMaxRowsSingle = 384;      // bf16: single-CTA kernels up to here
+constexpr double kSmBytesPerUs = 106e3;      // one SM's streaming rate cap, single-CTA kernels (bytes/µs)
+constexpr double kSmBytesPerUsPair = 75.7e3; // the same per SM of a CTA pair
+constexpr double kLoadLatencyUs = 2.07;      // TMA load latency under load
+constexpr double kHbmBytesPerUs = 6.01e6;    // HBM rate the streaming kernels reach (bytes/µs)
+constexpr double kABytesWeight = 0.365;      // A's bytes (L2-resident, shared by a row of tiles) against B's
 constexpr double kKStepUs = 0.27;            // tensor time of a 64-deep K step of a 256-wide tile per SM
-constexpr double kIssueFloorUs = 0.25;       // the MMA-issuing thread's minimum per stage (waits, commit)
-constexpr double kFillUs = 2.0;              // filling the ring at the start of a unit
-constexpr double kLaunchUs = 7.0;            // the reduction: dependent launch, wait for the GEMM, tail
+constexpr double kIssueFloorUs = 0.206;      // the MMA-issuing thread's minimum per stage (waits, commit)
+constexpr double kFillUs = 0.455;            // filling the ring at the start of a unit
+constexpr double kLaunchUs = 4.55;           // the reduction: dependent launch, wait for the GEMM, tail
+constexpr double kBoundNorm = 7.34;          // exponent of the p-norm that combines the three bounds
 
 double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int64_t slots, int splits) {
     const int64_t tiles = ceil_div(M, v.tile_m) * ceil_div(N, v.tile_n);
@@ -410,7 +417,8 @@ double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int64_t sl
     const double elem = v.fp8 ? 1.0 : 2.0;
     const double stage_a = double(a_rows_for(v, M)) * hk::kRowBytes * v.atoms;
     const double stage_b = double(v.tile_n / v.cg) * hk::kRowBytes * v.atoms;
-    const double sm_rate = std::min(kSmBytesPerUs, (stage_a + stage_b) * v.stages / kLoadLatencyUs);
+    const double cap = v.cg == 2 ? kSmBytesPerUsPair : kSmBytesPerUs;
+    const double sm_rate = std::min(cap, (stage_a + stage_b) * v.stages / kLoadLatencyUs);
     const double t_stream = waves * ((stage_a * kABytesWeight + stage_b) * kb / sm_rate + kFillUs);
     const double n_pad = double(ceil_div(N, v.tile_n) * v.tile_n);
     const double partials = splits > 1 ? 4.0 * splits * M * n_pad : 0.0;
@@ -418,7 +426,10 @@ double estimate_us(const Variant& v, int64_t M, int64_t N, int64_t K, int64_t sl
     const double t_hbm = (operands + (splits > 1 ? partials : 2.0 * M * N)) / kHbmBytesPerUs;
     const double t_mma = waves * kb * std::max(kKStepUs * v.atoms * (double(v.tile_n) / 256.0), kIssueFloorUs);
     const double t_reduce = splits > 1 ? (2.0 * partials + 2.0 * M * N) / kHbmBytesPerUs + kLaunchUs : 0.0;
-    return std::max(t_stream, std::max(t_hbm, t_mma)) + t_reduce;
+    const double t_gemm = std::pow(std::pow(t_stream, kBoundNorm) + std::pow(t_hbm, kBoundNorm) +
+                                       std::pow(t_mma, kBoundNorm),
+                                   1.0 / kBoundNorm);
+    return t_gemm + t_reduce;
 }
 
 void choose_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo* di, int max_units_cap, bool allow_split,
@@ -430,8 +441,9 @@ void choose_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo* di, int max_
         const Variant& v = kVariants[i];
         if (v.fp8 != fp8 || v.mx) continue;
         if (a_rows_for(v, M) > v.a_rows_max) continue;   // short A stages serve only M up to their rows
-        const int64_t max_single = fp8 ? int64_t(hk::kCtaM) : kMaxRowsSingle;
-        if (forced_kernel != HK_KERNEL_AUTO ? v.id != forced_kernel : ((M > max_single) != (v.cg == 2))) continue;
+        const bool single_ok = M <= (fp8 ? int64_t(hk::kCtaM) : kMaxRowsSingle);
+        const bool pair_ok = M > hk::kCtaM;
+        if (forced_kernel != HK_KERNEL_AUTO ? v.id != forced_kernel : !(v.cg == 2 ? pair_ok : single_ok)) continue;
         const int64_t k_blocks = ceil_div(K, v.k_elems);
         int64_t slots = di->max_units[i];
         if (max_units_cap > 0 && max_units_cap < slots) slots = max_units_cap;

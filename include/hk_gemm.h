@@ -86,13 +86,16 @@ typedef enum hk_status {
 
 /* Kernel variants (hk_gemm_config.kernel). A "pair" kernel runs on clusters
  * of two CTAs (tcgen05 cta_group::2) with 256-row output tiles; a "single"
- * kernel runs one CTA per output tile of 128 rows and suits M <= 128. */
-#define HK_KERNEL_AUTO 0            /* chosen by the plan's time model: single-CTA kernels for M <= 384 (E4M3: 128), pairs above */
+ * kernel runs one CTA per output tile of 128 rows and suits M <= 128. The
+ * 256x128 pair (bf16 only) streams a narrower slice of B per pair: for
+ * 128 < M <= 256 with few output tiles it fills the GPU without a K split. */
+#define HK_KERNEL_AUTO 0            /* chosen by the plan's time model: single-CTA kernels for M <= 128, pairs above 384 (E4M3: 128), either between */
 #define HK_KERNEL_PAIR_256x256 1
 #define HK_KERNEL_SINGLE_128x256 2
 #define HK_KERNEL_SINGLE_128x192 3
 #define HK_KERNEL_SINGLE_128x128 4
 #define HK_KERNEL_SINGLE_128x64 5
+#define HK_KERNEL_PAIR_256x128 6
 
 /* Tuning knobs of a plan. Zero in any field selects the default. */
 typedef struct hk_gemm_config {

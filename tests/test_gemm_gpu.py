@@ -162,12 +162,13 @@ def test_stream_argument(hk):
 
 # (label, M, N, K, plan options, expected kernel id, expected stages or 0, expected K splits)
 TIMEOUT_CASES = [
-    ("pair bf16", 512, 512, 512, {}, 1, 0, 1),
+    ("pair bf16", 512, 512, 512, {"kernel": 1}, 1, 0, 1),
     ("single 128x256, 16-row A stages", 1, 512, 512, {"kernel": 2}, 2, 6, 1),
     ("single 128x256, 64-row A stages", 40, 512, 512, {"kernel": 2}, 2, 5, 1),
     ("single 128x64", 100, 512, 512, {"kernel": 5}, 5, 0, 1),
     ("single 128x256, split K", 64, 1024, 2048, {"kernel": 2, "split_k": 4}, 2, 0, 4),
     ("pair bf16, split K", 512, 512, 2048, {"kernel": 1, "split_k": 2}, 1, 0, 2),
+    ("pair 256x128", 256, 640, 512, {"kernel": 6}, 6, 8, 1),
     ("fp8 pair", 512, 512, 512, {"input_type": 1}, 1, 0, 1),
     ("fp8 single 128x192", 128, 600, 512, {"input_type": 1, "kernel": 3}, 3, 0, 1),
 ]
@@ -310,7 +311,7 @@ def run_plan(hk, A_bits, B_bits, **cfg):
     return full[:M, :N], info
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4, 5, 6])
 @pytest.mark.parametrize("M,N,K", VARIANT_SHAPES)
 def test_kernel_variants_integer_bitexact(hk, kernel, M, N, K):
     A = synth.int_bf16(M, K, 1200 + M)
@@ -320,7 +321,7 @@ def test_kernel_variants_integer_bitexact(hk, kernel, M, N, K):
     assert_bitexact(got, oracle.gemm(A, B), f"kernel {kernel} int {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("kernel", [2, 3, 4, 5])
+@pytest.mark.parametrize("kernel", [2, 3, 4, 5, 6])
 def test_kernel_variants_normal(hk, kernel):
     M, N, K = 200, 777, 1500
     A = synth.normal_bf16(M, K, 31)
@@ -332,9 +333,10 @@ def test_kernel_variants_normal(hk, kernel):
 def test_automatic_kernel_choice(hk):
     assert hk.Plan(128, 28672, 8192).info()["kernel"] == 3      # 150 tiles of 128x192 ~ one per SM
     assert hk.Plan(8192, 8192, 8192).info()["kernel"] == 1
-    assert hk.Plan(385, 4096, 4096).info()["kernel"] == 1       # above 384 rows: CTA pairs
-    assert hk.Plan(129, 4096, 4096).info()["ctas_per_unit"] == 1  # up to 384 rows: single-CTA tiles (measured faster)
-    assert hk.Plan(256, 8192, 8192).info()["ctas_per_unit"] == 1
+    assert hk.Plan(385, 4096, 4096).info()["ctas_per_unit"] == 2  # above 384 rows: CTA pairs
+    assert hk.Plan(129, 4096, 4096).info()["ctas_per_unit"] == 1  # a 129-row pair tile would be half empty
+    assert hk.Plan(256, 8192, 8192).info()["kernel"] == 6       # 64 pairs of 256x128: one wave, no K split
+    assert hk.Plan(384, 8192, 8192).info()["kernel"] == 3       # 3 x 43 tiles of 128x192 (measured best)
     assert hk.Plan(200, 4096, 4096, input_type=hk.HK_INPUT_E4M3).info()["kernel"] == 1   # E4M3: pairs above 128
     small = hk.Plan(64, 1024, 1024).info()
     assert small["kernel"] == 5 and small["ctas_per_unit"] == 1  # 16 tiles: narrowest tiles spread widest
@@ -375,7 +377,7 @@ def run_split(hk, A_bits, B_bits, ws_fill=0, runs=1, **cfg):
 
 
 @pytest.mark.parametrize("kernel,splits,M,N,K", [
-    (1, 2, 300, 200, 1000), (1, 5, 257, 520, 2049), (2, 3, 100, 700, 900), (3, 7, 64, 1000, 2000),
+    (1, 2, 300, 200, 1000), (1, 5, 257, 520, 2049), (6, 3, 200, 700, 1000), (2, 3, 100, 700, 900), (3, 7, 64, 1000, 2000),
     (4, 16, 128, 300, 1030), (5, 4, 1, 77, 640), (3, 2, 200, 600, 128)])
 def test_split_k_integer_bitexact(hk, kernel, splits, M, N, K):
     A = synth.int_bf16(M, K, 1300 + M)
@@ -395,11 +397,12 @@ def test_split_k_normal_and_deterministic(hk):
 
 
 def test_split_k_automatic_for_small_m(hk):
+    """64 x 2048 x 8192: 16-32 output tiles for 152 SMs, so the plan splits K."""
     A = synth.normal_bf16(64, 8192, 43)
-    B = synth.normal_bf16(8192, 8192, 44)
+    B = synth.normal_bf16(2048, 8192, 44)
     outs, info = run_split(hk, A, B)
     assert info["split_k"] > 1 and info["ctas_per_unit"] == 1
-    r, c = synth.sample_positions(64, 8192, 45, count=2048)
+    r, c = synth.sample_positions(64, 2048, 45, count=2048)
     ref, _ = oracle.gemm_entries(A, B, r, c)
     assert_close(outs[0][r, c], ref, 8192, 1, 1, "auto split")
     assert hk.Plan(8192, 8192, 8192).info()["split_k"] == 1          # full waves: never split
@@ -445,14 +448,27 @@ def test_tail_split_integer_bitexact(hk, M, N, K):
     assert_bitexact(got, whole, "split vs whole")
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 1024, 640), (600, 1000, 320), (130, 4100, 136)])
+def test_tail_split_narrow_pair_integer_bitexact(hk, M, N, K):
+    """The 256x128 pair's last partial round runs as 256x64 halves."""
+    A = synth.int_bf16(M, K, 1450 + M)
+    B = synth.int_bf16(N, K, 2450 + N)
+    got, info = run_plan(hk, A, B, kernel=6)
+    assert info["kernel"] == 6 and info["tile_n"] == 128 and info["tail_split_tiles"] > 0
+    assert_bitexact(got, oracle.gemm(A, B), f"narrow pair tail split {M}x{N}x{K}")
+    whole, info2 = run_plan(hk, A, B, kernel=6, flags=hk.HK_FLAG_NO_TAIL_SPLIT)
+    assert info2["tail_split_tiles"] == 0
+    assert_bitexact(got, whole, "split vs whole")
+
+
 def test_tail_split_normal_matches_whole_tiles(hk):
     M, N, K = 1024, 2000, 1000          # 4 x 8 = 32 tiles: all run as halves
     A = synth.normal_bf16(M, K, 61)
     B = synth.normal_bf16(N, K, 62)
-    got, info = run_plan(hk, A, B)
+    got, info = run_plan(hk, A, B, kernel=1)
     assert info["tail_split_tiles"] > 0
     assert_close(got, oracle.gemm(A, B), K, 1, 1, "tail split normal")
-    whole, _ = run_plan(hk, A, B, flags=2)
+    whole, _ = run_plan(hk, A, B, kernel=1, flags=2)
     assert_close(got, whole, K, 1, 1, "split vs whole")
 
 
