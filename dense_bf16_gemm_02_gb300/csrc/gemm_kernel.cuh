@@ -536,7 +536,11 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                                                    : static_cast<const void*>(&tmap_b_half);
                 const uint32_t stage_bytes = half < 0 ? p.expect_bytes : p.expect_bytes_half;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    if (!wait_bounded(p, empty_bar(stage), phase ^ 1u, kErrProducerEmpty)) {
+                    // a full ring ahead of the MMAs: the wait may suspend the thread (the
+                    // probes otherwise cost instructions, not time: measured no change in
+                    // kernel cycles either way)
+                    if (!(mbar_try_wait(empty_bar(stage), phase ^ 1u) ||
+                          wait_bounded_suspend(p, empty_bar(stage), phase ^ 1u, kErrProducerEmpty))) {
                         abort_seen = true;
                         break;
                     }
