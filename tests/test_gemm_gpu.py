@@ -725,10 +725,25 @@ def test_residual_padded_leading_dimension(hk):
     assert_bitexact(got, oracle.gemm_epilogue(A, B, None, 0, residual=R), "ldr > N")
 
 
-@pytest.mark.parametrize("kernel,splits", [(4, 4), (1, 3), (2, 2)])
+@pytest.mark.parametrize("M,N,K", [(257, 600, 128), (520, 1030, 264)])
+def test_fused_epilogue_narrow_pair_integer_bitexact(hk, M, N, K):
+    """The 256x128 pair kernel, its 256x64 tail halves included (10 and 27
+    tiles: every tile runs as two halves), with bias and ReLU, then with a
+    residual added after the activation."""
+    A = synth.int_bf16(M, K, 1950 + M)
+    B = synth.int_bf16(N, K, 2950 + N)
+    bias = synth.int_bf16(1, N, 3950 + N)[0]
+    R = synth.int_bf16(M, N, 4950 + N, -40, 40)
+    got = run_epilogue(hk, A, B, bias, 1, split_k=1, kernel=6)
+    assert_bitexact(got, oracle.gemm_epilogue(A, B, bias, 1), f"narrow pair relu + bias {M}x{N}x{K}")
+    got = run_fused(hk, A, B, bias, R, 1, split_k=1, kernel=6)
+    assert_bitexact(got, oracle.gemm_epilogue(A, B, bias, 1, residual=R), f"narrow pair residual {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("kernel,splits", [(4, 4), (1, 3), (2, 2), (6, 3)])
 def test_residual_in_split_k_reduction(hk, kernel, splits):
     """A K split adds bias, activation and R in its reduction kernel."""
-    M, N, K = (300 if kernel == 1 else 64), 1200, 2048
+    M, N, K = (300 if kernel in (1, 6) else 64), 1200, 2048
     A = synth.int_bf16(M, K, 81)
     B = synth.int_bf16(N, K, 82)
     bias = synth.int_bf16(1, N, 83)[0]
