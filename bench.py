@@ -355,6 +355,32 @@ def workload_config(w) -> dict:
     return cfg
 
 
+# Pause before a timed block. The GPU's clock depends on its recent load (it
+# runs faster for a while after a pause than under continuous work; measured
+# at 8192^3: whichever of two kernels is timed first after a 2 s pause reads
+# 10-15 % higher), so our timed region and the library's context block both
+# start after the same warm-up and the same pause.
+TIMED_PAUSE_S = 0.3
+
+
+def time_library(call, dev, warmup: int, n: int) -> float:
+    """Mean ms per call of `call`, under the protocol of our timed region:
+    `warmup` calls, a TIMED_PAUSE_S pause, then `n` back-to-back calls
+    between CUDA events on the current stream."""
+    import torch
+    for _ in range(max(3, warmup)):
+        call()
+    torch.cuda.synchronize(dev)
+    time.sleep(TIMED_PAUSE_S)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record()
+    for _ in range(n):
+        call()
+    c1.record()
+    torch.cuda.synchronize(dev)
+    return c0.elapsed_time(c1) / n
+
+
 # ---------------------------------------------------------------- GPU arm --
 
 def run_hk(args, w):
@@ -429,8 +455,7 @@ def run_hk(args, w):
     # ---- device-resident timed region: K launches, one event between each
     events = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     sampler = ClockSampler(local) if rank == 0 else None
-    if sampler:
-        time.sleep(0.3)
+    time.sleep(TIMED_PAUSE_S)   # (also lets the clock sampler start)
     barrier(world)
     torch.cuda.synchronize(dev)
     t_host0 = time.time()
@@ -528,21 +553,14 @@ def run_hk(args, w):
                 s_a = torch.tensor(sa, dtype=torch.float32, device=dev)
                 s_b = torch.tensor(sb, dtype=torch.float32, device=dev)
                 lib_call = lambda: torch._scaled_mm(A8, B8.t(), scale_a=s_a, scale_b=s_b, out_dtype=torch.bfloat16)
-                what = "torch._scaled_mm (cuBLASLt FP8) on the same GPU and inputs, timed after ours; context only"
+                what = ("torch._scaled_mm (cuBLASLt FP8) on the same GPU and inputs, timed after ours with the same "
+                        "warm-up and pause; context only")
             else:
                 lib_call = lambda: torch.matmul(A, B.t(), out=C)
-                what = "torch.matmul (cuBLAS) on the same GPU and inputs, timed after ours; context only"
-            for _ in range(3):
-                lib_call()
-            torch.cuda.synchronize(dev)
-            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                what = ("torch.matmul (cuBLAS) on the same GPU and inputs, timed after ours with the same warm-up "
+                        "and pause; context only")
             n_ctx = max(5, args.steps)   # as many back-to-back calls as our timed region
-            c0.record()
-            for _ in range(n_ctx):
-                lib_call()
-            c1.record()
-            torch.cuda.synchronize(dev)
-            ms = c0.elapsed_time(c1) / n_ctx
+            ms = time_library(lib_call, dev, args.warmup, n_ctx)
             cublas = {"value": flops / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_gemm": ms, "launches": n_ctx,
                       "what": what}
         except Exception as exc:   # context only: never fails the bench
@@ -718,8 +736,7 @@ def run_mx(args, w):
     torch.cuda.synchronize(dev)
     events = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     sampler = ClockSampler(local) if rank == 0 else None
-    if sampler:
-        time.sleep(0.3)
+    time.sleep(TIMED_PAUSE_S)   # (also lets the clock sampler start)
     barrier(world)
     torch.cuda.synchronize(dev)
     t_host0 = time.time()
@@ -790,19 +807,11 @@ def run_mx(args, w):
             a8, b8 = A.view(torch.float8_e4m3fn), B.view(torch.float8_e4m3fn)
             sa8, sb8 = SA.view(torch.float8_e8m0fnu), SB.view(torch.float8_e8m0fnu)
             call = lambda: torch._scaled_mm(a8, b8.t(), scale_a=sa8, scale_b=sb8, out_dtype=torch.bfloat16)
-            for _ in range(3):
-                call()
-            torch.cuda.synchronize(dev)
-            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             n_ctx = max(5, args.steps)   # as many back-to-back calls as our timed region
-            c0.record()
-            for _ in range(n_ctx):
-                call()
-            c1.record()
-            torch.cuda.synchronize(dev)
-            ms = c0.elapsed_time(c1) / n_ctx
+            ms = time_library(call, dev, args.warmup, n_ctx)
             ctx = {"value": flops / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_gemm": ms, "launches": n_ctx,
-                   "what": "torch._scaled_mm with e8m0 block scales (cuBLASLt) on the same GPU and inputs; context only"}
+                   "what": "torch._scaled_mm with e8m0 block scales (cuBLASLt) on the same GPU and inputs, timed after "
+                           "ours with the same warm-up and pause; context only"}
         except Exception as exc:
             ctx = {"unavailable": str(exc)[:200]}
 
@@ -987,8 +996,7 @@ def run_attn(args, w):
 
     events = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     sampler = ClockSampler(local) if rank == 0 else None
-    if sampler:
-        time.sleep(0.3)
+    time.sleep(TIMED_PAUSE_S)   # (also lets the clock sampler start)
     barrier(world)
     torch.cuda.synchronize(dev)
     t_host0 = time.time()
@@ -1064,20 +1072,11 @@ def run_attn(args, w):
         try:
             import torch.nn.functional as F
             call = lambda: F.scaled_dot_product_attention(Q, K, V, is_causal=w.causal, enable_gqa=True)
-            for _ in range(3):
-                call()
-            torch.cuda.synchronize(dev)
-            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             n_ctx = max(3, args.steps)   # as many back-to-back calls as our timed region
-            c0.record()
-            for _ in range(n_ctx):
-                call()
-            c1.record()
-            torch.cuda.synchronize(dev)
-            ms = c0.elapsed_time(c1) / n_ctx
+            ms = time_library(call, dev, args.warmup, n_ctx)
             sdpa = {"value": flops / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_call": ms, "launches": n_ctx,
                     "what": "torch scaled_dot_product_attention (enable_gqa) on the same GPU and inputs, "
-                            "timed after ours; context only"}
+                            "timed after ours with the same warm-up and pause; context only"}
         except Exception as exc:
             sdpa = {"unavailable": str(exc)[:200]}
 
