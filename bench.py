@@ -55,8 +55,10 @@ MEASURED_TRAFFIC = {
     # the GEMM kernel alone (the split-K reduction reads the fp32 partials and writes C)
     "decode_64x8192x28672": {"source_digest": "13ee8632a893ab49", "bytes_per_launch": 473519360 + 3435520},
     # attention: captured at B2 (one launch); the B16 figure scales it by 8 (traffic grows with B)
-    "attn_gqa_b2_s4096_d128": {"source_digest": "325cd38bad1c92ef", "bytes_per_launch": 200060160 + 110417152},
-    "attn_gqa_b16_s4096_d128": {"source_digest": "325cd38bad1c92ef", "bytes_per_launch": 8 * (200060160 + 110417152)},
+    "attn_gqa_b2_s4096_d128": {"source_digest": "89f7a7a6da310d8d", "bytes_per_launch": 199923456 + 110883584},
+    "attn_gqa_b16_s4096_d128": {"source_digest": "89f7a7a6da310d8d", "bytes_per_launch": 8 * (199923456 + 110883584)},
+    # D = 64 captured at the bench's own size (one launch)
+    "attn_gqa_b16_s4096_d64": {"source_digest": "89f7a7a6da310d8d", "bytes_per_launch": 2865444352 + 548965888},
 }
 
 
