@@ -70,12 +70,13 @@ typedef enum hk_status {
 /* Plan flags (hk_gemm_config.flags). */
 #define HK_FLAG_NONE 0u
 /* Test only: the producer withholds its arrival on the first shared-memory
- * stage, so a bounded wait on that stage runs out (the MMA issuer's; for
- * MXFP8 the scale copier's) and the call reports HK_ERR_TIMEOUT through the
- * device status word. No GPU fault is caused. */
+ * stage, so a bounded wait on that stage runs out (the MMA issuer's) and
+ * the call reports HK_ERR_TIMEOUT through the device status word. No GPU
+ * fault is caused. */
 #define HK_FLAG_FAULT_DROP_ARRIVE 0x1u
 /* Keep the tiles of the last partial round whole (by default, when they fill
- * at most half of the CTA pairs, each runs as two 256x128 halves). */
+ * at most half of the CTA pairs, each runs as two halves of half the tile's
+ * width: 256x128 for the 256x256 pair, 256x64 for the 256x128 pair). */
 #define HK_FLAG_NO_TAIL_SPLIT 0x2u
 
 /* Fused epilogue activations: C = bf16(act(A·Bᵀ + bias) [+ R]). */
