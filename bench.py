@@ -383,6 +383,22 @@ def time_library(call, dev, warmup: int, n: int) -> float:
     return c0.elapsed_time(c1) / n
 
 
+def launch_spread(call, stream, n: int) -> list:
+    """Durations (ms) of `n` launches of `call` with an event between each, for
+    the spread (p10/p90) of launch times. Taken after the timed region, not in
+    it: an event between two launches keeps the second from starting early as
+    a programmatic dependent of the first, which slows back-to-back steps."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(n):
+            call()
+            ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+
+
 # ---------------------------------------------------------------- GPU arm --
 
 def run_hk(args, w):
@@ -454,8 +470,8 @@ def run_hk(args, w):
     if hk.hk_gemm_last_device_status(local) != hk.HK_OK:
         raise RuntimeError("device status after warm-up: " + hk.hk_gemm_last_error_string())
 
-    # ---- device-resident timed region: K launches, one event between each
-    events = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    # ---- device-resident timed region: K back-to-back launches between two events
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(2)]   # the timed region's two ends
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(TIMED_PAUSE_S)   # (also lets the clock sampler start)
     barrier(world)
@@ -465,12 +481,11 @@ def run_hk(args, w):
         events[0].record(stream)
         for i in range(args.steps):
             step()
-            events[i + 1].record(stream)
+        events[1].record(stream)
     torch.cuda.synchronize(dev)
     t_host1 = time.time()
     barrier(world)
-    elapsed_ms = events[0].elapsed_time(events[-1])
-    per_launch = [events[i].elapsed_time(events[i + 1]) for i in range(args.steps)]
+    elapsed_ms = events[0].elapsed_time(events[1])
     if hk.hk_gemm_last_device_status(local) != hk.HK_OK:
         raise RuntimeError("device status after timing: " + hk.hk_gemm_last_error_string())
     clocks = None
@@ -478,6 +493,8 @@ def run_hk(args, w):
         time.sleep(0.15)
         sampler.stop()
         clocks = sampler.summary(t_host0, t_host1)
+    # per-launch spread, outside the timed region
+    per_launch = launch_spread(step, stream, min(args.steps, 20))
     elapsed_max = max_over_ranks(world, elapsed_ms)
 
     # ---- end to end: pinned host inputs -> device -> GEMM -> host result.
@@ -577,7 +594,7 @@ def run_hk(args, w):
     peaks, peaks_src = load_peaks()
     peak, tensor_src = tensor_peak(peaks, peaks_src, elapsed_max / 1e3, fp8)
     value = replica_value(flops, args.steps, world, elapsed_max)
-    mean_launch_ms = statistics.mean(per_launch)
+    mean_launch_ms = elapsed_ms / args.steps   # the timed region's mean, back to back
     nbytes = gemm_bytes(w.M, w.N, w.K) if not fp8 else float(w.M * w.K + w.N * w.K + 2 * w.M * w.N)
     hbm_bound = flops / nbytes < peak * 1e12 / (float(peaks["hbm_gbs"]) * 1e9)   # below the roofline knee
     if hbm_bound:
@@ -610,6 +627,7 @@ def run_hk(args, w):
                      "algorithmic_bytes_per_launch": nbytes,
                      "mean_launch_ms": mean_launch_ms, "p10_launch_ms": float(np.percentile(per_launch, 10)),
                      "p90_launch_ms": float(np.percentile(per_launch, 90)),
+                     "spread_source": "p10/p90: launches timed one by one after the timed region",
                      "kernel": f"gemm_bf16_kernel ({info['tile_m']}x{info['tile_n']}, "
                                f"{info['ctas_per_unit']} CTA(s) per tile)",
                      "source_digest": digest},
@@ -736,7 +754,7 @@ def run_mx(args, w):
         for _ in range(args.warmup):
             launch(A, B, SA, SB, C)
     torch.cuda.synchronize(dev)
-    events = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(2)]   # the timed region's two ends
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(TIMED_PAUSE_S)   # (also lets the clock sampler start)
     barrier(world)
@@ -746,12 +764,11 @@ def run_mx(args, w):
         events[0].record(stream)
         for i in range(args.steps):
             launch(A, B, SA, SB, C)
-            events[i + 1].record(stream)
+        events[1].record(stream)
     torch.cuda.synchronize(dev)
     t_host1 = time.time()
     barrier(world)
-    elapsed_ms = events[0].elapsed_time(events[-1])
-    per_launch = [events[i].elapsed_time(events[i + 1]) for i in range(args.steps)]
+    elapsed_ms = events[0].elapsed_time(events[1])
     if hk.hk_gemm_last_device_status(local) != hk.HK_OK:
         raise RuntimeError("device status after timing: " + hk.hk_gemm_last_error_string())
     clocks = None
@@ -759,6 +776,8 @@ def run_mx(args, w):
         time.sleep(0.15)
         sampler.stop()
         clocks = sampler.summary(t_host0, t_host1)
+    # per-launch spread, outside the timed region
+    per_launch = launch_spread(lambda: launch(A, B, SA, SB, C), stream, min(args.steps, 20))
     elapsed_max = max_over_ranks(world, elapsed_ms)
 
     # end to end: pinned host A, B, scales -> device -> GEMM -> C to pinned host (three streams)
@@ -825,7 +844,7 @@ def run_mx(args, w):
     peaks, peaks_src = load_peaks()
     peak, peak_source = tensor_peak(peaks, peaks_src, elapsed_max / 1e3, fp8=True)
     value = replica_value(flops, args.steps, world, elapsed_max)
-    mean_launch_ms = statistics.mean(per_launch)
+    mean_launch_ms = elapsed_ms / args.steps   # the timed region's mean, back to back
     achieved = flops / (mean_launch_ms / 1e3) / 1e12
     digest = kernel_source_digest("gemm")
     tr = MEASURED_TRAFFIC.get(w.name)
@@ -843,6 +862,7 @@ def run_mx(args, w):
                      "algorithmic_bytes_per_launch": float(w.M * w.K + w.N * w.K + (w.M + w.N) * kb + 2 * w.M * w.N),
                      "mean_launch_ms": mean_launch_ms, "p10_launch_ms": float(np.percentile(per_launch, 10)),
                      "p90_launch_ms": float(np.percentile(per_launch, 90)),
+                     "spread_source": "p10/p90: launches timed one by one after the timed region",
                      "kernel": ("mx_scale_blocks_kernel + gemm_bf16_kernel<2, 256, fp8, mx>" if w.M > 128 else "mx_scale_blocks_kernel + gemm_bf16_kernel<1, 192, fp8, mx>"), "source_digest": digest},
         "e2e": {"value": replica_value(flops, e2e_steps, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(sum(h.numel() for h in hosts)), "d2h_bytes_per_step": int(C_h[0].numel() * 2),
@@ -996,7 +1016,7 @@ def run_attn(args, w):
     if hk.hk_gemm_last_device_status(local) != hk.HK_OK:
         raise RuntimeError("device status after warm-up: " + hk.hk_gemm_last_error_string())
 
-    events = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(2)]   # the timed region's two ends
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(TIMED_PAUSE_S)   # (also lets the clock sampler start)
     barrier(world)
@@ -1006,12 +1026,11 @@ def run_attn(args, w):
         events[0].record(stream)
         for i in range(args.steps):
             launch(Q, K, V, O)
-            events[i + 1].record(stream)
+        events[1].record(stream)
     torch.cuda.synchronize(dev)
     t_host1 = time.time()
     barrier(world)
-    elapsed_ms = events[0].elapsed_time(events[-1])
-    per_launch = [events[i].elapsed_time(events[i + 1]) for i in range(args.steps)]
+    elapsed_ms = events[0].elapsed_time(events[1])
     if hk.hk_gemm_last_device_status(local) != hk.HK_OK:
         raise RuntimeError("device status after timing: " + hk.hk_gemm_last_error_string())
     clocks = None
@@ -1019,6 +1038,8 @@ def run_attn(args, w):
         time.sleep(0.15)
         sampler.stop()
         clocks = sampler.summary(t_host0, t_host1)
+    # per-launch spread, outside the timed region
+    per_launch = launch_spread(lambda: launch(Q, K, V, O), stream, min(args.steps, 20))
     elapsed_max = max_over_ranks(world, elapsed_ms)
 
     # ---- end to end: pinned host Q, K, V -> device -> attention -> O to pinned host,
@@ -1090,7 +1111,7 @@ def run_attn(args, w):
     peaks, peaks_src = load_peaks()
     peak, peak_source = tensor_peak(peaks, peaks_src, elapsed_max / 1e3)
     value = replica_value(flops, args.steps, world, elapsed_max)
-    mean_launch_ms = statistics.mean(per_launch)
+    mean_launch_ms = elapsed_ms / args.steps   # the timed region's mean, back to back
     achieved = flops / (mean_launch_ms / 1e3) / 1e12
     digest = kernel_source_digest("attention")
     tr = MEASURED_TRAFFIC.get(w.name)
@@ -1109,6 +1130,7 @@ def run_attn(args, w):
                      "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": attn_bytes(w),
                      "mean_launch_ms": mean_launch_ms, "p10_launch_ms": float(np.percentile(per_launch, 10)),
                      "p90_launch_ms": float(np.percentile(per_launch, 90)),
+                     "spread_source": "p10/p90: launches timed one by one after the timed region",
                      "kernel": f"attn_fwd_kernel<{w.D}>", "source_digest": digest},
         "e2e": {"value": replica_value(flops, e2e_steps, world, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": int(O_h[0].numel() * 2), "steps": e2e_steps,

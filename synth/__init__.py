@@ -52,6 +52,8 @@ WORKLOADS = {
     # decode-regime projections (one token; a batch of 64) over a 448 MiB weight matrix, 3.5x the L2
     "decode_1x28672x8192": Workload("decode_1x28672x8192", 11, 1, 28672, 8192, 0.02, False),
     "decode_64x8192x28672": Workload("decode_64x8192x28672", 12, 64, 8192, 28672, 0.02, True),
+    # 256 rows over an 8192 x 8192 weight matrix: just below the roofline knee (the 256x128 pair's shape)
+    "decode_256x8192x8192": Workload("decode_256x8192x8192", 13, 256, 8192, 8192, 0.02, True),
 }
 
 # FP8 (E4M3) workloads: operands N(0,1) rounded to E4M3, per-tensor scales

@@ -56,7 +56,7 @@ def test_decode_workloads_are_hbm_bound_and_larger_than_l2():
     import synth
     peaks = dict(bench.FALLBACK_PEAKS)
     knee = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)   # flop per byte
-    for name in ("decode_1x28672x8192", "decode_64x8192x28672"):
+    for name in ("decode_1x28672x8192", "decode_64x8192x28672", "decode_256x8192x8192"):
         w = synth.WORKLOADS[name]
         ai = bench.gemm_flops(w.M, w.N, w.K) / bench.gemm_bytes(w.M, w.N, w.K)
         assert ai < knee, name

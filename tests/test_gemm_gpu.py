@@ -280,6 +280,10 @@ def test_workload_decode_batch_64(hk):
     _check_workload(hk, "decode_64x8192x28672", via_plan=True)
 
 
+def test_workload_decode_batch_256(hk):
+    _check_workload(hk, "decode_256x8192x8192", via_plan=True)
+
+
 # ------------------------------------------------------ kernel variants --
 
 VARIANT_SHAPES = [(1, 1, 1), (100, 300, 70), (128, 1000, 520), (257, 130, 64), (700, 452, 1000)]
