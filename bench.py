@@ -45,15 +45,15 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # sources whose digest is given (the code of those sources, comments and
 # layout excluded).
 MEASURED_TRAFFIC = {
-    "gemm_8192": {"source_digest": "13ee8632a893ab49", "bytes_per_launch": 1058053632 + 126183936},
+    "gemm_8192": {"source_digest": "5eb7e0d144e6d903", "bytes_per_launch": 1085094144 + 125301248},
     # inputs smaller than L2 (warm): DRAM traffic is below the algorithmic bytes
-    "gemm_4096": {"source_digest": "13ee8632a893ab49", "bytes_per_launch": 83129344 + 14001152},
-    "skinny_128x28672x8192": {"source_digest": "13ee8632a893ab49", "bytes_per_launch": 471983616 + 3238912},
-    "fp8_gemm_8192": {"source_digest": "13ee8632a893ab49", "bytes_per_launch": 345034752 + 115610368},
+    "gemm_4096": {"source_digest": "5eb7e0d144e6d903", "bytes_per_launch": 81968896 + 13829376},
+    "skinny_128x28672x8192": {"source_digest": "5eb7e0d144e6d903", "bytes_per_launch": 471965696 + 3182848},
+    "fp8_gemm_8192": {"source_digest": "5eb7e0d144e6d903", "bytes_per_launch": 338380032 + 114954752},
     # the block-scaled GEMM kernel alone (the scale arrangement kernel moves ~8 MB more)
-    "mxfp8_gemm_8192": {"source_digest": "13ee8632a893ab49", "bytes_per_launch": 359329280 + 116552192},
+    "mxfp8_gemm_8192": {"source_digest": "5eb7e0d144e6d903", "bytes_per_launch": 352365568 + 115679232},
     # the GEMM kernel alone (the split-K reduction reads the fp32 partials and writes C)
-    "decode_64x8192x28672": {"source_digest": "13ee8632a893ab49", "bytes_per_launch": 473519360 + 3435520},
+    "decode_64x8192x28672": {"source_digest": "5eb7e0d144e6d903", "bytes_per_launch": 473502208 + 3217408},
     # attention: captured at B2 (one launch); the B16 figure scales it by 8 (traffic grows with B)
     "attn_gqa_b2_s4096_d128": {"source_digest": "89f7a7a6da310d8d", "bytes_per_launch": 199923456 + 110883584},
     "attn_gqa_b16_s4096_d128": {"source_digest": "89f7a7a6da310d8d", "bytes_per_launch": 8 * (199923456 + 110883584)},

@@ -275,7 +275,12 @@ __device__ __forceinline__ float epilogue_op(float x, float bias, int act) {
     switch (act) {
         case 1: return fmaxf(x, 0.0f);
         case 2: return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));   // x·Φ(x)
-        case 3: return x / (1.0f + expf(-x));                                  // x·σ(x)
+        // x·σ(x) through CUDA's fast exponential and division intrinsics: their few
+        // fp32 ulps of error are far below the bf16 rounding that follows; for
+        // x below about -87 the quotient comes out 0 instead of a value under
+        // 1e-36 in magnitude. Measured: 9.6 % -> 5.5 % over the plain GEMM at
+        // 8192^3, against expf and an IEEE division
+        case 3: return __fdividef(x, 1.0f + __expf(-x));
         default: return x;
     }
 }
