@@ -334,7 +334,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w),
+        "data": "synthetic", "config": workload_config(w, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
                          "sample": f"{rows_per_step} full rows of C per step ({rows_per_step}x{w.N}x{w.K})"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -343,7 +343,13 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w) -> dict:
+def parallelism(world: int) -> str:
+    return "replicas" if world > 1 else "single GPU"
+
+
+def workload_config(w, world: int = 1, epilogue: str = "none") -> dict:
+    """The workload as both arms name it (the kernel's own choices go under
+    the line's `kernel_config`, so that the two arms' configs are equal)."""
     elem = 1 if is_fp8(w) else 2
     cfg = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
            "layout": "A MxK row-major, B NxK row-major, C MxN row-major (C = A·Bᵀ)",
@@ -351,7 +357,7 @@ def workload_config(w) -> dict:
                      f"seeds {1000 + w.wid}/{2000 + w.wid}",
            "l2": "no flush: inputs larger than L2 (A+B = %d MiB > 126 MiB)" % ((w.M + w.N) * w.K * elem >> 20)
            if (w.M + w.N) * w.K * elem > 126 << 20 else "inputs smaller than L2 (warm L2)",
-           "accumulate": "fp32", "output": "bf16"}
+           "accumulate": "fp32", "output": "bf16", "parallelism": parallelism(world), "epilogue": epilogue}
     if elem == 1:
         cfg["scales"] = list(synth.FP8_SCALES)
     return cfg
@@ -614,11 +620,10 @@ def run_hk(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic",
-        "config": dict(workload_config(w), parallelism="replicas" if world > 1 else "single GPU",
-                       epilogue=args.epilogue,
-                       tile=f"{info['tile_m']}x{info['tile_n']}x{info['tile_k']} per "
-                            f"{'CTA pair' if info['ctas_per_unit'] == 2 else 'CTA'}",
-                       stages=info["stages"], grid_ctas=info["grid_ctas"], group_m=info["group_m"]),
+        "config": workload_config(w, world, args.epilogue),
+        "kernel_config": {"tile": f"{info['tile_m']}x{info['tile_n']}x{info['tile_k']} per "
+                                  f"{'CTA pair' if info['ctas_per_unit'] == 2 else 'CTA'}",
+                          "stages": info["stages"], "grid_ctas": info["grid_ctas"], "group_m": info["group_m"]},
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": bound, "achieved": achieved, "peak": rf_peak, "unit": rf_unit,
                      "frac": achieved / rf_peak, "traffic": traffic,
@@ -655,15 +660,14 @@ def run_hk(args, w):
 MX_METRIC = "MXFP8 GEMM TFLOPS at 1 GB300 and % of dense-FP8 tensor peak"
 
 
-def mx_config(w) -> dict:
+def mx_config(w, world: int = 1) -> dict:
     return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
             "layout": "A MxK, B NxK E4M3 row-major; SFA Mx(K/32), SFB Nx(K/32) UE8M0; C MxN bf16 (C = A·Bᵀ)",
             "values": f"E4M3 of N(0,1), seeds {1000 + w.wid}/{2000 + w.wid}; scales uniform 2^-3..2^3, "
                       f"seeds {3100 + w.wid}/{3200 + w.wid}",
             "l2": "no flush: inputs larger than L2 (A+B = %d MiB > 126 MiB)" % ((w.M + w.N) * w.K >> 20)
             if (w.M + w.N) * w.K > 126 << 20 else "inputs smaller than L2 (warm L2)",
-            "block": 32, "accumulate": "fp32", "output": "bf16",
-            "tile": "256x256 per CTA pair (M > 128; 128x192 per CTA otherwise)"}
+            "block": 32, "accumulate": "fp32", "output": "bf16", "parallelism": parallelism(world)}
 
 
 def oracle_mx_rows_timed(A, B, SA, SB, rows, with_values: bool = False):
@@ -719,7 +723,7 @@ def run_reference_mx(args, w):
     print(json.dumps({
         "impl": "reference", "metric": MX_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": mx_config(w),
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": mx_config(w, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
                          "sample": f"{rows_per_step} full rows of C per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
@@ -853,7 +857,8 @@ def run_mx(args, w):
         "metric": MX_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 (mx)", "data": "synthetic",
-        "config": dict(mx_config(w), parallelism="replicas" if world > 1 else "single GPU"),
+        "config": mx_config(w, world),
+        "kernel_config": {"tile": "256x256 per CTA pair (M > 128; 128x192 per CTA otherwise)"},
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
                      "traffic": traffic,
@@ -903,13 +908,13 @@ def attn_bytes(w) -> float:
     return 2.0 * w.D * w.S * w.B * (2 * w.Hq + 2 * w.Hkv)
 
 
-def attn_config(w) -> dict:
+def attn_config(w, world: int = 1) -> dict:
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D, "causal": w.causal,
             "layout": "Q, O [B, Hq, S, D]; K, V [B, Hkv, S, D]; bf16 row-major",
             "values": f"N(0,1) rounded to bf16, seeds {4000 + w.wid}/{5000 + w.wid}/{6000 + w.wid}",
             "l2": "no flush: Q alone is %d MiB > 126 MiB" % (w.B * w.Hq * w.S * w.D * 2 >> 20)
             if w.B * w.Hq * w.S * w.D * 2 > 126 << 20 else "inputs smaller than L2 (warm L2)",
-            "softmax_scale": "1/sqrt(D)", "accumulate": "fp32", "output": "bf16"}
+            "softmax_scale": "1/sqrt(D)", "accumulate": "fp32", "output": "bf16", "parallelism": parallelism(world)}
 
 
 def oracle_attn_rows_timed(Q, K, V, w, rows, with_values: bool = False):
@@ -977,7 +982,7 @@ def run_reference_attn(args, w):
         "impl": "reference", "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": attn_config(w),
+        "config": attn_config(w, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
                          "sample": f"query rows 0..{rows - 1} of head (0,0) per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -1121,8 +1126,8 @@ def run_attn(args, w):
         "metric": ATTN_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(attn_config(w), parallelism="replicas" if world > 1 else "single GPU",
-                       tile="2x128 query rows per CTA, 128-key blocks"),
+        "config": attn_config(w, world),
+        "kernel_config": {"tile": "2x128 query rows per CTA, 128-key blocks"},
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                      "frac": achieved / peak, "traffic": traffic,

@@ -40,6 +40,28 @@ def test_workload_config_names_the_shape():
     assert "larger than L2" in c["l2"]
 
 
+def test_both_arms_build_config_from_the_workload_alone():
+    """The GPU arm and the reference arm print one `config` for one workload:
+    every line's config comes from the workload builders, which hold no
+    kernel choice (tile, stages, grid, raster group)."""
+    import re
+    import synth
+    src = open(bench.__file__).read()
+    configs = re.findall(r'"config":\s*([^\n]*)', src)
+    assert len(configs) >= 6
+    for c in configs:
+        assert re.match(r"(workload_config|mx_config|attn_config)\(w(, world(, args\.epilogue)?)?\),?$", c.strip()), c
+    kernel_keys = {"tile", "stages", "grid_ctas", "group_m"}
+    built = [bench.workload_config(w, 1) for w in synth.WORKLOADS.values()]
+    built += [bench.workload_config(w, 1) for w in synth.FP8_WORKLOADS.values()]
+    built += [bench.mx_config(w, 1) for w in synth.MX_WORKLOADS.values()]
+    built += [bench.attn_config(w, 1) for w in synth.ATTN_WORKLOADS.values()]
+    assert len(built) >= 14
+    for c in built:
+        assert not kernel_keys & set(c), c["workload"]
+        assert c["parallelism"] == "single GPU", c["workload"]
+
+
 def test_tensor_peak_burst_or_sustained_by_timed_length():
     peaks = {"bf16_tflops": 1937.8, "bf16_tflops_sustained": 1734.0, "hbm_gbs": 6773.9}
     short, src_short = bench.tensor_peak(peaks, "measured", 0.06)

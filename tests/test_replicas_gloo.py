@@ -74,3 +74,7 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["unit"] == "TFLOP/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["value"] > 0
+    import synth
+    # the same config as the GPU arm's line at this N (the kernel's choices sit apart, in kernel_config)
+    assert d["config"] == bench.workload_config(synth.WORKLOADS["gemm_256"], 2)
+    assert d["config"]["parallelism"] == "replicas"
