@@ -45,15 +45,17 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # sources whose digest is given (the code of those sources, comments and
 # layout excluded).
 MEASURED_TRAFFIC = {
-    "gemm_8192": {"source_digest": "5eb7e0d144e6d903", "bytes_per_launch": 1085094144 + 125301248},
+    "gemm_8192": {"source_digest": "cb16790c5d83d15d", "bytes_per_launch": 1069123584 + 126451968},
     # inputs smaller than L2 (warm): DRAM traffic is below the algorithmic bytes
-    "gemm_4096": {"source_digest": "5eb7e0d144e6d903", "bytes_per_launch": 81968896 + 13829376},
-    "skinny_128x28672x8192": {"source_digest": "5eb7e0d144e6d903", "bytes_per_launch": 471965696 + 3182848},
-    "fp8_gemm_8192": {"source_digest": "5eb7e0d144e6d903", "bytes_per_launch": 338380032 + 114954752},
+    "gemm_4096": {"source_digest": "cb16790c5d83d15d", "bytes_per_launch": 81972736 + 13856256},
+    "skinny_128x28672x8192": {"source_digest": "cb16790c5d83d15d", "bytes_per_launch": 471965184 + 3204864},
+    "fp8_gemm_8192": {"source_digest": "cb16790c5d83d15d", "bytes_per_launch": 344409600 + 115722240},
     # the block-scaled GEMM kernel alone (the scale arrangement kernel moves ~8 MB more)
-    "mxfp8_gemm_8192": {"source_digest": "5eb7e0d144e6d903", "bytes_per_launch": 352365568 + 115679232},
+    "mxfp8_gemm_8192": {"source_digest": "cb16790c5d83d15d", "bytes_per_launch": 359903744 + 117093888},
     # the GEMM kernel alone (the split-K reduction reads the fp32 partials and writes C)
-    "decode_64x8192x28672": {"source_digest": "5eb7e0d144e6d903", "bytes_per_launch": 473502208 + 3217408},
+    "decode_64x8192x28672": {"source_digest": "cb16790c5d83d15d", "bytes_per_launch": 473511680 + 3490560},
+    # one launch, no K split (the 256x112 pair): B read once, A and C
+    "decode_256x8192x8192": {"source_digest": "cb16790c5d83d15d", "bytes_per_launch": 138511360 + 3212288},
     # attention: captured at B2 (one launch); the B16 figure scales it by 8 (traffic grows with B)
     "attn_gqa_b2_s4096_d128": {"source_digest": "89f7a7a6da310d8d", "bytes_per_launch": 199923456 + 110883584},
     "attn_gqa_b16_s4096_d128": {"source_digest": "89f7a7a6da310d8d", "bytes_per_launch": 8 * (199923456 + 110883584)},
@@ -1178,7 +1180,7 @@ def _calib_warm_us(fn, reps: int = 25) -> float:
 
 
 def sweep_plans(shapes) -> None:
-    """Every plan a shape can be forced to (kernel ids 1-6, K splits 1, 2, 3, 4,
+    """Every plan a shape can be forced to (every kernel id, K splits 1, 2, 3, 4,
     6, 8, 12), warm back-to-back calls between CUDA events, next to
     torch.matmul (cuBLAS) on the same inputs; per shape the automatic plan's
     time and every candidate sorted by time. The plan's time model
@@ -1210,7 +1212,7 @@ def sweep_plans(shapes) -> None:
         auto.close()
         t_lib = _calib_warm_us(lambda: torch.matmul(A, B.t()))
         res = []
-        for kernel in (1, 2, 3, 4, 5, 6):
+        for kernel in hk.KERNELS:
             for split in (1, 2, 3, 4, 6, 8, 12):
                 try:
                     plan = hk.Plan(M, N, K, kernel=kernel, split_k=split)

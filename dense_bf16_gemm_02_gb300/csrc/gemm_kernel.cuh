@@ -88,11 +88,18 @@ struct Geometry {
     static constexpr int kARowsMax = kARows;                          // rows of A a stage holds
     static constexpr int kAAtomBytes = kARowsMax * kRowBytes;         // one K atom of A
     static constexpr int kAStageBytes = kAAtomBytes * kAtoms;
-    static_assert(kTileN_ % (16 * kCG) == 0 && kTileN_ >= 32 && kTileN_ <= 256, "MMA N");
+    static_assert(kTileN_ % 16 == 0 && kTileN_ >= 32 && kTileN_ <= 256, "MMA N");
     static constexpr int kTileM = kCtaM * kCG;              // rows of C per tile
     static constexpr int kTileN = kTileN_;                  // columns of C per tile (MMA N)
     static constexpr int kBRows = kTileN / kCG;             // rows of B each CTA loads per stage
     static_assert(kBRows % 8 == 0, "B rows fill whole 8-row swizzle atoms");
+    // Half-width units (the tail split) need a valid MMA N of kTileN / 2 and
+    // whole swizzle atoms of B in each CTA's half: not so for a 112-wide pair.
+    static constexpr bool kHalves = kTileN % (16 * kCG) == 0 && (kTileN / kCG / 2) % 8 == 0;
+    // Epilogue: 32-column chunks, the last one narrower when kTileN is not a
+    // multiple of 32 (16 columns for a 112-wide tile)
+    static constexpr int kEpiChunks = (kTileN + kEpiCols - 1) / kEpiCols;
+    static constexpr int kLastChunkCols = kTileN - (kEpiChunks - 1) * kEpiCols;
     static constexpr int kBAtomBytes = kBRows * kRowBytes;            // one K atom of B
     static constexpr int kBBytes = kBAtomBytes * kAtoms;
     static constexpr int kAtomElems = kFp8 ? 128 : 64;     // K elements per atom (one TMA box)
@@ -109,7 +116,10 @@ struct Geometry {
     static constexpr int kSfCols = kSfColsPerAtom * kAtoms;                  // TMEM columns per K block
     static constexpr int kStageBytes = kAStageBytes + kBBytes;              // operands of one K block
     static constexpr int kFixed = kEpiWarps * 2 * kEpiBufBytes + 256 + 1024;   // epilogue, barriers, alignment
-    static constexpr int kMaxStages = kARows < kCtaM ? 12 : 8;
+    // Ring depth cap: 8 for the 128-row tiles of the large shapes; the short-A
+    // single-CTA kernels and the pairs narrower than 128 columns (streaming
+    // kernels, latency-bound: bytes in flight set their rate) take what fits.
+    static constexpr int kMaxStages = (kARows < kCtaM || (kCG == 2 && kTileN_ < 128)) ? 12 : 8;
     // MXFP8: the scales of a K block travel in their own ring of
     // kStages + kSfAhead slots (shared memory and TMEM), loaded kSfAhead K
     // blocks ahead of the operands, so that copying them into TMEM is off the
@@ -138,7 +148,10 @@ struct Geometry {
     static constexpr int kOffTmemHolder = kOffBars + kNumBars * 8;   // [0]: TMEM address, [1..2]: epilogue flags
     static constexpr int kSmemBytes = kOffTmemHolder + 16 + 1024;   // + slack for aligning the base
     static_assert(kSmemBytes <= kSmemLimit, "shared memory");
-    static constexpr int kAccCols = kTileN;                 // TMEM columns per accumulator
+    // TMEM columns per accumulator: the tile's width in whole 32-column chunks
+    // (the epilogue reads 32 columns at a time; a 112-wide tile's last read
+    // takes 16 columns past its accumulator, inside the accumulator's stride)
+    static constexpr int kAccCols = kEpiChunks * kEpiCols;
     // Two accumulators (the epilogue of one tile overlaps the MMAs of the
     // next) unless they and the scale ring do not fit TMEM's 512 columns: the
     // 256-wide block-scaled tile keeps one, which its epilogue reads whole
@@ -151,8 +164,9 @@ struct Geometry {
     static constexpr uint32_t kIdesc = kMx    ? idesc_mxf8_f32(kTileM, kTileN)
                                        : kFp8 ? idesc_e4m3_f32(kTileM, kTileN)
                                               : idesc_bf16_f32(kTileM, kTileN);
-    static constexpr uint32_t kIdescHalf =
-        kFp8 ? idesc_e4m3_f32(kTileM, kTileN / 2) : idesc_bf16_f32(kTileM, kTileN / 2);
+    static constexpr uint32_t kIdescHalf = !kHalves ? kIdesc
+                                           : kFp8   ? idesc_e4m3_f32(kTileM, kTileN / 2)
+                                                    : idesc_bf16_f32(kTileM, kTileN / 2);
 };
 
 // error bits written to the status word when a bounded wait runs out
@@ -806,6 +820,31 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2_rn(v[2 * i], v[2 * i + 1]);
             store_packed(w, row0, col0);
         };
+        // The last, narrower chunk of a tile whose width is not a multiple of 32
+        // (16 columns of a 112-wide tile): the 32 values are computed as for a
+        // full chunk (the upper 16 come from TMEM columns past the accumulator
+        // and are dropped), and this lane's row gets the first kLastChunkCols
+        // by plain stores, 16-byte ones where they fit inside N (C's rows are
+        // 16-byte aligned, as its tensor map requires, and col0 is a multiple of 16).
+        auto store_chunk_narrow = [&](uint32_t (&v)[32], int row, int col0, const uint32_t (&r)[16]) {
+            if (p.bias != nullptr || p.act != 0 || p.alpha != 1.0f || p.residual != nullptr) apply_epilogue(p, v, col0, r);
+            constexpr int kCols = G::kLastChunkCols;
+            uint32_t w[kCols / 2];
+#pragma unroll
+            for (int i = 0; i < kCols / 2; ++i) w[i] = pack_bf16x2_rn(v[2 * i], v[2 * i + 1]);
+            if (row >= p.M) return;
+            uint16_t* const crow = p.c_ptr + static_cast<int64_t>(row) * p.ldc;
+            if (col0 + kCols <= p.N) {
+                uint4* const dst = reinterpret_cast<uint4*>(crow + col0);
+#pragma unroll
+                for (int q = 0; q < kCols / 8; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < kCols; ++e)   // static indices keep w[] in registers
+                    if (col0 + e < p.N)
+                        crow[col0 + e] = static_cast<uint16_t>((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
+            }
+        };
 
         int local = 0;
         const int total = p.total_units;
@@ -814,7 +853,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             unit_info(p, u, t, split, half);
             int tm, tn;
             tile_coords(p, t, tm, tn);
-            const int chunks = (half < 0 ? G::kTileN : G::kTileN / 2) / kEpiCols;
+            const int chunks = half < 0 ? G::kEpiChunks : (G::kTileN / 2) / kEpiCols;
             const int col_base = tn * G::kTileN + (half < 0 ? 0 : half * (G::kTileN / 2));
             const int buf = G::kAccBufs == 2 ? (local & 1) : 0;
             const uint32_t acc_phase = G::kAccBufs == 2 ? ((local >> 1) & 1) : (local & 1);
@@ -849,6 +888,7 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             if constexpr (G::kAccBufs == 1) {
                 // one accumulator: read all of it (as bf16 pairs), release it, then store.
                 // Such tiles never split K, never come in halves and have no fused epilogue.
+                static_assert(G::kLastChunkCols == kEpiCols, "one accumulator: whole 32-column chunks");
                 constexpr int kChunks = G::kTileN / kEpiCols;
                 uint32_t w[kChunks][16];
 #pragma unroll
@@ -898,14 +938,24 @@ gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                             else mbar_arrive(acc_empty_bar(buf));
                         }
                     }
+                    // (only whole-width units have a narrow last chunk: no half units then)
+                    const bool narrow = G::kLastChunkCols < kEpiCols && c == chunks - 1;
                     if (p.splits == 1) {
-                        store_chunk(v, row0, col_base + c * kEpiCols, r);
+                        if constexpr (G::kLastChunkCols < kEpiCols) {
+                            if (narrow) store_chunk_narrow(v, row, col_base + c * kEpiCols, r);
+                            else store_chunk(v, row0, col_base + c * kEpiCols, r);
+                        } else {
+                            store_chunk(v, row0, col_base + c * kEpiCols, r);
+                        }
                     } else if (row < p.M) {
+                        // this split's partial (rows of n_pad = tiles_n × kTileN columns)
                         float4* dst = reinterpret_cast<float4*>(part_row + c * kEpiCols);
+                        const int n4 = narrow ? G::kLastChunkCols / 4 : kEpiCols / 4;
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                                 __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                            if (j < n4)
+                                dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
                     }
                 }
             }

@@ -74,6 +74,7 @@ struct Variant {
     int k_elems;       // K elements per pipeline stage
     int atoms;         // 128-byte K atoms per stage (TMA boxes per operand and stage)
     int sf_bytes;      // MXFP8: bytes of scale blocks per K block and CTA
+    bool halves;       // the tail split may run its tiles as two half-width units
     KernelFn fn;
     const char* name;
 };
@@ -82,7 +83,8 @@ template <int kCG, int kTileN, bool kFp8, bool kMx = false, int kARows = hk::kCt
 constexpr Variant make_variant(int id, const char* name) {
     using G = hk::Geometry<kCG, kTileN, kFp8, kMx, kARows, kAtoms>;
     return Variant{id, kCG, G::kTileM, G::kTileN, G::kStages, G::kSmemBytes, kFp8, kMx, G::kARowsMax, G::kKElems,
-                   kAtoms, G::kSfBytes, &hk::gemm_bf16_kernel<kCG, kTileN, kFp8, kMx, kARows, kAtoms>, name};
+                   kAtoms, G::kSfBytes, G::kHalves, &hk::gemm_bf16_kernel<kCG, kTileN, kFp8, kMx, kARows, kAtoms>,
+                   name};
 }
 
 const Variant kVariants[] = {
@@ -99,6 +101,8 @@ const Variant kVariants[] = {
     make_variant<1, 64, false, false, 64>(HK_KERNEL_SINGLE_128x64, "single 128x64, 64-row A"),
     make_variant<2, 256, false, false, hk::kCtaM, HK_PAIR_ATOMS>(HK_KERNEL_PAIR_256x256, "pair 256x256"),
     make_variant<2, 128, false, false>(HK_KERNEL_PAIR_256x128, "pair 256x128"),
+    // 8192 columns make 74 tiles of 112 for the 76 pairs of a GB300 (64 of 128)
+    make_variant<2, 112, false, false>(HK_KERNEL_PAIR_256x112, "pair 256x112"),
     make_variant<1, 256, false>(HK_KERNEL_SINGLE_128x256, "single 128x256"),
     make_variant<1, 192, false>(HK_KERNEL_SINGLE_128x192, "single 128x192"),
     make_variant<1, 128, false>(HK_KERNEL_SINGLE_128x128, "single 128x128"),
@@ -534,7 +538,7 @@ hk_status fill_plan(hk_gemm_plan* p, int64_t M, int64_t N, int64_t K, int64_t ld
     // round takes about half as long. No workspace is involved.
     g.tail_start = -1;
     g.total_units = g.num_tiles * splits;
-    if (v->cg == 2 && splits == 1 && g.num_tiles > 0 && !(p->cfg.flags & HK_FLAG_NO_TAIL_SPLIT)) {
+    if (v->cg == 2 && v->halves && splits == 1 && g.num_tiles > 0 && !(p->cfg.flags & HK_FLAG_NO_TAIL_SPLIT)) {
         const int64_t rounds = ceil_div(g.num_tiles, units);
         const int64_t last = g.num_tiles - (rounds - 1) * units;
         if (2 * last <= units) {

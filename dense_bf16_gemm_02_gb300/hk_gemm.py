@@ -30,8 +30,9 @@ HK_KERNEL_SINGLE_128x192 = 3
 HK_KERNEL_SINGLE_128x128 = 4
 HK_KERNEL_SINGLE_128x64 = 5
 HK_KERNEL_PAIR_256x128 = 6
+HK_KERNEL_PAIR_256x112 = 7
 KERNELS = (HK_KERNEL_PAIR_256x256, HK_KERNEL_SINGLE_128x256, HK_KERNEL_SINGLE_128x192,
-           HK_KERNEL_SINGLE_128x128, HK_KERNEL_SINGLE_128x64, HK_KERNEL_PAIR_256x128)
+           HK_KERNEL_SINGLE_128x128, HK_KERNEL_SINGLE_128x64, HK_KERNEL_PAIR_256x128, HK_KERNEL_PAIR_256x112)
 
 HK_ACT_NONE = 0
 HK_ACT_RELU = 1

@@ -88,8 +88,13 @@ typedef enum hk_status {
 /* Kernel variants (hk_gemm_config.kernel). A "pair" kernel runs on clusters
  * of two CTAs (tcgen05 cta_group::2) with 256-row output tiles; a "single"
  * kernel runs one CTA per output tile of 128 rows and suits M <= 128. The
- * 256x128 pair (bf16 only) streams a narrower slice of B per pair: for
- * 128 < M <= 256 with few output tiles it fills the GPU without a K split. */
+ * 256x128 and 256x112 pairs (bf16 only) stream a narrower slice of B per
+ * pair: for 128 < M <= 256 with few output tiles they fill the GPU without a
+ * K split (N = 8192 makes 74 tiles of 112 for the 76 pairs of a GB300, 64 of
+ * 128), and its 23 KB stages leave room for a ninth in the ring (the
+ * streaming rate of these shapes grows with the bytes in flight). The 256x112
+ * pair never runs the last round's tiles as half-width units
+ * (HK_FLAG_NO_TAIL_SPLIT is implied). */
 #define HK_KERNEL_AUTO 0            /* chosen by the plan's time model: single-CTA kernels for M <= 128, pairs above 384 (E4M3: 128), either between */
 #define HK_KERNEL_PAIR_256x256 1
 #define HK_KERNEL_SINGLE_128x256 2
@@ -97,6 +102,7 @@ typedef enum hk_status {
 #define HK_KERNEL_SINGLE_128x128 4
 #define HK_KERNEL_SINGLE_128x64 5
 #define HK_KERNEL_PAIR_256x128 6
+#define HK_KERNEL_PAIR_256x112 7
 
 /* Tuning knobs of a plan. Zero in any field selects the default. */
 typedef struct hk_gemm_config {

@@ -169,6 +169,7 @@ TIMEOUT_CASES = [
     ("single 128x256, split K", 64, 1024, 2048, {"kernel": 2, "split_k": 4}, 2, 0, 4),
     ("pair bf16, split K", 512, 512, 2048, {"kernel": 1, "split_k": 2}, 1, 0, 2),
     ("pair 256x128", 256, 640, 512, {"kernel": 6}, 6, 8, 1),
+    ("pair 256x112", 256, 640, 512, {"kernel": 7}, 7, 9, 1),
     ("fp8 pair", 512, 512, 512, {"input_type": 1}, 1, 0, 1),
     ("fp8 single 128x192", 128, 600, 512, {"input_type": 1, "kernel": 3}, 3, 0, 1),
 ]
@@ -315,7 +316,7 @@ def run_plan(hk, A_bits, B_bits, **cfg):
     return full[:M, :N], info
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4, 5, 6, 7])
 @pytest.mark.parametrize("M,N,K", VARIANT_SHAPES)
 def test_kernel_variants_integer_bitexact(hk, kernel, M, N, K):
     A = synth.int_bf16(M, K, 1200 + M)
@@ -325,7 +326,7 @@ def test_kernel_variants_integer_bitexact(hk, kernel, M, N, K):
     assert_bitexact(got, oracle.gemm(A, B), f"kernel {kernel} int {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("kernel", [2, 3, 4, 5, 6])
+@pytest.mark.parametrize("kernel", [2, 3, 4, 5, 6, 7])
 def test_kernel_variants_normal(hk, kernel):
     M, N, K = 200, 777, 1500
     A = synth.normal_bf16(M, K, 31)
@@ -339,7 +340,7 @@ def test_automatic_kernel_choice(hk):
     assert hk.Plan(8192, 8192, 8192).info()["kernel"] == 1
     assert hk.Plan(385, 4096, 4096).info()["ctas_per_unit"] == 2  # above 384 rows: CTA pairs
     assert hk.Plan(129, 4096, 4096).info()["ctas_per_unit"] == 1  # a 129-row pair tile would be half empty
-    assert hk.Plan(256, 8192, 8192).info()["kernel"] == 6       # 64 pairs of 256x128: one wave, no K split
+    assert hk.Plan(256, 8192, 8192).info()["kernel"] == 7       # 74 pairs of 256x112 (9 stages): one wave, no K split
     assert hk.Plan(384, 8192, 8192).info()["kernel"] == 3       # 3 x 43 tiles of 128x192 (measured best)
     assert hk.Plan(200, 4096, 4096, input_type=hk.HK_INPUT_E4M3).info()["kernel"] == 1   # E4M3: pairs above 128
     small = hk.Plan(64, 1024, 1024).info()
@@ -382,7 +383,8 @@ def run_split(hk, A_bits, B_bits, ws_fill=0, runs=1, **cfg):
 
 @pytest.mark.parametrize("kernel,splits,M,N,K", [
     (1, 2, 300, 200, 1000), (1, 5, 257, 520, 2049), (6, 3, 200, 700, 1000), (2, 3, 100, 700, 900), (3, 7, 64, 1000, 2000),
-    (4, 16, 128, 300, 1030), (5, 4, 1, 77, 640), (3, 2, 200, 600, 128)])
+    (4, 16, 128, 300, 1030), (5, 4, 1, 77, 640), (3, 2, 200, 600, 128), (7, 3, 200, 1000, 1000),
+    (7, 2, 260, 1120, 520)])
 def test_split_k_integer_bitexact(hk, kernel, splits, M, N, K):
     A = synth.int_bf16(M, K, 1300 + M)
     B = synth.int_bf16(N, K, 2300 + N)
@@ -463,6 +465,40 @@ def test_tail_split_narrow_pair_integer_bitexact(hk, M, N, K):
     whole, info2 = run_plan(hk, A, B, kernel=6, flags=hk.HK_FLAG_NO_TAIL_SPLIT)
     assert info2["tail_split_tiles"] == 0
     assert_bitexact(got, whole, "split vs whole")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 8192, 256), (300, 1000, 264), (200, 112, 64), (257, 230, 136),
+                                   (512, 2240, 72)])
+def test_pair_256x112_integer_bitexact(hk, M, N, K):
+    """The 112-wide pair: a tile's last 16 columns go out by plain stores (all
+    inside N, partly past it at N = 1000 and 230, or wholly past it), and a
+    partial last round keeps whole tiles (no half-width units: N / 2 = 56 is no
+    MMA width). N = 8192 is 74 tiles; 512 x 2240 is 40 tiles, whose last
+    round on 12 pairs holds 4 (a half-splitting pair would split it)."""
+    A = synth.int_bf16(M, K, 1470 + M)
+    B = synth.int_bf16(N, K, 2470 + N)
+    got, info = run_plan(hk, A, B, kernel=7)
+    assert info["kernel"] == 7 and info["tile_n"] == 112 and info["tail_split_tiles"] == 0
+    assert info["num_tiles"] == -(-M // 256) * -(-N // 112)
+    assert_bitexact(got, oracle.gemm(A, B), f"pair 256x112 {M}x{N}x{K}")
+    if N == 2240:
+        few, info2 = run_plan(hk, A, B, kernel=7, max_clusters=12)
+        assert info2["tail_split_tiles"] == 0
+        assert_bitexact(few, got, "12 pairs vs all")
+
+
+@pytest.mark.parametrize("M,N,K", [(257, 600, 128), (300, 1000, 264)])
+def test_fused_epilogue_pair_256x112_integer_bitexact(hk, M, N, K):
+    """Bias and ReLU, then a residual after the activation, on the 112-wide
+    pair (the narrow last chunk of every tile included)."""
+    A = synth.int_bf16(M, K, 1960 + M)
+    B = synth.int_bf16(N, K, 2960 + N)
+    bias = synth.int_bf16(1, N, 3960 + N)[0]
+    R = synth.int_bf16(M, N, 4960 + N, -40, 40)
+    got = run_epilogue(hk, A, B, bias, 1, split_k=1, kernel=7)
+    assert_bitexact(got, oracle.gemm_epilogue(A, B, bias, 1), f"pair 112 relu + bias {M}x{N}x{K}")
+    got = run_fused(hk, A, B, bias, R, 1, split_k=1, kernel=7)
+    assert_bitexact(got, oracle.gemm_epilogue(A, B, bias, 1, residual=R), f"pair 112 residual {M}x{N}x{K}")
 
 
 def test_tail_split_normal_matches_whole_tiles(hk):
@@ -744,10 +780,10 @@ def test_fused_epilogue_narrow_pair_integer_bitexact(hk, M, N, K):
     assert_bitexact(got, oracle.gemm_epilogue(A, B, bias, 1, residual=R), f"narrow pair residual {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("kernel,splits", [(4, 4), (1, 3), (2, 2), (6, 3)])
+@pytest.mark.parametrize("kernel,splits", [(4, 4), (1, 3), (2, 2), (6, 3), (7, 2)])
 def test_residual_in_split_k_reduction(hk, kernel, splits):
     """A K split adds bias, activation and R in its reduction kernel."""
-    M, N, K = (300 if kernel in (1, 6) else 64), 1200, 2048
+    M, N, K = (300 if kernel in (1, 6, 7) else 64), 1200, 2048
     A = synth.int_bf16(M, K, 81)
     B = synth.int_bf16(N, K, 82)
     bias = synth.int_bf16(1, N, 83)[0]
