@@ -336,7 +336,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(w, world),
+        "data": "synthetic", "config": workload_config(w, world, "none", args.cold_l2),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
                          "sample": f"{rows_per_step} full rows of C per step ({rows_per_step}x{w.N}x{w.K})"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -349,7 +349,10 @@ def parallelism(world: int) -> str:
     return "replicas" if world > 1 else "single GPU"
 
 
-def workload_config(w, world: int = 1, epilogue: str = "none") -> dict:
+L2_FLUSH_BYTES = 256 << 20   # written before each timed launch with --cold-l2 (GB300 L2: 126 MiB)
+
+
+def workload_config(w, world: int = 1, epilogue: str = "none", cold_l2: bool = False) -> dict:
     """The workload as both arms name it (the kernel's own choices go under
     the line's `kernel_config`, so that the two arms' configs are equal)."""
     elem = 1 if is_fp8(w) else 2
@@ -357,8 +360,10 @@ def workload_config(w, world: int = 1, epilogue: str = "none") -> dict:
            "layout": "A MxK row-major, B NxK row-major, C MxN row-major (C = A·Bᵀ)",
            "values": f"N(0,1)·{w.scale} rounded to {'E4M3' if elem == 1 else 'bf16'}, "
                      f"seeds {1000 + w.wid}/{2000 + w.wid}",
-           "l2": "no flush: inputs larger than L2 (A+B = %d MiB > 126 MiB)" % ((w.M + w.N) * w.K * elem >> 20)
-           if (w.M + w.N) * w.K * elem > 126 << 20 else "inputs smaller than L2 (warm L2)",
+           "l2": ("flushed: %d MiB written before each timed launch, outside its two events"
+                  % (L2_FLUSH_BYTES >> 20)) if cold_l2 else
+                 "no flush: inputs larger than L2 (A+B = %d MiB > 126 MiB)" % ((w.M + w.N) * w.K * elem >> 20)
+                 if (w.M + w.N) * w.K * elem > 126 << 20 else "inputs smaller than L2 (warm L2)",
            "accumulate": "fp32", "output": "bf16", "parallelism": parallelism(world), "epilogue": epilogue}
     if elem == 1:
         cfg["scales"] = list(synth.FP8_SCALES)
@@ -389,6 +394,22 @@ def time_library(call, dev, warmup: int, n: int) -> float:
     c1.record()
     torch.cuda.synchronize(dev)
     return c0.elapsed_time(c1) / n
+
+
+def time_cold(call, flush, stream, n: int) -> list:
+    """Durations (ms) of `n` calls of `call` on `stream`, each after `flush`
+    (a buffer larger than L2) is overwritten and timed alone between its own
+    two CUDA events, so that no call finds its operands in L2."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n)]
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            flush.fill_(i & 0x7F)
+            ev[2 * i].record(stream)
+            call()
+            ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(n)]
 
 
 def launch_spread(call, stream, n: int) -> list:
@@ -479,21 +500,27 @@ def run_hk(args, w):
         raise RuntimeError("device status after warm-up: " + hk.hk_gemm_last_error_string())
 
     # ---- device-resident timed region: K back-to-back launches between two events
+    # (--cold-l2: each launch after a write of a buffer larger than L2, timed alone)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if args.cold_l2 else None
     events = [torch.cuda.Event(enable_timing=True) for _ in range(2)]   # the timed region's two ends
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(TIMED_PAUSE_S)   # (also lets the clock sampler start)
     barrier(world)
     torch.cuda.synchronize(dev)
     t_host0 = time.time()
-    with torch.cuda.stream(stream):
-        events[0].record(stream)
-        for i in range(args.steps):
-            step()
-        events[1].record(stream)
+    cold_ms = None
+    if flush is not None:
+        cold_ms = time_cold(step, flush, stream, args.steps)
+    else:
+        with torch.cuda.stream(stream):
+            events[0].record(stream)
+            for i in range(args.steps):
+                step()
+            events[1].record(stream)
     torch.cuda.synchronize(dev)
     t_host1 = time.time()
     barrier(world)
-    elapsed_ms = events[0].elapsed_time(events[1])
+    elapsed_ms = sum(cold_ms) if cold_ms is not None else events[0].elapsed_time(events[1])
     if hk.hk_gemm_last_device_status(local) != hk.HK_OK:
         raise RuntimeError("device status after timing: " + hk.hk_gemm_last_error_string())
     clocks = None
@@ -501,8 +528,8 @@ def run_hk(args, w):
         time.sleep(0.15)
         sampler.stop()
         clocks = sampler.summary(t_host0, t_host1)
-    # per-launch spread, outside the timed region
-    per_launch = launch_spread(step, stream, min(args.steps, 20))
+    # per-launch spread, outside the timed region (cold: the timed launches themselves)
+    per_launch = cold_ms if cold_ms is not None else launch_spread(step, stream, min(args.steps, 20))
     elapsed_max = max_over_ranks(world, elapsed_ms)
 
     # ---- end to end: pinned host inputs -> device -> GEMM -> host result.
@@ -587,7 +614,15 @@ def run_hk(args, w):
                 what = ("torch.matmul (cuBLAS) on the same GPU and inputs, timed after ours with the same warm-up "
                         "and pause; context only")
             n_ctx = max(5, args.steps)   # as many back-to-back calls as our timed region
-            ms = time_library(lib_call, dev, args.warmup, n_ctx)
+            if flush is not None:
+                for _ in range(max(3, args.warmup)):
+                    lib_call()
+                torch.cuda.synchronize(dev)
+                time.sleep(TIMED_PAUSE_S)
+                ms = sum(time_cold(lib_call, flush, torch.cuda.current_stream(dev), n_ctx)) / n_ctx
+                what += "; each call after the same L2 flush, timed alone"
+            else:
+                ms = time_library(lib_call, dev, args.warmup, n_ctx)
             cublas = {"value": flops / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_gemm": ms, "launches": n_ctx,
                       "what": what}
         except Exception as exc:   # context only: never fails the bench
@@ -616,13 +651,13 @@ def run_hk(args, w):
     digest = kernel_source_digest()
     traffic = None
     tr = MEASURED_TRAFFIC.get(w.name)
-    if tr and tr.get("source_digest") == digest:
+    if tr and tr.get("source_digest") == digest and not args.cold_l2:   # (captured without a flush)
         traffic = tr["bytes_per_launch"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16", "data": "synthetic",
-        "config": workload_config(w, world, args.epilogue),
+        "config": workload_config(w, world, args.epilogue, args.cold_l2),
         "kernel_config": {"tile": f"{info['tile_m']}x{info['tile_n']}x{info['tile_k']} per "
                                   f"{'CTA pair' if info['ctas_per_unit'] == 2 else 'CTA'}",
                           "stages": info["stages"], "grid_ctas": info["grid_ctas"], "group_m": info["group_m"]},
@@ -634,7 +669,8 @@ def run_hk(args, w):
                      "algorithmic_bytes_per_launch": nbytes,
                      "mean_launch_ms": mean_launch_ms, "p10_launch_ms": float(np.percentile(per_launch, 10)),
                      "p90_launch_ms": float(np.percentile(per_launch, 90)),
-                     "spread_source": "p10/p90: launches timed one by one after the timed region",
+                     "spread_source": "p10/p90: the timed launches, each after an L2 flush" if args.cold_l2 else
+                                      "p10/p90: launches timed one by one after the timed region",
                      "kernel": f"gemm_bf16_kernel ({info['tile_m']}x{info['tile_n']}, "
                                f"{info['ctas_per_unit']} CTA(s) per tile)",
                      "source_digest": digest},
@@ -1247,6 +1283,9 @@ def main(argv=None):
                     choices=sorted(ALL_WORKLOADS) + sorted(synth.ATTN_WORKLOADS) + sorted(synth.MX_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cublas-context", action="store_true")
+    ap.add_argument("--cold-l2", action="store_true",
+                    help="GEMM workloads: write a %d MiB buffer before each timed launch and time each launch "
+                         "alone (operands never in L2)" % (L2_FLUSH_BYTES >> 20))
     ap.add_argument("--epilogue", default="none", choices=["none", "bias", "bias_relu", "bias_gelu", "bias_silu"],
                     help="fused epilogue of each step (hk_gemm_bf16_epilogue)")
     ap.add_argument("--group-m", type=int, default=0,
@@ -1263,6 +1302,8 @@ def main(argv=None):
         l2_latency()
         return 0
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
+    if args.cold_l2 and (args.workload in synth.MX_WORKLOADS or args.workload in synth.ATTN_WORKLOADS):
+        ap.error("--cold-l2 applies to the bf16 and E4M3 GEMM workloads")
     if args.workload in synth.MX_WORKLOADS:
         w = synth.MX_WORKLOADS[args.workload]
         return run_reference_mx(args, w) if args.impl == "reference" else run_mx(args, w)

@@ -50,7 +50,8 @@ def test_both_arms_build_config_from_the_workload_alone():
     configs = re.findall(r'"config":\s*([^\n]*)', src)
     assert len(configs) >= 6
     for c in configs:
-        assert re.match(r"(workload_config|mx_config|attn_config)\(w(, world(, args\.epilogue)?)?\),?$", c.strip()), c
+        assert re.match(r'(workload_config|mx_config|attn_config)\(w(, world(, (args\.epilogue|"none"), args\.cold_l2)?)?\),?$',
+                        c.strip()), c
     kernel_keys = {"tile", "stages", "grid_ctas", "group_m"}
     built = [bench.workload_config(w, 1) for w in synth.WORKLOADS.values()]
     built += [bench.workload_config(w, 1) for w in synth.FP8_WORKLOADS.values()]
@@ -60,6 +61,21 @@ def test_both_arms_build_config_from_the_workload_alone():
     for c in built:
         assert not kernel_keys & set(c), c["workload"]
         assert c["parallelism"] == "single GPU", c["workload"]
+
+
+def test_reference_arm_names_the_cold_l2_protocol():
+    """--cold-l2 changes the workload's `l2` entry in both arms alike."""
+    import json
+    import subprocess
+    import sys
+    import synth
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "gemm_256", "--cold-l2",
+                        "--steps", "1", "--warmup", "0"], cwd=os.path.dirname(os.path.abspath(bench.__file__)),
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    assert d["config"] == bench.workload_config(synth.WORKLOADS["gemm_256"], 1, "none", True)
+    assert d["config"]["l2"].startswith("flushed: 256 MiB")
 
 
 def test_tensor_peak_burst_or_sustained_by_timed_length():
