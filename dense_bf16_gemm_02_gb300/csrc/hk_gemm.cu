@@ -376,7 +376,7 @@ int a_rows_for(const Variant& v, int64_t M) {
 
 // Kernel choice by a small time model. Automatic choice among single-CTA
 // kernels (128-row tiles, four widths) for M <= kMaxRowsSingle (bf16; 128 for
-// E4M3) and CTA pairs (256-row tiles: 256 or, bf16, 128 wide) for M > 128;
+// E4M3) and CTA pairs (256-row tiles: 256, or for bf16 128 or 112 wide) for M > 128;
 // between the two limits both compete. K is split only when one wave of
 // tiles leaves work-unit slots idle and a workspace may be used. Estimated
 // time of a candidate (µs):
